@@ -1,0 +1,199 @@
+/*
+ * txl.h - C ABI of the GB300 (sm_103a) Transformer-XL relative-position
+ * attention library.
+ *
+ * The operations follow "Transformer-XL: Attentive Language Models Beyond a
+ * Fixed-Length Context" (Dai et al.):
+ *   - §3.2, segment-level recurrence: the hidden states of earlier segments are
+ *     cached (a memory of length M per layer) and prepended, without gradient,
+ *     to the current segment as extended context for keys and values;
+ *   - §3.3, the relative score
+ *       A_ij = q_i.k_j + q_i.W_kR R_{i-j} + u.k_j + v.W_kR R_{i-j}
+ *     with the sinusoid table R, then a masked softmax over the extended
+ *     context and a product with the values (the N-layer summary);
+ *   - Appendix B, the reversed table Q_k = W_kR R_{M+L-1-k} and the left shift
+ *     that turns q Q^T into the position term, which the kernel realises by
+ *     index arithmetic inside its tiles.
+ *
+ * Conventions for every entry point:
+ *   - All pointers are device pointers unless stated otherwise.  The caller owns
+ *     every buffer; the library keeps no reference after the call returns.
+ *   - Work is enqueued on `stream` (a cudaStream_t; NULL is the legacy default
+ *     stream) and the call returns once it is launched.  Inputs must stay valid
+ *     and unmodified until the stream reaches the work.
+ *   - Arguments are validated on the host before anything is launched; a bad
+ *     argument returns an error code and enqueues nothing.
+ *   - Kernels that wait on on-chip barriers give up after a time limit and
+ *     record TXL_ERR_TIMEOUT in a device status word; txl_device_status()
+ *     reads and clears it.
+ *   - Return values are txl_status codes (0 = success).
+ */
+#ifndef TXL_H
+#define TXL_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+    TXL_OK = 0,
+    TXL_ERR_INVALID_ARG = -1, /* null pointer, negative size, bad dtype code */
+    TXL_ERR_UNSUPPORTED = -2, /* a shape or dtype this build has no kernel for */
+    TXL_ERR_MISALIGNED = -3,  /* a pointer breaks the stated alignment */
+    TXL_ERR_SHAPE = -4,       /* sizes inconsistent with each other */
+    TXL_ERR_CUDA = -5,        /* a CUDA runtime or driver call failed */
+    TXL_ERR_TIMEOUT = -6,     /* a kernel gave up waiting on an on-chip barrier */
+    TXL_ERR_WORKSPACE = -7    /* workspace missing or too small for the request */
+} txl_status;
+
+typedef enum {
+    TXL_F32 = 0, /* IEEE binary32 */
+    TXL_BF16 = 1 /* bfloat16 */
+} txl_dtype;
+
+/* Human-readable name of a status code (static string, never NULL). */
+const char *txl_status_string(int status);
+
+/* Library version: major*10000 + minor*100 + patch. */
+int txl_version(void);
+
+/*
+ * txl_rel_pos_emb - the sinusoid relative encoding table R of §3.3 ("R is a
+ * sinusoid encoding matrix without learnable parameters"; row p stands for a
+ * relative distance of p), written in Appendix B's reversed row order.
+ *
+ *   R     [K][d_model], dtype `dtype` (TXL_F32 or TXL_BF16), row-major.
+ *         Row rho holds distance p = K-1-rho:
+ *           R[rho][2k]   = sin(p * w_k),  R[rho][2k+1] = cos(p * w_k),
+ *           w_k = 10000^(-2k/d_model).
+ *         Multiplying by W_kR^T gives the per-head operand `r` of
+ *         txl_relattn_fwd.
+ *   K >= 1, d_model even and >= 2.  R must be 4-byte aligned.
+ * Errors: TXL_ERR_INVALID_ARG (null R, K < 1, odd or non-positive d_model,
+ * bad dtype), TXL_ERR_MISALIGNED, TXL_ERR_CUDA.
+ */
+int txl_rel_pos_emb(void *R, int K, int d_model, int dtype, void *stream);
+
+/*
+ * txl_relattn_workspace_size - bytes of device workspace txl_relattn_fwd needs
+ * when it splits the key range of a head over `n_splits` thread blocks
+ * (n_splits <= 1 needs none).  Pure host arithmetic.
+ */
+size_t txl_relattn_workspace_size(int B, int H, int L, int dh, int n_splits);
+
+/*
+ * txl_relattn_fwd - forward relative-position attention of one layer over the
+ * extended context (§3.2 recurrence, §3.3 score and N-layer summary,
+ * Appendix B shift).
+ *
+ * With K = M + L keys (memory rows first, then the segment), for every batch
+ * b, head h, query i in [0,L) and key j in [0,K):
+ *   delta  = M + i - j                        (relative distance)
+ *   A_ij   = scale * ((q_i + u).k_j + (q_i + v_bias).r[row(delta)])  if delta >= 0
+ *   A_ij   = -inf                                                     otherwise
+ *   out_i  = sum_j softmax_j(A_i.) v_j,   lse_i = log sum_j exp(A_ij)
+ * where r[row] = W_kR R_{distance} in Appendix B's reversed order: with
+ * r_rows rows per head, row(delta) = r_rows - 1 - delta.  A table built for
+ * exactly K keys has r_rows = K; a longer table (r_rows > K, e.g. cached for the
+ * largest memory) is used as is.
+ *
+ * Layouts (dense, row-major, innermost dimension dh contiguous):
+ *   q   [B][H][L][dh]        k, v [B][H][K][dh]
+ *   r   [H][r_rows][dh]      u, v_bias [H][dh]
+ *   out [B][H][L][dh]        lse [B][H][L] fp32, natural log (may be NULL)
+ * dtype TXL_BF16: q, k, v, r, u, v_bias and out are bf16; scores, softmax and
+ *   accumulation are fp32 on the tensor cores (tcgen05).  dh must be 64; q, k,
+ *   v and r must be 16-byte aligned.
+ * dtype TXL_F32: every tensor is fp32 and the arithmetic is fp32 on the CUDA
+ *   cores (no TF32).  dh must be 64.
+ * M >= 0, L >= 1, r_rows >= K, B >= 1, H >= 1.
+ *
+ * n_splits: 0 lets the library choose; 1 processes each head's keys in one
+ * thread block; n > 1 splits the key range over n blocks and merges their
+ * partial results (needs txl_relattn_workspace_size(B,H,L,dh,n) bytes of
+ * workspace, 256-byte aligned, owned by the caller, contents undefined on
+ * return).  A workspace that is NULL or too small limits the automatic choice
+ * to 1 and makes an explicit n > 1 fail with TXL_ERR_WORKSPACE.
+ *
+ * Errors: TXL_ERR_INVALID_ARG, TXL_ERR_UNSUPPORTED (dh != 64, bad dtype),
+ * TXL_ERR_MISALIGNED, TXL_ERR_SHAPE (r_rows < K), TXL_ERR_WORKSPACE,
+ * TXL_ERR_CUDA.
+ */
+int txl_relattn_fwd(const void *q, const void *k, const void *v, const void *r, int r_rows,
+                    const void *u, const void *v_bias, void *out, float *lse, int B, int H,
+                    int M, int L, int dh, float scale, int dtype, int n_splits,
+                    void *workspace, size_t workspace_bytes, void *stream);
+
+/*
+ * Segment memory of one layer (§3.2: "cache a predefined length-M old hidden
+ * states spanning (possibly) multiple segments"), kept as a ring buffer.
+ *
+ *   mem  [B][capacity][d] on the device, owned by the caller.
+ *   txl_mem_state lives in HOST memory and is owned by the caller:
+ *     head     slot that receives the next row
+ *     fill     rows currently held (0..capacity)
+ *     capacity M, the memory length
+ * Logical row t (0 = oldest) of the fill rows sits in slot
+ * (head - fill + t) mod capacity.  Initialise with {0, 0, M}.
+ */
+typedef struct {
+    int head;
+    int fill;
+    int capacity;
+} txl_mem_state;
+
+/*
+ * txl_mem_concat - the extended context h~ = [SG(m) o h] of §3.2 / §3.3 for
+ * the current segment: ext[b] = the fill memory rows oldest-first, then the L
+ * rows of h_new.  SG (stop-gradient) is the identity in a forward pass.
+ *   ext   [B][fill + L][d]   h_new [B][L][d]   same dtype (TXL_F32 / TXL_BF16)
+ * Rows are copied in 16-byte units: d * element size must be a multiple of 16
+ * and every pointer 16-byte aligned.
+ * Errors: TXL_ERR_INVALID_ARG, TXL_ERR_MISALIGNED, TXL_ERR_SHAPE, TXL_ERR_CUDA.
+ */
+int txl_mem_concat(void *ext, const void *mem, const txl_mem_state *st, const void *h_new,
+                   int B, int L, int d, int dtype, void *stream);
+
+/*
+ * txl_mem_update - advance the memory with the current segment's states:
+ * the memory becomes the newest `capacity` rows of [m o h_new] (§3.2, the
+ * summary's m^n_tau).  Writes at most min(L, capacity) rows into the ring and
+ * updates *st on the host (head advances by L mod capacity, fill saturates at
+ * capacity).  Same layout and alignment rules as txl_mem_concat.
+ * Errors: TXL_ERR_INVALID_ARG, TXL_ERR_MISALIGNED, TXL_ERR_SHAPE, TXL_ERR_CUDA;
+ * *st is unchanged on error.
+ */
+int txl_mem_update(void *mem, txl_mem_state *st, const void *h_new, int B, int L, int d,
+                   int dtype, void *stream);
+
+/*
+ * txl_device_status - synchronise `stream`, then read and clear the device
+ * status word in which kernels record barrier time-outs.  Returns TXL_OK,
+ * TXL_ERR_TIMEOUT or TXL_ERR_CUDA.
+ */
+int txl_device_status(void *stream);
+
+/*
+ * txl_set_wait_limit_ns - time limit, in nanoseconds, after which a kernel's
+ * on-chip barrier wait gives up (default 1e9).  Applies to later launches from
+ * this process.  Returns the previous value.
+ */
+uint64_t txl_set_wait_limit_ns(uint64_t ns);
+
+/*
+ * txl_debug_wait_timeout - launch one small kernel that waits on a barrier no
+ * one will complete, with the time limit `ns`; it must give up, record the
+ * time-out and return.  Lets a test check the time-out path without hanging
+ * anything.  Returns the status txl_device_status() reports afterwards
+ * (TXL_ERR_TIMEOUT when the path works).
+ */
+int txl_debug_wait_timeout(uint64_t ns, void *stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* TXL_H */

@@ -1,0 +1,64 @@
+"""The streaming 12-layer stack on the GPU against the oracle's explicit
+recomputation of the last segment from the stored memories.
+
+"Transformer-XL: Attentive Language Models Beyond a Fixed-Length Context",
+§3.2 (each layer caches the last M states of its input and reuses them as
+extended context) and the §3.3 N-layer summary.  The GPU runs all segments
+with its kernels (memory concat/update, positional table, attention) and torch
+for projections, LayerNorm and the feed-forward.  Before the last segment its
+memories are read back; the oracle then computes that segment in fp64 from
+those memories with the same bf16-rounded parameters and the per-pair
+relative vectors, and the top-layer states are compared.
+"""
+
+import math
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import txl_inputs
+from parity import compare, dev
+from transformer_xl_relative_pos_gb300.model import XLStack
+
+pytestmark = pytest.mark.gpu
+
+
+def rounded(t, dtype=torch.bfloat16):
+    return t.to(dtype).double().numpy()
+
+
+def run_stack(w, n_layer=None, n_seg=None):
+    params = txl_inputs.draw_stack(w)
+    if n_layer is not None:
+        params["layers"] = params["layers"][:n_layer]
+    stack = XLStack(params, w.H, w.M, dev(), torch.bfloat16)
+    tokens = params["tokens"][: (n_seg or w.n_seg)]
+    for s in range(tokens.shape[0] - 1):
+        stack.segment(tokens[s])
+    mems = [m.double().cpu().numpy() for m in stack.memories()]
+    h_gpu = stack.segment(tokens[-1]).double().cpu().numpy()
+    torch.cuda.synchronize()
+    layers64 = [{k: rounded(v) for k, v in lay.items()} for lay in params["layers"]]
+    h_or, _ = oracle.segment_forward(tokens[-1].numpy(), rounded(params["emb"]), layers64, mems,
+                                     rounded(params["u"]), rounded(params["v_bias"]), w.H, w.M,
+                                     1.0 / math.sqrt(w.dh))
+    return h_gpu, h_or, stack, mems
+
+
+def test_small_stack_memory_fill_and_wrap():
+    # 3 layers, L=64 and M=100: the memories fill over two segments, then wrap.
+    base = txl_inputs.WORKLOADS["c5_stack12_L512_M512"]
+    w = txl_inputs.Workload("small_stack", B=2, H=2, dh=64, L=64, M=100, d_model=128,
+                            dtype="bf16", seed=41, d_ff=256, n_layer=3, n_seg=5, vocab=base.vocab)
+    h_gpu, h_or, stack, mems = run_stack(w)
+    assert all(m.shape[1] == 100 for m in mems)
+    compare(h_gpu, h_or, 6e-2, 1.5e-2, what="small stack")
+
+
+def test_c5_stack12_last_segment():
+    w = txl_inputs.WORKLOADS["c5_stack12_L512_M512"]
+    h_gpu, h_or, stack, mems = run_stack(w)
+    assert len(mems) == 12 and all(m.shape == (w.B, w.M, w.d_model) for m in mems)
+    compare(h_gpu, h_or, 1e-1, 2e-2, what="c5 top layer")

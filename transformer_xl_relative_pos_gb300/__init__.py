@@ -1,0 +1,38 @@
+"""GB300 (sm_103a) Transformer-XL relative-position attention.
+
+Thin Python binding over the C ABI of ``libtxl_gb300.so`` (``include/txl.h``).
+Every function here only marshals arguments (tensor pointers, sizes, the
+current CUDA stream) and raises on a non-zero status; all computation runs in
+the library's CUDA kernels.  There is no CPU fallback: without the built
+library every call raises.
+
+Functions follow "Transformer-XL: Attentive Language Models Beyond a
+Fixed-Length Context" (§3.2 segment-level recurrence, §3.3 relative score and
+N-layer summary, Appendix B reversed table and shift):
+
+  rel_pos_emb     sinusoid table R in Appendix B's reversed row order
+  relattn_fwd     fused relative-position attention over [memory ; segment]
+  mem_concat      extended context [SG(m) o h] from the ring-buffer memory
+  mem_update      advance the memory to the newest M states
+"""
+
+from __future__ import annotations
+
+from ._lib import (  # noqa: F401
+    F32,
+    BF16,
+    MemState,
+    TxlError,
+    debug_wait_timeout,
+    device_status,
+    lib,
+    lib_path,
+    mem_concat,
+    mem_update,
+    rel_pos_emb,
+    relattn_fwd,
+    set_wait_limit_ns,
+    status_string,
+    version,
+    workspace_size,
+)

@@ -1,0 +1,200 @@
+"""ctypes binding of the C ABI in ``include/txl.h`` (argument marshalling only)."""
+
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+
+import torch
+
+from . import build as _build
+
+F32 = 0
+BF16 = 1
+
+_lock = threading.Lock()
+_lib = None
+
+_c_int, _c_size, _c_p, _c_float, _c_u64 = (ctypes.c_int, ctypes.c_size_t, ctypes.c_void_p,
+                                           ctypes.c_float, ctypes.c_uint64)
+
+
+class TxlError(RuntimeError):
+    """A non-zero txl_status returned by the library."""
+
+    def __init__(self, status: int, message: str):
+        super().__init__(message)
+        self.status = status
+
+
+class MemState(ctypes.Structure):
+    """txl_mem_state: host-side ring-buffer state of one layer's memory."""
+
+    _fields_ = [("head", ctypes.c_int), ("fill", ctypes.c_int), ("capacity", ctypes.c_int)]
+
+    def __repr__(self):
+        return f"MemState(head={self.head}, fill={self.fill}, capacity={self.capacity})"
+
+
+def lib_path() -> str:
+    return _build.LIB_PATH
+
+
+def lib():
+    """Load ``libtxl_gb300.so``; build it first when the sources are newer.
+
+    Raises if it cannot be built or loaded: nothing falls back to another
+    implementation."""
+    global _lib
+    with _lock:
+        if _lib is None:
+            path = _build.build() if os.environ.get("TXL_NO_BUILD") != "1" else _build.LIB_PATH
+            if not os.path.exists(path):
+                raise TxlError(-5, f"CUDA library missing: {path}")
+            L = ctypes.CDLL(path)
+            sig = {
+                "txl_status_string": (ctypes.c_char_p, [_c_int]),
+                "txl_version": (_c_int, []),
+                "txl_rel_pos_emb": (_c_int, [_c_p, _c_int, _c_int, _c_int, _c_p]),
+                "txl_relattn_workspace_size": (_c_size, [_c_int, _c_int, _c_int, _c_int, _c_int]),
+                "txl_relattn_fwd": (_c_int, [_c_p, _c_p, _c_p, _c_p, _c_int, _c_p, _c_p, _c_p, _c_p,
+                                             _c_int, _c_int, _c_int, _c_int, _c_int, _c_float,
+                                             _c_int, _c_int, _c_p, _c_size, _c_p]),
+                "txl_mem_concat": (_c_int, [_c_p, _c_p, ctypes.POINTER(MemState), _c_p, _c_int,
+                                            _c_int, _c_int, _c_int, _c_p]),
+                "txl_mem_update": (_c_int, [_c_p, ctypes.POINTER(MemState), _c_p, _c_int, _c_int,
+                                            _c_int, _c_int, _c_p]),
+                "txl_device_status": (_c_int, [_c_p]),
+                "txl_set_wait_limit_ns": (_c_u64, [_c_u64]),
+                "txl_debug_wait_timeout": (_c_int, [_c_u64, _c_p]),
+            }
+            for name, (res, args) in sig.items():
+                fn = getattr(L, name)
+                fn.restype = res
+                fn.argtypes = args
+            _lib = L
+    return _lib
+
+
+def status_string(status: int) -> str:
+    return lib().txl_status_string(int(status)).decode()
+
+
+def version() -> int:
+    return int(lib().txl_version())
+
+
+def _check(rc: int, what: str):
+    if rc != 0:
+        raise TxlError(rc, f"{what}: {status_string(rc)} ({rc})")
+
+
+def _stream(t: torch.Tensor | None = None, stream=None):
+    if stream is None:
+        dev = t.device if t is not None else torch.device("cuda", torch.cuda.current_device())
+        stream = torch.cuda.current_stream(dev)
+    return ctypes.c_void_p(stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream))
+
+
+def _dev(t: torch.Tensor, name: str, dtype=None) -> int:
+    if not isinstance(t, torch.Tensor):
+        raise TypeError(f"{name} must be a torch.Tensor")
+    if not t.is_cuda:
+        raise ValueError(f"{name} must be a CUDA tensor (the library takes device pointers)")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    if dtype is not None and t.dtype != dtype:
+        raise ValueError(f"{name} must be {dtype}, got {t.dtype}")
+    return t.data_ptr()
+
+
+def _code(dtype: torch.dtype) -> int:
+    if dtype == torch.float32:
+        return F32
+    if dtype == torch.bfloat16:
+        return BF16
+    raise ValueError(f"unsupported dtype {dtype} (float32 or bfloat16)")
+
+
+def rel_pos_emb(K: int, d_model: int, dtype=torch.float32, device=None, out=None, stream=None):
+    """Sinusoid relative table R [K, d_model]; row rho holds distance K-1-rho."""
+    if out is None:
+        dev = device if device is not None else torch.device("cuda", torch.cuda.current_device())
+        out = torch.empty(K, d_model, dtype=dtype, device=dev)
+    _check(lib().txl_rel_pos_emb(_dev(out, "R"), int(K), int(d_model), _code(out.dtype),
+                                 _stream(out, stream)), "txl_rel_pos_emb")
+    return out
+
+
+def workspace_size(B: int, H: int, L: int, dh: int, n_splits: int) -> int:
+    return int(lib().txl_relattn_workspace_size(int(B), int(H), int(L), int(dh), int(n_splits)))
+
+
+def relattn_fwd(q, k, v, r, u, v_bias, M: int, scale: float, *, out=None, lse=None,
+                n_splits: int = 0, workspace=None, stream=None):
+    """Relative-position attention of one layer.
+
+    q [B,H,L,dh]; k, v [B,H,M+L,dh] (memory rows first); r [H,r_rows,dh] in the
+    reversed order (row rho = W_kR R_{r_rows-1-rho}); u, v_bias [H,dh].  All
+    bf16 (tensor-core path) or all fp32 (CUDA-core path).  ``lse``: True to
+    return log-sum-exp [B,H,L] (fp32), or a tensor to fill.  Returns ``out``
+    or ``(out, lse)``."""
+    B, H, L, dh = q.shape
+    dt = q.dtype
+    code = _code(dt)
+    if out is None:
+        out = torch.empty_like(q)
+    want_lse = lse is not None and lse is not False
+    if lse is True:
+        lse = torch.empty(B, H, L, dtype=torch.float32, device=q.device)
+    lse_ptr = _dev(lse, "lse", torch.float32) if want_lse else None
+    ws_ptr, ws_bytes = None, 0
+    if workspace is not None:
+        ws_ptr, ws_bytes = _dev(workspace, "workspace"), workspace.numel() * workspace.element_size()
+    rc = lib().txl_relattn_fwd(
+        _dev(q, "q", dt), _dev(k, "k", dt), _dev(v, "v", dt), _dev(r, "r", dt), int(r.shape[1]),
+        _dev(u, "u", dt), _dev(v_bias, "v_bias", dt), _dev(out, "out", dt), lse_ptr,
+        int(B), int(H), int(M), int(L), int(dh), float(scale), code, int(n_splits),
+        ws_ptr, int(ws_bytes), _stream(q, stream))
+    _check(rc, "txl_relattn_fwd")
+    return (out, lse) if want_lse else out
+
+
+def mem_concat(mem, state: MemState, h_new, out=None, stream=None):
+    """Extended context [memory (oldest first) ; h_new] as [B, fill+L, d]."""
+    B, L, d = h_new.shape
+    if out is None:
+        out = torch.empty(B, state.fill + L, d, dtype=h_new.dtype, device=h_new.device)
+    mem_ptr = _dev(mem, "mem", h_new.dtype) if mem is not None and mem.numel() else None
+    h_ptr = _dev(h_new, "h_new") if h_new.numel() else None
+    ext_ptr = _dev(out, "ext", h_new.dtype) if out.numel() else None
+    _check(lib().txl_mem_concat(ext_ptr, mem_ptr, ctypes.byref(state), h_ptr, int(B), int(L),
+                                int(d), _code(h_new.dtype), _stream(h_new, stream)),
+           "txl_mem_concat")
+    return out
+
+
+def mem_update(mem, state: MemState, h_new, stream=None):
+    """Append h_new [B, L, d] to the ring-buffer memory mem [B, capacity, d];
+    advances ``state`` in place."""
+    B, L, d = h_new.shape
+    mem_ptr = _dev(mem, "mem", h_new.dtype) if mem is not None and mem.numel() else None
+    h_ptr = _dev(h_new, "h_new") if h_new.numel() else None
+    _check(lib().txl_mem_update(mem_ptr, ctypes.byref(state), h_ptr, int(B),
+                                int(L), int(d), _code(h_new.dtype), _stream(h_new, stream)),
+           "txl_mem_update")
+    return state
+
+
+def device_status(stream=None) -> int:
+    """Synchronise and return (and clear) the kernels' device status word."""
+    return int(lib().txl_device_status(_stream(None, stream)))
+
+
+def set_wait_limit_ns(ns: int) -> int:
+    return int(lib().txl_set_wait_limit_ns(int(ns)))
+
+
+def debug_wait_timeout(ns: int, stream=None) -> int:
+    return int(lib().txl_debug_wait_timeout(int(ns), _stream(None, stream)))

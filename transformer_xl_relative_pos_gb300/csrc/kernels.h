@@ -1,0 +1,64 @@
+// Internal launch interface between the C-ABI layer (txl_api.cu) and the
+// kernels.  Not part of the public ABI.
+#pragma once
+
+#include <cstddef>
+#include <cstdint>
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+
+namespace txl {
+
+// Tile shape of the tensor-core attention kernel.
+constexpr int kTcBM = 128;  // query rows per tile (TMEM lanes)
+constexpr int kTcBN = 128;  // keys per tile
+constexpr int kTcDH = 64;   // head size
+
+struct TcParams {
+    int B, H, M, L, K;
+    int r_off;        // r_rows - K: row offset of the K-key table inside r
+    int n_qtiles;     // ceil(L / kTcBM)
+    int n_splits;     // key-range splits per query tile
+    float scale_log2; // scale * log2(e)
+    const __nv_bfloat16 *u;  // [H][64]
+    const __nv_bfloat16 *vb; // [H][64]
+    __nv_bfloat16 *out;      // [B][H][L][64]            (n_splits == 1)
+    float *lse;              // [B][H][L] natural log or null
+    float *part_o;           // [n_splits][B*H][L][64]   (n_splits > 1)
+    float *part_lse;         // [n_splits][B*H][L], log2 domain
+    unsigned int *status;    // device status word
+    unsigned long long wait_ns;
+};
+
+// Dynamic shared memory the tensor-core kernel needs (bytes).
+size_t tc_smem_bytes();
+
+cudaError_t launch_relattn_tc(const CUtensorMap &tm_q, const CUtensorMap &tm_k,
+                              const CUtensorMap &tm_v, const CUtensorMap &tm_r,
+                              const TcParams &p, cudaStream_t s);
+
+cudaError_t launch_relattn_combine(const float *part_o, const float *part_lse,
+                                   __nv_bfloat16 *out, float *lse, int n_splits, int rows,
+                                   cudaStream_t s);
+
+struct F32Params {
+    const float *q, *k, *v, *r, *u, *vb;
+    float *out, *lse;
+    int B, H, M, L, K, r_rows;
+    float scale;
+};
+
+cudaError_t launch_relattn_f32(const F32Params &p, cudaStream_t s);
+
+cudaError_t launch_rel_pos_emb(void *R, int K, int d_model, bool bf16, cudaStream_t s);
+
+// Row copies for the segment memory; row_vec = row bytes / 16.
+cudaError_t launch_mem_concat(uint4 *ext, const uint4 *mem, const uint4 *h_new, int B,
+                              int fill, int head, int cap, int L, int row_vec, cudaStream_t s);
+cudaError_t launch_mem_write(uint4 *mem, const uint4 *h_new, int B, int L, int first_row,
+                             int head, int cap, int row_vec, cudaStream_t s);
+
+cudaError_t launch_wait_probe(unsigned int *status, unsigned long long wait_ns, cudaStream_t s);
+
+} // namespace txl

@@ -1,0 +1,77 @@
+// Sinusoid relative-position table R for Transformer-XL.
+//
+// "Transformer-XL: Attentive Language Models Beyond a Fixed-Length Context",
+// §3.3: R is a sinusoid encoding matrix without learnable parameters whose row
+// p encodes a relative distance of p; Appendix B orders the rows by decreasing
+// distance (Q_k uses R_{M+L-1-k}).  Output row rho holds distance p = K-1-rho:
+//   R[rho][2k] = sin(p w_k),  R[rho][2k+1] = cos(p w_k),  w_k = 10000^(-2k/d).
+//
+// Accuracy: the angle p*w_k reaches K radians, so it is formed in
+// double-float (w_k split into two floats per block, computed once in fp64),
+// reduced modulo 2*pi by Cody and Waite's method (W. J. Cody, W. Waite,
+// "Software Manual for the Elementary Functions", 1980) with 2*pi split into
+// three floats, and only then passed to sincosf.  The split used here was
+// derived from a 50-digit value of 2*pi: C1 and C2 keep 8 significant bits each
+// so that n*C1 and n*C2 are exact for n < 2^16 (angles below ~4e5 rad).
+#include "kernels.h"
+
+namespace txl {
+namespace {
+
+constexpr float kTwoPiC1 = 6.28125f;                   // 0x1.92p+2
+constexpr float kTwoPiC2 = 0x1.fap-10f;                // 0.00193023681640625
+constexpr float kTwoPiC3 = 0x1.54442ep-18f;            // 5.0703634e-06
+constexpr float kInvTwoPi = 0x1.45f306p-3f;            // 1/(2 pi) rounded to fp32
+constexpr int kRowsPerBlock = 16;
+
+__global__ void rel_pos_emb_kernel(void *R, int K, int d, int bf16)
+{
+    extern __shared__ float w_split[];  // [d/2] high parts, then [d/2] low parts
+    const int half = d / 2;
+    float *whi = w_split;
+    float *wlo = w_split + half;
+    const double ln1e4 = 9.210340371976184;  // ln(10000)
+    for (int k = threadIdx.x; k < half; k += blockDim.x) {
+        const double w = exp(-(2.0 * k / d) * ln1e4);
+        const float hi = (float)w;
+        whi[k] = hi;
+        wlo[k] = (float)(w - (double)hi);
+    }
+    __syncthreads();
+    const int rho0 = blockIdx.x * kRowsPerBlock;
+    const int rows = min(kRowsPerBlock, K - rho0);
+    for (int e = threadIdx.x; e < rows * half; e += blockDim.x) {
+        const int rho = rho0 + e / half;
+        const int k = e % half;
+        const float pf = (float)(K - 1 - rho);  // exact: K < 2^24
+        // angle = p * (whi + wlo) as a_hi + a_lo
+        const float a_hi = pf * whi[k];
+        const float a_lo = fmaf(pf, wlo[k], fmaf(pf, whi[k], -a_hi));
+        const float n = rintf(a_hi * kInvTwoPi);
+        float r = fmaf(-n, kTwoPiC1, a_hi);
+        r = fmaf(-n, kTwoPiC2, r);
+        r += a_lo;
+        r = fmaf(-n, kTwoPiC3, r);
+        float sn, cs;
+        sincosf(r, &sn, &cs);
+        const size_t o = (size_t)rho * d + 2 * k;
+        if (bf16) {
+            reinterpret_cast<__nv_bfloat162 *>(R)[o / 2] = __floats2bfloat162_rn(sn, cs);
+        } else {
+            reinterpret_cast<float2 *>(R)[o / 2] = make_float2(sn, cs);
+        }
+    }
+}
+
+} // namespace
+
+cudaError_t launch_rel_pos_emb(void *R, int K, int d_model, bool bf16, cudaStream_t s)
+{
+    const int blocks = (K + kRowsPerBlock - 1) / kRowsPerBlock;
+    const size_t shm = sizeof(float) * (size_t)d_model;
+    if (shm > 48 * 1024) return cudaErrorInvalidValue;
+    rel_pos_emb_kernel<<<blocks, 256, shm, s>>>(R, K, d_model, bf16 ? 1 : 0);
+    return cudaGetLastError();
+}
+
+} // namespace txl

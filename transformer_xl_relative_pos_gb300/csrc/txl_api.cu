@@ -1,0 +1,346 @@
+// C-ABI entry points declared in include/txl.h: argument validation, TMA
+// descriptor construction, launch configuration and the device status word.
+// All arithmetic happens in the kernels (relattn_tc.cu, relattn_f32.cu,
+// relpos.cu, mem.cu); this file only checks and dispatches.
+#include <algorithm>
+#include <cstdio>
+#include <cstring>
+#include <mutex>
+
+#include <cudaTypedefs.h>
+
+#include "kernels.h"
+#include "txl.h"
+
+namespace {
+
+// Kernels OR their failure bits into this word (bit 0: barrier time-out).
+__device__ unsigned int g_status_word;
+
+unsigned long long g_wait_ns = 1000000000ull;
+
+constexpr int kMaxDevices = 64;
+
+cudaStream_t as_stream(void *s) { return reinterpret_cast<cudaStream_t>(s); }
+
+bool aligned(const void *p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+int cuda_status(cudaError_t e)
+{
+    if (e == cudaSuccess) return TXL_OK;
+    return TXL_ERR_CUDA;
+}
+
+// Device address of g_status_word for the current device (looked up once).
+unsigned int *status_word(cudaError_t *err)
+{
+    static std::mutex mu;
+    static unsigned int *addr[kMaxDevices] = {};
+    int dev = 0;
+    *err = cudaGetDevice(&dev);
+    if (*err != cudaSuccess) return nullptr;
+    if (dev < 0 || dev >= kMaxDevices) {
+        *err = cudaErrorInvalidDevice;
+        return nullptr;
+    }
+    std::lock_guard<std::mutex> lock(mu);
+    if (!addr[dev]) {
+        void *p = nullptr;
+        *err = cudaGetSymbolAddress(&p, g_status_word);
+        if (*err != cudaSuccess) return nullptr;
+        addr[dev] = static_cast<unsigned int *>(p);
+    }
+    return addr[dev];
+}
+
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn()
+{
+    static std::once_flag once;
+    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+    std::call_once(once, [] {
+        void *p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000,
+                                             cudaEnableDefault, &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+    });
+    return fn;
+}
+
+// 3-D bf16 view [outer][rows][64] with a 64 x 128 box and 128-byte swizzle.
+bool make_map(CUtensorMap *map, const void *base, long long rows, long long outer)
+{
+    auto fn = encode_fn();
+    if (!fn) return false;
+    const cuuint64_t dims[3] = {64, (cuuint64_t)rows, (cuuint64_t)outer};
+    const cuuint64_t strides[2] = {64 * 2, (cuuint64_t)rows * 64 * 2};
+    const cuuint32_t box[3] = {64, 128, 1};
+    const cuuint32_t estr[3] = {1, 1, 1};
+    CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void *>(base), dims,
+                    strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                    CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                    CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS;
+}
+
+int sm_count()
+{
+    static int n[kMaxDevices] = {};
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return 148;
+    if (!n[dev]) {
+        int v = 0;
+        if (cudaDeviceGetAttribute(&v, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || v <= 0)
+            v = 148;
+        n[dev] = v;
+    }
+    return n[dev];
+}
+
+size_t workspace_bytes_for(int B, int H, int L, int dh, int n_splits)
+{
+    if (n_splits <= 1) return 0;
+    const size_t rows = (size_t)B * H * L;
+    size_t o = (size_t)n_splits * rows * dh * sizeof(float);
+    o = (o + 255) & ~(size_t)255;
+    return o + (size_t)n_splits * rows * sizeof(float);
+}
+
+// Key-range splits when the caller lets the library choose: split only when the
+// (batch, head, query tile) units leave SMs idle, and keep >= 4 key tiles per
+// split.
+int auto_splits(int units, int n_key_tiles)
+{
+    const int sms = sm_count();
+    if (units >= sms) return 1;
+    int s = (sms + units - 1) / units;
+    const int max_s = n_key_tiles / 4;
+    if (s > max_s) s = max_s;
+    return s < 1 ? 1 : s;
+}
+
+} // namespace
+
+extern "C" {
+
+const char *txl_status_string(int status)
+{
+    switch (status) {
+    case TXL_OK: return "ok";
+    case TXL_ERR_INVALID_ARG: return "invalid argument";
+    case TXL_ERR_UNSUPPORTED: return "unsupported shape or dtype";
+    case TXL_ERR_MISALIGNED: return "misaligned pointer";
+    case TXL_ERR_SHAPE: return "inconsistent sizes";
+    case TXL_ERR_CUDA: return "CUDA error";
+    case TXL_ERR_TIMEOUT: return "kernel barrier wait timed out";
+    case TXL_ERR_WORKSPACE: return "workspace missing or too small";
+    default: return "unknown status";
+    }
+}
+
+int txl_version(void) { return 100; }
+
+uint64_t txl_set_wait_limit_ns(uint64_t ns)
+{
+    const uint64_t old = g_wait_ns;
+    g_wait_ns = ns;
+    return old;
+}
+
+int txl_rel_pos_emb(void *R, int K, int d_model, int dtype, void *stream)
+{
+    if (!R || K < 1 || d_model < 2 || (d_model & 1)) return TXL_ERR_INVALID_ARG;
+    if (dtype != TXL_F32 && dtype != TXL_BF16) return TXL_ERR_INVALID_ARG;
+    if (!aligned(R, dtype == TXL_F32 ? 8 : 4)) return TXL_ERR_MISALIGNED;
+    if (K >= (1 << 24) || d_model > 12288) return TXL_ERR_UNSUPPORTED;
+    return cuda_status(txl::launch_rel_pos_emb(R, K, d_model, dtype == TXL_BF16, as_stream(stream)));
+}
+
+size_t txl_relattn_workspace_size(int B, int H, int L, int dh, int n_splits)
+{
+    if (B < 1 || H < 1 || L < 1 || dh < 1) return 0;
+    return workspace_bytes_for(B, H, L, dh, n_splits);
+}
+
+int txl_relattn_fwd(const void *q, const void *k, const void *v, const void *r, int r_rows,
+                    const void *u, const void *v_bias, void *out, float *lse, int B, int H,
+                    int M, int L, int dh, float scale, int dtype, int n_splits,
+                    void *workspace, size_t workspace_bytes, void *stream)
+{
+    if (!q || !k || !v || !r || !u || !v_bias || !out) return TXL_ERR_INVALID_ARG;
+    if (B < 1 || H < 1 || M < 0 || L < 1 || dh < 1 || n_splits < 0) return TXL_ERR_INVALID_ARG;
+    if (dtype != TXL_F32 && dtype != TXL_BF16) return TXL_ERR_INVALID_ARG;
+    if (!(scale == scale)) return TXL_ERR_INVALID_ARG;  // NaN
+    const long long K = (long long)M + L;
+    if (K > 0x7fffffffLL / 2 || r_rows < K) return TXL_ERR_SHAPE;
+    if (dh != 64) return TXL_ERR_UNSUPPORTED;
+    cudaStream_t s = as_stream(stream);
+
+    if (dtype == TXL_F32) {
+        for (const void *p : {q, k, v, r, u, v_bias, (const void *)out})
+            if (!aligned(p, 4)) return TXL_ERR_MISALIGNED;
+        if (lse && !aligned(lse, 4)) return TXL_ERR_MISALIGNED;
+        if (n_splits > 1) return TXL_ERR_UNSUPPORTED;
+        txl::F32Params p{};
+        p.q = static_cast<const float *>(q);
+        p.k = static_cast<const float *>(k);
+        p.v = static_cast<const float *>(v);
+        p.r = static_cast<const float *>(r);
+        p.u = static_cast<const float *>(u);
+        p.vb = static_cast<const float *>(v_bias);
+        p.out = static_cast<float *>(out);
+        p.lse = lse;
+        p.B = B;
+        p.H = H;
+        p.M = M;
+        p.L = L;
+        p.K = (int)K;
+        p.r_rows = r_rows;
+        p.scale = scale;
+        return cuda_status(txl::launch_relattn_f32(p, s));
+    }
+
+    // bf16 tensor-core path
+    for (const void *p : {q, k, v, r, u, v_bias, (const void *)out})
+        if (!aligned(p, 16)) return TXL_ERR_MISALIGNED;
+    if (lse && !aligned(lse, 4)) return TXL_ERR_MISALIGNED;
+    const long long BH = (long long)B * H;
+    if (BH * L > 0x7fffffffLL || BH > 0x7fffffffLL / 64) return TXL_ERR_UNSUPPORTED;
+    const int n_qtiles = (L + txl::kTcBM - 1) / txl::kTcBM;
+    const int jmax_all = (int)std::min<long long>(K - 1, (long long)M + L - 1);
+    const int n_key_tiles = jmax_all / txl::kTcBN + 1;
+    int splits = n_splits;
+    if (splits == 0) {
+        splits = auto_splits((int)std::min<long long>(BH * n_qtiles, 1 << 30), n_key_tiles);
+        if (splits > 1 && (!workspace ||
+                           workspace_bytes < workspace_bytes_for(B, H, L, dh, splits) ||
+                           !aligned(workspace, 256)))
+            splits = 1;
+    }
+    if (splits > n_key_tiles) splits = n_key_tiles;
+    if (splits > 1) {
+        if (!workspace || workspace_bytes < workspace_bytes_for(B, H, L, dh, splits))
+            return TXL_ERR_WORKSPACE;
+        if (!aligned(workspace, 256)) return TXL_ERR_MISALIGNED;
+    }
+    if (BH * n_qtiles * splits > 0x7fffffffLL) return TXL_ERR_UNSUPPORTED;
+
+    CUtensorMap tq, tk, tv, tr;
+    if (!make_map(&tq, q, L, BH) || !make_map(&tk, k, K, BH) || !make_map(&tv, v, K, BH) ||
+        !make_map(&tr, r, r_rows, H))
+        return TXL_ERR_CUDA;
+
+    cudaError_t err;
+    unsigned int *status = status_word(&err);
+    if (!status) return TXL_ERR_CUDA;
+
+    txl::TcParams p{};
+    p.B = B;
+    p.H = H;
+    p.M = M;
+    p.L = L;
+    p.K = (int)K;
+    p.r_off = r_rows - (int)K;
+    p.n_qtiles = n_qtiles;
+    p.n_splits = splits;
+    p.scale_log2 = scale * 1.4426950408889634f;
+    p.u = static_cast<const __nv_bfloat16 *>(u);
+    p.vb = static_cast<const __nv_bfloat16 *>(v_bias);
+    p.out = static_cast<__nv_bfloat16 *>(out);
+    p.lse = lse;
+    p.status = status;
+    p.wait_ns = g_wait_ns;
+    if (splits > 1) {
+        const size_t rows = (size_t)BH * L;
+        size_t off = (size_t)splits * rows * dh * sizeof(float);
+        off = (off + 255) & ~(size_t)255;
+        p.part_o = static_cast<float *>(workspace);
+        p.part_lse = reinterpret_cast<float *>(static_cast<char *>(workspace) + off);
+        p.lse = nullptr;
+    }
+    err = txl::launch_relattn_tc(tq, tk, tv, tr, p, s);
+    if (err != cudaSuccess) return TXL_ERR_CUDA;
+    if (splits > 1) {
+        err = txl::launch_relattn_combine(p.part_o, p.part_lse, p.out, lse, splits,
+                                          (int)(BH * L), s);
+        if (err != cudaSuccess) return TXL_ERR_CUDA;
+    }
+    return TXL_OK;
+}
+
+int txl_mem_concat(void *ext, const void *mem, const txl_mem_state *st, const void *h_new,
+                   int B, int L, int d, int dtype, void *stream)
+{
+    if (!st || B < 1 || L < 0 || d < 1) return TXL_ERR_INVALID_ARG;
+    if (dtype != TXL_F32 && dtype != TXL_BF16) return TXL_ERR_INVALID_ARG;
+    if (st->capacity < 0 || st->fill < 0 || st->fill > st->capacity || st->head < 0 ||
+        (st->capacity > 0 && st->head >= st->capacity) || (st->capacity == 0 && st->head != 0))
+        return TXL_ERR_SHAPE;
+    if (st->fill + L == 0) return TXL_OK;  // empty extended context
+    if (!ext || (L > 0 && !h_new) || (st->fill > 0 && !mem)) return TXL_ERR_INVALID_ARG;
+    const size_t esz = dtype == TXL_F32 ? 4 : 2;
+    if (((size_t)d * esz) % 16 != 0) return TXL_ERR_MISALIGNED;
+    if (!aligned(ext, 16) || (h_new && !aligned(h_new, 16)) || (mem && !aligned(mem, 16)))
+        return TXL_ERR_MISALIGNED;
+    const int row_vec = (int)((size_t)d * esz / 16);
+    return cuda_status(txl::launch_mem_concat(
+        static_cast<uint4 *>(ext), static_cast<const uint4 *>(mem),
+        static_cast<const uint4 *>(h_new), B, st->fill, st->head, st->capacity, L, row_vec,
+        as_stream(stream)));
+}
+
+int txl_mem_update(void *mem, txl_mem_state *st, const void *h_new, int B, int L, int d,
+                   int dtype, void *stream)
+{
+    if (!st || B < 1 || L < 0 || d < 1) return TXL_ERR_INVALID_ARG;
+    if (dtype != TXL_F32 && dtype != TXL_BF16) return TXL_ERR_INVALID_ARG;
+    if (st->capacity < 0 || st->fill < 0 || st->fill > st->capacity || st->head < 0 ||
+        (st->capacity > 0 && st->head >= st->capacity) || (st->capacity == 0 && st->head != 0))
+        return TXL_ERR_SHAPE;
+    if (st->capacity == 0 || L == 0) return TXL_OK;  // nothing to keep or nothing new
+    if (!mem || !h_new) return TXL_ERR_INVALID_ARG;
+    const size_t esz = dtype == TXL_F32 ? 4 : 2;
+    if (((size_t)d * esz) % 16 != 0) return TXL_ERR_MISALIGNED;
+    if (!aligned(mem, 16) || !aligned(h_new, 16)) return TXL_ERR_MISALIGNED;
+    const int row_vec = (int)((size_t)d * esz / 16);
+    const int cap = st->capacity;
+    const int first = L > cap ? L - cap : 0;  // older rows would be overwritten anyway
+    cudaError_t e = txl::launch_mem_write(static_cast<uint4 *>(mem),
+                                          static_cast<const uint4 *>(h_new), B, L, first,
+                                          st->head, cap, row_vec, as_stream(stream));
+    if (e != cudaSuccess) return TXL_ERR_CUDA;
+    st->head = (int)(((long long)st->head + L) % cap);
+    st->fill = (int)std::min<long long>((long long)st->fill + L, cap);
+    return TXL_OK;
+}
+
+int txl_device_status(void *stream)
+{
+    cudaError_t err;
+    unsigned int *w = status_word(&err);
+    if (!w) return TXL_ERR_CUDA;
+    if (cudaStreamSynchronize(as_stream(stream)) != cudaSuccess) return TXL_ERR_CUDA;
+    unsigned int v = 0;
+    if (cudaMemcpy(&v, w, sizeof(v), cudaMemcpyDeviceToHost) != cudaSuccess) return TXL_ERR_CUDA;
+    if (v != 0) {
+        const unsigned int zero = 0;
+        if (cudaMemcpy(w, &zero, sizeof(zero), cudaMemcpyHostToDevice) != cudaSuccess)
+            return TXL_ERR_CUDA;
+        return TXL_ERR_TIMEOUT;
+    }
+    return TXL_OK;
+}
+
+int txl_debug_wait_timeout(uint64_t ns, void *stream)
+{
+    cudaError_t err;
+    unsigned int *w = status_word(&err);
+    if (!w) return TXL_ERR_CUDA;
+    if (ns == 0 || ns > 10000000000ull) return TXL_ERR_INVALID_ARG;  // at most 10 s
+    err = txl::launch_wait_probe(w, ns, as_stream(stream));
+    if (err != cudaSuccess) return TXL_ERR_CUDA;
+    return txl_device_status(stream);
+}
+
+} // extern "C"

@@ -1,0 +1,126 @@
+"""Layer glue around the kernels: projections and the streaming N-layer stack.
+
+"Transformer-XL: Attentive Language Models Beyond a Fixed-Length Context",
+§3.3 N-layer summary, for n = 1..N:
+    h~  = [SG(m^{n-1}) o h^{n-1}]                      -> mem_concat (kernel)
+    q, k, v = h W_q^T, h~ W_kE^T, h~ W_v^T             -> torch matmul
+    a   = Masked-Softmax(A) v                           -> relattn_fwd (kernel)
+    o   = LayerNorm(Linear(a) + h^{n-1})                -> torch
+    h^n = Positionwise-Feed-Forward(o)                  -> torch (ReLU MLP,
+                                                           residual, LayerNorm)
+and the memory of each layer advances to the newest M states of its input
+(§3.2)                                                  -> mem_update (kernel).
+The relative table r = W_kR R is built from rel_pos_emb (kernel) and one matmul
+and is cached per (layer, K): R has no parameters and W_kR is fixed at
+evaluation.
+
+Torch is used here for the dense projections, LayerNorm and the feed-forward
+only; the attention, the positional table and the memory run in the CUDA
+library.
+"""
+
+from __future__ import annotations
+
+import math
+
+import torch
+
+from . import _lib as txl
+
+LN_EPS = 1e-5
+
+
+def project_heads(x: torch.Tensor, W: torch.Tensor, H: int) -> torch.Tensor:
+    """x [B, T, d] times W^T ([H*dh, d]) -> contiguous [B, H, T, dh]."""
+    B, T, _ = x.shape
+    y = x @ W.t()
+    return y.view(B, T, H, -1).transpose(1, 2).contiguous()
+
+
+def rel_table_heads(R_rev: torch.Tensor, W_kR: torch.Tensor, H: int) -> torch.Tensor:
+    """r = R W_kR^T split per head: [K, d] x [H*dh, d]^T -> [H, K, dh]."""
+    K = R_rev.shape[0]
+    return (R_rev @ W_kR.t()).view(K, H, -1).transpose(0, 1).contiguous()
+
+
+def attention_operands(h_ext, M: int, W_q, W_kE, W_v, W_kR, R_rev, H: int, dtype):
+    """q, k, v, r for one layer from the extended context h_ext [B, M+L, d]
+    (memory rows first) and the reversed table R_rev [M+L, d].  Products are
+    formed in fp32 and rounded once to ``dtype``."""
+    f = lambda t: t.float()
+    h = f(h_ext)
+    q = project_heads(h[:, M:], f(W_q), H).to(dtype)
+    k = project_heads(h, f(W_kE), H).to(dtype)
+    v = project_heads(h, f(W_v), H).to(dtype)
+    r = rel_table_heads(f(R_rev), f(W_kR), H).to(dtype)
+    return q, k, v, r
+
+
+def layer_norm(x: torch.Tensor) -> torch.Tensor:
+    return torch.nn.functional.layer_norm(x.float(), (x.shape[-1],), eps=LN_EPS)
+
+
+class XLStack:
+    """Evaluation-mode Transformer-XL stack with per-layer ring-buffer memories.
+
+    params: draws from ``txl_inputs.draw_stack`` (CPU fp32); weights are moved
+    to ``device`` in ``dtype``.  ``segment(tokens)`` processes one segment
+    [B, L] and returns the top layer's states [B, L, d] (``dtype``)."""
+
+    def __init__(self, params: dict, H: int, M: int, device, dtype=torch.bfloat16):
+        self.H, self.M, self.dtype, self.device = H, M, dtype, torch.device(device)
+        to = lambda t: t.to(device=self.device, dtype=dtype).contiguous()
+        self.emb = to(params["emb"])
+        self.u = to(params["u"])
+        self.v_bias = to(params["v_bias"])
+        self.layers = [{k: to(v) for k, v in lay.items()} for lay in params["layers"]]
+        self.d = self.emb.shape[1]
+        self.dh = self.u.shape[1]
+        self.scale = 1.0 / math.sqrt(self.dh)
+        self.mems = None
+        self.states = None
+        self._r_cache = {}
+
+    def reset(self, B: int):
+        self.mems = [torch.zeros(B, self.M, self.d, dtype=self.dtype, device=self.device)
+                     for _ in self.layers]
+        self.states = [txl.MemState(0, 0, self.M) for _ in self.layers]
+
+    def memories(self):
+        """Each layer's memory in logical order (oldest first), [B, fill, d]."""
+        out = []
+        for mem, st in zip(self.mems, self.states):
+            B = mem.shape[0]
+            empty = torch.empty(B, 0, self.d, dtype=self.dtype, device=self.device)
+            out.append(txl.mem_concat(mem, st, empty))
+        return out
+
+    def _r(self, n: int, K: int) -> torch.Tensor:
+        key = (n, K)
+        if key not in self._r_cache:
+            R = txl.rel_pos_emb(K, self.d, dtype=torch.float32, device=self.device)
+            self._r_cache[key] = rel_table_heads(R, self.layers[n]["W_kR"].float(),
+                                                 self.H).to(self.dtype)
+        return self._r_cache[key]
+
+    def segment(self, tokens: torch.Tensor) -> torch.Tensor:
+        B, L = tokens.shape
+        if self.mems is None or self.mems[0].shape[0] != B:
+            self.reset(B)
+        h = self.emb[tokens.to(self.device)]
+        for n, lay in enumerate(self.layers):
+            st = self.states[n]
+            M_cur = st.fill
+            ext = txl.mem_concat(self.mems[n], st, h)
+            q = project_heads(h, lay["W_q"], self.H)
+            k = project_heads(ext, lay["W_kE"], self.H)
+            v = project_heads(ext, lay["W_v"], self.H)
+            a = txl.relattn_fwd(q, k, v, self._r(n, M_cur + L), self.u, self.v_bias, M_cur,
+                                self.scale)
+            a = a.transpose(1, 2).reshape(B, L, -1)
+            o = layer_norm((a @ lay["W_o"].t()).float() + lay["b_o"].float() + h.float())
+            f = torch.relu(o.to(self.dtype) @ lay["W_1"].t() + lay["b_1"])
+            h_next = layer_norm(o + (f @ lay["W_2"].t()).float() + lay["b_2"].float())
+            txl.mem_update(self.mems[n], st, h)
+            h = h_next.to(self.dtype)
+        return h
