@@ -1,0 +1,469 @@
+#!/usr/bin/env python3
+"""Benchmark of the Transformer-XL relative-attention hot path on GB300.
+
+A step is one layer-segment of evaluation with state reuse ("Transformer-XL:
+Attentive Language Models Beyond a Fixed-Length Context", §3.2 and §3.3), at
+the word-level large evaluation shape: batch 16, 16 heads of 64, segment
+L = 128, memory M = 1600 (K = 1728 keys), d_model = 1024, bf16 operands:
+    txl_rel_pos_emb   sinusoid table R [K, d_model]
+    txl_relattn_fwd   fused relative-position attention (tcgen05/TMEM/TMA)
+    txl_mem_update    memory ring advanced by the segment's L states
+The q/k/v/r projections (torch matmuls) are set-up work outside the step, as
+the attention operands of an evaluation segment; r is the projection of the
+same table the step recomputes.
+
+Metric: relative-attention forward TFLOP/s (6*L*K*d_head FLOPs per head and
+call, masked entries included) plus tokens/s and the fraction of the measured
+bf16 tensor-core peak.
+
+Timing: W eager warm-up steps, then K steps replayed from a CUDA graph (the
+graph holds the same launches; it removes host launch overhead), bracketed by
+a barrier and device synchronisation, timed with CUDA events on the launching
+stream, max over ranks.  Three input sets rotate so that every step's inputs
+were last touched more than two L2-sizes of traffic ago.
+
+``--impl reference`` times the fp64 CPU oracle instead (the reference arm).
+"""
+
+from __future__ import annotations
+
+import argparse
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+import txl_inputs  # noqa: E402
+
+METRIC = "rel-attn fwd TFLOP/s + tokens/s at L=128,M=1600; % of GB300 bf16 TC peak"
+N_SETS = 3
+RING_PERIOD = 25        # M / gcd(M, L) segments bring the ring head back to 0
+GRAPH_CHUNK = 1500      # steps per graph when K is large (multiple of 3 * 25)
+
+
+def parse_args():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=30000)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--e2e-steps", type=int, default=30)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    return ap.parse_args()
+
+
+def peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            d = json.load(f)
+        return {"hbm_gbs": d["hbm_gbs"], "bf16_tflops": d["bf16_tflops"],
+                "bf16_tflops_sustained": d.get("bf16_tflops_sustained"), "source": "measured"}
+    return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0,
+            "source": "fallback"}
+
+
+# ---------------------------------------------------------------------------
+# distributed plumbing (one process per GPU; the path shards with no exchange)
+# ---------------------------------------------------------------------------
+
+def dist_setup(args):
+    import torch
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        import torch.distributed as dist
+        backend = "nccl" if torch.cuda.is_available() and args.impl == "ours" else "gloo"
+        if backend == "nccl":
+            torch.cuda.set_device(local)
+        dist.init_process_group(backend=backend)
+    elif torch.cuda.is_available():
+        torch.cuda.set_device(local)
+    return world, rank, local
+
+
+def barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def max_over_ranks(x: float, world: int) -> float:
+    if world == 1:
+        return x
+    import torch
+    import torch.distributed as dist
+    dev = torch.device("cuda", torch.cuda.current_device()) if dist.get_backend() == "nccl" else "cpu"
+    t = torch.tensor([x], dtype=torch.float64, device=dev)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+# ---------------------------------------------------------------------------
+# clocks during the timed region
+# ---------------------------------------------------------------------------
+
+class ClockSampler:
+    FIELDS = ("timestamp,index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.index = index
+        self.f = tempfile.NamedTemporaryFile("w+", suffix=".csv", delete=False)
+        try:
+            self.p = subprocess.Popen(["nvidia-smi", f"--id={index}", f"--query-gpu={self.FIELDS}",
+                                       "--format=csv,noheader,nounits", "-lms", "100"],
+                                      stdout=self.f, stderr=subprocess.DEVNULL)
+        except OSError:
+            self.p = None
+
+    def stop(self):
+        if self.p is not None:
+            self.p.terminate()
+            try:
+                self.p.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.p.kill()
+        self.f.flush()
+        self.f.seek(0)
+        rows = [ln.strip().split(", ") for ln in self.f.read().splitlines() if ln.strip()]
+        self.f.close()
+        os.unlink(self.f.name)
+        return rows
+
+    @staticmethod
+    def summarise(rows, t0: float, t1: float):
+        def ts(r):
+            try:
+                return time.mktime(time.strptime(r[0].split(".")[0], "%Y/%m/%d %H:%M:%S")) + \
+                    float("0." + r[0].split(".")[1]) if "." in r[0] else 0.0
+            except (ValueError, IndexError):
+                return 0.0
+        inside = [r for r in rows if len(r) >= 10 and t0 - 0.15 <= ts(r) <= t1 + 0.15]
+        note = "samples inside the timed region"
+        if not inside:
+            inside = [r for r in rows if len(r) >= 10]
+            note = "timed region shorter than the sampling period: samples from warm-up and timed steps"
+        if not inside:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0,
+                    "note": "nvidia-smi unavailable"}
+        sm = [float(r[2]) for r in inside if r[2].replace(".", "").isdigit()]
+        mx = [float(r[3]) for r in inside if r[3].replace(".", "").isdigit()]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[k] for r in inside for k in range(4) if r[6 + k].strip() == "Active"})
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(mx) if mx else None, "reasons": reasons,
+                "samples": len(inside), "note": note}
+
+
+# ---------------------------------------------------------------------------
+# the CPU oracle as a baseline (bounded sample)
+# ---------------------------------------------------------------------------
+
+def oracle_inputs(w):
+    """Seeded operands of the workload's shape for timing the oracle; the scale
+    is that of a projection of N(0,1) states by N(0,0.02) weights."""
+    s = 0.02 * math.sqrt(w.d_model)
+    d = txl_inputs.draw_heads(w.B, w.H, w.L, w.M, w.dh, w.seed, std=s, bias_std=0.02)
+    f = lambda t: t.double().numpy()
+    return f(d["q"]), f(d["k"]), f(d["v"]), f(d["r"]), f(d["u"]), f(d["v_bias"])
+
+
+def time_oracle(w, pairs_per_rep: int, min_seconds: float, max_reps: int):
+    import oracle
+    q, k, v, rel, u, vb = oracle_inputs(w)
+    bh = list(range(min(pairs_per_rep, w.B * w.H)))
+    reps, t = 0, 0.0
+    while reps < max_reps and (reps == 0 or t < min_seconds):
+        t0 = time.perf_counter()
+        oracle.relattn(q, k, v, rel, u, vb, w.M, w.L, 1.0 / math.sqrt(w.dh), bh=bh)
+        t += time.perf_counter() - t0
+        reps += 1
+    flops = 6.0 * w.L * w.K * w.dh * len(bh) * reps
+    return {"value": flops / t / 1e12, "unit": "TFLOP/s", "cores": oracle.max_threads(),
+            "kind": "oracle", "seconds": round(t, 3),
+            "sample": f"{w.name}: {len(bh)} of {w.B * w.H} (batch, head) slices per call, "
+                      f"{reps} call(s), fp64 C oracle with OpenMP"}
+
+
+def run_reference(args, world, rank):
+    w = txl_inputs.WORKLOADS[txl_inputs.HEADLINE]
+    if rank != 0:
+        return
+    import oracle
+    cores = oracle.max_threads()
+    pairs = max(1, min(w.B * w.H, cores))
+    q, k, v, rel, u, vb = oracle_inputs(w)
+    bh = list(range(pairs))
+    run = lambda: oracle.relattn(q, k, v, rel, u, vb, w.M, w.L, 1.0 / math.sqrt(w.dh), bh=bh)
+    t0 = time.perf_counter()
+    run()
+    t_step = time.perf_counter() - t0
+    steps = max(1, min(args.steps, int(120.0 / max(t_step, 1e-3))))
+    for _ in range(max(0, min(args.warmup, 3) - 1)):
+        run()
+    t0 = time.perf_counter()
+    for _ in range(steps):
+        run()
+    t = time.perf_counter() - t0
+    flops = 6.0 * w.L * w.K * w.dh * pairs * steps
+    val = flops / t / 1e12
+    line = {
+        "impl": "reference", "metric": METRIC, "value": val, "unit": "TFLOP/s", "n_gpus": args.gpus,
+        "steps": steps, "warmup": args.warmup, "ms_per_step": 1e3 * t / steps,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic",
+        "config": {"workload": w.name, "B": w.B, "H": w.H, "L": w.L, "M": w.M, "K": w.K,
+                   "dh": w.dh, "d_model": w.d_model,
+                   "sample": f"{pairs} of {w.B * w.H} (batch, head) slices per step"},
+        "tokens_per_s": pairs * w.L * steps / t / (w.H),
+        "cpu_baseline": {"value": val, "unit": "TFLOP/s", "cores": cores, "kind": "oracle",
+                         "sample": f"{pairs} (batch, head) slices of {w.name} per step, "
+                                   f"{steps} steps (capped at ~120 s)"},
+        "e2e": {"value": val, "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+# ---------------------------------------------------------------------------
+# our arm
+# ---------------------------------------------------------------------------
+
+def build_operands(w, dev):
+    import torch
+    import transformer_xl_relative_pos_gb300 as txl
+    from transformer_xl_relative_pos_gb300 import model
+    raw = txl_inputs.draw_layer(w)
+    h_ext = raw["h_ext"].to(dev)
+    R = txl.rel_pos_emb(w.K, w.d_model, dtype=torch.float32, device=dev)
+    q, k, v, r = model.attention_operands(h_ext, w.M, raw["W_q"].to(dev), raw["W_kE"].to(dev),
+                                          raw["W_v"].to(dev), raw["W_kR"].to(dev), R, w.H,
+                                          torch.bfloat16)
+    h_seg = h_ext[:, w.M:].to(torch.bfloat16).contiguous()   # the segment's states [B, L, d]
+    mem = h_ext[:, :w.M].to(torch.bfloat16).contiguous()     # a full memory [B, M, d]
+    u = raw["u"].to(dev, torch.bfloat16)
+    vb = raw["v_bias"].to(dev, torch.bfloat16)
+    torch.cuda.synchronize()
+    return {"q": q, "k": k, "v": v, "r": r, "u": u, "v_bias": vb, "h": h_seg, "mem": mem}
+
+
+def run_ours(args, world, rank, local):
+    import torch
+    import transformer_xl_relative_pos_gb300 as txl
+
+    w = txl_inputs.WORKLOADS[txl_inputs.HEADLINE]
+    dev = torch.device("cuda", local)
+    pk = peaks()
+    base = build_operands(w, dev)
+    scale = 1.0 / math.sqrt(w.dh)
+    ws = torch.empty(max(txl.workspace_size(w.B, w.H, w.L, w.dh, 8), 256), dtype=torch.uint8,
+                     device=dev)
+    sets = []
+    for s in range(N_SETS):
+        sets.append({
+            "q": base["q"].clone(), "k": base["k"].clone(), "v": base["v"].clone(),
+            "h": base["h"].clone(), "mem": base["mem"].clone(),
+            "out": torch.empty_like(base["q"]),
+            "R": torch.empty(w.K, w.d_model, dtype=torch.float32, device=dev),
+            "st": txl.MemState(0, w.M, w.M),
+        })
+    r, u, vb = base["r"], base["u"], base["v_bias"]
+    del base
+    torch.cuda.synchronize()
+
+    def step(i, times=None):
+        s = sets[i % N_SETS]
+        txl.rel_pos_emb(w.K, w.d_model, out=s["R"])
+        if times is not None:
+            times[0].record()
+        txl.relattn_fwd(s["q"], s["k"], s["v"], r, u, vb, w.M, scale, out=s["out"], workspace=ws)
+        if times is not None:
+            times[1].record()
+        txl.mem_update(s["mem"], s["st"], s["h"])
+
+    # Kernel launches per step (the attention may add a split merge).
+    units = w.B * w.H * ((w.L + 127) // 128)
+    sms = torch.cuda.get_device_properties(dev).multi_processor_count
+    launches_per_step = 3 + (1 if units < sms else 0)
+
+    for i in range(max(args.warmup, 3)):
+        step(i)
+    torch.cuda.synchronize()
+    assert txl.device_status() == 0
+
+    K = max(1, args.steps)
+    if K <= 2 * GRAPH_CHUNK:
+        chunk, reps = K, 1
+    else:
+        chunk = GRAPH_CHUNK
+        reps = max(1, round(K / GRAPH_CHUNK))
+        K = chunk * reps
+    # Events around the attention launches inside the graph time the kernel
+    # over the timed region itself.  Events recorded during capture must be
+    # "external" ones; without that option the kernel is timed in a separate
+    # graph of attention launches only.
+    n_ev = min(chunk, 64)
+    try:
+        evs = [(torch.cuda.Event(enable_timing=True, external=True),
+                torch.cuda.Event(enable_timing=True, external=True)) for _ in range(n_ev)]
+    except TypeError:
+        evs = None
+
+    def capture(with_events):
+        g = torch.cuda.CUDAGraph()
+        cap_stream = torch.cuda.Stream(dev)
+        cap_stream.wait_stream(torch.cuda.current_stream(dev))
+        with torch.cuda.stream(cap_stream):
+            with torch.cuda.graph(g, stream=cap_stream):
+                for i in range(chunk):
+                    step(i, evs[i] if (with_events and i < n_ev) else None)
+        torch.cuda.current_stream(dev).wait_stream(cap_stream)
+        return g
+
+    attn_timing = "events around each attention launch inside the timed graph"
+    try:
+        g = capture(evs is not None)
+    except RuntimeError:
+        evs = None
+        g = capture(False)
+    g.replay()  # untimed replay: graph upload and warm caches
+    torch.cuda.synchronize()
+
+    stream = torch.cuda.current_stream(dev)
+    sampler = ClockSampler(local) if rank == 0 else None
+    time.sleep(0.3 if sampler else 0.0)
+    barrier(world)
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    wall0 = time.time()
+    e0.record(stream)
+    for _ in range(reps):
+        g.replay()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    wall1 = time.time()
+    barrier(world)
+    clocks = ClockSampler.summarise(sampler.stop(), wall0, wall1) if sampler else None
+    t_ms = max_over_ranks(e0.elapsed_time(e1), world)
+    status = txl.device_status()
+    if evs is not None:
+        attn_ms = statistics.mean(a.elapsed_time(b) for a, b in evs)
+    else:
+        attn_timing = "separate graph of attention launches on the rotating sets"
+        ga = torch.cuda.CUDAGraph()
+        cs = torch.cuda.Stream(dev)
+        cs.wait_stream(torch.cuda.current_stream(dev))
+        with torch.cuda.stream(cs):
+            with torch.cuda.graph(ga, stream=cs):
+                for i in range(300):
+                    s_ = sets[i % N_SETS]
+                    txl.relattn_fwd(s_["q"], s_["k"], s_["v"], r, u, vb, w.M, scale,
+                                    out=s_["out"], workspace=ws)
+        torch.cuda.current_stream(dev).wait_stream(cs)
+        ga.replay()
+        torch.cuda.synchronize()
+        a_, b_ = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a_.record()
+        ga.replay()
+        b_.record()
+        torch.cuda.synchronize()
+        attn_ms = a_.elapsed_time(b_) / 300
+
+    flops_step = w.flops()
+    value = flops_step * K * world / (t_ms * 1e-3) / 1e12
+    tokens = w.B * w.L * K * world / (t_ms * 1e-3)
+
+    # ---- end to end through the public API with host buffers ----------------
+    e2e = None
+    if rank == 0 and args.e2e_steps > 0:
+        hs = sets[0]
+        host = {k: hs[k].cpu().pin_memory() for k in ("q", "k", "v", "h")}
+        out_h = torch.empty(hs["out"].shape, dtype=hs["out"].dtype).pin_memory()
+        h2d = sum(t.numel() * t.element_size() for t in host.values())
+        d2h = out_h.numel() * out_h.element_size()
+        dev_in = {k: torch.empty_like(hs[k]) for k in host}
+        st = txl.MemState(0, w.M, w.M)
+        def e2e_step():
+            for k2, t in host.items():
+                dev_in[k2].copy_(t, non_blocking=True)
+            txl.rel_pos_emb(w.K, w.d_model, out=hs["R"])
+            txl.relattn_fwd(dev_in["q"], dev_in["k"], dev_in["v"], r, u, vb, w.M, scale,
+                            out=hs["out"], workspace=ws)
+            txl.mem_update(hs["mem"], st, dev_in["h"])
+            out_h.copy_(hs["out"], non_blocking=True)
+        for _ in range(3):
+            e2e_step()
+        torch.cuda.synchronize()
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record()
+        for _ in range(args.e2e_steps):
+            e2e_step()
+        b.record()
+        torch.cuda.synchronize()
+        t_e2e = a.elapsed_time(b) * 1e-3
+        e2e = {"value": flops_step * args.e2e_steps / t_e2e / 1e12, "unit": "TFLOP/s",
+               "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+               "steps": args.e2e_steps, "ms_per_step": 1e3 * t_e2e / args.e2e_steps}
+
+    if rank != 0:
+        return
+    # ---- roofline of the attention kernel -----------------------------------
+    bytes_alg = 2 * (w.B * w.H * w.L * w.dh * 2 + 2 * w.B * w.H * w.K * w.dh) + w.H * w.K * w.dh * 2
+    attn_s = attn_ms * 1e-3
+    achieved_gbs = bytes_alg / attn_s / 1e9
+    roofline = {"bound": "hbm", "achieved": achieved_gbs, "peak": pk["hbm_gbs"], "unit": "GB/s",
+                "frac": achieved_gbs / pk["hbm_gbs"], "traffic": None,
+                "kernel": "relattn_fwd_tc_kernel", "launch_us": attn_ms * 1e3,
+                "timing": attn_timing,
+                "tensor_tflops": flops_step / attn_s / 1e12,
+                "tensor_frac": flops_step / attn_s / 1e12 / pk["bf16_tflops"],
+                "peak_source": pk["source"] + " (MEASURED_PEAKS.json burst figures)"}
+    cpu = None
+    if not args.no_cpu_baseline:
+        cpu = time_oracle(w, pairs_per_rep=w.B * w.H, min_seconds=10.0, max_reps=6)
+    line = {
+        "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world, "steps": K,
+        "warmup": max(args.warmup, 3), "ms_per_step": t_ms / K, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "config": {"workload": w.name, "B": w.B, "H": w.H, "L": w.L, "M": w.M, "K": w.K,
+                   "dh": w.dh, "d_model": w.d_model,
+                   "step": "rel_pos_emb + relattn_fwd + mem_update",
+                   "l2": f"{N_SETS} rotating input sets (>2x L2 of traffic between reuses)",
+                   "launch": f"CUDA graph of {chunk} steps x {reps} replays"},
+        "tokens_per_s": tokens,
+        "pct_bf16_peak": 100.0 * value / pk["bf16_tflops"],
+        "attn_us": attn_ms * 1e3,
+        "clocks": clocks,
+        "e2e": e2e,
+        "gpu_launches": launches_per_step * K,
+        "device_status": status,
+        "roofline": roofline,
+        "cpu_baseline": cpu,
+    }
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    args = parse_args()
+    world, rank, local = dist_setup(args)
+    if args.impl == "reference":
+        run_reference(args, world, rank)
+    else:
+        run_ours(args, world, rank, local)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

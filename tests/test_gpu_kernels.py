@@ -35,7 +35,7 @@ def test_barrier_wait_times_out_and_reports():
 # ---------------------------------------------------------------------------
 
 @pytest.mark.parametrize("K,d", [(1, 2), (32, 64), (1024, 512), (1728, 1024), (3928, 1024),
-                                 (70000, 8)])
+                                 (70000, 8), (300, 8192)])
 def test_rel_pos_emb_matches_oracle(K, d):
     R = txl.rel_pos_emb(K, d, dtype=torch.float32, device=dev())
     want = oracle.reversed_table(oracle.sinusoid_table(K, d))

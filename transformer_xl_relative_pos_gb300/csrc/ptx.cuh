@@ -118,6 +118,15 @@ __device__ __forceinline__ void tma_load_3d_hint(void *smem_dst, const CUtensorM
         : "memory");
 }
 
+// Pull a 3-D tile into L2 ahead of its shared-memory load (no completion signal).
+__device__ __forceinline__ void tma_prefetch_3d(const CUtensorMap *map, int c0, int c1, int c2)
+{
+    asm volatile("cp.async.bulk.prefetch.tensor.3d.L2.global [%0, {%1, %2, %3}];" ::"l"(
+                     reinterpret_cast<uint64_t>(map)),
+                 "r"(c0), "r"(c1), "r"(c2)
+                 : "memory");
+}
+
 __device__ __forceinline__ uint64_t policy_evict_first()
 {
     uint64_t p;

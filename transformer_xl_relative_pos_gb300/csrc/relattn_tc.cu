@@ -2,31 +2,36 @@
 // relative-position attention, bf16 operands, fp32 accumulation.
 //
 // "Transformer-XL: Attentive Language Models Beyond a Fixed-Length Context":
-//   §3.3 score  A_ij = (q_i + u).k_j + (q_i + v).W_kR R_{i-j}   (terms (a)+(c), (b)+(d))
+//   §3.3 score  A_ij = (q_i + u).k_j + (q_i + v).W_kR R_{i-j}
 //   §3.3 summary: masked softmax over the extended context, times v
-//   Appendix B: with the reversed table Q (row rho = W_kR R_{K-1-rho}), row i of
-//   the position term is row i of q Q^T shifted left by L-1-i.
+//   Appendix B: with the reversed table Q (row rho = W_kR R_{K-1-rho}) the
+//   position term of row i is row i of q Q^T shifted left by L-1-i.
 //
 // One thread block handles 128 query rows of one (batch, head) and a range of
-// 128-key tiles.  Per key tile, in TMEM (fp32, lane = query row):
-//   S  [128 x 128]  = (q + u) K^T                            content term
-//   W  [128 x 256]  = (q + v) Qwin^T                         position window
-// where Qwin is the 255 (+1) consecutive rows of the reversed table that any
-// (row, key) pair of the tile can index.  Row il of the tile needs window
-// column jj + 127 - il for key jj: the Appendix B shift, applied by index
-// arithmetic when the softmax warps read W (through a small per-thread
-// shared-memory skew buffer), so no L x K matrix exists anywhere.
+// 128-key tiles.  Everything accumulates in TMEM (fp32, lane = query row):
+//   S      [128 x 128]  = q K_t^T   + 1 (u.k_j)            content term, tile t
+//   Bt[c]  [128 x 128]  = q Qc^T    + 1 (v.r_rho)          position term, chunk c
+// where chunk c is rows [c*128 + L-128-i0, +128) of the reversed table.  Key
+// tile t needs chunks t and t+1 (a 256-column window: row il of the tile reads
+// window column jj + 127 - il for key jj, the Appendix B shift), so each chunk
+// is multiplied once and kept in one of two TMEM slots while two consecutive
+// key tiles read it.  The shift is applied when the softmax warps read the
+// window, through a per-thread shared-memory skew buffer; no L x K matrix
+// exists anywhere.
+//
+// The bias terms u.k_j and v.r_rho are exact in fp32: q enters the MMA as
+// given, and the biases come from small MMAs [K tile | table chunk] x [u ; v]^T
+// whose fp32 results the softmax warps split into bf16 hi + lo pairs; a fifth
+// MMA K-step multiplies a column of ones by those pairs.
 //
 // Warp roles (256 threads):
-//   warp 0      TMA producer: q tile once, then K, V and 128-row chunks of the
-//               reversed table through shared-memory rings (mbarrier handshakes)
-//   warp 1      MMA issuer (one thread): S and W for tile t+1 as soon as the
-//               softmax has read tile t's S and W, then O += P V for tile t
+//   warp 0      TMA producer: q tile once, then K, V and table chunks through
+//               shared-memory rings, with L2 prefetches further ahead
+//   warp 1      MMA issuer (one thread)
 //   warp 2      TMEM allocator
-//   warps 4..7  softmax: thread = query row; forms q+u and q+v once, then per
-//               tile gathers S + shifted W, masks (key after query), keeps a
-//               running max with lazy rescaling, exponentiates (ex2), writes P
-//               (bf16, 128-byte swizzled) to shared memory; finally O / l.
+//   warps 4..7  softmax: thread = query row.  Per tile: gather S + shifted
+//               window, mask, running max (lazy rescale), exp2, P (bf16) to
+//               shared memory; convert the next tile's biases; finally O / l.
 //
 // Every barrier wait is bounded: on time-out the block records an error in the
 // device status word, raises a block-wide abort flag, drains its own in-flight
@@ -41,33 +46,47 @@ using namespace ptx;
 
 constexpr int BM = kTcBM, BN = kTcBN, DH = kTcDH;
 constexpr int NS = 2;                  // K / V ring stages
-constexpr int NR = NS + 1;             // reversed-table chunk slots
+constexpr int NR = 3;                  // table-chunk ring slots
+constexpr int PF = 3;                  // L2 prefetch distance (tiles)
 constexpr int TILE = BM * DH * 2;      // 16384 bytes: 128 rows x 128 bytes
+constexpr int EXT = 4096;              // bias-column tile: 128 rows x 16 bytes, then
+                                       // 2 KB of zeros for K columns 8..15
 constexpr int SKEW_STRIDE = 68;        // floats per skew row (bank-conflict free)
-constexpr uint32_t TM_S = 0, TM_W = 128, TM_O = 384, TM_COLS = 512;
+
+// TMEM columns
+constexpr uint32_t TM_S = 0;           // content scores
+constexpr uint32_t TM_B = 128;         // two 128-column table-chunk slots
+constexpr uint32_t TM_O = 384;         // output accumulator (64 columns)
+constexpr uint32_t TM_BK = 448;        // k.u / k.v for the next key tile (16 columns)
+constexpr uint32_t TM_BR = 464;        // r.u / r.v for the next table chunk
+constexpr uint32_t TM_BR2 = 480;       // second table chunk of the first tile
+constexpr uint32_t TM_COLS = 512;
 
 // Shared-memory layout (offsets from a 1024-byte aligned base).
-constexpr int OFF_Q = 0;                        // q + u (written over the raw q tile)
-constexpr int OFF_QV = OFF_Q + TILE;            // q + v
-constexpr int OFF_K = OFF_QV + TILE;            // NS stages
-constexpr int OFF_V = OFF_K + NS * TILE;        // NS stages
-constexpr int OFF_R = OFF_V + NS * TILE;        // NR chunks
-constexpr int OFF_P = OFF_R + NR * TILE;        // keys 0-63, keys 64-127
-constexpr int OFF_SKEW = OFF_P + 2 * TILE;      // 128 rows x SKEW_STRIDE floats
+constexpr int OFF_Q = 0;
+constexpr int OFF_K = OFF_Q + TILE;               // NS stages
+constexpr int OFF_V = OFF_K + NS * TILE;          // NS stages
+constexpr int OFF_R = OFF_V + NS * TILE;          // NR slots
+constexpr int OFF_P = OFF_R + NR * TILE;          // keys 0-63, keys 64-127
+constexpr int OFF_UB = OFF_P + 2 * TILE;          // [u ; v ; 0 x 14] 16 x 128 bytes, swizzled
+constexpr int OFF_AEXT = OFF_UB + 2048;           // ones column: rows [1, 1, 0 x 6]
+constexpr int OFF_KEXT = OFF_AEXT + EXT;          // NS tiles of (hi, lo) of k.u
+constexpr int OFF_REXT = OFF_KEXT + NS * EXT;     // NR tiles of (hi, lo) of v.r
+constexpr int OFF_SKEW = OFF_REXT + NR * EXT;     // 128 rows x SKEW_STRIDE floats
 constexpr int OFF_BAR = OFF_SKEW + BM * SKEW_STRIDE * 4;
-constexpr int N_BAR = 2 + 4 * NS + 2 * NR + 5;
+constexpr int N_BAR = 1 + 4 * NS + 2 * NR + 8;
 constexpr int OFF_MISC = OFF_BAR + N_BAR * 8;
 constexpr int SMEM_USED = OFF_MISC + 16;
-constexpr int SMEM_BYTES = SMEM_USED + 1024;    // slack for the manual alignment
+constexpr int SMEM_BYTES = SMEM_USED + 1024;      // slack for the manual alignment
 
 static_assert(SMEM_BYTES <= 232448, "shared memory budget exceeded");
-static_assert(OFF_BAR % 8 == 0, "barrier alignment");
+static_assert(OFF_UB % 1024 == 0, "swizzled tiles need 1024-byte alignment");
 
 struct Bars {
-    uint64_t *q_full, *q_ready;
+    uint64_t *q_full;
     uint64_t *k_full, *k_empty, *v_full, *v_empty;
     uint64_t *r_full, *r_empty;
-    uint64_t *s_full, *s_free, *p_full, *o_done, *drain;
+    uint64_t *prep, *bias_full, *ext_full, *s_full, *s_free, *p_full, *o_done, *drain;
 };
 
 __device__ __forceinline__ Bars make_bars(uint8_t *smem)
@@ -75,14 +94,16 @@ __device__ __forceinline__ Bars make_bars(uint8_t *smem)
     uint64_t *b = reinterpret_cast<uint64_t *>(smem + OFF_BAR);
     Bars x;
     x.q_full = b;
-    x.q_ready = b + 1;
-    x.k_full = b + 2;
+    x.k_full = b + 1;
     x.k_empty = x.k_full + NS;
     x.v_full = x.k_empty + NS;
     x.v_empty = x.v_full + NS;
     x.r_full = x.v_empty + NS;
     x.r_empty = x.r_full + NR;
-    x.s_full = x.r_empty + NR;
+    x.prep = x.r_empty + NR;
+    x.bias_full = x.prep + 1;
+    x.ext_full = x.bias_full + 1;
+    x.s_full = x.ext_full + 1;
     x.s_free = x.s_full + 1;
     x.p_full = x.s_free + 1;
     x.o_done = x.p_full + 1;
@@ -96,7 +117,7 @@ __device__ __forceinline__ void fail(const TcParams &p, volatile int *abort_flag
     atomicOr(p.status, 1u);
 }
 
-// Empty registers "fence": uses of r cannot move above an earlier asm volatile.
+// Uses of r cannot move above an earlier asm volatile (the TMEM load wait).
 __device__ __forceinline__ void reg_fence(uint32_t (&r)[32])
 {
     asm volatile(""
@@ -113,12 +134,24 @@ __device__ __forceinline__ void tmem_wait_ld()
     asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
 }
 
+__device__ __forceinline__ void tmem_ld_x2(uint32_t taddr, uint32_t &a, uint32_t &b)
+{
+    asm volatile("tcgen05.ld.sync.aligned.32x32b.x2.b32 {%0, %1}, [%2];"
+                 : "=r"(a), "=r"(b)
+                 : "r"(taddr));
+}
+
 __device__ __forceinline__ void st_shared_v4(uint32_t addr, uint32_t a, uint32_t b, uint32_t c,
                                              uint32_t d)
 {
     asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(a), "r"(b), "r"(c),
                  "r"(d)
                  : "memory");
+}
+
+__device__ __forceinline__ void st_shared_b32(uint32_t addr, uint32_t a)
+{
+    asm volatile("st.shared.b32 [%0], %1;" ::"r"(addr), "r"(a) : "memory");
 }
 
 __device__ __forceinline__ float ld_shared_f32(uint32_t addr)
@@ -128,8 +161,65 @@ __device__ __forceinline__ float ld_shared_f32(uint32_t addr)
     return v;
 }
 
-__device__ __forceinline__ float bf16lo(uint32_t w) { return __uint_as_float(w << 16); }
-__device__ __forceinline__ float bf16hi(uint32_t w) { return __uint_as_float(w & 0xffff0000u); }
+__device__ __forceinline__ float max3f(float a, float b, float c)
+{
+    float d;
+    asm("max.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
+    return d;
+}
+
+__device__ __forceinline__ uint64_t pack2(float lo, float hi)
+{
+    uint64_t r;
+    asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(lo), "f"(hi));
+    return r;
+}
+
+__device__ __forceinline__ void unpack2(uint64_t v, float &lo, float &hi)
+{
+    asm("mov.b64 {%0, %1}, %2;" : "=f"(lo), "=f"(hi) : "l"(v));
+}
+
+__device__ __forceinline__ uint64_t fma2(uint64_t a, uint64_t b, uint64_t c)
+{
+    uint64_t d;
+    asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(a), "l"(b), "l"(c));
+    return d;
+}
+
+__device__ __forceinline__ uint64_t add2(uint64_t a, uint64_t b)
+{
+    uint64_t d;
+    asm("add.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+    return d;
+}
+
+// 2^x on the SFU.
+__device__ __forceinline__ float ex2f(float x)
+{
+    float y;
+    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
+
+// Descriptor of a bias-column tile: K-major, no swizzle; rows 16 bytes apart,
+// 8-row core matrices 128 bytes apart (stride offset), and the second
+// core-matrix column (K 8..15) 2 KB further (leading offset), in the tile's own
+// zero half.  Every address either offset can reach stays inside the tile and
+// the shared-memory regions that follow it.
+__device__ __forceinline__ uint64_t sdesc_ext(uint32_t addr)
+{
+    return (uint64_t)((addr & 0x3FFFFu) >> 4) | ((uint64_t)(2048u >> 4) << 16) |
+           ((uint64_t)(128u >> 4) << 32) | (1ull << 46);
+}
+
+// hi + lo bf16 pair whose sum is x to about 2^-17 relative.
+__device__ __forceinline__ uint32_t split_bf16(float x)
+{
+    const __nv_bfloat16 hi = __float2bfloat16_rn(x);
+    const __nv_bfloat16 lo = __float2bfloat16_rn(x - __bfloat162float(hi));
+    return (uint32_t)__bfloat16_as_ushort(hi) | ((uint32_t)__bfloat16_as_ushort(lo) << 16);
+}
 
 __global__ void __launch_bounds__(256, 1)
     relattn_fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_q,
@@ -180,7 +270,6 @@ __global__ void __launch_bounds__(256, 1)
 
     if (threadIdx.x == 0) {
         mbar_init(bar.q_full, 1);
-        mbar_init(bar.q_ready, 128);
         for (int s = 0; s < NS; ++s) {
             mbar_init(bar.k_full + s, 1);
             mbar_init(bar.k_empty + s, 1);
@@ -191,6 +280,9 @@ __global__ void __launch_bounds__(256, 1)
             mbar_init(bar.r_full + s, 1);
             mbar_init(bar.r_empty + s, 1);
         }
+        mbar_init(bar.prep, 128);
+        mbar_init(bar.bias_full, 1);
+        mbar_init(bar.ext_full, 128);
         mbar_init(bar.s_full, 1);
         mbar_init(bar.s_free, 128);
         mbar_init(bar.p_full, 128);
@@ -208,6 +300,9 @@ __global__ void __launch_bounds__(256, 1)
     tc_fence_after_sync();
     const uint32_t tmem = *tmem_slot;
     const uint64_t wait_ns = p.wait_ns;
+    // First row of table chunk c (local index): the window of key tile t starts
+    // at t*BN + L-1-i0-(BM-1), plus the row offset of a longer table.
+    const int r_base = p.L - BM - i0 + p.r_off + t_begin * BN;
 
     if (warp == 0) {
         // ===================== TMA producer =====================================
@@ -218,38 +313,39 @@ __global__ void __launch_bounds__(256, 1)
             prefetch_tensormap(&tm_r);
             const uint64_t pol_stream = policy_evict_first();  // K, V: read once
             const uint64_t pol_keep = policy_evict_last();     // table: shared by the batch
-            // Row of the reversed table at which chunk c starts: the window of key
-            // tile t begins at t*BN + L-1-i0-(BM-1), plus the table's row offset.
-            const int r_base = p.L - BM - i0 + p.r_off;
             bool ok = true;
             int kc = 0, vc = 0, rc = 0;  // copies issued into the K, V and table rings
-
+            auto load_r = [&](int c) -> bool {
+                const int rs = c % NR;
+                if (!mbar_wait(bar.r_empty + rs, ((c / NR) & 1) ^ 1, abort_flag, wait_ns))
+                    return false;
+                mbar_arrive_expect_tx(bar.r_full + rs, TILE);
+                tma_load_3d_hint(smem + OFF_R + rs * TILE, &tm_r, bar.r_full + rs, 0,
+                                 r_base + c * BN, h, pol_keep);
+                rc = c + 1;
+                return true;
+            };
             mbar_arrive_expect_tx(bar.q_full, TILE);
             tma_load_3d(smem + OFF_Q, &tm_q, bar.q_full, 0, i0, bh);
-            mbar_arrive_expect_tx(bar.r_full + 0, TILE);
-            tma_load_3d_hint(smem + OFF_R, &tm_r, bar.r_full + 0, 0, t_begin * BN + r_base, h,
-                             pol_keep);
-            rc = 1;
-
-            for (int it = 0; it < T; ++it) {
+            for (int c = 0; c < min(PF, T); ++c) {
+                tma_prefetch_3d(&tm_k, 0, (t_begin + c) * BN, bh);
+                tma_prefetch_3d(&tm_v, 0, (t_begin + c) * BN, bh);
+            }
+            ok = load_r(0);
+            for (int it = 0; it < T && ok; ++it) {
                 const int t = t_begin + it;
                 const int st = it % NS;
                 const uint32_t ph = (it / NS) & 1;
+                if (it + PF < T) {
+                    tma_prefetch_3d(&tm_k, 0, (t + PF) * BN, bh);
+                    tma_prefetch_3d(&tm_v, 0, (t + PF) * BN, bh);
+                }
                 if (!(ok = mbar_wait(bar.k_empty + st, ph ^ 1, abort_flag, wait_ns))) break;
                 mbar_arrive_expect_tx(bar.k_full + st, TILE);
                 tma_load_3d_hint(smem + OFF_K + st * TILE, &tm_k, bar.k_full + st, 0, t * BN, bh,
                                  pol_stream);
                 kc = it + 1;
-
-                const int lc = it + 1;  // table chunk used as the second half of tile it
-                const int rs = lc % NR;
-                if (!(ok = mbar_wait(bar.r_empty + rs, ((lc / NR) & 1) ^ 1, abort_flag, wait_ns)))
-                    break;
-                mbar_arrive_expect_tx(bar.r_full + rs, TILE);
-                tma_load_3d_hint(smem + OFF_R + rs * TILE, &tm_r, bar.r_full + rs, 0,
-                                 (t + 1) * BN + r_base, h, pol_keep);
-                rc = lc + 1;
-
+                if (!(ok = load_r(it + 1))) break;
                 if (!(ok = mbar_wait(bar.v_empty + st, ph ^ 1, abort_flag, wait_ns))) break;
                 mbar_arrive_expect_tx(bar.v_full + st, TILE);
                 tma_load_3d_hint(smem + OFF_V + st * TILE, &tm_v, bar.v_full + st, 0, t * BN, bh,
@@ -276,54 +372,90 @@ __global__ void __launch_bounds__(256, 1)
     } else if (warp == 1) {
         // ===================== MMA issuer =======================================
         if (lane == 0) {
-            constexpr uint32_t ID_S = idesc_bf16_f32(128, 128, false);
+            constexpr uint32_t ID_N128 = idesc_bf16_f32(128, 128, false);
+            constexpr uint32_t ID_N16 = idesc_bf16_f32(128, 16, false);
             constexpr uint32_t ID_O = idesc_bf16_f32(128, 64, true);
             const uint32_t sQ = smem_u32(smem + OFF_Q);
-            const uint32_t sQV = smem_u32(smem + OFF_QV);
             const uint32_t sK = smem_u32(smem + OFF_K);
             const uint32_t sV = smem_u32(smem + OFF_V);
             const uint32_t sR = smem_u32(smem + OFF_R);
             const uint32_t sP = smem_u32(smem + OFF_P);
+            const uint32_t sUB = smem_u32(smem + OFF_UB);
+            const uint32_t sAX = smem_u32(smem + OFF_AEXT);
+            const uint32_t sKX = smem_u32(smem + OFF_KEXT);
+            const uint32_t sRX = smem_u32(smem + OFF_REXT);
+            const uint64_t d_aext = sdesc_ext(sAX);
 
-            auto issue_scores = [&](int it) -> bool {
-                const int st = it % NS;
-                if (!mbar_wait(bar.k_full + st, (it / NS) & 1, abort_flag, wait_ns)) return false;
-                const int c0 = it, c1 = it + 1;
-                if (!mbar_wait(bar.r_full + c0 % NR, (c0 / NR) & 1, abort_flag, wait_ns))
-                    return false;
-                if (!mbar_wait(bar.r_full + c1 % NR, (c1 / NR) & 1, abort_flag, wait_ns))
-                    return false;
-                tc_fence_after_sync();
-                const uint32_t kb = sK + st * TILE;
-                const uint32_t r0 = sR + (c0 % NR) * TILE;
-                const uint32_t r1 = sR + (c1 % NR) * TILE;
+            // [tile rows] x [u ; v]^T into a 16-column TMEM region.
+            auto bias_mma = [&](uint32_t tcol, uint32_t a_tile) {
 #pragma unroll
                 for (int kk = 0; kk < DH / 16; ++kk)
-                    mma_bf16_ss(tmem + TM_S, sdesc_sw128(sQ + kk * 32), sdesc_sw128(kb + kk * 32),
-                                ID_S, kk);
+                    mma_bf16_ss(tmem + tcol, sdesc_sw128(a_tile + kk * 32),
+                                sdesc_sw128(sUB + kk * 32), ID_N16, kk);
+            };
+            // 128 x 128 scores q X^T plus the ext K-step (ones x bias pairs).
+            auto score_mma = [&](uint32_t tcol, uint32_t b_tile, uint32_t ext_tile) {
 #pragma unroll
                 for (int kk = 0; kk < DH / 16; ++kk)
-                    mma_bf16_ss(tmem + TM_W, sdesc_sw128(sQV + kk * 32),
-                                sdesc_sw128(r0 + kk * 32), ID_S, kk);
-#pragma unroll
-                for (int kk = 0; kk < DH / 16; ++kk)
-                    mma_bf16_ss(tmem + TM_W + 128, sdesc_sw128(sQV + kk * 32),
-                                sdesc_sw128(r1 + kk * 32), ID_S, kk);
-                mma_commit(bar.s_full);
-                mma_commit(bar.k_empty + st);
-                mma_commit(bar.r_empty + c0 % NR);
-                return true;
+                    mma_bf16_ss(tmem + tcol, sdesc_sw128(sQ + kk * 32),
+                                sdesc_sw128(b_tile + kk * 32), ID_N128, kk);
+                mma_bf16_ss(tmem + tcol, d_aext, sdesc_ext(ext_tile), ID_N128, 1);
+            };
+            auto wait_k = [&](int it) {
+                return mbar_wait(bar.k_full + it % NS, (it / NS) & 1, abort_flag, wait_ns);
+            };
+            auto wait_r = [&](int c) {
+                return mbar_wait(bar.r_full + c % NR, (c / NR) & 1, abort_flag, wait_ns);
             };
 
-            bool ok = mbar_wait(bar.q_ready, 0, abort_flag, wait_ns);
+            bool ok = mbar_wait(bar.prep, 0, abort_flag, wait_ns) &&
+                      mbar_wait(bar.q_full, 0, abort_flag, wait_ns);
+            // Prologue: biases of key tile 0 and table chunks 0 and 1.
+            if (ok) ok = wait_k(0) && wait_r(0) && wait_r(1);
             if (ok) {
                 tc_fence_after_sync();
-                ok = issue_scores(0);
+                bias_mma(TM_BK, sK);
+                bias_mma(TM_BR, sR);
+                bias_mma(TM_BR2, sR + TILE);
+                mma_commit(bar.bias_full);
+            }
+            // Scores of tile 0: S(0), chunks 0 and 1.
+            if (ok) ok = mbar_wait(bar.ext_full, 0, abort_flag, wait_ns);
+            if (ok) {
+                tc_fence_after_sync();
+                score_mma(TM_S, sK, sKX);
+                score_mma(TM_B, sR, sRX);
+                score_mma(TM_B + 128, sR + TILE, sRX + EXT);
+                mma_commit(bar.s_full);
+                mma_commit(bar.k_empty);
+                mma_commit(bar.r_empty + 0);
+                mma_commit(bar.r_empty + 1);
+            }
+            // Biases of tile 1: key tile 1 and chunk 2.
+            if (ok && T > 1) {
+                ok = wait_k(1) && wait_r(2);
+                if (ok) {
+                    tc_fence_after_sync();
+                    bias_mma(TM_BK, sK + TILE);
+                    bias_mma(TM_BR, sR + 2 * TILE);
+                    mma_commit(bar.bias_full);
+                }
             }
             for (int it = 0; it < T && ok; ++it) {
                 if (!(ok = mbar_wait(bar.s_free, it & 1, abort_flag, wait_ns))) break;
-                tc_fence_after_sync();
-                if (it + 1 < T && !(ok = issue_scores(it + 1))) break;
+                if (it + 1 < T) {
+                    // Scores of tile it+1: S from key tile it+1, table chunk it+2
+                    // into the slot chunk it just left.
+                    if (!(ok = mbar_wait(bar.ext_full, (it + 1) & 1, abort_flag, wait_ns))) break;
+                    tc_fence_after_sync();
+                    const int st = (it + 1) % NS;
+                    const int c = it + 2;
+                    score_mma(TM_S, sK + st * TILE, sKX + st * EXT);
+                    score_mma(TM_B + (c & 1) * 128, sR + (c % NR) * TILE, sRX + (c % NR) * EXT);
+                    mma_commit(bar.s_full);
+                    mma_commit(bar.k_empty + st);
+                    mma_commit(bar.r_empty + c % NR);
+                }
                 if (!(ok = mbar_wait(bar.p_full, it & 1, abort_flag, wait_ns))) break;
                 const int st = it % NS;
                 if (!(ok = mbar_wait(bar.v_full + st, (it / NS) & 1, abort_flag, wait_ns))) break;
@@ -337,6 +469,14 @@ __global__ void __launch_bounds__(256, 1)
                 }
                 mma_commit(bar.o_done);
                 mma_commit(bar.v_empty + st);
+                if (it + 2 < T) {
+                    // Biases of tile it+2: key tile it+2 and table chunk it+3.
+                    if (!(ok = wait_k(it + 2) && wait_r(it + 3))) break;
+                    tc_fence_after_sync();
+                    bias_mma(TM_BK, sK + ((it + 2) % NS) * TILE);
+                    bias_mma(TM_BR, sR + ((it + 3) % NR) * TILE);
+                    mma_commit(bar.bias_full);
+                }
             }
             // Every MMA issued above completes before TMEM is released.
             mma_commit(bar.drain);
@@ -347,52 +487,70 @@ __global__ void __launch_bounds__(256, 1)
     } else if (warp >= 4) {
         // ===================== softmax warps ====================================
         const int wq = warp - 4;          // TMEM lane quarter of this warp
-        const int row = wq * 32 + lane;   // query row within the tile
-        const int i = i0 + row;           // query index within the segment
+        const int row = wq * 32 + lane;   // query row within the tile (also the key /
+                                          // table row for the bias conversions)
+        const int i = i0 + row;
         const uint32_t lane_off = (uint32_t)(wq * 32) << 16;
         const uint32_t tS = tmem + lane_off + TM_S;
-        // This warp's rows need window columns [96-32wq, 96-32wq+160).
-        const uint32_t tW = tmem + lane_off + TM_W + (uint32_t)(96 - 32 * wq);
+        const uint32_t tB = tmem + lane_off + TM_B;
         const uint32_t tO = tmem + lane_off + TM_O;
         const uint32_t skew = smem_u32(smem + OFF_SKEW) + (uint32_t)row * SKEW_STRIDE * 4;
-        // Reading key y of a 32-key piece: column (31 - lane + y) of the two staged
-        // window chunks.
+        // Key y of a 32-key piece sits at column (31 - lane + y) of the two
+        // staged window chunks.
         const uint32_t skew_rd = skew + (uint32_t)(31 - lane) * 4;
+        const uint32_t sKX = smem_u32(smem + OFF_KEXT);
+        const uint32_t sRX = smem_u32(smem + OFF_REXT);
 
-        bool ok = mbar_wait(bar.q_full, 0, abort_flag, wait_ns);
-        ok = __all_sync(0xffffffffu, ok);
-        if (ok) {
-            // q + u (in place) and q + v, rounded once to bf16.
-            uint8_t *qrow = smem + OFF_Q + row * 128;
-            uint8_t *qvrow = smem + OFF_QV + row * 128;
-            const uint4 *uh = reinterpret_cast<const uint4 *>(p.u + h * DH);
-            const uint4 *vh = reinterpret_cast<const uint4 *>(p.vb + h * DH);
+        // ---- one-time operands: [u ; v] tile, ones column, zeroed ext tiles ----
+        {
+            uint8_t *ub = smem + OFF_UB;
+            if (row < 16) {
+                const uint4 *src = (row == 0) ? reinterpret_cast<const uint4 *>(p.u + h * DH)
+                                 : (row == 1) ? reinterpret_cast<const uint4 *>(p.vb + h * DH)
+                                              : nullptr;
 #pragma unroll
-            for (int c = 0; c < 8; ++c) {
-                const int phys = c ^ (row & 7);
-                const uint4 qq = *reinterpret_cast<const uint4 *>(qrow + phys * 16);
-                const uint4 uu = __ldg(uh + c);
-                const uint4 vv = __ldg(vh + c);
-                const uint32_t qw[4] = {qq.x, qq.y, qq.z, qq.w};
-                const uint32_t uw[4] = {uu.x, uu.y, uu.z, uu.w};
-                const uint32_t vw[4] = {vv.x, vv.y, vv.z, vv.w};
-                uint32_t ou[4], ov[4];
-#pragma unroll
-                for (int e = 0; e < 4; ++e) {
-                    const float ql = bf16lo(qw[e]), qh = bf16hi(qw[e]);
-                    ou[e] = pack_bf16x2(ql + bf16lo(uw[e]), qh + bf16hi(uw[e]));
-                    ov[e] = pack_bf16x2(ql + bf16lo(vw[e]), qh + bf16hi(vw[e]));
+                for (int c = 0; c < 8; ++c) {
+                    const uint4 val = src ? __ldg(src + c) : make_uint4(0, 0, 0, 0);
+                    *reinterpret_cast<uint4 *>(ub + row * 128 + ((c ^ (row & 7)) * 16)) = val;
                 }
-                *reinterpret_cast<uint4 *>(qrow + phys * 16) = make_uint4(ou[0], ou[1], ou[2], ou[3]);
-                *reinterpret_cast<uint4 *>(qvrow + phys * 16) =
-                    make_uint4(ov[0], ov[1], ov[2], ov[3]);
             }
+            // Ones column: row i = [1, 1, 0, 0, 0, 0, 0, 0] (bf16 1.0 = 0x3f80); then
+            // zero the second half of that tile and all of the bias tiles.
+            *reinterpret_cast<uint4 *>(smem + OFF_AEXT + row * 16) =
+                make_uint4(0x3f803f80u, 0u, 0u, 0u);
+            *reinterpret_cast<uint4 *>(smem + OFF_AEXT + 2048 + row * 16) = make_uint4(0, 0, 0, 0);
+            for (int o = row * 16; o < (NS + NR) * EXT; o += 128 * 16)
+                *reinterpret_cast<uint4 *>(smem + OFF_KEXT + o) = make_uint4(0, 0, 0, 0);
             fence_proxy_async_smem();
+            mbar_arrive(bar.prep);
         }
-        mbar_arrive(bar.q_ready);
 
-        const float sl2 = p.scale_log2;
-        float m_ref = -INFINITY;  // running max (log2 units), lazily updated
+        // Bias conversion: fp32 k.u (key row) and v.r (table row) from TMEM into
+        // (hi, lo) bf16 pairs in the ext tiles.
+        auto convert = [&](int phase, uint32_t kext, uint32_t rext, uint32_t rext2) -> bool {
+            const bool got = __all_sync(0xffffffffu,
+                                        mbar_wait(bar.bias_full, phase & 1, abort_flag, wait_ns));
+            if (!got) return false;
+            tc_fence_after_sync();
+            uint32_t ku, kv, ru, rv, r2u = 0, r2v = 0;
+            tmem_ld_x2(tmem + lane_off + TM_BK, ku, kv);
+            tmem_ld_x2(tmem + lane_off + TM_BR, ru, rv);
+            if (rext2) tmem_ld_x2(tmem + lane_off + TM_BR2, r2u, r2v);
+            asm volatile("tcgen05.wait::ld.sync.aligned;"
+                         : "+r"(ku), "+r"(kv), "+r"(ru), "+r"(rv), "+r"(r2u), "+r"(r2v)::"memory");
+            st_shared_b32(kext + row * 16, split_bf16(__uint_as_float(ku)));
+            st_shared_b32(rext + row * 16, split_bf16(__uint_as_float(rv)));
+            if (rext2) st_shared_b32(rext2 + row * 16, split_bf16(__uint_as_float(r2v)));
+            fence_proxy_async_smem();
+            tc_fence_before_sync();
+            mbar_arrive(bar.ext_full);
+            return true;
+        };
+
+        bool ok = convert(0, sKX, sRX, sRX + EXT);
+
+        const uint64_t sl2x2 = pack2(p.scale_log2, p.scale_log2);
+        float m_ref = -INFINITY;  // running max (scaled, log2 units), lazily updated
         float l_sum = 0.f;
         const uint32_t p_row = smem_u32(smem + OFF_P) + (uint32_t)row * 128;
 
@@ -402,16 +560,21 @@ __global__ void __launch_bounds__(256, 1)
             if (!ok) break;
             tc_fence_after_sync();
 
-            // ---- gather: x[jj] = S[row][jj] + W[row][jj + 127 - row] ------------
+            // ---- gather: x[jj] = S[row][jj] + window[row][jj + 127 - row] -------
+            // Window columns of this warp: [96-32wq, 96-32wq+160) of the virtual
+            // 256-column window; chunk it sits in slot it&1, chunk it+1 in the other.
+            const uint32_t wbase = (uint32_t)((it & 1) * 128 + 96 - 32 * wq);
             float x[BN];
+            uint32_t wa[32], wb[32], s[32];
+            tmem_ld32(tB + (wbase & 255u), wa);
+            tmem_ld32(tB + ((wbase + 32u) & 255u), wb);
+            tmem_ld32(tS, s);
+            tmem_wait_ld();
+            reg_fence(wa);
+            reg_fence(wb);
+            reg_fence(s);
 #pragma unroll
             for (int pc = 0; pc < BN / 32; ++pc) {
-                uint32_t wa[32], wb[32];
-                tmem_ld32(tW + 32 * pc, wa);
-                tmem_ld32(tW + 32 * (pc + 1), wb);
-                tmem_wait_ld();
-                reg_fence(wa);
-                reg_fence(wb);
 #pragma unroll
                 for (int c = 0; c < 8; ++c)
                     st_shared_v4(skew + c * 16, wa[4 * c], wa[4 * c + 1], wa[4 * c + 2],
@@ -420,40 +583,60 @@ __global__ void __launch_bounds__(256, 1)
                 for (int c = 0; c < 8; ++c)
                     st_shared_v4(skew + 128 + c * 16, wb[4 * c], wb[4 * c + 1], wb[4 * c + 2],
                                  wb[4 * c + 3]);
-                uint32_t s[32];
-                tmem_ld32(tS + 32 * pc, s);
-                tmem_wait_ld();
-                reg_fence(s);
 #pragma unroll
                 for (int y = 0; y < 32; ++y)
                     x[32 * pc + y] = __uint_as_float(s[y]) + ld_shared_f32(skew_rd + y * 4);
+                if (pc + 1 < BN / 32) {
+#pragma unroll
+                    for (int e = 0; e < 32; ++e) wa[e] = wb[e];
+                    tmem_ld32(tB + ((wbase + 32u * (pc + 2)) & 255u), wb);
+                    tmem_ld32(tS + 32 * (pc + 1), s);
+                    tmem_wait_ld();
+                    reg_fence(wb);
+                    reg_fence(s);
+                }
             }
             tc_fence_before_sync();
             mbar_arrive(bar.s_free);
 
-            // ---- scale, mask, tile max ------------------------------------------
+            // ---- biases of the next tile (key tile it+1, table chunk it+2) -------
+            if (it + 1 < T) {
+                const int st = (it + 1) % NS, c = it + 2;
+                if (!(ok = convert(it + 1, sKX + st * EXT, sRX + (c % NR) * EXT, 0))) break;
+            }
+
+            // ---- mask, tile max ---------------------------------------------------
             const bool need_mask = (j0 + BN - 1 > i0 + p.M) || (j0 + BN > p.K);
-            float mt = -INFINITY;
             if (need_mask) {
                 const int jlim = min(i + p.M, p.K - 1) - j0;  // last visible key (tile-local)
 #pragma unroll
-                for (int jj = 0; jj < BN; ++jj) {
-                    x[jj] = (jj <= jlim) ? x[jj] * sl2 : -INFINITY;
-                    mt = fmaxf(mt, x[jj]);
-                }
-            } else {
+                for (int jj = 0; jj < BN; ++jj)
+                    if (jj > jlim) x[jj] = -INFINITY;
+            }
+            // 8 independent max3 chains over the 128 scores, then a small tree.
+            float mx[8];
 #pragma unroll
-                for (int jj = 0; jj < BN; ++jj) {
-                    x[jj] *= sl2;
-                    mt = fmaxf(mt, x[jj]);
+            for (int a = 0; a < 8; ++a) mx[a] = max3f(x[2 * a], x[2 * a + 1], x[16 + 2 * a]);
+#pragma unroll
+            for (int a = 0; a < 8; ++a) mx[a] = max3f(mx[a], x[16 + 2 * a + 1], x[32 + 2 * a]);
+#pragma unroll
+            for (int jj = 32; jj < BN; jj += 16) {
+#pragma unroll
+                for (int a = 0; a < 8; ++a) {
+                    const int e0 = jj + 2 * a + 1, e1 = jj + 16 + 2 * a;
+                    mx[a] = (e1 < BN) ? max3f(mx[a], x[e0], x[e1]) : fmaxf(mx[a], x[e0]);
                 }
             }
+            float mt = max3f(max3f(mx[0], mx[1], mx[2]), max3f(mx[3], mx[4], mx[5]),
+                             fmaxf(mx[6], mx[7]));
+            mt *= p.scale_log2;  // scores scale by a positive constant
+
             // Lazy rescale: move the reference max only when the tile max exceeds
             // it by more than 8 (a factor 256); exact after the final division.
             float alpha = 1.f;
             const bool resc = mt > m_ref + 8.f;
             if (resc) {
-                alpha = ex2(m_ref - mt);  // 0 when m_ref is -inf
+                alpha = ex2f(m_ref - mt);  // 0 when m_ref is -inf
                 l_sum *= alpha;
                 m_ref = mt;
             }
@@ -482,22 +665,31 @@ __global__ void __launch_bounds__(256, 1)
             }
 
             // ---- exponentiate, row sum, P (bf16, 128-byte swizzled K-major) -----
-            float rs = 0.f;
+            const uint64_t nmu = pack2(-mu, -mu);
+            uint64_t acc[4] = {0, 0, 0, 0};
 #pragma unroll
             for (int c = 0; c < BN / 8; ++c) {
                 uint32_t pk[4];
 #pragma unroll
                 for (int e = 0; e < 4; ++e) {
-                    const float p0 = ex2(x[8 * c + 2 * e] - mu);
-                    const float p1 = ex2(x[8 * c + 2 * e + 1] - mu);
-                    rs += p0 + p1;
+                    const uint64_t a =
+                        fma2(pack2(x[8 * c + 2 * e], x[8 * c + 2 * e + 1]), sl2x2, nmu);
+                    float a0, a1;
+                    unpack2(a, a0, a1);
+                    const float p0 = ex2f(a0), p1 = ex2f(a1);
+                    acc[e] = add2(acc[e], pack2(p0, p1));
                     pk[e] = pack_bf16x2(p0, p1);
                 }
                 const int half = c >> 3;
                 const int phys = (c & 7) ^ (row & 7);
                 st_shared_v4(p_row + half * TILE + phys * 16, pk[0], pk[1], pk[2], pk[3]);
             }
-            l_sum += rs;
+            {
+                const uint64_t s01 = add2(add2(acc[0], acc[1]), add2(acc[2], acc[3]));
+                float a0, a1;
+                unpack2(s01, a0, a1);
+                l_sum += a0 + a1;
+            }
             fence_proxy_async_smem();
             tc_fence_before_sync();
             mbar_arrive(bar.p_full);

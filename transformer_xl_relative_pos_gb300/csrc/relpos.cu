@@ -7,12 +7,14 @@
 //   R[rho][2k] = sin(p w_k),  R[rho][2k+1] = cos(p w_k),  w_k = 10000^(-2k/d).
 //
 // Accuracy: the angle p*w_k reaches K radians, so it is formed in
-// double-float (w_k split into two floats per block, computed once in fp64),
+// double-float (w_k split into two floats, computed on the host in long double),
 // reduced modulo 2*pi by Cody and Waite's method (W. J. Cody, W. Waite,
 // "Software Manual for the Elementary Functions", 1980) with 2*pi split into
 // three floats, and only then passed to sincosf.  The split used here was
 // derived from a 50-digit value of 2*pi: C1 and C2 keep 8 significant bits each
 // so that n*C1 and n*C2 are exact for n < 2^16 (angles below ~4e5 rad).
+#include <cmath>
+
 #include "kernels.h"
 
 namespace txl {
@@ -22,9 +24,50 @@ constexpr float kTwoPiC1 = 6.28125f;                   // 0x1.92p+2
 constexpr float kTwoPiC2 = 0x1.fap-10f;                // 0.00193023681640625
 constexpr float kTwoPiC3 = 0x1.54442ep-18f;            // 5.0703634e-06
 constexpr float kInvTwoPi = 0x1.45f306p-3f;            // 1/(2 pi) rounded to fp32
-constexpr int kRowsPerBlock = 16;
+constexpr int kMaxHalf = 2048;                         // frequencies passed by value
 
-__global__ void rel_pos_emb_kernel(void *R, int K, int d, int bf16)
+// w_k = 10000^(-2k/d) as (hi, lo) floats, computed on the host in long double.
+struct Freqs {
+    float2 w[kMaxHalf];
+};
+
+__device__ __forceinline__ float2 sincos_pw(float pf, float whi, float wlo)
+{
+    // angle = p * (whi + wlo) as a_hi + a_lo (p exact: p < 2^24)
+    const float a_hi = pf * whi;
+    const float a_lo = fmaf(pf, wlo, fmaf(pf, whi, -a_hi));
+    const float n = rintf(a_hi * kInvTwoPi);
+    float r = fmaf(-n, kTwoPiC1, a_hi);
+    r = fmaf(-n, kTwoPiC2, r);
+    r += a_lo;
+    r = fmaf(-n, kTwoPiC3, r);
+    float sn, cs;
+    sincosf(r, &sn, &cs);
+    return make_float2(sn, cs);
+}
+
+__device__ __forceinline__ void store_pair(void *R, size_t pair, float2 v, int bf16)
+{
+    if (bf16)
+        reinterpret_cast<__nv_bfloat162 *>(R)[pair] = __floats2bfloat162_rn(v.x, v.y);
+    else
+        reinterpret_cast<float2 *>(R)[pair] = v;
+}
+
+// One thread per (row, k) pair.
+__global__ void rel_pos_emb_kernel(void *R, int K, int half, int bf16, const __grid_constant__ Freqs f)
+{
+    const long long e = blockIdx.x * (long long)blockDim.x + threadIdx.x;
+    if (e >= (long long)K * half) return;
+    const int rho = (int)(e / half);
+    const int k = (int)(e - (long long)rho * half);
+    const float2 w = f.w[k];
+    store_pair(R, (size_t)e, sincos_pw((float)(K - 1 - rho), w.x, w.y), bf16);
+}
+
+// Widths beyond the by-value table: each block derives the frequencies in fp64.
+constexpr int kRowsPerBlock = 16;
+__global__ void rel_pos_emb_wide_kernel(void *R, int K, int d, int bf16)
 {
     extern __shared__ float w_split[];  // [d/2] high parts, then [d/2] low parts
     const int half = d / 2;
@@ -43,23 +86,8 @@ __global__ void rel_pos_emb_kernel(void *R, int K, int d, int bf16)
     for (int e = threadIdx.x; e < rows * half; e += blockDim.x) {
         const int rho = rho0 + e / half;
         const int k = e % half;
-        const float pf = (float)(K - 1 - rho);  // exact: K < 2^24
-        // angle = p * (whi + wlo) as a_hi + a_lo
-        const float a_hi = pf * whi[k];
-        const float a_lo = fmaf(pf, wlo[k], fmaf(pf, whi[k], -a_hi));
-        const float n = rintf(a_hi * kInvTwoPi);
-        float r = fmaf(-n, kTwoPiC1, a_hi);
-        r = fmaf(-n, kTwoPiC2, r);
-        r += a_lo;
-        r = fmaf(-n, kTwoPiC3, r);
-        float sn, cs;
-        sincosf(r, &sn, &cs);
-        const size_t o = (size_t)rho * d + 2 * k;
-        if (bf16) {
-            reinterpret_cast<__nv_bfloat162 *>(R)[o / 2] = __floats2bfloat162_rn(sn, cs);
-        } else {
-            reinterpret_cast<float2 *>(R)[o / 2] = make_float2(sn, cs);
-        }
+        store_pair(R, (size_t)rho * half + k, sincos_pw((float)(K - 1 - rho), whi[k], wlo[k]),
+                   bf16);
     }
 }
 
@@ -67,10 +95,30 @@ __global__ void rel_pos_emb_kernel(void *R, int K, int d, int bf16)
 
 cudaError_t launch_rel_pos_emb(void *R, int K, int d_model, bool bf16, cudaStream_t s)
 {
+    const int half = d_model / 2;
+    if (half <= kMaxHalf) {
+        // The table depends on d_model only; keep the last one per host thread.
+        thread_local Freqs f;
+        thread_local int f_d = 0;
+        if (f_d != d_model) {
+            for (int k = 0; k < half; ++k) {
+                const long double w =
+                    powl(10000.0L, -2.0L * (long double)k / (long double)d_model);
+                const float hi = (float)w;
+                f.w[k] = make_float2(hi, (float)(w - (long double)hi));
+            }
+            f_d = d_model;
+        }
+        const long long n = (long long)K * half;
+        const long long blocks = (n + 255) / 256;
+        if (blocks > 0x7fffffffLL) return cudaErrorInvalidValue;
+        rel_pos_emb_kernel<<<(unsigned)blocks, 256, 0, s>>>(R, K, half, bf16 ? 1 : 0, f);
+        return cudaGetLastError();
+    }
     const int blocks = (K + kRowsPerBlock - 1) / kRowsPerBlock;
     const size_t shm = sizeof(float) * (size_t)d_model;
     if (shm > 48 * 1024) return cudaErrorInvalidValue;
-    rel_pos_emb_kernel<<<blocks, 256, shm, s>>>(R, K, d_model, bf16 ? 1 : 0);
+    rel_pos_emb_wide_kernel<<<blocks, 256, shm, s>>>(R, K, d_model, bf16 ? 1 : 0);
     return cudaGetLastError();
 }
 
