@@ -33,16 +33,27 @@ __global__ void mem_concat_kernel(uint4 *__restrict__ ext, const uint4 *__restri
     for (int c = threadIdx.x; c < row_vec; c += blockDim.x) dst[c] = src[c];
 }
 
-// mem[b][(head + l) mod cap] = h_new[b][l] for l in [first_row, L)
+// mem[b][(head + l) mod cap] = h_new[b][l] for l in [first_row, L).  Each block
+// copies kRowsPerBlock rows so that every thread has several loads in flight.
+constexpr int kRowsPerBlock = 4;
 __global__ void mem_write_kernel(uint4 *__restrict__ mem, const uint4 *__restrict__ h_new, int L,
                                  int first_row, int head, int cap, int row_vec)
 {
-    const int l = first_row + blockIdx.x;
+    const int l0 = first_row + blockIdx.x * kRowsPerBlock;
     const int b = blockIdx.y;
-    const int slot = (int)(((long long)head + l) % cap);
-    const uint4 *src = h_new + ((size_t)b * L + l) * row_vec;
-    uint4 *dst = mem + ((size_t)b * cap + slot) * row_vec;
-    for (int c = threadIdx.x; c < row_vec; c += blockDim.x) dst[c] = src[c];
+    const int nrows = min(kRowsPerBlock, L - l0);
+    for (int c = threadIdx.x; c < row_vec; c += blockDim.x) {
+        uint4 v[kRowsPerBlock];
+#pragma unroll
+        for (int r = 0; r < kRowsPerBlock; ++r)
+            if (r < nrows) v[r] = h_new[((size_t)b * L + l0 + r) * row_vec + c];
+#pragma unroll
+        for (int r = 0; r < kRowsPerBlock; ++r)
+            if (r < nrows) {
+                const int slot = (int)(((long long)head + l0 + r) % cap);
+                mem[((size_t)b * cap + slot) * row_vec + c] = v[r];
+            }
+    }
 }
 
 int threads_for(int row_vec) { return row_vec >= 256 ? 256 : ((row_vec + 31) / 32) * 32; }
@@ -66,8 +77,9 @@ cudaError_t launch_mem_write(uint4 *mem, const uint4 *h_new, int B, int L, int f
     const int rows = L - first_row;
     if (rows <= 0 || B == 0) return cudaSuccess;
     if (B > 65535) return cudaErrorInvalidValue;
-    mem_write_kernel<<<dim3(rows, B), threads_for(row_vec), 0, s>>>(mem, h_new, L, first_row,
-                                                                    head, cap, row_vec);
+    const int blocks = (rows + kRowsPerBlock - 1) / kRowsPerBlock;
+    mem_write_kernel<<<dim3(blocks, B), threads_for(row_vec), 0, s>>>(mem, h_new, L, first_row,
+                                                                      head, cap, row_vec);
     return cudaGetLastError();
 }
 

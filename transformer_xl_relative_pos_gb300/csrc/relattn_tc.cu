@@ -24,6 +24,9 @@
 // whose fp32 results the softmax warps split into bf16 hi + lo pairs; a fifth
 // MMA K-step multiplies a column of ones by those pairs.
 //
+// P goes from the softmax registers to TMEM (tcgen05.st) and the PV product
+// takes its A operand from there.
+//
 // Warp roles (256 threads):
 //   warp 0      TMA producer: q tile once, then K, V and table chunks through
 //               shared-memory rings, with L2 prefetches further ahead
@@ -31,7 +34,7 @@
 //   warp 2      TMEM allocator
 //   warps 4..7  softmax: thread = query row.  Per tile: gather S + shifted
 //               window, mask, running max (lazy rescale), exp2, P (bf16) to
-//               shared memory; convert the next tile's biases; finally O / l.
+//               TMEM; convert the next tile's biases; finally O / l.
 //
 // Every barrier wait is bounded: on time-out the block records an error in the
 // device status word, raises a block-wide abort flag, drains its own in-flight
@@ -45,13 +48,14 @@ namespace {
 using namespace ptx;
 
 constexpr int BM = kTcBM, BN = kTcBN, DH = kTcDH;
-constexpr int NS = 2;                  // K / V ring stages
-constexpr int NR = 3;                  // table-chunk ring slots
+constexpr int NS = 3;                  // K / V ring stages
+constexpr int NR = 2;                  // table-chunk ring slots
 constexpr int PF = 3;                  // L2 prefetch distance (tiles)
 constexpr int TILE = BM * DH * 2;      // 16384 bytes: 128 rows x 128 bytes
 constexpr int EXT = 4096;              // bias-column tile: 128 rows x 16 bytes, then
                                        // 2 KB of zeros for K columns 8..15
-constexpr int SKEW_STRIDE = 68;        // floats per skew row (bank-conflict free)
+constexpr int SKEW_STRIDE = 100;       // floats per skew row: a 3 x 32 ring + 4 pad
+                                       // (stride = 4 mod 32: conflict-free both ways)
 
 // TMEM columns
 constexpr uint32_t TM_S = 0;           // content scores
@@ -60,6 +64,9 @@ constexpr uint32_t TM_O = 384;         // output accumulator (64 columns)
 constexpr uint32_t TM_BK = 448;        // k.u / k.v for the next key tile (16 columns)
 constexpr uint32_t TM_BR = 464;        // r.u / r.v for the next table chunk
 constexpr uint32_t TM_BR2 = 480;       // second table chunk of the first tile
+constexpr uint32_t TM_P = 448;         // P (bf16 pairs, 64 columns); shares the bias
+                                       // columns, which are read before P is written
+                                       // and refilled only after PV has read P
 constexpr uint32_t TM_COLS = 512;
 
 // Shared-memory layout (offsets from a 1024-byte aligned base).
@@ -67,8 +74,7 @@ constexpr int OFF_Q = 0;
 constexpr int OFF_K = OFF_Q + TILE;               // NS stages
 constexpr int OFF_V = OFF_K + NS * TILE;          // NS stages
 constexpr int OFF_R = OFF_V + NS * TILE;          // NR slots
-constexpr int OFF_P = OFF_R + NR * TILE;          // keys 0-63, keys 64-127
-constexpr int OFF_UB = OFF_P + 2 * TILE;          // [u ; v ; 0 x 14] 16 x 128 bytes, swizzled
+constexpr int OFF_UB = OFF_R + NR * TILE;         // [u ; v ; 0 x 14] 16 x 128 bytes, swizzled
 constexpr int OFF_AEXT = OFF_UB + 2048;           // ones column: rows [1, 1, 0 x 6]
 constexpr int OFF_KEXT = OFF_AEXT + EXT;          // NS tiles of (hi, lo) of k.u
 constexpr int OFF_REXT = OFF_KEXT + NS * EXT;     // NR tiles of (hi, lo) of v.r
@@ -330,6 +336,7 @@ __global__ void __launch_bounds__(256, 1)
             for (int c = 0; c < min(PF, T); ++c) {
                 tma_prefetch_3d(&tm_k, 0, (t_begin + c) * BN, bh);
                 tma_prefetch_3d(&tm_v, 0, (t_begin + c) * BN, bh);
+                tma_prefetch_3d(&tm_r, 0, r_base + (c + 1) * BN, h);
             }
             ok = load_r(0);
             for (int it = 0; it < T && ok; ++it) {
@@ -339,6 +346,7 @@ __global__ void __launch_bounds__(256, 1)
                 if (it + PF < T) {
                     tma_prefetch_3d(&tm_k, 0, (t + PF) * BN, bh);
                     tma_prefetch_3d(&tm_v, 0, (t + PF) * BN, bh);
+                    tma_prefetch_3d(&tm_r, 0, r_base + (it + PF + 1) * BN, h);
                 }
                 if (!(ok = mbar_wait(bar.k_empty + st, ph ^ 1, abort_flag, wait_ns))) break;
                 mbar_arrive_expect_tx(bar.k_full + st, TILE);
@@ -379,7 +387,6 @@ __global__ void __launch_bounds__(256, 1)
             const uint32_t sK = smem_u32(smem + OFF_K);
             const uint32_t sV = smem_u32(smem + OFF_V);
             const uint32_t sR = smem_u32(smem + OFF_R);
-            const uint32_t sP = smem_u32(smem + OFF_P);
             const uint32_t sUB = smem_u32(smem + OFF_UB);
             const uint32_t sAX = smem_u32(smem + OFF_AEXT);
             const uint32_t sKX = smem_u32(smem + OFF_KEXT);
@@ -393,13 +400,20 @@ __global__ void __launch_bounds__(256, 1)
                     mma_bf16_ss(tmem + tcol, sdesc_sw128(a_tile + kk * 32),
                                 sdesc_sw128(sUB + kk * 32), ID_N16, kk);
             };
-            // 128 x 128 scores q X^T plus the ext K-step (ones x bias pairs).
-            auto score_mma = [&](uint32_t tcol, uint32_t b_tile, uint32_t ext_tile) {
+            // 128 x 128 scores q X^T (four K-steps), then the ext K-step that adds
+            // the bias pairs (ones x (hi, lo)).
+            auto score_main = [&](uint32_t tcol, uint32_t b_tile) {
 #pragma unroll
                 for (int kk = 0; kk < DH / 16; ++kk)
                     mma_bf16_ss(tmem + tcol, sdesc_sw128(sQ + kk * 32),
                                 sdesc_sw128(b_tile + kk * 32), ID_N128, kk);
+            };
+            auto score_ext = [&](uint32_t tcol, uint32_t ext_tile) {
                 mma_bf16_ss(tmem + tcol, d_aext, sdesc_ext(ext_tile), ID_N128, 1);
+            };
+            auto score_mma = [&](uint32_t tcol, uint32_t b_tile, uint32_t ext_tile) {
+                score_main(tcol, b_tile);
+                score_ext(tcol, ext_tile);
             };
             auto wait_k = [&](int it) {
                 return mbar_wait(bar.k_full + it % NS, (it / NS) & 1, abort_flag, wait_ns);
@@ -416,7 +430,7 @@ __global__ void __launch_bounds__(256, 1)
                 tc_fence_after_sync();
                 bias_mma(TM_BK, sK);
                 bias_mma(TM_BR, sR);
-                bias_mma(TM_BR2, sR + TILE);
+                bias_mma(TM_BR2, sR + (1 % NR) * TILE);
                 mma_commit(bar.bias_full);
             }
             // Scores of tile 0: S(0), chunks 0 and 1.
@@ -425,19 +439,19 @@ __global__ void __launch_bounds__(256, 1)
                 tc_fence_after_sync();
                 score_mma(TM_S, sK, sKX);
                 score_mma(TM_B, sR, sRX);
-                score_mma(TM_B + 128, sR + TILE, sRX + EXT);
+                score_mma(TM_B + 128, sR + (1 % NR) * TILE, sRX + (1 % NR) * EXT);
                 mma_commit(bar.s_full);
                 mma_commit(bar.k_empty);
                 mma_commit(bar.r_empty + 0);
-                mma_commit(bar.r_empty + 1);
+                mma_commit(bar.r_empty + 1 % NR);
             }
             // Biases of tile 1: key tile 1 and chunk 2.
             if (ok && T > 1) {
                 ok = wait_k(1) && wait_r(2);
                 if (ok) {
                     tc_fence_after_sync();
-                    bias_mma(TM_BK, sK + TILE);
-                    bias_mma(TM_BR, sR + 2 * TILE);
+                    bias_mma(TM_BK, sK + (1 % NS) * TILE);
+                    bias_mma(TM_BR, sR + (2 % NR) * TILE);
                     mma_commit(bar.bias_full);
                 }
             }
@@ -445,13 +459,17 @@ __global__ void __launch_bounds__(256, 1)
                 if (!(ok = mbar_wait(bar.s_free, it & 1, abort_flag, wait_ns))) break;
                 if (it + 1 < T) {
                     // Scores of tile it+1: S from key tile it+1, table chunk it+2
-                    // into the slot chunk it just left.
-                    if (!(ok = mbar_wait(bar.ext_full, (it + 1) & 1, abort_flag, wait_ns))) break;
+                    // into the slot chunk it just left.  The bias K-steps wait for
+                    // the softmax warps' conversion; the main ones need not.
                     tc_fence_after_sync();
                     const int st = (it + 1) % NS;
                     const int c = it + 2;
-                    score_mma(TM_S, sK + st * TILE, sKX + st * EXT);
-                    score_mma(TM_B + (c & 1) * 128, sR + (c % NR) * TILE, sRX + (c % NR) * EXT);
+                    score_main(TM_S, sK + st * TILE);
+                    score_main(TM_B + (c & 1) * 128, sR + (c % NR) * TILE);
+                    if (!(ok = mbar_wait(bar.ext_full, (it + 1) & 1, abort_flag, wait_ns))) break;
+                    tc_fence_after_sync();
+                    score_ext(TM_S, sKX + st * EXT);
+                    score_ext(TM_B + (c & 1) * 128, sRX + (c % NR) * EXT);
                     mma_commit(bar.s_full);
                     mma_commit(bar.k_empty + st);
                     mma_commit(bar.r_empty + c % NR);
@@ -462,15 +480,15 @@ __global__ void __launch_bounds__(256, 1)
                 tc_fence_after_sync();
                 const uint32_t vb = sV + st * TILE;
 #pragma unroll
-                for (int kk = 0; kk < BN / 16; ++kk) {
-                    const uint32_t a = sP + (kk >> 2) * TILE + (kk & 3) * 32;
-                    mma_bf16_ss(tmem + TM_O, sdesc_sw128(a), sdesc_sw128(vb + kk * 2048), ID_O,
+                for (int kk = 0; kk < BN / 16; ++kk)
+                    mma_bf16_ts(tmem + TM_O, tmem + TM_P + 8 * kk, sdesc_sw128(vb + kk * 2048), ID_O,
                                 (it > 0 || kk > 0) ? 1u : 0u);
-                }
                 mma_commit(bar.o_done);
                 mma_commit(bar.v_empty + st);
                 if (it + 2 < T) {
-                    // Biases of tile it+2: key tile it+2 and table chunk it+3.
+                    // Biases of tile it+2: key tile it+2 and table chunk it+3.  Their
+                    // TMEM columns hold P until this PV has completed.
+                    if (!(ok = mbar_wait(bar.o_done, it & 1, abort_flag, wait_ns))) break;
                     if (!(ok = wait_k(it + 2) && wait_r(it + 3))) break;
                     tc_fence_after_sync();
                     bias_mma(TM_BK, sK + ((it + 2) % NS) * TILE);
@@ -525,6 +543,15 @@ __global__ void __launch_bounds__(256, 1)
             mbar_arrive(bar.prep);
         }
 
+        // Second half of a bias conversion: (hi, lo) pairs of already loaded
+        // fp32 k.u and v.r values into the ext tiles.
+        auto convert_store = [&](uint32_t ku, uint32_t rv, uint32_t kext, uint32_t rext) {
+            st_shared_b32(kext + row * 16, split_bf16(__uint_as_float(ku)));
+            st_shared_b32(rext + row * 16, split_bf16(__uint_as_float(rv)));
+            fence_proxy_async_smem();
+            tc_fence_before_sync();
+            mbar_arrive(bar.ext_full);
+        };
         // Bias conversion: fp32 k.u (key row) and v.r (table row) from TMEM into
         // (hi, lo) bf16 pairs in the ext tiles.
         auto convert = [&](int phase, uint32_t kext, uint32_t rext, uint32_t rext2) -> bool {
@@ -547,12 +574,12 @@ __global__ void __launch_bounds__(256, 1)
             return true;
         };
 
-        bool ok = convert(0, sKX, sRX, sRX + EXT);
+        bool ok = convert(0, sKX, sRX, sRX + (1 % NR) * EXT);
 
         const uint64_t sl2x2 = pack2(p.scale_log2, p.scale_log2);
         float m_ref = -INFINITY;  // running max (scaled, log2 units), lazily updated
         float l_sum = 0.f;
-        const uint32_t p_row = smem_u32(smem + OFF_P) + (uint32_t)row * 128;
+        const uint32_t tP = tmem + lane_off + TM_P;
 
         for (int it = 0; it < T && ok; ++it) {
             const int j0 = (t_begin + it) * BN;
@@ -562,9 +589,17 @@ __global__ void __launch_bounds__(256, 1)
 
             // ---- gather: x[jj] = S[row][jj] + window[row][jj + 127 - row] -------
             // Window columns of this warp: [96-32wq, 96-32wq+160) of the virtual
-            // 256-column window; chunk it sits in slot it&1, chunk it+1 in the other.
+            // 256-column window (five 32-column chunks); table chunk it sits in
+            // TMEM slot it&1, chunk it+1 in the other.  Each window chunk c goes
+            // once through a 3-slot shared-memory ring (slot c % 3); key y of
+            // piece pc is ring column (32*pc + 31 - lane + y), which for pc = 2
+            // wraps from slot 2 to slot 0 when y > lane.
             const uint32_t wbase = (uint32_t)((it & 1) * 128 + 96 - 32 * wq);
+            uint32_t bku = 0, bkv = 0, bru = 0, brv = 0;  // next tile's bias values
             float x[BN];
+            float mx[8];  // 8 independent running-max chains over the gathered scores
+#pragma unroll
+            for (int a = 0; a < 8; ++a) mx[a] = -INFINITY;
             uint32_t wa[32], wb[32], s[32];
             tmem_ld32(tB + (wbase & 255u), wa);
             tmem_ld32(tB + ((wbase + 32u) & 255u), wb);
@@ -574,58 +609,89 @@ __global__ void __launch_bounds__(256, 1)
             reg_fence(wb);
             reg_fence(s);
 #pragma unroll
+            for (int c = 0; c < 8; ++c)
+                st_shared_v4(skew + c * 16, wa[4 * c], wa[4 * c + 1], wa[4 * c + 2], wa[4 * c + 3]);
+#pragma unroll
+            for (int c = 0; c < 8; ++c)
+                st_shared_v4(skew + 128 + c * 16, wb[4 * c], wb[4 * c + 1], wb[4 * c + 2],
+                             wb[4 * c + 3]);
+#pragma unroll
             for (int pc = 0; pc < BN / 32; ++pc) {
-#pragma unroll
-                for (int c = 0; c < 8; ++c)
-                    st_shared_v4(skew + c * 16, wa[4 * c], wa[4 * c + 1], wa[4 * c + 2],
-                                 wa[4 * c + 3]);
-#pragma unroll
-                for (int c = 0; c < 8; ++c)
-                    st_shared_v4(skew + 128 + c * 16, wb[4 * c], wb[4 * c + 1], wb[4 * c + 2],
-                                 wb[4 * c + 3]);
-#pragma unroll
-                for (int y = 0; y < 32; ++y)
-                    x[32 * pc + y] = __uint_as_float(s[y]) + ld_shared_f32(skew_rd + y * 4);
+                // Next window chunk and next S piece are loaded while this piece
+                // is read from the ring.
                 if (pc + 1 < BN / 32) {
+                    tmem_ld32(tB + ((wbase + 32u * (pc + 2)) & 255u), wa);
+                    tmem_ld32(tS + 32 * (pc + 1), wb);
+                }
+                if (pc + 1 == BN / 32 && it + 1 < T) {
+                    // The next tile's biases: their TMEM loads overlap this piece.
+                    ok = __all_sync(0xffffffffu, mbar_wait(bar.bias_full, (it + 1) & 1, abort_flag,
+                                                           wait_ns));
+                    if (ok) {
+                        tc_fence_after_sync();
+                        tmem_ld_x2(tmem + lane_off + TM_BK, bku, bkv);
+                        tmem_ld_x2(tmem + lane_off + TM_BR, bru, brv);
+                    }
+                }
+                const uint32_t rd = skew_rd + (uint32_t)((pc % 3) * 128);
+                if (pc % 3 == 2) {
 #pragma unroll
-                    for (int e = 0; e < 32; ++e) wa[e] = wb[e];
-                    tmem_ld32(tB + ((wbase + 32u * (pc + 2)) & 255u), wb);
-                    tmem_ld32(tS + 32 * (pc + 1), s);
+                    for (int y = 0; y < 32; ++y) {
+                        const uint32_t a = rd + y * 4 - ((y > lane) ? 384u : 0u);
+                        x[32 * pc + y] = __uint_as_float(s[y]) + ld_shared_f32(a);
+                    }
+                } else {
+#pragma unroll
+                    for (int y = 0; y < 32; ++y)
+                        x[32 * pc + y] = __uint_as_float(s[y]) + ld_shared_f32(rd + y * 4);
+                }
+#pragma unroll
+                for (int a = 0; a < 8; ++a) {
+                    mx[a] = max3f(mx[a], x[32 * pc + 4 * a], x[32 * pc + 4 * a + 1]);
+                    mx[a] = max3f(mx[a], x[32 * pc + 4 * a + 2], x[32 * pc + 4 * a + 3]);
+                }
+                if (pc + 1 < BN / 32) {
                     tmem_wait_ld();
+                    reg_fence(wa);
                     reg_fence(wb);
-                    reg_fence(s);
+                    // chunk pc+2 replaces chunk pc-1, which no later piece reads
+                    const uint32_t slot = skew + (uint32_t)(((pc + 2) % 3) * 128);
+#pragma unroll
+                    for (int c = 0; c < 8; ++c)
+                        st_shared_v4(slot + c * 16, wa[4 * c], wa[4 * c + 1], wa[4 * c + 2],
+                                     wa[4 * c + 3]);
+#pragma unroll
+                    for (int e = 0; e < 32; ++e) s[e] = wb[e];
                 }
             }
+            if (!ok) break;
+            asm volatile("tcgen05.wait::ld.sync.aligned;"
+                         : "+r"(bku), "+r"(bkv), "+r"(bru), "+r"(brv)::"memory");
             tc_fence_before_sync();
             mbar_arrive(bar.s_free);
 
             // ---- biases of the next tile (key tile it+1, table chunk it+2) -------
             if (it + 1 < T) {
                 const int st = (it + 1) % NS, c = it + 2;
-                if (!(ok = convert(it + 1, sKX + st * EXT, sRX + (c % NR) * EXT, 0))) break;
+                convert_store(bku, brv, sKX + st * EXT, sRX + (c % NR) * EXT);
             }
 
-            // ---- mask, tile max ---------------------------------------------------
+            // ---- mask (keys after the query, keys past K), tile max --------------
             const bool need_mask = (j0 + BN - 1 > i0 + p.M) || (j0 + BN > p.K);
             if (need_mask) {
                 const int jlim = min(i + p.M, p.K - 1) - j0;  // last visible key (tile-local)
 #pragma unroll
+                for (int a = 0; a < 8; ++a) mx[a] = -INFINITY;
+#pragma unroll
                 for (int jj = 0; jj < BN; ++jj)
                     if (jj > jlim) x[jj] = -INFINITY;
-            }
-            // 8 independent max3 chains over the 128 scores, then a small tree.
-            float mx[8];
 #pragma unroll
-            for (int a = 0; a < 8; ++a) mx[a] = max3f(x[2 * a], x[2 * a + 1], x[16 + 2 * a]);
+                for (int pc = 0; pc < BN / 32; ++pc)
 #pragma unroll
-            for (int a = 0; a < 8; ++a) mx[a] = max3f(mx[a], x[16 + 2 * a + 1], x[32 + 2 * a]);
-#pragma unroll
-            for (int jj = 32; jj < BN; jj += 16) {
-#pragma unroll
-                for (int a = 0; a < 8; ++a) {
-                    const int e0 = jj + 2 * a + 1, e1 = jj + 16 + 2 * a;
-                    mx[a] = (e1 < BN) ? max3f(mx[a], x[e0], x[e1]) : fmaxf(mx[a], x[e0]);
-                }
+                    for (int a = 0; a < 8; ++a) {
+                        mx[a] = max3f(mx[a], x[32 * pc + 4 * a], x[32 * pc + 4 * a + 1]);
+                        mx[a] = max3f(mx[a], x[32 * pc + 4 * a + 2], x[32 * pc + 4 * a + 3]);
+                    }
             }
             float mt = max3f(max3f(mx[0], mx[1], mx[2]), max3f(mx[3], mx[4], mx[5]),
                              fmaxf(mx[6], mx[7]));
@@ -664,25 +730,23 @@ __global__ void __launch_bounds__(256, 1)
                 }
             }
 
-            // ---- exponentiate, row sum, P (bf16, 128-byte swizzled K-major) -----
+            // ---- exponentiate, row sum, P (bf16 pairs) into TMEM -----------------
             const uint64_t nmu = pack2(-mu, -mu);
             uint64_t acc[4] = {0, 0, 0, 0};
 #pragma unroll
-            for (int c = 0; c < BN / 8; ++c) {
-                uint32_t pk[4];
+            for (int half = 0; half < 2; ++half) {
+                uint32_t pk[32];
 #pragma unroll
-                for (int e = 0; e < 4; ++e) {
-                    const uint64_t a =
-                        fma2(pack2(x[8 * c + 2 * e], x[8 * c + 2 * e + 1]), sl2x2, nmu);
+                for (int e = 0; e < 32; ++e) {
+                    const int jj = 64 * half + 2 * e;
+                    const uint64_t a = fma2(pack2(x[jj], x[jj + 1]), sl2x2, nmu);
                     float a0, a1;
                     unpack2(a, a0, a1);
                     const float p0 = ex2f(a0), p1 = ex2f(a1);
-                    acc[e] = add2(acc[e], pack2(p0, p1));
+                    acc[e & 3] = add2(acc[e & 3], pack2(p0, p1));
                     pk[e] = pack_bf16x2(p0, p1);
                 }
-                const int half = c >> 3;
-                const int phys = (c & 7) ^ (row & 7);
-                st_shared_v4(p_row + half * TILE + phys * 16, pk[0], pk[1], pk[2], pk[3]);
+                tmem_st32(tP + 32 * half, pk);
             }
             {
                 const uint64_t s01 = add2(add2(acc[0], acc[1]), add2(acc[2], acc[3]));
@@ -690,7 +754,7 @@ __global__ void __launch_bounds__(256, 1)
                 unpack2(s01, a0, a1);
                 l_sum += a0 + a1;
             }
-            fence_proxy_async_smem();
+            tmem_st_wait();
             tc_fence_before_sync();
             mbar_arrive(bar.p_full);
         }

@@ -54,15 +54,30 @@ __device__ __forceinline__ void store_pair(void *R, size_t pair, float2 v, int b
         reinterpret_cast<float2 *>(R)[pair] = v;
 }
 
-// One thread per (row, k) pair.
-__global__ void rel_pos_emb_kernel(void *R, int K, int half, int bf16, const __grid_constant__ Freqs f)
+// Block = 64 frequency pairs x 4 rows of threads, covering 32 rows.  The
+// block's 64 frequencies are staged from the parameter bank into shared memory
+// once (parameter-bank reads are fast only when a warp reads one address).
+constexpr int kPairsPerBlock = 64;
+constexpr int kRowsPerTile = 32;
+__global__ void __launch_bounds__(256)
+    rel_pos_emb_kernel(void *R, int K, int half, int bf16, const __grid_constant__ Freqs f)
 {
-    const long long e = blockIdx.x * (long long)blockDim.x + threadIdx.x;
-    if (e >= (long long)K * half) return;
-    const int rho = (int)(e / half);
-    const int k = (int)(e - (long long)rho * half);
-    const float2 w = f.w[k];
-    store_pair(R, (size_t)e, sincos_pw((float)(K - 1 - rho), w.x, w.y), bf16);
+    __shared__ float2 w[kPairsPerBlock];
+    const int k0 = blockIdx.x * kPairsPerBlock;
+    const int tk = threadIdx.x % kPairsPerBlock;
+    const int tr = threadIdx.x / kPairsPerBlock;  // 0..3
+    if (threadIdx.x < kPairsPerBlock && k0 + threadIdx.x < half) w[threadIdx.x] = f.w[k0 + threadIdx.x];
+    __syncthreads();
+    const int k = k0 + tk;
+    if (k >= half) return;
+    const float2 wk = w[tk];
+    const int rho0 = blockIdx.y * kRowsPerTile;
+#pragma unroll 4
+    for (int r = tr; r < kRowsPerTile; r += 4) {
+        const int rho = rho0 + r;
+        if (rho >= K) break;
+        store_pair(R, (size_t)rho * half + k, sincos_pw((float)(K - 1 - rho), wk.x, wk.y), bf16);
+    }
 }
 
 // Widths beyond the by-value table: each block derives the frequencies in fp64.
@@ -109,10 +124,10 @@ cudaError_t launch_rel_pos_emb(void *R, int K, int d_model, bool bf16, cudaStrea
             }
             f_d = d_model;
         }
-        const long long n = (long long)K * half;
-        const long long blocks = (n + 255) / 256;
-        if (blocks > 0x7fffffffLL) return cudaErrorInvalidValue;
-        rel_pos_emb_kernel<<<(unsigned)blocks, 256, 0, s>>>(R, K, half, bf16 ? 1 : 0, f);
+        const dim3 grid((half + kPairsPerBlock - 1) / kPairsPerBlock,
+                        (K + kRowsPerTile - 1) / kRowsPerTile);
+        if (grid.y > 65535u) return cudaErrorInvalidValue;
+        rel_pos_emb_kernel<<<grid, 256, 0, s>>>(R, K, half, bf16 ? 1 : 0, f);
         return cudaGetLastError();
     }
     const int blocks = (K + kRowsPerBlock - 1) / kRowsPerBlock;
