@@ -239,11 +239,16 @@ def run_reference(args, world, rank):
 # our arm
 # ---------------------------------------------------------------------------
 
-def build_operands(w, dev):
+def rank_seed(base: int, rank: int) -> int:
+    """Each rank draws its own batch (weak scaling over disjoint units)."""
+    return base + 1000 * rank
+
+
+def build_operands(w, dev, rank=0):
     import torch
     import transformer_xl_relative_pos_gb300 as txl
     from transformer_xl_relative_pos_gb300 import model
-    raw = txl_inputs.draw_layer(w)
+    raw = txl_inputs.draw_layer(w, seed=rank_seed(w.seed, rank))
     h_ext = raw["h_ext"].to(dev)
     R = txl.rel_pos_emb(w.K, w.d_model, dtype=torch.float32, device=dev)
     q, k, v, r = model.attention_operands(h_ext, w.M, raw["W_q"].to(dev), raw["W_kE"].to(dev),
@@ -264,7 +269,7 @@ def run_ours(args, world, rank, local):
     w = txl_inputs.WORKLOADS[txl_inputs.HEADLINE]
     dev = torch.device("cuda", local)
     pk = peaks()
-    base = build_operands(w, dev)
+    base = build_operands(w, dev, rank)
     scale = 1.0 / math.sqrt(w.dh)
     ws = torch.empty(max(txl.workspace_size(w.B, w.H, w.L, w.dh, 8), 256), dtype=torch.uint8,
                      device=dev)

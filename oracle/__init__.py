@@ -224,6 +224,13 @@ def layer_forward(h, mem, lay: dict, u, v_bias, H: int, scale: float, bh=None):
     a, _ = relattn(q, k, v, rel, u, v_bias, M, L, scale)
     B = h.shape[0]
     a = a.transpose(0, 2, 1, 3).reshape(B, L, -1)
+    return layer_post(a, h, lay)
+
+
+def layer_post(a, h, lay: dict):
+    """The rest of the layer after attention (§3.3 summary):
+    o = LayerNorm(Linear(a) + h);  h' = LayerNorm(o + W_2 ReLU(W_1 o + b_1) + b_2)."""
+    a, h = _f64(a), _f64(h)
     o = layer_norm(a @ _f64(lay["W_o"]).T + _f64(lay["b_o"]) + h)
     f = np.maximum(o @ _f64(lay["W_1"]).T + _f64(lay["b_1"]), 0.0)
     return layer_norm(o + f @ _f64(lay["W_2"]).T + _f64(lay["b_2"]))

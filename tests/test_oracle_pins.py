@@ -317,3 +317,25 @@ def test_bh_subset_matches_full():
         np.testing.assert_array_equal(part[b, h], full[b, h])
         np.testing.assert_array_equal(lpart[b, h], lfull[b, h])
     assert np.isnan(part[0, 0]).all()
+
+
+# ---------------------------------------------------------------------------
+# Layer glue of the stack model: LayerNorm and the position-wise feed-forward
+# ---------------------------------------------------------------------------
+
+def test_oracle_layer_glue():
+    g = torch.Generator().manual_seed(71)
+    B, L, d, hd, f = 2, 5, 12, 8, 20
+    r = lambda *s: torch.randn(*s, generator=g, dtype=torch.float64)
+    a, h = r(B, L, hd), r(B, L, d)
+    lay = {"W_o": r(d, hd), "b_o": r(d), "W_1": r(f, d), "b_1": r(f), "W_2": r(d, f), "b_2": r(d)}
+    F = torch.nn.functional
+    x = r(3, 7, d) * 3 + 1
+    np.testing.assert_allclose(oracle.layer_norm(x.numpy()),
+                               F.layer_norm(x, (d,), eps=oracle.LN_EPS).numpy(), rtol=1e-12,
+                               atol=1e-12)
+    o = F.layer_norm(F.linear(a, lay["W_o"], lay["b_o"]) + h, (d,), eps=1e-5)
+    want = F.layer_norm(o + F.linear(F.relu(F.linear(o, lay["W_1"], lay["b_1"])), lay["W_2"],
+                                     lay["b_2"]), (d,), eps=1e-5)
+    got = oracle.layer_post(a.numpy(), h.numpy(), {k: v.numpy() for k, v in lay.items()})
+    np.testing.assert_allclose(got, want.numpy(), rtol=1e-11, atol=1e-11)
