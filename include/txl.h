@@ -128,6 +128,42 @@ int txl_relattn_fwd(const void *q, const void *k, const void *v, const void *r, 
                     void *workspace, size_t workspace_bytes, void *stream);
 
 /*
+ * TXL_NOALLOC_SCRATCH_BYTES - size of the scratch array built into the library
+ * for txl_relattn_fwd_noalloc (32 MiB).
+ */
+#define TXL_NOALLOC_SCRATCH_BYTES (32u * 1024u * 1024u)
+
+/*
+ * txl_relattn_fwd_noalloc - txl_relattn_fwd for callers that cannot allocate
+ * device memory when they run it (for example plugins of inference engines
+ * whose execute step must not allocate, or runtimes whose device memory budget
+ * is fixed at start-up).  The paper has no counterpart: this is a property of
+ * the library, not of the method.
+ *
+ * Same arguments, layouts, results and errors as txl_relattn_fwd, without the
+ * workspace.  When a head's key range is split over several blocks, the
+ * partial results go to a scratch array that is part of the library: one
+ * device array of TXL_NOALLOC_SCRATCH_BYTES that every GPU which loads the
+ * library holds until the process exits.  The call itself allocates nothing
+ * (no cudaMalloc, cudaFree or allocating library routine).
+ *   - n_splits > 1 whose partial results need more than the scratch
+ *     (txl_relattn_workspace_size(B, H, L, dh, n_splits) bytes) returns
+ *     TXL_ERR_WORKSPACE and launches nothing; n_splits = 0 chooses a split
+ *     that fits (or none).
+ *   - Every call shares the array and leaves its partial results in it; calls
+ *     that may run at the same time on the GPU (other streams, or other host
+ *     threads without ordering) race on it and must be serialised by the
+ *     caller.
+ *   - The first call on a device looks up the array's device address (a
+ *     runtime query, done once per device with that device current); make that
+ *     first call before any stream capture.
+ */
+int txl_relattn_fwd_noalloc(const void *q, const void *k, const void *v, const void *r,
+                            int r_rows, const void *u, const void *v_bias, void *out, float *lse,
+                            int B, int H, int M, int L, int dh, float scale, int dtype,
+                            int n_splits, void *stream);
+
+/*
  * Segment memory of one layer (§3.2: "cache a predefined length-M old hidden
  * states spanning (possibly) multiple segments"), kept as a ring buffer.
  *

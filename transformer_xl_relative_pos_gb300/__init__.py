@@ -31,6 +31,7 @@ from ._lib import (  # noqa: F401
     mem_update,
     rel_pos_emb,
     relattn_fwd,
+    relattn_fwd_noalloc,
     set_wait_limit_ns,
     status_string,
     version,

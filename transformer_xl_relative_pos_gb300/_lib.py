@@ -61,6 +61,9 @@ def lib():
                 "txl_relattn_fwd": (_c_int, [_c_p, _c_p, _c_p, _c_p, _c_int, _c_p, _c_p, _c_p, _c_p,
                                              _c_int, _c_int, _c_int, _c_int, _c_int, _c_float,
                                              _c_int, _c_int, _c_p, _c_size, _c_p]),
+                "txl_relattn_fwd_noalloc": (_c_int, [_c_p, _c_p, _c_p, _c_p, _c_int, _c_p, _c_p,
+                                                     _c_p, _c_p, _c_int, _c_int, _c_int, _c_int,
+                                                     _c_int, _c_float, _c_int, _c_int, _c_p]),
                 "txl_mem_concat": (_c_int, [_c_p, _c_p, ctypes.POINTER(MemState), _c_p, _c_int,
                                             _c_int, _c_int, _c_int, _c_p]),
                 "txl_mem_update": (_c_int, [_c_p, ctypes.POINTER(MemState), _c_p, _c_int, _c_int,
@@ -158,6 +161,31 @@ def relattn_fwd(q, k, v, r, u, v_bias, M: int, scale: float, *, out=None, lse=No
         int(B), int(H), int(M), int(L), int(dh), float(scale), code, int(n_splits),
         ws_ptr, int(ws_bytes), _stream(q, stream))
     _check(rc, "txl_relattn_fwd")
+    return (out, lse) if want_lse else out
+
+
+def relattn_fwd_noalloc(q, k, v, r, u, v_bias, M: int, scale: float, *, out=None, lse=None,
+                        n_splits: int = 0, stream=None):
+    """relattn_fwd for callers that cannot allocate device memory at call time:
+    split-key partial results go to the library's own scratch array (shared by
+    all calls; calls that overlap on the GPU race on it).  The C entry point
+    allocates nothing; a caller that cannot allocate passes ``out`` (and
+    ``lse``) in, otherwise this wrapper creates them."""
+    B, H, L, dh = q.shape
+    dt = q.dtype
+    code = _code(dt)
+    if out is None:
+        out = torch.empty_like(q)
+    want_lse = lse is not None and lse is not False
+    if lse is True:
+        lse = torch.empty(B, H, L, dtype=torch.float32, device=q.device)
+    lse_ptr = _dev(lse, "lse", torch.float32) if want_lse else None
+    rc = lib().txl_relattn_fwd_noalloc(
+        _dev(q, "q", dt), _dev(k, "k", dt), _dev(v, "v", dt), _dev(r, "r", dt), int(r.shape[1]),
+        _dev(u, "u", dt), _dev(v_bias, "v_bias", dt), _dev(out, "out", dt), lse_ptr,
+        int(B), int(H), int(M), int(L), int(dh), float(scale), code, int(n_splits),
+        _stream(q, stream))
+    _check(rc, "txl_relattn_fwd_noalloc")
     return (out, lse) if want_lse else out
 
 
