@@ -141,6 +141,31 @@ def test_relattn_bf16_key_splits(n_splits):
     compare(lse.cpu().numpy(), want_lse, TOL_BF16, what=f"lse split {n_splits}")
 
 
+# Launch shapes: one block per (batch, head, query tile) (n_splits 1) with
+# more units than SMs, the automatic choice (0), and a key range split over
+# seven blocks whose partial results are merged (7); plus many 1-row heads over
+# a long memory.
+@pytest.mark.parametrize("n_splits,B,H,L,M", [(1, 8, 16, 300, 100), (0, 8, 16, 300, 100),
+                                              (1, 4, 40, 128, 200), (0, 4, 40, 128, 200),
+                                              (7, 1, 2, 200, 900), (0, 3, 1, 1, 2000)])
+def test_relattn_bf16_schedules(n_splits, B, H, L, M):
+    case = heads_case(B, H, L, M, seed=700 + 13 * n_splits + L)
+    out, lse = run_gpu(case, M, 0.125, n_splits=n_splits)
+    want, want_lse = run_oracle(case, M, 0.125)
+    what = f"schedule {n_splits} B{B} H{H} L{L} M{M}"
+    compare(out.float().cpu().numpy(), want, TOL_BF16, TOL_BF16_RMS, what=what)
+    compare(lse.cpu().numpy(), want_lse, TOL_BF16, what="lse " + what)
+
+
+def test_relattn_bf16_merge_is_repeatable():
+    # Split key ranges are merged in a fixed order: the result is bitwise stable.
+    B, H, L, M = 2, 2, 130, 900
+    case = heads_case(B, H, L, M, seed=77)
+    a = run_gpu(case, M, 0.125, n_splits=5, want_lse=False)
+    for _ in range(3):
+        assert torch.equal(a, run_gpu(case, M, 0.125, n_splits=5, want_lse=False))
+
+
 def test_relattn_bf16_longer_table():
     # A table built for a longer memory: only its last K rows are used.
     B, H, L, M = 1, 2, 128, 200

@@ -67,18 +67,36 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t *bar, uint32_t parity)
     return ok != 0;
 }
 
+// try_wait with a suspend-time hint: while the phase is incomplete the thread
+// may sleep in the barrier (it wakes when the phase completes) for up to
+// hint_ns, instead of spinning on issue slots other warps of its SM
+// sub-partition need.
+__device__ __forceinline__ bool mbar_try_wait_sleep(uint64_t *bar, uint32_t parity,
+                                                    uint32_t hint_ns)
+{
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(smem_u32(bar)), "r"(parity), "r"(hint_ns)
+        : "memory");
+    return ok != 0;
+}
+
 // Bounded wait for the phase of `parity` to complete.  Returns false if the
 // time limit passed or another thread of the block raised `abort_flag`; the
-// caller then records the failure and leaves its loop.
+// caller then records the failure and leaves its loop.  Between polls the
+// thread sleeps in the barrier (at most 20 us, so the abort flag and the limit
+// are still checked).
 __device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity,
                                           const volatile int *abort_flag, uint64_t limit_ns)
 {
     if (mbar_try_wait(bar, parity)) return true;
     const uint64_t t0 = globaltimer_ns();
     while (true) {
-#pragma unroll 1
-        for (int i = 0; i < 32; ++i)
-            if (mbar_try_wait(bar, parity)) return true;
+        if (mbar_try_wait_sleep(bar, parity, 20000u)) return true;
         if (*abort_flag) return false;
         if (globaltimer_ns() - t0 > limit_ns) return false;
     }
