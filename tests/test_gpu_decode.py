@@ -1,0 +1,82 @@
+"""GPU parity of the short-segment (decode) path against the fp64 oracle.
+
+Generation feeds one or a few new tokens per step and attends to a long cached
+memory ("Transformer-XL: Attentive Language Models Beyond a Fixed-Length
+Context", §3.2 recurrence with a longer memory at evaluation, §3.3 score,
+Appendix B reversed table).  txl_relattn_fwd takes such calls (bf16, L <= 3)
+through a split-K kernel on the CUDA cores: q + u and q + v in fp32, scores,
+softmax and P.V in fp32, so the output differs from the exact value only by
+its bf16 rounding (2^-9 relative) and fp32 sums.  Tolerances: max |err| <= 1e-2
+on O(1) outputs, rms(err)/rms(out) <= 4e-3, log-sum-exp <= 1e-3.  L = 5 and 8
+check the hand-over to the tensor-core kernel (whose P is bf16) under the same
+tolerances.
+"""
+
+import math
+
+import numpy as np
+import pytest
+import torch
+
+import transformer_xl_relative_pos_gb300 as txl
+from parity import compare, dev, heads_case, run_gpu, run_oracle
+
+pytestmark = pytest.mark.gpu
+
+TOL = 1e-2
+TOL_RMS = 4e-3
+TOL_LSE = 1e-3
+
+
+def check(case, M, n_splits=0, workspace=True, what=""):
+    scale = 1.0 / math.sqrt(64)
+    out, lse = run_gpu(case, M, scale, n_splits=n_splits, workspace=workspace)
+    want, want_lse = run_oracle(case, M, scale)
+    compare(out.float().cpu().numpy(), want, TOL, TOL_RMS, what=what)
+    compare(lse.cpu().numpy(), want_lse, TOL_LSE, what="lse " + what)
+    return out
+
+
+# Query counts of the decode kernel (1..3) and past it, memories that end
+# inside, at and just past a 128-key block, and none.
+@pytest.mark.parametrize("L", [1, 2, 3, 5, 8])
+@pytest.mark.parametrize("M", [0, 1, 127, 128, 300, 2000])
+def test_decode_matches_oracle(L, M):
+    B, H = 2, 3
+    case = heads_case(B, H, L, M, seed=1000 + 17 * L + M)
+    check(case, M, what=f"decode L={L} M={M}")
+
+
+@pytest.mark.parametrize("n_splits,workspace", [(1, False), (0, False), (3, True), (7, True),
+                                                (40, True)])
+def test_decode_key_ranges(n_splits, workspace):
+    # One block per head for all keys, the automatic choice without a
+    # workspace (no split possible), explicit splits, and more splits than
+    # 128-key chunks (capped).
+    B, H, L, M = 2, 2, 3, 1500
+    case = heads_case(B, H, L, M, seed=77 + n_splits)
+    check(case, M, n_splits=n_splits, workspace=workspace, what=f"splits {n_splits}")
+
+
+def test_decode_longer_table_and_sharp_scores():
+    # A table built for a longer memory (only its last K rows are used) and
+    # large scores, where the running-max rescale across chunks matters.
+    B, H, L, M = 1, 2, 2, 900
+    case = heads_case(B, H, L, M, seed=5, std=2.5, bias_std=2.5, extra_rows=333)
+    check(case, M, what="long table, sharp")
+
+
+def test_decode_full_memory_sampled():
+    # The long-memory evaluation shape (M = 3800) with one new token for a
+    # batch of 8 x 16 heads; every head is checked against the oracle.
+    B, H, L, M = 8, 16, 1, 3800
+    case = heads_case(B, H, L, M, seed=11)
+    check(case, M, what="M=3800 L=1")
+
+
+def test_decode_repeatable():
+    B, H, L, M = 2, 2, 3, 2000
+    case = heads_case(B, H, L, M, seed=9)
+    a = run_gpu(case, M, 0.125, want_lse=False)
+    for _ in range(2):
+        assert torch.equal(a, run_gpu(case, M, 0.125, want_lse=False))

@@ -69,13 +69,14 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn()
 }
 
 // 3-D bf16 view [outer][rows][64] with a 64 x 128 box and 128-byte swizzle.
-bool make_map(CUtensorMap *map, const void *base, long long rows, long long outer)
+bool make_map(CUtensorMap *map, const void *base, long long rows, long long outer,
+              unsigned box_rows = 128)
 {
     auto fn = encode_fn();
     if (!fn) return false;
     const cuuint64_t dims[3] = {64, (cuuint64_t)rows, (cuuint64_t)outer};
     const cuuint64_t strides[2] = {64 * 2, (cuuint64_t)rows * 64 * 2};
-    const cuuint32_t box[3] = {64, 128, 1};
+    const cuuint32_t box[3] = {64, box_rows, 1};
     const cuuint32_t estr[3] = {1, 1, 1};
     CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void *>(base), dims,
                     strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
@@ -118,6 +119,70 @@ int auto_splits(int units, int n_key_tiles)
     const int max_s = n_key_tiles / 4;
     if (s > max_s) s = max_s;
     return s < 1 ? 1 : s;
+}
+
+// Short segments (L <= 8): split-K decode kernel on the CUDA cores, then the
+// log-sum-exp merge of the key ranges when there are several.
+int relattn_decode(const void *q, const void *k, const void *v, const void *r, int r_rows,
+                   const void *u, const void *v_bias, void *out, float *lse, int B, int H, int M,
+                   int L, float scale, int n_splits, void *workspace, size_t workspace_bytes,
+                   cudaStream_t s)
+{
+    const long long K = (long long)M + L;
+    const long long BH = (long long)B * H;
+    const int per_block = txl::decode_keys_per_block();
+    const int max_splits = (int)((K + per_block - 1) / per_block);
+    int splits = n_splits;
+    if (splits == 0) {
+        // about eight blocks per SM, and no more key ranges than the workspace holds
+        const long long want = (8LL * sm_count() + BH - 1) / BH;
+        splits = (int)std::max<long long>(1, std::min<long long>(want, max_splits));
+        while (splits > 1 && (!workspace || !aligned(workspace, 256) ||
+                              workspace_bytes < workspace_bytes_for(B, H, L, 64, splits)))
+            --splits;
+    }
+    if (splits > max_splits) splits = max_splits;
+    if (splits > 1) {
+        if (!workspace || workspace_bytes < workspace_bytes_for(B, H, L, 64, splits))
+            return TXL_ERR_WORKSPACE;
+        if (!aligned(workspace, 256)) return TXL_ERR_MISALIGNED;
+    }
+    if (BH * splits > 0x7fffffffLL) return TXL_ERR_UNSUPPORTED;
+
+    txl::DecodeParams p{};
+    p.B = B;
+    p.H = H;
+    p.M = M;
+    p.L = L;
+    p.K = (int)K;
+    p.r_rows = r_rows;
+    p.r_off = r_rows - (int)K;
+    p.n_splits = splits;
+    p.scale_log2 = scale * 1.4426950408889634f;
+    p.q = static_cast<const __nv_bfloat16 *>(q);
+    p.k = static_cast<const __nv_bfloat16 *>(k);
+    p.v = static_cast<const __nv_bfloat16 *>(v);
+    p.r = static_cast<const __nv_bfloat16 *>(r);
+    p.u = static_cast<const __nv_bfloat16 *>(u);
+    p.vb = static_cast<const __nv_bfloat16 *>(v_bias);
+    p.out = static_cast<__nv_bfloat16 *>(out);
+    p.lse = lse;
+    if (splits > 1) {
+        const size_t rows = (size_t)BH * L;
+        size_t off = (size_t)splits * rows * 64 * sizeof(float);
+        off = (off + 255) & ~(size_t)255;
+        p.part_o = static_cast<float *>(workspace);
+        p.part_lse = reinterpret_cast<float *>(static_cast<char *>(workspace) + off);
+        p.lse = nullptr;
+    }
+    cudaError_t err = txl::launch_relattn_decode(p, s);
+    if (err != cudaSuccess) return TXL_ERR_CUDA;
+    if (splits > 1) {
+        err = txl::launch_relattn_combine(p.part_o, p.part_lse, p.out, lse, splits,
+                                          (int)(BH * L), s);
+        if (err != cudaSuccess) return TXL_ERR_CUDA;
+    }
+    return TXL_OK;
 }
 
 } // namespace
@@ -207,6 +272,9 @@ int txl_relattn_fwd(const void *q, const void *k, const void *v, const void *r, 
     if (lse && !aligned(lse, 4)) return TXL_ERR_MISALIGNED;
     const long long BH = (long long)B * H;
     if (BH * L > 0x7fffffffLL || BH > 0x7fffffffLL / 64) return TXL_ERR_UNSUPPORTED;
+    if (L <= txl::kDecodeMaxL)
+        return relattn_decode(q, k, v, r, r_rows, u, v_bias, out, lse, B, H, M, L, scale, n_splits,
+                              workspace, workspace_bytes, s);
     const int n_qtiles = (L + txl::kTcBM - 1) / txl::kTcBM;
     const int jmax_all = (int)std::min<long long>(K - 1, (long long)M + L - 1);
     const int n_key_tiles = jmax_all / txl::kTcBN + 1;
