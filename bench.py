@@ -82,6 +82,9 @@ def parse_args():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--e2e-steps", type=int, default=30)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--table9", action="store_true",
+                    help="per-token evaluation time, vanilla window recompute vs state reuse "
+                         "(one attention layer), instead of the headline step")
     return ap.parse_args()
 
 
@@ -515,8 +518,73 @@ def run_ours(args, world, rank, local):
     print(json.dumps(line), flush=True)
 
 
+# Evaluation speed ("Transformer-XL: Attentive Language Models Beyond a
+# Fixed-Length Context", §4.5, Table 9; the vanilla evaluation procedure is
+# §3.1): for each new token the vanilla model processes a whole window of A
+# positions from scratch (L = A queries, no memory), while Transformer-XL
+# reuses the cached states (L = 1 new query against M = A - 1 memory rows, or
+# a segment of 128 queries against A - 128 rows, per token / 128).  Attention of
+# one layer only, random bf16 operands, H = 16 heads of 64; times graph-replayed.
+TABLE9_PAPER = {800: 363, 1800: 773, 2800: 1409, 3800: 1874}
+
+
+def attn_call_us(B, H, L, M, reps=10, per=20):
+    import torch
+    import transformer_xl_relative_pos_gb300 as txl
+    dev = torch.device("cuda", 0)
+    K = M + L
+    g = torch.Generator(device=dev).manual_seed(B * 7919 + L * 31 + M)
+    mk = lambda *sh: (torch.randn(*sh, device=dev, generator=g) * 0.5).to(torch.bfloat16)
+    q, k, v, r = mk(B, H, L, 64), mk(B, H, K, 64), mk(B, H, K, 64), mk(H, K, 64)
+    u, vb = mk(H, 64) * 0.2, mk(H, 64) * 0.2
+    out = torch.empty(B, H, L, 64, device=dev, dtype=torch.bfloat16)
+    ws = torch.empty(max(txl.workspace_size(B, H, L, 64, 8), 256), dtype=torch.uint8, device=dev)
+    stream = torch.cuda.Stream()
+    call = lambda: txl.relattn_fwd(q, k, v, r, u, vb, M, 0.125, out=out, workspace=ws)
+    with torch.cuda.stream(stream):
+        for _ in range(3):
+            call()
+    torch.cuda.synchronize()
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph, stream=stream):
+        for _ in range(per):
+            call()
+    graph.replay()
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    with torch.cuda.stream(stream):
+        for _ in range(reps):
+            graph.replay()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    assert txl.device_status() == 0
+    return e0.elapsed_time(e1) * 1e3 / (reps * per)
+
+
+def run_table9(args):
+    import torch
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    for B in (1, 16):
+        for A in sorted(TABLE9_PAPER):
+            vanilla = attn_call_us(B, 16, A, 0)
+            xl_tok = attn_call_us(B, 16, 1, A - 1)
+            xl_seg = attn_call_us(B, 16, 128, A - 128) / 128
+            print(json.dumps({"table9": {
+                "attn_len": A, "B": B, "H": 16, "d_head": 64, "dtype": "bf16",
+                "vanilla_us_per_token": vanilla, "xl_decode_us_per_token": xl_tok,
+                "xl_segment128_us_per_token": xl_seg,
+                "slowdown_vs_decode": vanilla / xl_tok, "slowdown_vs_segment128": vanilla / xl_seg,
+                "paper_slowdown": TABLE9_PAPER[A],
+                "note": "one attention layer; the paper's ratio is for the whole model"}}), flush=True)
+
+
 def main():
     args = parse_args()
+    if args.table9:
+        run_table9(args)
+        return
     world, rank, local = dist_setup(args)
     if args.impl == "reference":
         run_reference(args, world, rank)

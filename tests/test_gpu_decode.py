@@ -80,3 +80,18 @@ def test_decode_repeatable():
     a = run_gpu(case, M, 0.125, want_lse=False)
     for _ in range(2):
         assert torch.equal(a, run_gpu(case, M, 0.125, want_lse=False))
+
+
+@pytest.mark.parametrize("L,M", [(800, 0), (1, 799), (128, 672)])
+def test_evaluation_speed_shapes(L, M):
+    # The three ways of computing the attention of a window of 800 positions
+    # compared by the evaluation-speed measurement (§4.5, Table 9): the vanilla
+    # window from scratch, and state reuse with one or 128 new queries.
+    B, H = 1, 2
+    case = heads_case(B, H, L, M, seed=4500 + L)
+    scale = 1.0 / math.sqrt(64)
+    out, lse = run_gpu(case, M, scale)
+    want, want_lse = run_oracle(case, M, scale)
+    tol = TOL if L <= 3 else 2e-2  # the tensor-core path rounds P to bf16
+    compare(out.float().cpu().numpy(), want, tol, 1e-2, what=f"window L={L} M={M}")
+    compare(lse.cpu().numpy(), want_lse, 2e-2, what=f"lse window L={L} M={M}")
