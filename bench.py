@@ -82,6 +82,9 @@ def parse_args():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--e2e-steps", type=int, default=30)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--stack", action="store_true",
+                    help="per-segment time of the 12-layer streaming stack (config 5), with and "
+                         "without cached projected memory keys/values, instead of the headline step")
     ap.add_argument("--table9", action="store_true",
                     help="per-token evaluation time, vanilla window recompute vs state reuse "
                          "(one attention layer), instead of the headline step")
@@ -580,8 +583,43 @@ def run_table9(args):
                 "note": "one attention layer; the paper's ratio is for the whole model"}}), flush=True)
 
 
+def run_stack(args):
+    """Per-segment time of the streaming stack on the 12-layer, 16-segment
+    workload (B=16, H=8, L=M=512, d=512), memories full, with and without the
+    cached projected memory keys/values.  Torch does the projections, LayerNorm
+    and feed-forward; the kernels do the table, the attention and the rings."""
+    import torch
+    from transformer_xl_relative_pos_gb300.model import XLStack
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    w = txl_inputs.WORKLOADS["c5_stack12_L512_M512"]
+    params = txl_inputs.draw_stack(w)
+    tokens = params["tokens"].to(dev)
+    for cache_kv in (True, False):
+        stack = XLStack(params, w.H, w.M, dev, torch.bfloat16, cache_kv=cache_kv)
+        n_warm = 3  # memories are full after the first segment (L = M)
+        for s_ in range(n_warm):
+            stack.segment(tokens[s_])
+        torch.cuda.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record()
+        n_timed = tokens.shape[0] - n_warm
+        for s_ in range(n_warm, tokens.shape[0]):
+            stack.segment(tokens[s_])
+        e1.record()
+        torch.cuda.synchronize()
+        ms = e0.elapsed_time(e1) / n_timed
+        print(json.dumps({"stack": {
+            "workload": w.name, "layers": len(params["layers"]), "B": w.B, "H": w.H, "L": w.L,
+            "M": w.M, "d_model": w.d_model, "cache_kv": cache_kv, "segments_timed": n_timed,
+            "ms_per_segment": ms, "tokens_per_s": w.B * w.L / (ms * 1e-3)}}), flush=True)
+
+
 def main():
     args = parse_args()
+    if args.stack:
+        run_stack(args)
+        return
     if args.table9:
         run_table9(args)
         return

@@ -29,11 +29,11 @@ def rounded(t, dtype=torch.bfloat16):
     return t.to(dtype).double().numpy()
 
 
-def run_stack(w, n_layer=None, n_seg=None):
+def run_stack(w, n_layer=None, n_seg=None, cache_kv=False):
     params = txl_inputs.draw_stack(w)
     if n_layer is not None:
         params["layers"] = params["layers"][:n_layer]
-    stack = XLStack(params, w.H, w.M, dev(), torch.bfloat16)
+    stack = XLStack(params, w.H, w.M, dev(), torch.bfloat16, cache_kv=cache_kv)
     tokens = params["tokens"][: (n_seg or w.n_seg)]
     for s in range(tokens.shape[0] - 1):
         stack.segment(tokens[s])
@@ -47,14 +47,17 @@ def run_stack(w, n_layer=None, n_seg=None):
     return h_gpu, h_or, stack, mems
 
 
-def test_small_stack_memory_fill_and_wrap():
+@pytest.mark.parametrize("cache_kv", [True, False])
+def test_small_stack_memory_fill_and_wrap(cache_kv):
     # 3 layers, L=64 and M=100: the memories fill over two segments, then wrap.
+    # With cache_kv the memory's keys and values come from the projected rings,
+    # without it they are re-projected from the hidden-state memory.
     base = txl_inputs.WORKLOADS["c5_stack12_L512_M512"]
     w = txl_inputs.Workload("small_stack", B=2, H=2, dh=64, L=64, M=100, d_model=128,
                             dtype="bf16", seed=41, d_ff=256, n_layer=3, n_seg=5, vocab=base.vocab)
-    h_gpu, h_or, stack, mems = run_stack(w)
+    h_gpu, h_or, stack, mems = run_stack(w, cache_kv=cache_kv)
     assert all(m.shape[1] == 100 for m in mems)
-    compare(h_gpu, h_or, 6e-2, 1.5e-2, what="small stack")
+    compare(h_gpu, h_or, 6e-2, 1.5e-2, what=f"small stack cache_kv={cache_kv}")
 
 
 def test_c5_stack12_last_segment():
@@ -62,3 +65,27 @@ def test_c5_stack12_last_segment():
     h_gpu, h_or, stack, mems = run_stack(w)
     assert len(mems) == 12 and all(m.shape == (w.B, w.M, w.d_model) for m in mems)
     compare(h_gpu, h_or, 1e-1, 2e-2, what="c5 top layer")
+
+
+def test_cached_kv_rings_match_projected_memory():
+    # After the memories have filled and wrapped, each layer's key and value
+    # rings hold the projections of that layer's hidden-state memory.
+    from transformer_xl_relative_pos_gb300 import _lib as txl
+    from transformer_xl_relative_pos_gb300.model import project_heads
+    base = txl_inputs.WORKLOADS["c5_stack12_L512_M512"]
+    w = txl_inputs.Workload("ring_stack", B=2, H=2, dh=64, L=48, M=100, d_model=128,
+                            dtype="bf16", seed=43, d_ff=256, n_layer=3, n_seg=4, vocab=base.vocab)
+    params = txl_inputs.draw_stack(w)
+    stack = XLStack(params, w.H, w.M, dev(), torch.bfloat16, cache_kv=True)
+    for s in range(w.n_seg):
+        stack.segment(params["tokens"][s])
+    for n, (mem, lay) in enumerate(zip(stack.memories(), stack.layers)):
+        ks, vs = stack.kv_states[n]
+        empty = torch.empty(w.B * w.H, 0, w.dh, dtype=torch.bfloat16, device=dev())
+        k_ring = txl.mem_concat(stack.kmems[n], ks, empty).view(w.B, w.H, -1, w.dh)
+        v_ring = txl.mem_concat(stack.vmems[n], vs, empty).view(w.B, w.H, -1, w.dh)
+        k_mem = project_heads(mem, lay["W_kE"], w.H)
+        v_mem = project_heads(mem, lay["W_v"], w.H)
+        # the same bf16 products, possibly summed in another order by the GEMM
+        compare(k_ring.float().cpu().numpy(), k_mem.float().cpu().numpy(), 5e-3, what=f"k ring {n}")
+        compare(v_ring.float().cpu().numpy(), v_mem.float().cpu().numpy(), 5e-3, what=f"v ring {n}")

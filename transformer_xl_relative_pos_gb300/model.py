@@ -10,6 +10,14 @@
                                                            residual, LayerNorm)
 and the memory of each layer advances to the newest M states of its input
 (§3.2)                                                  -> mem_update (kernel).
+With ``cache_kv`` the stack also keeps, per layer, rings of the memory's
+projected keys and values: the memory rows and W_kE, W_v do not change at
+evaluation, so k and v of the memory are the ones projected when those states
+were the segment, and each segment projects only its own L rows (2·M·d²
+multiply-adds saved per layer and projection); the rings are the same kernels
+on a [B·H, M, d_head] view.  It is off by default: the attention takes k and v
+as one contiguous tensor, so the rings are copied out every segment, and on
+this hardware that copy costs more than re-projecting the memory.
 The relative table r = W_kR R is built from rel_pos_emb (kernel) and one matmul
 and is cached per (layer, K): R has no parameters and W_kR is fixed at
 evaluation.
@@ -67,8 +75,10 @@ class XLStack:
     to ``device`` in ``dtype``.  ``segment(tokens)`` processes one segment
     [B, L] and returns the top layer's states [B, L, d] (``dtype``)."""
 
-    def __init__(self, params: dict, H: int, M: int, device, dtype=torch.bfloat16):
+    def __init__(self, params: dict, H: int, M: int, device, dtype=torch.bfloat16,
+                 cache_kv: bool = False):
         self.H, self.M, self.dtype, self.device = H, M, dtype, torch.device(device)
+        self.cache_kv = cache_kv
         to = lambda t: t.to(device=self.device, dtype=dtype).contiguous()
         self.emb = to(params["emb"])
         self.u = to(params["u"])
@@ -85,6 +95,13 @@ class XLStack:
         self.mems = [torch.zeros(B, self.M, self.d, dtype=self.dtype, device=self.device)
                      for _ in self.layers]
         self.states = [txl.MemState(0, 0, self.M) for _ in self.layers]
+        # projected memory: [B*H, M, dh] rings of k and v per layer, each with its
+        # own ring state (they advance exactly as the hidden-state ring)
+        ring = lambda: torch.zeros(B * self.H, self.M, self.dh, dtype=self.dtype, device=self.device)
+        self.kmems = [ring() for _ in self.layers] if self.cache_kv else None
+        self.vmems = [ring() for _ in self.layers] if self.cache_kv else None
+        self.kv_states = ([(txl.MemState(0, 0, self.M), txl.MemState(0, 0, self.M))
+                           for _ in self.layers] if self.cache_kv else None)
 
     def memories(self):
         """Each layer's memory in logical order (oldest first), [B, fill, d]."""
@@ -111,10 +128,18 @@ class XLStack:
         for n, lay in enumerate(self.layers):
             st = self.states[n]
             M_cur = st.fill
-            ext = txl.mem_concat(self.mems[n], st, h)
             q = project_heads(h, lay["W_q"], self.H)
-            k = project_heads(ext, lay["W_kE"], self.H)
-            v = project_heads(ext, lay["W_v"], self.H)
+            if self.cache_kv:
+                # only the segment's rows are projected; the memory's come from the rings
+                ks, vs = self.kv_states[n]
+                k_new = project_heads(h, lay["W_kE"], self.H).view(B * self.H, L, self.dh)
+                v_new = project_heads(h, lay["W_v"], self.H).view(B * self.H, L, self.dh)
+                k = txl.mem_concat(self.kmems[n], ks, k_new).view(B, self.H, M_cur + L, self.dh)
+                v = txl.mem_concat(self.vmems[n], vs, v_new).view(B, self.H, M_cur + L, self.dh)
+            else:
+                ext = txl.mem_concat(self.mems[n], st, h)
+                k = project_heads(ext, lay["W_kE"], self.H)
+                v = project_heads(ext, lay["W_v"], self.H)
             a = txl.relattn_fwd(q, k, v, self._r(n, M_cur + L), self.u, self.v_bias, M_cur,
                                 self.scale)
             a = a.transpose(1, 2).reshape(B, L, -1)
@@ -122,5 +147,8 @@ class XLStack:
             f = torch.relu(o.to(self.dtype) @ lay["W_1"].t() + lay["b_1"])
             h_next = layer_norm(o + (f @ lay["W_2"].t()).float() + lay["b_2"].float())
             txl.mem_update(self.mems[n], st, h)
+            if self.cache_kv:
+                txl.mem_update(self.kmems[n], ks, k_new)
+                txl.mem_update(self.vmems[n], vs, v_new)
             h = h_next.to(self.dtype)
         return h
