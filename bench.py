@@ -51,8 +51,8 @@ import txl_inputs  # noqa: E402
 PROFILED_TRAFFIC = {
     "workload": "c3_word_large_L128_M1600",
     "sources": ("relattn_tc.cu", "ptx.cuh", "kernels.h"),
-    "sha256": "5312f5377e1431a0c546e71316ec5d40db08ea593187eaaae6bc9c9f561e2bf1",
-    "bytes_per_launch": 121090304 + 2868480,
+    "sha256": "81bbd42e24f3910cf9279abb67d751efeafcad264156e659d2f04c93c6b6adab",
+    "bytes_per_launch": 121080576 + 2516992,
 }
 
 

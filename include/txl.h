@@ -109,7 +109,9 @@ size_t txl_relattn_workspace_size(int B, int H, int L, int dh, int n_splits);
  *   v and r must be 16-byte aligned.  Segments of L <= 3 queries (decoding a
  *   few new tokens against a long memory) take a split-K kernel on the CUDA
  *   cores instead, all arithmetic in fp32 (no bf16 rounding of P); n_splits
- *   then counts key ranges of whole 128-key blocks per (b, h).
+ *   then counts key ranges per (b, h), each a whole number of 32-key chunks,
+ *   at most one per 128 keys (larger requests are capped, ranges that would
+ *   hold no key are dropped).
  * dtype TXL_F32: every tensor is fp32 and the arithmetic is fp32 on the CUDA
  *   cores (no TF32).  dh must be 64.
  * M >= 0, L >= 1, r_rows >= K, B >= 1, H >= 1.

@@ -19,10 +19,10 @@ INCLUDE = os.path.join(ROOT, "include")
 BUILD_DIR = os.path.join(PKG, "_build")
 LIB_PATH = os.path.join(PKG, "libtxl_gb300.so")
 
-SOURCES = ["txl_api.cu", "relattn_tc.cu", "relattn_decode.cu", "relattn_f32.cu", "relpos.cu",
-           "mem.cu", "relattn_noalloc.cu"]
-HEADERS = [os.path.join(CSRC, "kernels.h"), os.path.join(CSRC, "ptx.cuh"),
-           os.path.join(INCLUDE, "txl.h")]
+SOURCES = ["txl_api.cu", "relattn_tc.cu", "relattn_combine.cu", "relattn_decode.cu",
+           "relattn_f32.cu", "relpos.cu", "mem.cu", "relattn_noalloc.cu"]
+HEADERS = [os.path.join(CSRC, "kernels.h"), os.path.join(CSRC, "decode.h"),
+           os.path.join(CSRC, "ptx.cuh"), os.path.join(INCLUDE, "txl.h")]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 

@@ -42,33 +42,6 @@ cudaError_t launch_relattn_combine(const float *part_o, const float *part_lse,
                                    __nv_bfloat16 *out, float *lse, int n_splits, int rows,
                                    cudaStream_t s);
 
-// Short-segment (decode) kernel: L <= kDecodeMaxL queries per (batch, head);
-// the keys are split into n_splits ranges of whole 128-key blocks.
-constexpr int kDecodeMaxL = 3;
-
-struct DecodeParams {
-    int B, H, M, L, K;
-    int r_rows;         // table rows per head (>= K)
-    int r_off;          // r_rows - K
-    int n_splits;       // key ranges per (batch, head); > 1 writes partials
-    float scale_log2;   // scale * log2(e)
-    const __nv_bfloat16 *q;   // [B][H][L][64]
-    const __nv_bfloat16 *k;   // [B][H][K][64]
-    const __nv_bfloat16 *v;   // [B][H][K][64]
-    const __nv_bfloat16 *r;   // [H][r_rows][64]
-    const __nv_bfloat16 *u;   // [H][64]
-    const __nv_bfloat16 *vb;  // [H][64]
-    __nv_bfloat16 *out;       // [B][H][L][64]            (n_splits == 1)
-    float *lse;               // [B][H][L] natural log or null
-    float *part_o;            // [n_splits][B*H*L][64]   (n_splits > 1)
-    float *part_lse;          // [n_splits][B*H*L], log2 domain
-};
-
-// Keys one decode block covers per pass (its key range is a multiple of this).
-int decode_keys_per_block();
-
-cudaError_t launch_relattn_decode(const DecodeParams &p, cudaStream_t s);
-
 struct F32Params {
     const float *q, *k, *v, *r, *u, *vb;
     float *out, *lse;

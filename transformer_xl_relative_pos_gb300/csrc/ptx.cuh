@@ -136,6 +136,19 @@ __device__ __forceinline__ void tma_load_3d_hint(void *smem_dst, const CUtensorM
         : "memory");
 }
 
+// Contiguous global -> shared copy (cp.async.bulk) completing on an mbarrier,
+// with an L2 cache-policy hint.  Both addresses 16-byte aligned, bytes a
+// multiple of 16.
+__device__ __forceinline__ void bulk_load_hint(void *smem_dst, const void *gmem_src, uint32_t bytes,
+                                               uint64_t *bar, uint64_t policy)
+{
+    asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint"
+                 " [%0], [%1], %2, [%3], %4;" ::"r"(smem_u32(smem_dst)),
+                 "l"(reinterpret_cast<uint64_t>(gmem_src)), "r"(bytes), "r"(smem_u32(bar)),
+                 "l"(policy)
+                 : "memory");
+}
+
 // Pull a 3-D tile into L2 ahead of its shared-memory load (no completion signal).
 __device__ __forceinline__ void tma_prefetch_3d(const CUtensorMap *map, int c0, int c1, int c2)
 {

@@ -6,10 +6,13 @@
 //
 // With so few query rows the work is reading K, V and the table once: the
 // kernel is HBM-bound and runs on the CUDA cores in fp32.  Every warp works on
-// its own: it takes 32 keys at a time, and lane l holds dimensions 2l and 2l+1
-// of those keys' k and v rows and of the L + 31 table rows they need, read
-// straight from global memory (one 128-byte line per row and warp).  For query
-// row i and key j the score is
+// its own: it takes 32 keys at a time (a chunk) and streams each chunk's k and
+// v rows and the L + 31 table rows they need into a ring of shared-memory
+// stages with contiguous bulk copies (cp.async.bulk, one mbarrier per stage),
+// so that the next chunk's bytes are in flight while the current one is
+// computed and no registers are held by loads.  Lane l reads dimensions 2l and
+// 2l+1 of every row (one 128-byte row per warp access, conflict-free).  For
+// query row i and key j the score is
 //   A_ij = (q_i + u).k_j + (q_i + v).r[r_off + L-1 - i + j]        (j <= M + i)
 // where r is the reversed table (row K-1-d holds distance d; r_off = r_rows-K):
 // the Appendix B left shift by L-1-i is the table row index.  q + u and q + v
@@ -21,21 +24,46 @@
 // log2-sum-exp for the merge kernel.  The per-key work grows with L while the
 // bytes do not: from L = 4 on the tensor-core kernel is the faster path.
 #include "kernels.h"
+#include "decode.h"
 #include "ptx.cuh"
 
 namespace txl {
 namespace {
 
+using namespace ptx;
+
 constexpr int DH = kTcDH;         // 64: lane l owns dimensions 2l, 2l+1
 constexpr int WARPS = 4;          // warps per block
-constexpr int GK = 32;            // keys per warp step
+constexpr int GK = 32;            // keys per chunk
 constexpr int LMAX = kDecodeMaxL;
+constexpr int NSTG = 2;           // ring stages per warp
+constexpr int ROWB = DH * 2;      // bytes of one bf16 row
+constexpr int RROWS = GK + LMAX - 1;
+constexpr int ST_K = 0;                         // stage layout: 32 k rows,
+constexpr int ST_V = ST_K + GK * ROWB;          // 32 v rows,
+constexpr int ST_R = ST_V + GK * ROWB;          // up to 34 table rows
+constexpr int STAGE = ST_R + RROWS * ROWB;      // 12544 bytes
+constexpr int RING = NSTG * STAGE;              // per warp
+constexpr int OFF_BAR = WARPS * RING;
+constexpr int OFF_MERGE = OFF_BAR + WARPS * NSTG * 8;
+constexpr int MERGE_BYTES = WARPS * LMAX * (2 * 4 + 32 * 8);
+constexpr int OFF_FLAG = OFF_MERGE + MERGE_BYTES;
+constexpr int SMEM_BYTES = OFF_FLAG + 16;
+
+static_assert(STAGE % 16 == 0 && RING % 16 == 0, "bulk copies need 16-byte aligned stages");
 
 __device__ __forceinline__ float ex2f(float x)
 {
     float y;
     asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
     return y;
+}
+
+__device__ __forceinline__ uint32_t ld_shared_u32(uint32_t addr)
+{
+    uint32_t v;
+    asm volatile("ld.shared.b32 %0, [%1];" : "=r"(v) : "r"(addr));
+    return v;
 }
 
 __device__ __forceinline__ float lo_f(uint32_t w) { return __uint_as_float(w << 16); }
@@ -62,18 +90,56 @@ __device__ __forceinline__ float transpose_reduce(float (&v)[GK], int lane)
 template <int L>
 __global__ void __launch_bounds__(WARPS * 32) relattn_decode_kernel(const DecodeParams p)
 {
+    extern __shared__ __align__(128) uint8_t smem[];
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int split = blockIdx.x % p.n_splits;
     const int bh = blockIdx.x / p.n_splits;
     const int h = bh % p.H;
     const int K = p.K;
-    // Key range of this block: a whole number of warp steps.
-    const int span = ((K + p.n_splits - 1) / p.n_splits + WARPS * GK - 1) / (WARPS * GK) * (WARPS * GK);
+    // Key range of this block: a whole number of 32-key chunks, dealt to the
+    // block's warps in turn (chunk c to warp c mod 4).
+    const int span = decode_span(K, p.n_splits);
     const int k_begin = split * span, k_end = min(K, k_begin + span);
+    const int n_chunks = (k_end > k_begin) ? (k_end - k_begin + GK - 1) / GK : 0;
+    const int n_mine = (n_chunks > warp) ? (n_chunks - warp + WARPS - 1) / WARPS : 0;
 
-    const uint32_t *kw = reinterpret_cast<const uint32_t *>(p.k) + (size_t)bh * K * (DH / 2) + lane;
-    const uint32_t *vw = reinterpret_cast<const uint32_t *>(p.v) + (size_t)bh * K * (DH / 2) + lane;
-    const uint32_t *rw = reinterpret_cast<const uint32_t *>(p.r) + (size_t)h * p.r_rows * (DH / 2) + lane;
+    const uint8_t *kg = reinterpret_cast<const uint8_t *>(p.k) + (size_t)bh * K * ROWB;
+    const uint8_t *vg = reinterpret_cast<const uint8_t *>(p.v) + (size_t)bh * K * ROWB;
+    const uint8_t *rg = reinterpret_cast<const uint8_t *>(p.r) + ((size_t)h * p.r_rows + p.r_off) * ROWB;
+    uint8_t *ring = smem + warp * RING;
+    uint64_t *bars = reinterpret_cast<uint64_t *>(smem + OFF_BAR) + warp * NSTG;
+    volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + OFF_FLAG);
+
+    // Zero this warp's ring once: rows a chunk does not copy (past the key
+    // range) are then finite, so their zero probabilities give exact zeros.
+    for (int o = lane * 16; o < RING; o += 32 * 16)
+        *reinterpret_cast<uint4 *>(ring + o) = make_uint4(0, 0, 0, 0);
+    if (threadIdx.x == 0) *abort_flag = 0;
+    if (lane == 0) {
+        for (int s = 0; s < NSTG; ++s) mbar_init(bars + s, 1);
+        fence_barrier_init();
+    }
+    fence_proxy_async_smem();  // the zeros before the copies that overwrite them
+    __syncthreads();
+
+    const uint64_t pol_stream = policy_evict_first();  // k, v: read once
+    const uint64_t pol_keep = policy_evict_last();     // table: shared by the batch
+    // Copies of this warp's chunk n into stage n % NSTG (lane 0).  Only rows of
+    // the block's range and of the table are copied.
+    auto issue = [&](int n) {
+        const int j0 = k_begin + (warp + WARPS * n) * GK;
+        uint8_t *stg = ring + (n % NSTG) * STAGE;
+        const int rows = min(GK, k_end - j0);
+        const int rrows = min(min(GK + L - 1, K - j0), k_end - j0 + L - 1);
+        mbar_arrive_expect_tx(bars + n % NSTG, (uint32_t)(2 * rows + rrows) * ROWB);
+        bulk_load_hint(stg + ST_K, kg + (size_t)j0 * ROWB, rows * ROWB, bars + n % NSTG, pol_stream);
+        bulk_load_hint(stg + ST_V, vg + (size_t)j0 * ROWB, rows * ROWB, bars + n % NSTG, pol_stream);
+        bulk_load_hint(stg + ST_R, rg + (size_t)j0 * ROWB, rrows * ROWB, bars + n % NSTG, pol_keep);
+    };
+    int issued = 0;
+    if (lane == 0)
+        for (; issued < min(NSTG, n_mine); ++issued) issue(issued);
+    issued = __shfl_sync(0xffffffffu, issued, 0);
 
     // q + u and q + v, this lane's two dimensions, every row.
     float qu0[L], qu1[L], qv0[L], qv1[L];
@@ -99,20 +165,29 @@ __global__ void __launch_bounds__(WARPS * 32) relattn_decode_kernel(const Decode
         a1[i] = 0.f;
     }
 
-    for (int j0 = k_begin + warp * GK; j0 < k_end; j0 += WARPS * GK) {
-        // ---- this lane's dimensions of the 32 keys and their table rows ----
+    bool ok = true;
+    for (int n = 0; n < n_mine; ++n) {
+        const int j0 = k_begin + (warp + WARPS * n) * GK;
+        ok = __all_sync(0xffffffffu, mbar_wait(bars + n % NSTG, (n / NSTG) & 1, abort_flag, p.wait_ns));
+        if (!ok) break;
+        const uint32_t stg = smem_u32(ring + (n % NSTG) * STAGE) + 4 * lane;
+
+        // ---- this lane's words of the chunk's rows ---------------------------
         uint32_t kk[GK], vv[GK], rr[GK + L - 1];
 #pragma unroll
         for (int e = 0; e < GK; ++e) {
-            const int j = min(j0 + e, K - 1);  // rows past K are loaded clamped and masked
-            kk[e] = __ldcs(kw + (size_t)j * (DH / 2));
-            vv[e] = __ldcs(vw + (size_t)j * (DH / 2));
+            kk[e] = ld_shared_u32(stg + ST_K + e * ROWB);
+            vv[e] = ld_shared_u32(stg + ST_V + e * ROWB);
         }
-        // table rows r_off + j0 + e, e in [0, 32 + L - 1): row for (i, j) is e = j - j0 + L-1-i
+        // table row for (i, j) is e = j - j0 + L-1-i
 #pragma unroll
-        for (int e = 0; e < GK + L - 1; ++e) {
-            const int row = min(p.r_off + j0 + e, p.r_rows - 1);
-            rr[e] = __ldg(rw + (size_t)row * (DH / 2));
+        for (int e = 0; e < GK + L - 1; ++e) rr[e] = ld_shared_u32(stg + ST_R + e * ROWB);
+        // The stage is read: order the reads before the copy that refills it.
+        fence_proxy_async_smem();
+        __syncwarp();
+        if (n + NSTG < n_mine) {
+            if (lane == 0) issue(n + NSTG);
+            ++issued;
         }
 
 #pragma unroll
@@ -154,32 +229,45 @@ __global__ void __launch_bounds__(WARPS * 32) relattn_decode_kernel(const Decode
             a1[i] = b1;
         }
     }
+    if (!ok) {
+        // Time-out: record it, and let this warp's copies still in flight land
+        // before the block's shared memory is released (bounded waits).
+        if (lane == 0) {
+            *abort_flag = 1;
+            atomicOr(p.status, 1u);
+            const int zero = 0;
+            for (int n = max(0, issued - NSTG); n < issued; ++n)
+                mbar_wait(bars + n % NSTG, (n / NSTG) & 1, &zero, p.wait_ns);
+        }
+        __syncwarp();
+    }
 
     // ---- merge the block's warps: w = 2^(m_w - max), out = sum w a / sum w l ----
-    __shared__ float sm_m[WARPS][LMAX], sm_l[WARPS][LMAX];
-    __shared__ float2 sm_a[WARPS][LMAX][32];
+    float *sm_m = reinterpret_cast<float *>(smem + OFF_MERGE);         // [WARPS][LMAX]
+    float *sm_l = sm_m + WARPS * LMAX;                                   // [WARPS][LMAX]
+    float2 *sm_a = reinterpret_cast<float2 *>(sm_l + WARPS * LMAX);      // [WARPS][LMAX][32]
 #pragma unroll
     for (int i = 0; i < L; ++i) {
         if (lane == 0) {
-            sm_m[warp][i] = m[i];
-            sm_l[warp][i] = l[i];
+            sm_m[warp * LMAX + i] = m[i];
+            sm_l[warp * LMAX + i] = l[i];
         }
-        sm_a[warp][i][lane] = make_float2(a0[i], a1[i]);
+        sm_a[(warp * LMAX + i) * 32 + lane] = make_float2(a0[i], a1[i]);
     }
     __syncthreads();
     for (int i = warp; i < L; i += WARPS) {
         float mx = -INFINITY;
 #pragma unroll
-        for (int w = 0; w < WARPS; ++w) mx = fmaxf(mx, sm_m[w][i]);
+        for (int w = 0; w < WARPS; ++w) mx = fmaxf(mx, sm_m[w * LMAX + i]);
         float ls = 0.f, o0 = 0.f, o1 = 0.f;
         if (mx != -INFINITY) {
 #pragma unroll
             for (int w = 0; w < WARPS; ++w) {
-                const float mw = sm_m[w][i];
+                const float mw = sm_m[w * LMAX + i];
                 if (mw == -INFINITY) continue;
                 const float sw = ex2f(mw - mx);
-                ls += sw * sm_l[w][i];
-                const float2 aw = sm_a[w][i][lane];
+                ls += sw * sm_l[w * LMAX + i];
+                const float2 aw = sm_a[(w * LMAX + i) * 32 + lane];
                 o0 = fmaf(sw, aw.x, o0);
                 o1 = fmaf(sw, aw.y, o1);
             }
@@ -200,17 +288,61 @@ __global__ void __launch_bounds__(WARPS * 32) relattn_decode_kernel(const Decode
 }
 
 template <int L>
+cudaError_t set_smem_l()
+{
+    return cudaFuncSetAttribute(relattn_decode_kernel<L>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                SMEM_BYTES);
+}
+
+// The dynamic shared-memory attribute of the three instances, once per device.
+cudaError_t ensure_smem_attr()
+{
+    static bool done[64] = {};
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    if (dev >= 0 && dev < 64 && done[dev]) return cudaSuccess;
+    if ((e = set_smem_l<1>()) != cudaSuccess) return e;
+    if ((e = set_smem_l<2>()) != cudaSuccess) return e;
+    if ((e = set_smem_l<3>()) != cudaSuccess) return e;
+    if (dev >= 0 && dev < 64) done[dev] = true;
+    return cudaSuccess;
+}
+
+template <int L>
+int blocks_per_sm_l()
+{
+    int n = 0;
+    if (ensure_smem_attr() != cudaSuccess ||
+        cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, relattn_decode_kernel<L>, WARPS * 32,
+                                                      SMEM_BYTES) != cudaSuccess)
+        return 1;
+    return n < 1 ? 1 : n;
+}
+
+template <int L>
 cudaError_t launch_l(const DecodeParams &p, cudaStream_t s)
 {
     const long long blocks = (long long)p.B * p.H * p.n_splits;
     if (blocks <= 0 || blocks > 0x7fffffffLL) return cudaErrorInvalidValue;
-    relattn_decode_kernel<L><<<(unsigned)blocks, WARPS * 32, 0, s>>>(p);
+    cudaError_t e = ensure_smem_attr();
+    if (e != cudaSuccess) return e;
+    relattn_decode_kernel<L><<<(unsigned)blocks, WARPS * 32, SMEM_BYTES, s>>>(p);
     return cudaGetLastError();
 }
 
 } // namespace
 
-int decode_keys_per_block() { return WARPS * GK; }
+int decode_chunk_keys() { return GK; }
+
+int decode_blocks_per_sm(int L)
+{
+    static int cache[kDecodeMaxL + 1] = {};  // per query count; one device per process
+    if (L < 1 || L > kDecodeMaxL) return 1;
+    if (!cache[L]) cache[L] = (L == 1) ? blocks_per_sm_l<1>() : (L == 2) ? blocks_per_sm_l<2>()
+                                                                           : blocks_per_sm_l<3>();
+    return cache[L];
+}
 
 cudaError_t launch_relattn_decode(const DecodeParams &p, cudaStream_t s)
 {

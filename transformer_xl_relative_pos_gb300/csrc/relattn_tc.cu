@@ -814,35 +814,6 @@ __global__ void __launch_bounds__(256, 1)
     }
 }
 
-// Merge of split-key partial results: out = sum_s w_s o_s / sum_s w_s with
-// w_s = 2^(lse_s - max lse).  One warp per query row, two columns per lane.
-__global__ void relattn_combine_kernel(const float *__restrict__ part_o,
-                                       const float *__restrict__ part_lse,
-                                       __nv_bfloat16 *__restrict__ out, float *__restrict__ lse,
-                                       int n_splits, int rows)
-{
-    const int row = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
-    const int lane = threadIdx.x & 31;
-    if (row >= rows) return;
-    float mx = -INFINITY;
-    for (int s = 0; s < n_splits; ++s) mx = fmaxf(mx, part_lse[(size_t)s * rows + row]);
-    float wsum = 0.f, a0 = 0.f, a1 = 0.f;
-    for (int s = 0; s < n_splits; ++s) {
-        const float l = part_lse[(size_t)s * rows + row];
-        if (l == -INFINITY) continue;
-        const float w = exp2f(l - mx);
-        const float2 o = reinterpret_cast<const float2 *>(part_o + ((size_t)s * rows + row) * DH)[lane];
-        wsum += w;
-        a0 += w * o.x;
-        a1 += w * o.y;
-    }
-    const float inv = (wsum > 0.f) ? 1.f / wsum : 0.f;
-    reinterpret_cast<__nv_bfloat162 *>(out + (size_t)row * DH)[lane] =
-        __floats2bfloat162_rn(a0 * inv, a1 * inv);
-    if (lse && lane == 0)
-        lse[row] = (wsum > 0.f) ? (mx + log2f(wsum)) * 0.69314718055994531f : -INFINITY;
-}
-
 // Waits on a barrier nothing will complete; the bounded wait must give up and
 // record the time-out.  Used to test that path without hanging the device.
 __global__ void wait_probe_kernel(unsigned int *status, unsigned long long wait_ns)
@@ -888,17 +859,6 @@ cudaError_t launch_relattn_tc(const CUtensorMap &tm_q, const CUtensorMap &tm_k,
 cudaError_t launch_wait_probe(unsigned int *status, unsigned long long wait_ns, cudaStream_t s)
 {
     wait_probe_kernel<<<1, 32, 0, s>>>(status, wait_ns);
-    return cudaGetLastError();
-}
-
-cudaError_t launch_relattn_combine(const float *part_o, const float *part_lse,
-                                   __nv_bfloat16 *out, float *lse, int n_splits, int rows,
-                                   cudaStream_t s)
-{
-    const int warps = 8;
-    const int blocks = (rows + warps - 1) / warps;
-    relattn_combine_kernel<<<blocks, warps * 32, 0, s>>>(part_o, part_lse, out, lse, n_splits,
-                                                         rows);
     return cudaGetLastError();
 }
 

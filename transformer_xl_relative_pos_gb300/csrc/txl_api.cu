@@ -10,6 +10,7 @@
 #include <cudaTypedefs.h>
 
 #include "kernels.h"
+#include "decode.h"
 #include "txl.h"
 
 namespace {
@@ -130,18 +131,24 @@ int relattn_decode(const void *q, const void *k, const void *v, const void *r, i
 {
     const long long K = (long long)M + L;
     const long long BH = (long long)B * H;
-    const int per_block = txl::decode_keys_per_block();
-    const int max_splits = (int)((K + per_block - 1) / per_block);
+    // At most one split per 128 keys (four 32-key chunks), and only splits that
+    // own keys.
+    const int max_splits = (int)((K + 127) / 128);
     int splits = n_splits;
     if (splits == 0) {
-        // about eight blocks per SM, and no more key ranges than the workspace holds
-        const long long want = (8LL * sm_count() + BH - 1) / BH;
-        splits = (int)std::max<long long>(1, std::min<long long>(want, max_splits));
+        // One wave of resident blocks: each block streams its key range
+        // through its warps' copy rings, so long ranges amortise the first
+        // copies' latency, and a second, partly filled wave would cost a full
+        // block time.  No more key ranges than the workspace holds.
+        const long long slots = (long long)sm_count() * txl::decode_blocks_per_sm(L);
+        splits = (int)std::max<long long>(1, std::min<long long>(slots / BH, max_splits));
         while (splits > 1 && (!workspace || !aligned(workspace, 256) ||
                               workspace_bytes < workspace_bytes_for(B, H, L, 64, splits)))
             --splits;
     }
     if (splits > max_splits) splits = max_splits;
+    // Drop splits that would own no keys once ranges are rounded to chunks.
+    while (splits > 1 && (long long)(splits - 1) * txl::decode_span((int)K, splits) >= K) --splits;
     if (splits > 1) {
         if (!workspace || workspace_bytes < workspace_bytes_for(B, H, L, 64, splits))
             return TXL_ERR_WORKSPACE;
@@ -149,7 +156,13 @@ int relattn_decode(const void *q, const void *k, const void *v, const void *r, i
     }
     if (BH * splits > 0x7fffffffLL) return TXL_ERR_UNSUPPORTED;
 
+    cudaError_t serr = cudaSuccess;
+    unsigned int *status = status_word(&serr);
+    if (!status) return TXL_ERR_CUDA;
+
     txl::DecodeParams p{};
+    p.status = status;
+    p.wait_ns = g_wait_ns;
     p.B = B;
     p.H = H;
     p.M = M;
