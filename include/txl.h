@@ -106,7 +106,7 @@ size_t txl_relattn_workspace_size(int B, int H, int L, int dh, int n_splits);
  *   out [B][H][L][dh]        lse [B][H][L] fp32, natural log (may be NULL)
  * dtype TXL_BF16: q, k, v, r, u, v_bias and out are bf16; scores, softmax and
  *   accumulation are fp32 on the tensor cores (tcgen05).  dh must be 64; q, k,
- *   v and r must be 16-byte aligned.  Segments of L <= 3 queries (decoding a
+ *   v and r must be 16-byte aligned.  Segments of L <= 6 queries (decoding a
  *   few new tokens against a long memory) take a split-K kernel on the CUDA
  *   cores instead, all arithmetic in fp32 (no bf16 rounding of P); n_splits
  *   then counts key ranges per (b, h), each a whole number of 32-key chunks,

@@ -8,7 +8,7 @@ namespace txl {
 
 // Short-segment (decode) kernel: L <= kDecodeMaxL queries per (batch, head);
 // the keys are split into n_splits ranges of whole 32-key chunks.
-constexpr int kDecodeMaxL = 3;
+constexpr int kDecodeMaxL = 6;
 
 struct DecodeParams {
     int B, H, M, L, K;

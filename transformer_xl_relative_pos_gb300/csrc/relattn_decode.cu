@@ -1,4 +1,4 @@
-// Relative-position attention for short segments (L <= 3 queries) against a
+// Relative-position attention for short segments (L <= 6 queries) against a
 // long memory: the decode pattern of generation, one or a few new tokens per
 // step attending to the cached M states ("Transformer-XL: Attentive Language
 // Models Beyond a Fixed-Length Context", §3.2 recurrence and evaluation with a
@@ -10,29 +10,34 @@
 // v rows and the L + 31 table rows they need into a ring of shared-memory
 // stages with contiguous bulk copies (cp.async.bulk, one mbarrier per stage),
 // so that the next chunk's bytes are in flight while the current one is
-// computed and no registers are held by loads.  Lane l reads dimensions 2l and
-// 2l+1 of every row (one 128-byte row per warp access, conflict-free).  For
-// query row i and key j the score is
+// computed and no registers are held by loads.  The warp's lanes form four
+// groups of eight; group g takes keys 8g..8g+7 of the chunk and lane s of a
+// group dimensions 8s..8s+7 (16-byte shared-memory reads).  For query row i
+// and key j the score is
 //   A_ij = (q_i + u).k_j + (q_i + v).r[r_off + L-1 - i + j]        (j <= M + i)
 // where r is the reversed table (row K-1-d holds distance d; r_off = r_rows-K):
 // the Appendix B left shift by L-1-i is the table row index.  q + u and q + v
-// are formed in fp32 and never rounded.  Each lane sums its two dimensions of
-// all 32 keys; a transposing butterfly over the warp leaves lane l with the
-// whole score of key l.  Online softmax per row, P.V with the probabilities
-// broadcast by shuffles, then the block's warps merge their partial results
+// are formed in fp32 and never rounded (packed f32x2 FMAs).  Each lane sums its
+// eight dimensions of its group's eight keys; a transposing butterfly over the
+// group leaves lane l with the whole score of key l.  Online softmax per row
+// over the warp, P.V with each group's probabilities broadcast by shuffles
+// into per-group partial outputs (summed over the groups at the end), then the
+// block's warps merge their partial results
 // and the block writes the output, or its key range's normalised partial and
 // log2-sum-exp for the merge kernel.  The per-key work grows with L while the
-// bytes do not: from L = 4 on the tensor-core kernel is the faster path.
+// bytes do not: from L = 7 on the tensor-core kernel is the faster path.
 #include "kernels.h"
 #include "decode.h"
 #include "ptx.cuh"
+
+#include <utility>
 
 namespace txl {
 namespace {
 
 using namespace ptx;
 
-constexpr int DH = kTcDH;         // 64: lane l owns dimensions 2l, 2l+1
+constexpr int DH = kTcDH;         // 64
 constexpr int WARPS = 4;          // warps per block
 constexpr int GK = 32;            // keys per chunk
 constexpr int LMAX = kDecodeMaxL;
@@ -46,7 +51,7 @@ constexpr int STAGE = ST_R + RROWS * ROWB;      // 12544 bytes
 constexpr int RING = NSTG * STAGE;              // per warp
 constexpr int OFF_BAR = WARPS * RING;
 constexpr int OFF_MERGE = OFF_BAR + WARPS * NSTG * 8;
-constexpr int MERGE_BYTES = WARPS * LMAX * (2 * 4 + 32 * 8);
+constexpr int MERGE_BYTES = WARPS * LMAX * (2 + DH) * 4;
 constexpr int OFF_FLAG = OFF_MERGE + MERGE_BYTES;
 constexpr int SMEM_BYTES = OFF_FLAG + 16;
 
@@ -59,24 +64,62 @@ __device__ __forceinline__ float ex2f(float x)
     return y;
 }
 
-__device__ __forceinline__ uint32_t ld_shared_u32(uint32_t addr)
+__device__ __forceinline__ uint4 ld_shared_v4(uint32_t addr)
 {
-    uint32_t v;
-    asm volatile("ld.shared.b32 %0, [%1];" : "=r"(v) : "r"(addr));
+    uint4 v;
+    asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];"
+                 : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+                 : "r"(addr));
     return v;
 }
 
 __device__ __forceinline__ float lo_f(uint32_t w) { return __uint_as_float(w << 16); }
 __device__ __forceinline__ float hi_f(uint32_t w) { return __uint_as_float(w & 0xffff0000u); }
 
-// Lane l holds v[0..31], its share of 32 sums; afterwards lane l holds the whole
-// sum number l.  Five butterfly stages: a lane keeps the half of its values
-// whose index bit matches its own lane bit and sends the other half.
-__device__ __forceinline__ float transpose_reduce(float (&v)[GK], int lane)
+// Packed pairs of fp32 (f32x2 arithmetic).
+__device__ __forceinline__ uint64_t pack2(float lo, float hi)
+{
+    uint64_t r;
+    asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(lo), "f"(hi));
+    return r;
+}
+
+__device__ __forceinline__ void unpack2(uint64_t v, float &lo, float &hi)
+{
+    asm("mov.b64 {%0, %1}, %2;" : "=f"(lo), "=f"(hi) : "l"(v));
+}
+
+__device__ __forceinline__ uint64_t fma2(uint64_t a, uint64_t b, uint64_t c)
+{
+    uint64_t d;
+    asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(a), "l"(b), "l"(c));
+    return d;
+}
+
+__device__ __forceinline__ uint64_t mul2(uint64_t a, uint64_t b)
+{
+    uint64_t d;
+    asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+    return d;
+}
+
+// bf16 pair (dims 2c, 2c+1) as an fp32 pair.
+__device__ __forceinline__ uint64_t widen(uint32_t w) { return pack2(lo_f(w), hi_f(w)); }
+
+__device__ __forceinline__ uint32_t word(const uint4 &v, int c)
+{
+    return c == 0 ? v.x : c == 1 ? v.y : c == 2 ? v.z : v.w;
+}
+
+// The lanes of an 8-lane group hold v[0..7], their shares of 8 sums; afterwards
+// lane s of the group holds the whole sum number s.  Three butterfly stages: a
+// lane keeps the half of its values whose index bit matches its own lane bit
+// and sends the other half.
+__device__ __forceinline__ float transpose_reduce8(float (&v)[8], int sub)
 {
 #pragma unroll
-    for (int o = GK / 2; o >= 1; o >>= 1) {
-        const bool up = (lane & o) != 0;
+    for (int o = 4; o >= 1; o >>= 1) {
+        const bool up = (sub & o) != 0;
 #pragma unroll
         for (int k = 0; k < o; ++k) {
             const float keep = up ? v[k + o] : v[k];
@@ -141,28 +184,34 @@ __global__ void __launch_bounds__(WARPS * 32) relattn_decode_kernel(const Decode
         for (; issued < min(NSTG, n_mine); ++issued) issue(issued);
     issued = __shfl_sync(0xffffffffu, issued, 0);
 
-    // q + u and q + v, this lane's two dimensions, every row.
-    float qu0[L], qu1[L], qv0[L], qv1[L];
+    // q + u and q + v of this lane's eight dimensions (four fp32 pairs), every row.
+    const int g = lane >> 3, sub = lane & 7;
+    uint64_t qu[L][4], qv[L][4];
     {
-        const uint32_t uu = reinterpret_cast<const uint32_t *>(p.u)[h * (DH / 2) + lane];
-        const uint32_t vv = reinterpret_cast<const uint32_t *>(p.vb)[h * (DH / 2) + lane];
+        const uint4 uu = reinterpret_cast<const uint4 *>(p.u)[h * (DH / 8) + sub];
+        const uint4 vb = reinterpret_cast<const uint4 *>(p.vb)[h * (DH / 8) + sub];
 #pragma unroll
         for (int i = 0; i < L; ++i) {
-            const uint32_t qq = reinterpret_cast<const uint32_t *>(p.q)[((size_t)bh * L + i) * (DH / 2) + lane];
-            qu0[i] = lo_f(qq) + lo_f(uu);
-            qu1[i] = hi_f(qq) + hi_f(uu);
-            qv0[i] = lo_f(qq) + lo_f(vv);
-            qv1[i] = hi_f(qq) + hi_f(vv);
+            const uint4 qq = reinterpret_cast<const uint4 *>(p.q)[((size_t)bh * L + i) * (DH / 8) + sub];
+#pragma unroll
+            for (int c = 0; c < 4; ++c) {
+                const uint32_t w = word(qq, c), wu = word(uu, c), wv = word(vb, c);
+                qu[i][c] = pack2(lo_f(w) + lo_f(wu), hi_f(w) + hi_f(wu));
+                qv[i][c] = pack2(lo_f(w) + lo_f(wv), hi_f(w) + hi_f(wv));
+            }
         }
     }
 
-    float m[L], l[L], a0[L], a1[L];  // running max (log2 units) and sum; output dims 2l, 2l+1
+    // running max (log2 units) and sum per row; this group's partial output of
+    // dimensions 8 sub .. 8 sub + 7 (four pairs) per row
+    float m[L], l[L];
+    uint64_t acc[L][4];
 #pragma unroll
     for (int i = 0; i < L; ++i) {
         m[i] = -INFINITY;
         l[i] = 0.f;
-        a0[i] = 0.f;
-        a1[i] = 0.f;
+#pragma unroll
+        for (int c = 0; c < 4; ++c) acc[i][c] = 0;  // +0.0f pairs
     }
 
     bool ok = true;
@@ -170,18 +219,40 @@ __global__ void __launch_bounds__(WARPS * 32) relattn_decode_kernel(const Decode
         const int j0 = k_begin + (warp + WARPS * n) * GK;
         ok = __all_sync(0xffffffffu, mbar_wait(bars + n % NSTG, (n / NSTG) & 1, abort_flag, p.wait_ns));
         if (!ok) break;
-        const uint32_t stg = smem_u32(ring + (n % NSTG) * STAGE) + 4 * lane;
+        // this lane's 16 bytes of row 8g + s of each block of the stage
+        const uint32_t stg = smem_u32(ring + (n % NSTG) * STAGE) + (uint32_t)(8 * g * ROWB + 16 * sub);
 
-        // ---- this lane's words of the chunk's rows ---------------------------
-        uint32_t kk[GK], vv[GK], rr[GK + L - 1];
+        // ---- scores: this lane's words of its group's k and table rows --------
+        float sc_row[L];
+        {
+            uint4 kq[8], rq[8 + L - 1];
 #pragma unroll
-        for (int e = 0; e < GK; ++e) {
-            kk[e] = ld_shared_u32(stg + ST_K + e * ROWB);
-            vv[e] = ld_shared_u32(stg + ST_V + e * ROWB);
+            for (int e = 0; e < 8; ++e) kq[e] = ld_shared_v4(stg + ST_K + e * ROWB);
+            // table row for (i, key 8g + e) is 8g + e + L-1-i
+#pragma unroll
+            for (int e = 0; e < 8 + L - 1; ++e) rq[e] = ld_shared_v4(stg + ST_R + e * ROWB);
+#pragma unroll
+            for (int i = 0; i < L; ++i) {
+                float part[8];
+#pragma unroll
+                for (int e = 0; e < 8; ++e) {
+                    uint64_t a = 0;
+#pragma unroll
+                    for (int c = 0; c < 4; ++c) a = fma2(widen(word(kq[e], c)), qu[i][c], a);
+#pragma unroll
+                    for (int c = 0; c < 4; ++c)
+                        a = fma2(widen(word(rq[e + L - 1 - i], c)), qv[i][c], a);
+                    float x0, x1;
+                    unpack2(a, x0, x1);
+                    part[e] = x0 + x1;
+                }
+                sc_row[i] = transpose_reduce8(part, sub) * p.scale_log2;  // key j0 + lane
+            }
         }
-        // table row for (i, j) is e = j - j0 + L-1-i
+        // ---- the group's v rows (after the scores: fewer live registers) ------
+        uint4 vq[8];
 #pragma unroll
-        for (int e = 0; e < GK + L - 1; ++e) rr[e] = ld_shared_u32(stg + ST_R + e * ROWB);
+        for (int e = 0; e < 8; ++e) vq[e] = ld_shared_v4(stg + ST_V + e * ROWB);
         // The stage is read: order the reads before the copy that refills it.
         fence_proxy_async_smem();
         __syncwarp();
@@ -192,19 +263,10 @@ __global__ void __launch_bounds__(WARPS * 32) relattn_decode_kernel(const Decode
 
 #pragma unroll
         for (int i = 0; i < L; ++i) {
-            // ---- scores of row i for the 32 keys -----------------------------
-            float part[GK];
-#pragma unroll
-            for (int e = 0; e < GK; ++e) {
-                const uint32_t r2 = rr[e + (L - 1 - i)];
-                part[e] = fmaf(qu0[i], lo_f(kk[e]),
-                               fmaf(qu1[i], hi_f(kk[e]),
-                                    fmaf(qv0[i], lo_f(r2), qv1[i] * hi_f(r2))));
-            }
-            float s = transpose_reduce(part, lane) * p.scale_log2;  // key j0 + lane
+            float s = sc_row[i];
             const int j = j0 + lane;
             if (j >= k_end || j > p.M + i) s = -INFINITY;
-            // ---- online softmax -------------------------------------------------
+            // ---- online softmax over the warp's 32 keys --------------------------
             float mx = s;
 #pragma unroll
             for (int o = 16; o > 0; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
@@ -217,16 +279,17 @@ __global__ void __launch_bounds__(WARPS * 32) relattn_decode_kernel(const Decode
             for (int o = 16; o > 0; o >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, o);
             m[i] = m_new;
             l[i] = l[i] * sc + sum;
-            float b0 = a0[i] * sc, b1 = a1[i] * sc;
-            // ---- P.V: probability of key e from lane e -------------------------
+            const uint64_t sc2 = pack2(sc, sc);
 #pragma unroll
-            for (int e = 0; e < GK; ++e) {
-                const float pe = __shfl_sync(0xffffffffu, pj, e);
-                b0 = fmaf(pe, lo_f(vv[e]), b0);
-                b1 = fmaf(pe, hi_f(vv[e]), b1);
+            for (int c = 0; c < 4; ++c) acc[i][c] = mul2(acc[i][c], sc2);
+            // ---- P.V: probability of key 8g + e from lane 8g + e ----------------
+#pragma unroll
+            for (int e = 0; e < 8; ++e) {
+                const float pe = __shfl_sync(0xffffffffu, pj, (lane & 24) + e);
+                const uint64_t pe2 = pack2(pe, pe);
+#pragma unroll
+                for (int c = 0; c < 4; ++c) acc[i][c] = fma2(widen(word(vq[e], c)), pe2, acc[i][c]);
             }
-            a0[i] = b0;
-            a1[i] = b1;
         }
     }
     if (!ok) {
@@ -242,17 +305,34 @@ __global__ void __launch_bounds__(WARPS * 32) relattn_decode_kernel(const Decode
         __syncwarp();
     }
 
+    // ---- sum the four groups' partial outputs (same running max) -------------
+    float o8[L][8];
+#pragma unroll
+    for (int i = 0; i < L; ++i) {
+#pragma unroll
+        for (int c = 0; c < 4; ++c) unpack2(acc[i][c], o8[i][2 * c], o8[i][2 * c + 1]);
+#pragma unroll
+        for (int d = 0; d < 8; ++d) {
+            o8[i][d] += __shfl_xor_sync(0xffffffffu, o8[i][d], 8);
+            o8[i][d] += __shfl_xor_sync(0xffffffffu, o8[i][d], 16);
+        }
+    }
+
     // ---- merge the block's warps: w = 2^(m_w - max), out = sum w a / sum w l ----
-    float *sm_m = reinterpret_cast<float *>(smem + OFF_MERGE);         // [WARPS][LMAX]
-    float *sm_l = sm_m + WARPS * LMAX;                                   // [WARPS][LMAX]
-    float2 *sm_a = reinterpret_cast<float2 *>(sm_l + WARPS * LMAX);      // [WARPS][LMAX][32]
+    float *sm_m = reinterpret_cast<float *>(smem + OFF_MERGE);   // [WARPS][LMAX]
+    float *sm_l = sm_m + WARPS * LMAX;                             // [WARPS][LMAX]
+    float *sm_a = sm_l + WARPS * LMAX;                             // [WARPS][LMAX][64]
 #pragma unroll
     for (int i = 0; i < L; ++i) {
         if (lane == 0) {
             sm_m[warp * LMAX + i] = m[i];
             sm_l[warp * LMAX + i] = l[i];
         }
-        sm_a[(warp * LMAX + i) * 32 + lane] = make_float2(a0[i], a1[i]);
+        if (g == 0) {
+            float4 *dst = reinterpret_cast<float4 *>(sm_a + (warp * LMAX + i) * DH + 8 * sub);
+            dst[0] = make_float4(o8[i][0], o8[i][1], o8[i][2], o8[i][3]);
+            dst[1] = make_float4(o8[i][4], o8[i][5], o8[i][6], o8[i][7]);
+        }
     }
     __syncthreads();
     for (int i = warp; i < L; i += WARPS) {
@@ -267,7 +347,7 @@ __global__ void __launch_bounds__(WARPS * 32) relattn_decode_kernel(const Decode
                 if (mw == -INFINITY) continue;
                 const float sw = ex2f(mw - mx);
                 ls += sw * sm_l[w * LMAX + i];
-                const float2 aw = sm_a[(w * LMAX + i) * 32 + lane];
+                const float2 aw = reinterpret_cast<const float2 *>(sm_a + (w * LMAX + i) * DH)[lane];
                 o0 = fmaf(sw, aw.x, o0);
                 o1 = fmaf(sw, aw.y, o1);
             }
@@ -294,27 +374,11 @@ cudaError_t set_smem_l()
                                 SMEM_BYTES);
 }
 
-// The dynamic shared-memory attribute of the three instances, once per device.
-cudaError_t ensure_smem_attr()
-{
-    static bool done[64] = {};
-    int dev = 0;
-    cudaError_t e = cudaGetDevice(&dev);
-    if (e != cudaSuccess) return e;
-    if (dev >= 0 && dev < 64 && done[dev]) return cudaSuccess;
-    if ((e = set_smem_l<1>()) != cudaSuccess) return e;
-    if ((e = set_smem_l<2>()) != cudaSuccess) return e;
-    if ((e = set_smem_l<3>()) != cudaSuccess) return e;
-    if (dev >= 0 && dev < 64) done[dev] = true;
-    return cudaSuccess;
-}
-
 template <int L>
 int blocks_per_sm_l()
 {
     int n = 0;
-    if (ensure_smem_attr() != cudaSuccess ||
-        cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, relattn_decode_kernel<L>, WARPS * 32,
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, relattn_decode_kernel<L>, WARPS * 32,
                                                       SMEM_BYTES) != cudaSuccess)
         return 1;
     return n < 1 ? 1 : n;
@@ -325,10 +389,33 @@ cudaError_t launch_l(const DecodeParams &p, cudaStream_t s)
 {
     const long long blocks = (long long)p.B * p.H * p.n_splits;
     if (blocks <= 0 || blocks > 0x7fffffffLL) return cudaErrorInvalidValue;
-    cudaError_t e = ensure_smem_attr();
-    if (e != cudaSuccess) return e;
     relattn_decode_kernel<L><<<(unsigned)blocks, WARPS * 32, SMEM_BYTES, s>>>(p);
     return cudaGetLastError();
+}
+
+// Instances L = 1 .. kDecodeMaxL, indexed by L - 1.
+template <int... I>
+struct Table {
+    static constexpr cudaError_t (*set_smem[])() = {set_smem_l<I + 1>...};
+    static constexpr int (*blocks[])() = {blocks_per_sm_l<I + 1>...};
+    static constexpr cudaError_t (*launch[])(const DecodeParams &, cudaStream_t) = {launch_l<I + 1>...};
+};
+template <int... I>
+Table<I...> make_table(std::integer_sequence<int, I...>);
+using Inst = decltype(make_table(std::make_integer_sequence<int, kDecodeMaxL>{}));
+
+// The dynamic shared-memory attribute of every instance, once per device.
+cudaError_t ensure_smem_attr()
+{
+    static bool done[64] = {};
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    if (dev >= 0 && dev < 64 && done[dev]) return cudaSuccess;
+    for (int l = 0; l < kDecodeMaxL; ++l)
+        if ((e = Inst::set_smem[l]()) != cudaSuccess) return e;
+    if (dev >= 0 && dev < 64) done[dev] = true;
+    return cudaSuccess;
 }
 
 } // namespace
@@ -339,19 +426,16 @@ int decode_blocks_per_sm(int L)
 {
     static int cache[kDecodeMaxL + 1] = {};  // per query count; one device per process
     if (L < 1 || L > kDecodeMaxL) return 1;
-    if (!cache[L]) cache[L] = (L == 1) ? blocks_per_sm_l<1>() : (L == 2) ? blocks_per_sm_l<2>()
-                                                                           : blocks_per_sm_l<3>();
+    if (!cache[L]) cache[L] = (ensure_smem_attr() == cudaSuccess) ? Inst::blocks[L - 1]() : 1;
     return cache[L];
 }
 
 cudaError_t launch_relattn_decode(const DecodeParams &p, cudaStream_t s)
 {
-    switch (p.L) {
-    case 1: return launch_l<1>(p, s);
-    case 2: return launch_l<2>(p, s);
-    case 3: return launch_l<3>(p, s);
-    default: return cudaErrorInvalidValue;
-    }
+    if (p.L < 1 || p.L > kDecodeMaxL) return cudaErrorInvalidValue;
+    const cudaError_t e = ensure_smem_attr();
+    if (e != cudaSuccess) return e;
+    return Inst::launch[p.L - 1](p, s);
 }
 
 } // namespace txl
