@@ -88,6 +88,13 @@ def parse_args():
     ap.add_argument("--table9", action="store_true",
                     help="per-token evaluation time, vanilla window recompute vs state reuse "
                          "(one attention layer), instead of the headline step")
+    ap.add_argument("--decode", action="store_true",
+                    help="time decode-shaped calls (a few new tokens against a long memory) "
+                         "and their HBM bandwidth, instead of the headline step")
+    ap.add_argument("--shapes", nargs="*", default=None,
+                    help="with --decode: B,L,M triples (default: the long-memory decode set)")
+    ap.add_argument("--calls", type=int, default=10,
+                    help="with --decode: graph replays timed per shape (30 calls each)")
     return ap.parse_args()
 
 
@@ -531,27 +538,35 @@ def run_ours(args, world, rank, local):
 TABLE9_PAPER = {800: 363, 1800: 773, 2800: 1409, 3800: 1874}
 
 
-def attn_call_us(B, H, L, M, reps=10, per=20):
+def attn_call_us(B, H, L, M, reps=10, per=20, n_sets=1):
+    """Device time of one txl_relattn_fwd call (graph-replayed), random bf16
+    operands; with n_sets > 1 the calls rotate over that many input sets (k, v
+    and the table larger than L2 in total keeps the reads in HBM)."""
     import torch
     import transformer_xl_relative_pos_gb300 as txl
     dev = torch.device("cuda", 0)
     K = M + L
     g = torch.Generator(device=dev).manual_seed(B * 7919 + L * 31 + M)
     mk = lambda *sh: (torch.randn(*sh, device=dev, generator=g) * 0.5).to(torch.bfloat16)
-    q, k, v, r = mk(B, H, L, 64), mk(B, H, K, 64), mk(B, H, K, 64), mk(H, K, 64)
+    sets = [(mk(B, H, L, 64), mk(B, H, K, 64), mk(B, H, K, 64), mk(H, K, 64)) for _ in range(n_sets)]
     u, vb = mk(H, 64) * 0.2, mk(H, 64) * 0.2
     out = torch.empty(B, H, L, 64, device=dev, dtype=torch.bfloat16)
-    ws = torch.empty(max(txl.workspace_size(B, H, L, 64, 8), 256), dtype=torch.uint8, device=dev)
+    ws = torch.empty(max(txl.workspace_size(B, H, L, 64, 64), 256), dtype=torch.uint8, device=dev)
     stream = torch.cuda.Stream()
-    call = lambda: txl.relattn_fwd(q, k, v, r, u, vb, M, 0.125, out=out, workspace=ws)
+
+    def call(i):
+        q, k, v, r = sets[i % n_sets]
+        txl.relattn_fwd(q, k, v, r, u, vb, M, 0.125, out=out, workspace=ws)
+
     with torch.cuda.stream(stream):
-        for _ in range(3):
-            call()
+        for i in range(3):
+            call(i)
     torch.cuda.synchronize()
+    per = max(per, n_sets) // n_sets * n_sets
     graph = torch.cuda.CUDAGraph()
     with torch.cuda.graph(graph, stream=stream):
-        for _ in range(per):
-            call()
+        for i in range(per):
+            call(i)
     graph.replay()
     torch.cuda.synchronize()
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
@@ -581,6 +596,34 @@ def run_table9(args):
                 "slowdown_vs_decode": vanilla / xl_tok, "slowdown_vs_segment128": vanilla / xl_seg,
                 "paper_slowdown": TABLE9_PAPER[A],
                 "note": "one attention layer; the paper's ratio is for the whole model"}}), flush=True)
+
+
+# Decode steps (one to six new tokens against a long memory), H = 16 heads of
+# 64: the memory lengths of the long-memory evaluation (M = 1600 and 3800).
+DECODE_SHAPES = [(8, 1, 3800), (8, 2, 3800), (8, 3, 3800), (8, 4, 3800), (8, 6, 3800), (16, 1, 1600),
+                 (16, 6, 1600), (64, 1, 3800), (1, 1, 3800)]
+
+
+def run_decode(args):
+    """Graph-replayed time and achieved HBM bandwidth of decode-shaped calls
+    (L new queries per sequence against M cached positions)."""
+    import torch
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    pk = peaks()
+    shapes = [tuple(int(x) for x in s.split(",")) for s in args.shapes] if args.shapes else DECODE_SHAPES
+    H = 16
+    for B, L, M in shapes:
+        K = M + L
+        nbytes = 2 * (2 * B * H * K * 64 + H * K * 64 + 2 * B * H * L * 64)  # k, v, r, q, out (bf16)
+        n_sets = max(1, min(3, -(-3 * 126 * 2 ** 20 // nbytes)))  # > L2 of traffic between reuses
+        us = attn_call_us(B, H, L, M, reps=args.calls, per=30, n_sets=n_sets)
+        gbs = nbytes / (us * 1e-6) / 1e9
+        print(json.dumps({"decode": {
+            "B": B, "H": H, "L": L, "M": M, "dtype": "bf16", "us_per_call": us,
+            "algorithmic_bytes": nbytes, "achieved_gbs": gbs, "peak_gbs": pk["hbm_gbs"],
+            "hbm_frac": gbs / pk["hbm_gbs"], "input_sets": n_sets,
+            "path": "decode kernel" if L <= 6 else "tensor-core kernel"}}), flush=True)
 
 
 def run_stack(args):
@@ -622,6 +665,9 @@ def main():
         return
     if args.table9:
         run_table9(args)
+        return
+    if args.decode:
+        run_decode(args)
         return
     world, rank, local = dist_setup(args)
     if args.impl == "reference":
