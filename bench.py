@@ -629,8 +629,9 @@ def run_decode(args):
 def run_stack(args):
     """Per-segment time of the streaming stack on the 12-layer, 16-segment
     workload (B=16, H=8, L=M=512, d=512), memories full, with and without the
-    cached projected memory keys/values.  Torch does the projections, LayerNorm
-    and feed-forward; the kernels do the table, the attention and the rings."""
+    cached projected memory keys/values, launched eagerly or replayed from CUDA
+    graphs.  Torch does the projections, LayerNorm and feed-forward; the
+    kernels do the table, the attention and the rings."""
     import torch
     from transformer_xl_relative_pos_gb300.model import XLStack
     dev = torch.device("cuda", 0)
@@ -638,9 +639,9 @@ def run_stack(args):
     w = txl_inputs.WORKLOADS["c5_stack12_L512_M512"]
     params = txl_inputs.draw_stack(w)
     tokens = params["tokens"].to(dev)
-    for cache_kv in (True, False):
-        stack = XLStack(params, w.H, w.M, dev, torch.bfloat16, cache_kv=cache_kv)
-        n_warm = 3  # memories are full after the first segment (L = M)
+    for graphs, cache_kv in ((False, True), (False, False), (True, True), (True, False)):
+        stack = XLStack(params, w.H, w.M, dev, torch.bfloat16, cache_kv=cache_kv, graphs=graphs)
+        n_warm = 3  # memories are full after the first segment (L = M); graph captured in the third
         for s_ in range(n_warm):
             stack.segment(tokens[s_])
         torch.cuda.synchronize()
@@ -654,7 +655,8 @@ def run_stack(args):
         ms = e0.elapsed_time(e1) / n_timed
         print(json.dumps({"stack": {
             "workload": w.name, "layers": len(params["layers"]), "B": w.B, "H": w.H, "L": w.L,
-            "M": w.M, "d_model": w.d_model, "cache_kv": cache_kv, "segments_timed": n_timed,
+            "M": w.M, "d_model": w.d_model, "cache_kv": cache_kv, "cuda_graphs": graphs,
+            "segments_timed": n_timed,
             "ms_per_segment": ms, "tokens_per_s": w.B * w.L / (ms * 1e-3)}}), flush=True)
 
 

@@ -89,3 +89,27 @@ def test_cached_kv_rings_match_projected_memory():
         # the same bf16 products, possibly summed in another order by the GEMM
         compare(k_ring.float().cpu().numpy(), k_mem.float().cpu().numpy(), 5e-3, what=f"k ring {n}")
         compare(v_ring.float().cpu().numpy(), v_mem.float().cpu().numpy(), 5e-3, what=f"v ring {n}")
+
+
+@pytest.mark.parametrize("L,M,cache_kv", [(64, 64, False), (64, 128, True), (48, 80, False)])
+def test_graph_replayed_stack_matches_eager(L, M, cache_kv):
+    # Once the memories are full the stack replays each segment from a CUDA
+    # graph per ring position (one when L is a multiple of M, M / gcd(M, L)
+    # otherwise); every segment's output and the final memories must equal the
+    # eager stack's bit for bit (same kernels, same order, same operands).
+    base = txl_inputs.WORKLOADS["c5_stack12_L512_M512"]
+    w = txl_inputs.Workload("graph_stack", B=2, H=2, dh=64, L=L, M=M, d_model=128,
+                            dtype="bf16", seed=43, d_ff=256, n_layer=2, n_seg=9, vocab=base.vocab)
+    params = txl_inputs.draw_stack(w)
+    eager = XLStack(params, w.H, w.M, dev(), torch.bfloat16, cache_kv=cache_kv)
+    graphed = XLStack(params, w.H, w.M, dev(), torch.bfloat16, cache_kv=cache_kv, graphs=True)
+    for s in range(w.n_seg):
+        want = eager.segment(params["tokens"][s]).clone()
+        got = graphed.segment(params["tokens"][s]).clone()
+        torch.cuda.synchronize()
+        assert torch.equal(got, want), f"segment {s}"
+    assert len(graphed._graphs) == M // math.gcd(M, L)
+    for a, b in zip(eager.memories(), graphed.memories()):
+        assert torch.equal(a, b)
+    for sa, sb in zip(eager._rings(), graphed._rings()):
+        assert (sa.head, sa.fill) == (sb.head, sb.fill)

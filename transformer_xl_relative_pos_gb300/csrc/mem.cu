@@ -6,80 +6,118 @@
 // stop-gradient, in front of the current segment as extended context; §3.3's
 // summary writes this as h~ = [SG(m) o h].  SG is the identity in a forward pass.
 //
-// Both kernels are pure row copies in 16-byte units, one block per row;
-// HBM-bound.
+// Both kernels are pure copies of 16-byte vectors, flattened per batch row
+// over (row, vector) so that every block moves many rows whatever the row size
+// (128-byte rows of per-head projected keys as well as d_model-wide hidden
+// states); each thread keeps four vectors in flight.  HBM-bound.
 #include "kernels.h"
 
 namespace txl {
 namespace {
 
-// One block per (row, batch); the row's 16-byte vectors spread over the threads.
+constexpr int kThreads = 256;
+constexpr int kVecPerThread = 4;
+
+// Row and vector of flat index i: shift = log2(row_vec) when row_vec is a power
+// of two (every d_model and head size here), else -1 (one division).
+__device__ __forceinline__ int row_of(int i, int row_vec, int shift)
+{
+    return shift >= 0 ? (i >> shift) : i / row_vec;
+}
+
 // ext[b][t] = t < fill ? mem[b][(head - fill + t) mod cap] : h_new[b][t - fill]
-__global__ void mem_concat_kernel(uint4 *__restrict__ ext, const uint4 *__restrict__ mem,
-                                  const uint4 *__restrict__ h_new, int fill, int head, int cap,
-                                  int L, int row_vec)
+__global__ void __launch_bounds__(kThreads) mem_concat_kernel(uint4 *__restrict__ ext,
+                                                              const uint4 *__restrict__ mem,
+                                                              const uint4 *__restrict__ h_new,
+                                                              int fill, int head, int cap, int L,
+                                                              int row_vec, int shift)
 {
-    const int t = blockIdx.x;
-    const int b = blockIdx.y;
-    const uint4 *src;
-    if (t < fill) {
-        int slot = head - fill + t;
-        slot += (slot < 0) ? cap : 0;
-        src = mem + ((size_t)b * cap + slot) * row_vec;
-    } else {
-        src = h_new + ((size_t)b * L + (t - fill)) * row_vec;
+    const int rows = fill + L;
+    const int total = rows * row_vec;  // vectors of this batch row
+    const long long b = blockIdx.y;
+    const int base = blockIdx.x * kThreads * kVecPerThread + threadIdx.x;
+    uint4 v[kVecPerThread];
+#pragma unroll
+    for (int k = 0; k < kVecPerThread; ++k) {
+        const int i = base + k * kThreads;
+        if (i >= total) continue;
+        const int t = row_of(i, row_vec, shift);
+        const int c = i - t * row_vec;
+        const uint4 *src;
+        if (t < fill) {
+            int slot = head - fill + t;
+            slot += (slot < 0) ? cap : 0;
+            src = mem + (b * cap + slot) * row_vec + c;
+        } else {
+            src = h_new + (b * L + (t - fill)) * row_vec + c;
+        }
+        v[k] = __ldcs(src);
     }
-    uint4 *dst = ext + ((size_t)b * (fill + L) + t) * row_vec;
-    for (int c = threadIdx.x; c < row_vec; c += blockDim.x) dst[c] = src[c];
-}
-
-// mem[b][(head + l) mod cap] = h_new[b][l] for l in [first_row, L).  Each block
-// copies kRowsPerBlock rows so that every thread has several loads in flight.
-constexpr int kRowsPerBlock = 4;
-__global__ void mem_write_kernel(uint4 *__restrict__ mem, const uint4 *__restrict__ h_new, int L,
-                                 int first_row, int head, int cap, int row_vec)
-{
-    const int l0 = first_row + blockIdx.x * kRowsPerBlock;
-    const int b = blockIdx.y;
-    const int nrows = min(kRowsPerBlock, L - l0);
-    for (int c = threadIdx.x; c < row_vec; c += blockDim.x) {
-        uint4 v[kRowsPerBlock];
 #pragma unroll
-        for (int r = 0; r < kRowsPerBlock; ++r)
-            if (r < nrows) v[r] = h_new[((size_t)b * L + l0 + r) * row_vec + c];
-#pragma unroll
-        for (int r = 0; r < kRowsPerBlock; ++r)
-            if (r < nrows) {
-                const int slot = (int)(((long long)head + l0 + r) % cap);
-                mem[((size_t)b * cap + slot) * row_vec + c] = v[r];
-            }
+    for (int k = 0; k < kVecPerThread; ++k) {
+        const int i = base + k * kThreads;
+        if (i < total) ext[b * total + i] = v[k];
     }
 }
 
-int threads_for(int row_vec) { return row_vec >= 256 ? 256 : ((row_vec + 31) / 32) * 32; }
+// mem[b][(head + l) mod cap] = h_new[b][l] for l in [first_row, L).
+__global__ void __launch_bounds__(kThreads) mem_write_kernel(uint4 *__restrict__ mem,
+                                                             const uint4 *__restrict__ h_new,
+                                                             int L, int first_row, int head,
+                                                             int cap, int row_vec, int shift)
+{
+    const int total = (L - first_row) * row_vec;  // vectors of this batch row
+    const long long b = blockIdx.y;
+    const int base = blockIdx.x * kThreads * kVecPerThread + threadIdx.x;
+    uint4 v[kVecPerThread];
+    long long dst[kVecPerThread];
+#pragma unroll
+    for (int k = 0; k < kVecPerThread; ++k) {
+        const int i = base + k * kThreads;
+        dst[k] = -1;
+        if (i >= total) continue;
+        const int r = row_of(i, row_vec, shift);
+        const int c = i - r * row_vec;
+        const int l = first_row + r;
+        v[k] = __ldcs(h_new + (b * L + l) * row_vec + c);
+        dst[k] = (b * cap + (head + l) % cap) * row_vec + c;
+    }
+#pragma unroll
+    for (int k = 0; k < kVecPerThread; ++k)
+        if (dst[k] >= 0) mem[dst[k]] = v[k];
+}
+
+int shift_of(int row_vec)
+{
+    if (row_vec <= 0 || (row_vec & (row_vec - 1))) return -1;
+    int sh = 0;
+    while ((1 << sh) < row_vec) ++sh;
+    return sh;
+}
 
 } // namespace
 
 cudaError_t launch_mem_concat(uint4 *ext, const uint4 *mem, const uint4 *h_new, int B,
                               int fill, int head, int cap, int L, int row_vec, cudaStream_t s)
 {
-    const int rows = fill + L;
-    if (rows == 0 || B == 0) return cudaSuccess;
-    if (B > 65535) return cudaErrorInvalidValue;
-    mem_concat_kernel<<<dim3(rows, B), threads_for(row_vec), 0, s>>>(ext, mem, h_new, fill, head,
-                                                                     cap, L, row_vec);
+    const long long total = (long long)(fill + L) * row_vec;
+    if (total == 0 || B == 0) return cudaSuccess;
+    if (B > 65535 || total > 0x7fffffffLL - kThreads * kVecPerThread) return cudaErrorInvalidValue;
+    const unsigned blocks = (unsigned)((total + kThreads * kVecPerThread - 1) / (kThreads * kVecPerThread));
+    mem_concat_kernel<<<dim3(blocks, B), kThreads, 0, s>>>(ext, mem, h_new, fill, head, cap, L,
+                                                           row_vec, shift_of(row_vec));
     return cudaGetLastError();
 }
 
 cudaError_t launch_mem_write(uint4 *mem, const uint4 *h_new, int B, int L, int first_row,
                              int head, int cap, int row_vec, cudaStream_t s)
 {
-    const int rows = L - first_row;
-    if (rows <= 0 || B == 0) return cudaSuccess;
-    if (B > 65535) return cudaErrorInvalidValue;
-    const int blocks = (rows + kRowsPerBlock - 1) / kRowsPerBlock;
-    mem_write_kernel<<<dim3(blocks, B), threads_for(row_vec), 0, s>>>(mem, h_new, L, first_row,
-                                                                      head, cap, row_vec);
+    const long long total = (long long)(L - first_row) * row_vec;
+    if (total <= 0 || B == 0) return cudaSuccess;
+    if (B > 65535 || total > 0x7fffffffLL - kThreads * kVecPerThread) return cudaErrorInvalidValue;
+    const unsigned blocks = (unsigned)((total + kThreads * kVecPerThread - 1) / (kThreads * kVecPerThread));
+    mem_write_kernel<<<dim3(blocks, B), kThreads, 0, s>>>(mem, h_new, L, first_row, head, cap,
+                                                          row_vec, shift_of(row_vec));
     return cudaGetLastError();
 }
 

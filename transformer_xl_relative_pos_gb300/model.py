@@ -15,12 +15,21 @@ projected keys and values: the memory rows and W_kE, W_v do not change at
 evaluation, so k and v of the memory are the ones projected when those states
 were the segment, and each segment projects only its own L rows (2·M·d²
 multiply-adds saved per layer and projection); the rings are the same kernels
-on a [B·H, M, d_head] view.  It is off by default: the attention takes k and v
-as one contiguous tensor, so the rings are copied out every segment, and on
-this hardware that copy costs more than re-projecting the memory.
+on a [B·H, M, d_head] view.  The attention takes k and v as one contiguous
+tensor, so the rings are copied out every segment: replayed from CUDA graphs
+the cached stack is slightly faster than re-projecting the memory (the saved
+multiply-adds outweigh the copies), launched eagerly it is slower (four more
+launches per layer), so it is off by default.
 The relative table r = W_kR R is built from rel_pos_emb (kernel) and one matmul
 and is cached per (layer, K): R has no parameters and W_kR is fixed at
 evaluation.
+
+With ``graphs`` the stack replays each segment from a CUDA graph once the
+memories are full: every launch of a segment then has fixed shapes and
+pointers, and the ring heads come back to the same positions every
+M / gcd(M, L) segments, so one graph per ring position covers the stream (one
+graph when L is a multiple of M).  The host-side ring states advance exactly
+as the eager calls advance them.
 
 Torch is used here for the dense projections, LayerNorm and the feed-forward
 only; the attention, the positional table and the memory run in the CUDA
@@ -76,9 +85,13 @@ class XLStack:
     [B, L] and returns the top layer's states [B, L, d] (``dtype``)."""
 
     def __init__(self, params: dict, H: int, M: int, device, dtype=torch.bfloat16,
-                 cache_kv: bool = False):
+                 cache_kv: bool = False, graphs: bool = False):
         self.H, self.M, self.dtype, self.device = H, M, dtype, torch.device(device)
         self.cache_kv = cache_kv
+        self.graphs = graphs
+        self._graphs = {}        # ring head -> (graph, token buffer, output)
+        self._pool = None
+        self._full_segments = 0  # eager segments run with full memories
         to = lambda t: t.to(device=self.device, dtype=dtype).contiguous()
         self.emb = to(params["emb"])
         self.u = to(params["u"])
@@ -92,6 +105,8 @@ class XLStack:
         self._r_cache = {}
 
     def reset(self, B: int):
+        self._graphs = {}
+        self._full_segments = 0
         self.mems = [torch.zeros(B, self.M, self.d, dtype=self.dtype, device=self.device)
                      for _ in self.layers]
         self.states = [txl.MemState(0, 0, self.M) for _ in self.layers]
@@ -120,11 +135,52 @@ class XLStack:
                                                  self.H).to(self.dtype)
         return self._r_cache[key]
 
+    def _rings(self):
+        rings = list(self.states)
+        if self.cache_kv:
+            rings += [s for pair in self.kv_states for s in pair]
+        return rings
+
     def segment(self, tokens: torch.Tensor) -> torch.Tensor:
+        """One segment [B, L] -> the top layer's states [B, L, d].  With graphs
+        the result lives in the graph's memory and is overwritten by the next
+        replay of the same ring position."""
         B, L = tokens.shape
         if self.mems is None or self.mems[0].shape[0] != B:
             self.reset(B)
-        h = self.emb[tokens.to(self.device)]
+        full = self.M > 0 and self.states[0].fill == self.M
+        # capture only after one eager segment at full memory (warm-up of the
+        # library's and torch's lazily set-up state for these shapes)
+        if not (self.graphs and full and self._full_segments >= 1):
+            if full:
+                self._full_segments += 1
+            return self._segment(tokens.to(self.device))
+        key = self.states[0].head
+        if key not in self._graphs:
+            saved = [(st.head, st.fill) for st in self._rings()]
+            tok = torch.empty(B, L, dtype=torch.long, device=self.device)
+            tok.copy_(tokens)
+            graph = torch.cuda.CUDAGraph()
+            if self._pool is None:
+                self._pool = torch.cuda.graph_pool_handle()
+            with torch.cuda.graph(graph, pool=self._pool):
+                out = self._segment(tok)
+            # capture recorded the launches without running them: put the ring
+            # states back; the replay below runs the segment
+            for st, (head, fill) in zip(self._rings(), saved):
+                st.head, st.fill = head, fill
+            self._graphs[key] = (graph, tok, out)
+        graph, tok, out = self._graphs[key]
+        tok.copy_(tokens)
+        graph.replay()
+        for st in self._rings():  # what the eager mem_update calls do on the host
+            st.fill = min(st.fill + L, st.capacity)
+            st.head = (st.head + L) % st.capacity
+        return out
+
+    def _segment(self, tokens: torch.Tensor) -> torch.Tensor:
+        B, L = tokens.shape
+        h = self.emb[tokens]
         for n, lay in enumerate(self.layers):
             st = self.states[n]
             M_cur = st.fill
