@@ -51,8 +51,8 @@ import txl_inputs  # noqa: E402
 PROFILED_TRAFFIC = {
     "workload": "c3_word_large_L128_M1600",
     "sources": ("relattn_tc.cu", "ptx.cuh", "kernels.h"),
-    "sha256": "81bbd42e24f3910cf9279abb67d751efeafcad264156e659d2f04c93c6b6adab",
-    "bytes_per_launch": 121080576 + 2516992,
+    "sha256": "12c5e7c622f4ad5a73dcad9bb0143bc3dc3456078d5696609a51511ba3ca3f72",
+    "bytes_per_launch": 121081600 + 2525952,
 }
 
 

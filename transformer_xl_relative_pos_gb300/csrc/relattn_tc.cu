@@ -19,6 +19,12 @@
 // window, through a per-thread shared-memory skew buffer; no L x K matrix
 // exists anywhere.
 //
+// Key tile t and table chunk t+1 are one shared-memory pair [32 KB] whose two
+// halves are multiplied by q as a single N = 256 operand: TMEM holds
+// [even-chunk slot | S | odd-chunk slot], and the pair is laid out [chunk ; keys]
+// when chunk t+1 is even (its slot precedes S) and [keys ; chunk] when it is odd,
+// so that the 256 result columns of one MMA land on S and the chunk's slot.
+//
 // The bias terms u.k_j and v.r_rho are exact in fp32: q enters the MMA as
 // given, and the biases come from small MMAs [K tile | table chunk] x [u ; v]^T
 // whose fp32 results the softmax warps split into bf16 hi + lo pairs; a fifth
@@ -48,18 +54,21 @@ namespace {
 using namespace ptx;
 
 constexpr int BM = kTcBM, BN = kTcBN, DH = kTcDH;
-constexpr int NS = 3;                  // K / V ring stages
-constexpr int NR = 2;                  // table-chunk ring slots
+constexpr int NP = 2;                  // pair stages [key tile t, table chunk t+1]
+constexpr int NS = 3;                  // V ring stages
 constexpr int PF = 3;                  // L2 prefetch distance (tiles)
 constexpr int TILE = BM * DH * 2;      // 16384 bytes: 128 rows x 128 bytes
 constexpr int EXT = 4096;              // bias-column tile: 128 rows x 16 bytes, then
                                        // 2 KB of zeros for K columns 8..15
+constexpr int EXT2 = 8192;             // the same for a pair: 256 rows, then 4 KB of zeros
+constexpr int PAIR = 2 * TILE;
 constexpr int SKEW_STRIDE = 100;       // floats per skew row: a 3 x 32 ring + 4 pad
                                        // (stride = 4 mod 32: conflict-free both ways)
 
 // TMEM columns
-constexpr uint32_t TM_S = 0;           // content scores
-constexpr uint32_t TM_B = 128;         // two 128-column table-chunk slots
+constexpr uint32_t TM_CA = 0;          // table-chunk slot of even chunks
+constexpr uint32_t TM_S = 128;         // content scores
+constexpr uint32_t TM_CC = 256;        // table-chunk slot of odd chunks
 constexpr uint32_t TM_O = 384;         // output accumulator (64 columns)
 constexpr uint32_t TM_BK = 448;        // k.u / k.v for the next key tile (16 columns)
 constexpr uint32_t TM_BR = 464;        // r.u / r.v for the next table chunk
@@ -71,16 +80,16 @@ constexpr uint32_t TM_COLS = 512;
 
 // Shared-memory layout (offsets from a 1024-byte aligned base).
 constexpr int OFF_Q = 0;
-constexpr int OFF_K = OFF_Q + TILE;               // NS stages
-constexpr int OFF_V = OFF_K + NS * TILE;          // NS stages
-constexpr int OFF_R = OFF_V + NS * TILE;          // NR slots
-constexpr int OFF_UB = OFF_R + NR * TILE;         // [u ; v ; 0 x 14] 16 x 128 bytes, swizzled
+constexpr int OFF_PAIR = OFF_Q + TILE;            // NP pair stages
+constexpr int OFF_V = OFF_PAIR + NP * PAIR;       // NS stages
+constexpr int OFF_R0 = OFF_V + NS * TILE;         // table chunk 0 (first tile only)
+constexpr int OFF_UB = OFF_R0 + TILE;             // [u ; v ; 0 x 14] 16 x 128 bytes, swizzled
 constexpr int OFF_AEXT = OFF_UB + 2048;           // ones column: rows [1, 1, 0 x 6]
-constexpr int OFF_KEXT = OFF_AEXT + EXT;          // NS tiles of (hi, lo) of k.u
-constexpr int OFF_REXT = OFF_KEXT + NS * EXT;     // NR tiles of (hi, lo) of v.r
-constexpr int OFF_SKEW = OFF_REXT + NR * EXT;     // 128 rows x SKEW_STRIDE floats
+constexpr int OFF_PEXT = OFF_AEXT + EXT;          // NP pair tiles of (hi, lo) of k.u / v.r
+constexpr int OFF_R0EXT = OFF_PEXT + NP * EXT2;   // (hi, lo) of v.r of chunk 0
+constexpr int OFF_SKEW = OFF_R0EXT + EXT;         // 128 rows x SKEW_STRIDE floats
 constexpr int OFF_BAR = OFF_SKEW + BM * SKEW_STRIDE * 4;
-constexpr int N_BAR = 1 + 4 * NS + 2 * NR + 8;
+constexpr int N_BAR = 1 + 2 * NP + 2 * NS + 1 + 8;
 constexpr int OFF_MISC = OFF_BAR + N_BAR * 8;
 constexpr int SMEM_USED = OFF_MISC + 16;
 constexpr int SMEM_BYTES = SMEM_USED + 1024;      // slack for the manual alignment
@@ -90,8 +99,8 @@ static_assert(OFF_UB % 1024 == 0, "swizzled tiles need 1024-byte alignment");
 
 struct Bars {
     uint64_t *q_full;
-    uint64_t *k_full, *k_empty, *v_full, *v_empty;
-    uint64_t *r_full, *r_empty;
+    uint64_t *pair_full, *pair_empty, *v_full, *v_empty;
+    uint64_t *r0_full;
     uint64_t *prep, *bias_full, *ext_full, *s_full, *s_free, *p_full, *o_done, *drain;
 };
 
@@ -100,13 +109,12 @@ __device__ __forceinline__ Bars make_bars(uint8_t *smem)
     uint64_t *b = reinterpret_cast<uint64_t *>(smem + OFF_BAR);
     Bars x;
     x.q_full = b;
-    x.k_full = b + 1;
-    x.k_empty = x.k_full + NS;
-    x.v_full = x.k_empty + NS;
+    x.pair_full = b + 1;
+    x.pair_empty = x.pair_full + NP;
+    x.v_full = x.pair_empty + NP;
     x.v_empty = x.v_full + NS;
-    x.r_full = x.v_empty + NS;
-    x.r_empty = x.r_full + NR;
-    x.prep = x.r_empty + NR;
+    x.r0_full = x.v_empty + NS;
+    x.prep = x.r0_full + 1;
     x.bias_full = x.prep + 1;
     x.ext_full = x.bias_full + 1;
     x.s_full = x.ext_full + 1;
@@ -219,6 +227,14 @@ __device__ __forceinline__ uint64_t sdesc_ext(uint32_t addr)
            ((uint64_t)(128u >> 4) << 32) | (1ull << 46);
 }
 
+// The same for a pair's 256 rows: the zero half (K columns 8..15) starts 4 KB
+// after the tile.
+__device__ __forceinline__ uint64_t sdesc_ext2(uint32_t addr)
+{
+    return (uint64_t)((addr & 0x3FFFFu) >> 4) | ((uint64_t)(4096u >> 4) << 16) |
+           ((uint64_t)(128u >> 4) << 32) | (1ull << 46);
+}
+
 // hi + lo bf16 pair whose sum is x to about 2^-17 relative.
 __device__ __forceinline__ uint32_t split_bf16(float x)
 {
@@ -276,16 +292,15 @@ __global__ void __launch_bounds__(256, 1)
 
     if (threadIdx.x == 0) {
         mbar_init(bar.q_full, 1);
+        for (int s = 0; s < NP; ++s) {
+            mbar_init(bar.pair_full + s, 1);
+            mbar_init(bar.pair_empty + s, 1);
+        }
         for (int s = 0; s < NS; ++s) {
-            mbar_init(bar.k_full + s, 1);
-            mbar_init(bar.k_empty + s, 1);
             mbar_init(bar.v_full + s, 1);
             mbar_init(bar.v_empty + s, 1);
         }
-        for (int s = 0; s < NR; ++s) {
-            mbar_init(bar.r_full + s, 1);
-            mbar_init(bar.r_empty + s, 1);
-        }
+        mbar_init(bar.r0_full, 1);
         mbar_init(bar.prep, 128);
         mbar_init(bar.bias_full, 1);
         mbar_init(bar.ext_full, 128);
@@ -320,45 +335,51 @@ __global__ void __launch_bounds__(256, 1)
             const uint64_t pol_stream = policy_evict_first();  // K, V: read once
             const uint64_t pol_keep = policy_evict_last();     // table: shared by the batch
             bool ok = true;
-            int kc = 0, vc = 0, rc = 0;  // copies issued into the K, V and table rings
-            auto load_r = [&](int c) -> bool {
-                const int rs = c % NR;
-                if (!mbar_wait(bar.r_empty + rs, ((c / NR) & 1) ^ 1, abort_flag, wait_ns))
+            int pc = 0, vc = 0;  // copies issued into the pair and V rings
+            // Pair t: key tile t and table chunk t+1, [keys ; chunk] for even t.
+            auto load_pair = [&](int t) -> bool {
+                const int ps = t % NP;
+                if (!mbar_wait(bar.pair_empty + ps, ((t / NP) & 1) ^ 1, abort_flag, wait_ns))
                     return false;
-                mbar_arrive_expect_tx(bar.r_full + rs, TILE);
-                tma_load_3d_hint(smem + OFF_R + rs * TILE, &tm_r, bar.r_full + rs, 0,
-                                 r_base + c * BN, h, pol_keep);
-                rc = c + 1;
+                const bool kfirst = (t & 1) == 0;
+                uint8_t *st = smem + OFF_PAIR + ps * PAIR;
+                mbar_arrive_expect_tx(bar.pair_full + ps, PAIR);
+                tma_load_3d_hint(st + (kfirst ? 0 : TILE), &tm_k, bar.pair_full + ps, 0,
+                                 (t_begin + t) * BN, bh, pol_stream);
+                tma_load_3d_hint(st + (kfirst ? TILE : 0), &tm_r, bar.pair_full + ps, 0,
+                                 r_base + (t + 1) * BN, h, pol_keep);
+                pc = t + 1;
+                return true;
+            };
+            auto load_v = [&](int t) -> bool {
+                const int st = t % NS;
+                if (!mbar_wait(bar.v_empty + st, ((t / NS) & 1) ^ 1, abort_flag, wait_ns))
+                    return false;
+                mbar_arrive_expect_tx(bar.v_full + st, TILE);
+                tma_load_3d_hint(smem + OFF_V + st * TILE, &tm_v, bar.v_full + st, 0,
+                                 (t_begin + t) * BN, bh, pol_stream);
+                vc = t + 1;
                 return true;
             };
             mbar_arrive_expect_tx(bar.q_full, TILE);
             tma_load_3d(smem + OFF_Q, &tm_q, bar.q_full, 0, i0, bh);
+            mbar_arrive_expect_tx(bar.r0_full, TILE);
+            tma_load_3d_hint(smem + OFF_R0, &tm_r, bar.r0_full, 0, r_base, h, pol_keep);
             for (int c = 0; c < min(PF, T); ++c) {
                 tma_prefetch_3d(&tm_k, 0, (t_begin + c) * BN, bh);
                 tma_prefetch_3d(&tm_v, 0, (t_begin + c) * BN, bh);
                 tma_prefetch_3d(&tm_r, 0, r_base + (c + 1) * BN, h);
             }
-            ok = load_r(0);
+            ok = load_pair(0);
             for (int it = 0; it < T && ok; ++it) {
                 const int t = t_begin + it;
-                const int st = it % NS;
-                const uint32_t ph = (it / NS) & 1;
                 if (it + PF < T) {
                     tma_prefetch_3d(&tm_k, 0, (t + PF) * BN, bh);
                     tma_prefetch_3d(&tm_v, 0, (t + PF) * BN, bh);
                     tma_prefetch_3d(&tm_r, 0, r_base + (it + PF + 1) * BN, h);
                 }
-                if (!(ok = mbar_wait(bar.k_empty + st, ph ^ 1, abort_flag, wait_ns))) break;
-                mbar_arrive_expect_tx(bar.k_full + st, TILE);
-                tma_load_3d_hint(smem + OFF_K + st * TILE, &tm_k, bar.k_full + st, 0, t * BN, bh,
-                                 pol_stream);
-                kc = it + 1;
-                if (!(ok = load_r(it + 1))) break;
-                if (!(ok = mbar_wait(bar.v_empty + st, ph ^ 1, abort_flag, wait_ns))) break;
-                mbar_arrive_expect_tx(bar.v_full + st, TILE);
-                tma_load_3d_hint(smem + OFF_V + st * TILE, &tm_v, bar.v_full + st, 0, t * BN, bh,
-                                 pol_stream);
-                vc = it + 1;
+                if (it + 1 < T && !(ok = load_pair(it + 1))) break;
+                if (!(ok = load_v(it))) break;
             }
             if (!ok) {
                 fail(p, abort_flag);
@@ -369,28 +390,28 @@ __global__ void __launch_bounds__(256, 1)
                 const int zero = 0;
                 const volatile int *nz = &zero;
                 mbar_wait(bar.q_full, 0, nz, wait_ns);
-                for (int c = max(0, kc - NS); c < kc; ++c)
-                    mbar_wait(bar.k_full + c % NS, (c / NS) & 1, nz, wait_ns);
+                mbar_wait(bar.r0_full, 0, nz, wait_ns);
+                for (int c = max(0, pc - NP); c < pc; ++c)
+                    mbar_wait(bar.pair_full + c % NP, (c / NP) & 1, nz, wait_ns);
                 for (int c = max(0, vc - NS); c < vc; ++c)
                     mbar_wait(bar.v_full + c % NS, (c / NS) & 1, nz, wait_ns);
-                for (int c = max(0, rc - NR); c < rc; ++c)
-                    mbar_wait(bar.r_full + c % NR, (c / NR) & 1, nz, wait_ns);
             }
         }
     } else if (warp == 1) {
         // ===================== MMA issuer =======================================
         if (lane == 0) {
             constexpr uint32_t ID_N128 = idesc_bf16_f32(128, 128, false);
+            constexpr uint32_t ID_N256 = idesc_bf16_f32(128, 256, false);
             constexpr uint32_t ID_N16 = idesc_bf16_f32(128, 16, false);
             constexpr uint32_t ID_O = idesc_bf16_f32(128, 64, true);
             const uint32_t sQ = smem_u32(smem + OFF_Q);
-            const uint32_t sK = smem_u32(smem + OFF_K);
+            const uint32_t sPair = smem_u32(smem + OFF_PAIR);
             const uint32_t sV = smem_u32(smem + OFF_V);
-            const uint32_t sR = smem_u32(smem + OFF_R);
+            const uint32_t sR0 = smem_u32(smem + OFF_R0);
             const uint32_t sUB = smem_u32(smem + OFF_UB);
             const uint32_t sAX = smem_u32(smem + OFF_AEXT);
-            const uint32_t sKX = smem_u32(smem + OFF_KEXT);
-            const uint32_t sRX = smem_u32(smem + OFF_REXT);
+            const uint32_t sPX = smem_u32(smem + OFF_PEXT);
+            const uint32_t sR0X = smem_u32(smem + OFF_R0EXT);
             const uint64_t d_aext = sdesc_ext(sAX);
 
             // [tile rows] x [u ; v]^T into a 16-column TMEM region.
@@ -400,79 +421,75 @@ __global__ void __launch_bounds__(256, 1)
                     mma_bf16_ss(tmem + tcol, sdesc_sw128(a_tile + kk * 32),
                                 sdesc_sw128(sUB + kk * 32), ID_N16, kk);
             };
-            // 128 x 128 scores q X^T (four K-steps), then the ext K-step that adds
-            // the bias pairs (ones x (hi, lo)).
-            auto score_main = [&](uint32_t tcol, uint32_t b_tile) {
+            auto pair_k = [&](int t) { return sPair + (t % NP) * PAIR + ((t & 1) ? TILE : 0); };
+            auto pair_r = [&](int t) { return sPair + (t % NP) * PAIR + ((t & 1) ? 0 : TILE); };
+            // Pair t times q: S of tile t and table chunk t+1 in one N = 256 MMA
+            // per K-step (results on [S | odd slot] or [even slot | S]), then
+            // the ext K-step adding both halves' bias pairs.
+            auto score_pair = [&](int t) {
+                const uint32_t dcol = (t & 1) ? TM_CA : TM_S;
+                const uint32_t b = sPair + (t % NP) * PAIR;
 #pragma unroll
                 for (int kk = 0; kk < DH / 16; ++kk)
-                    mma_bf16_ss(tmem + tcol, sdesc_sw128(sQ + kk * 32),
-                                sdesc_sw128(b_tile + kk * 32), ID_N128, kk);
+                    mma_bf16_ss(tmem + dcol, sdesc_sw128(sQ + kk * 32), sdesc_sw128(b + kk * 32),
+                                ID_N256, kk);
             };
-            auto score_ext = [&](uint32_t tcol, uint32_t ext_tile) {
-                mma_bf16_ss(tmem + tcol, d_aext, sdesc_ext(ext_tile), ID_N128, 1);
+            auto score_pair_ext = [&](int t) {
+                const uint32_t dcol = (t & 1) ? TM_CA : TM_S;
+                mma_bf16_ss(tmem + dcol, d_aext, sdesc_ext2(sPX + (t % NP) * EXT2), ID_N256, 1);
             };
-            auto score_mma = [&](uint32_t tcol, uint32_t b_tile, uint32_t ext_tile) {
-                score_main(tcol, b_tile);
-                score_ext(tcol, ext_tile);
-            };
-            auto wait_k = [&](int it) {
-                return mbar_wait(bar.k_full + it % NS, (it / NS) & 1, abort_flag, wait_ns);
-            };
-            auto wait_r = [&](int c) {
-                return mbar_wait(bar.r_full + c % NR, (c / NR) & 1, abort_flag, wait_ns);
+            auto wait_pair = [&](int t) {
+                return mbar_wait(bar.pair_full + t % NP, (t / NP) & 1, abort_flag, wait_ns);
             };
 
             bool ok = mbar_wait(bar.prep, 0, abort_flag, wait_ns) &&
                       mbar_wait(bar.q_full, 0, abort_flag, wait_ns);
-            // Prologue: biases of key tile 0 and table chunks 0 and 1.
-            if (ok) ok = wait_k(0) && wait_r(0) && wait_r(1);
+            // Prologue: biases of pair 0 (key tile 0, chunk 1) and of chunk 0.
+            if (ok) ok = wait_pair(0) && mbar_wait(bar.r0_full, 0, abort_flag, wait_ns);
             if (ok) {
                 tc_fence_after_sync();
-                bias_mma(TM_BK, sK);
-                bias_mma(TM_BR, sR);
-                bias_mma(TM_BR2, sR + (1 % NR) * TILE);
+                bias_mma(TM_BK, pair_k(0));
+                bias_mma(TM_BR, pair_r(0));
+                bias_mma(TM_BR2, sR0);
                 mma_commit(bar.bias_full);
             }
-            // Scores of tile 0: S(0), chunks 0 and 1.
+            // Scores of tile 0: pair 0 (S and chunk 1), chunk 0 into the even slot.
             if (ok) ok = mbar_wait(bar.ext_full, 0, abort_flag, wait_ns);
             if (ok) {
                 tc_fence_after_sync();
-                score_mma(TM_S, sK, sKX);
-                score_mma(TM_B, sR, sRX);
-                score_mma(TM_B + 128, sR + (1 % NR) * TILE, sRX + (1 % NR) * EXT);
+                score_pair(0);
+                score_pair_ext(0);
+#pragma unroll
+                for (int kk = 0; kk < DH / 16; ++kk)
+                    mma_bf16_ss(tmem + TM_CA, sdesc_sw128(sQ + kk * 32), sdesc_sw128(sR0 + kk * 32),
+                                ID_N128, kk);
+                mma_bf16_ss(tmem + TM_CA, d_aext, sdesc_ext(sR0X), ID_N128, 1);
                 mma_commit(bar.s_full);
-                mma_commit(bar.k_empty);
-                mma_commit(bar.r_empty + 0);
-                mma_commit(bar.r_empty + 1 % NR);
+                mma_commit(bar.pair_empty);
             }
-            // Biases of tile 1: key tile 1 and chunk 2.
+            // Biases of tile 1: pair 1 (key tile 1, chunk 2).
             if (ok && T > 1) {
-                ok = wait_k(1) && wait_r(2);
+                ok = wait_pair(1);
                 if (ok) {
                     tc_fence_after_sync();
-                    bias_mma(TM_BK, sK + (1 % NS) * TILE);
-                    bias_mma(TM_BR, sR + (2 % NR) * TILE);
+                    bias_mma(TM_BK, pair_k(1));
+                    bias_mma(TM_BR, pair_r(1));
                     mma_commit(bar.bias_full);
                 }
             }
             for (int it = 0; it < T && ok; ++it) {
                 if (!(ok = mbar_wait(bar.s_free, it & 1, abort_flag, wait_ns))) break;
                 if (it + 1 < T) {
-                    // Scores of tile it+1: S from key tile it+1, table chunk it+2
-                    // into the slot chunk it just left.  The bias K-steps wait for
-                    // the softmax warps' conversion; the main ones need not.
+                    // Scores of tile it+1: pair it+1, whose chunk it+2 goes into
+                    // the slot chunk it just left.  The bias K-step waits for the
+                    // softmax warps' conversion; the main ones need not.
                     tc_fence_after_sync();
-                    const int st = (it + 1) % NS;
-                    const int c = it + 2;
-                    score_main(TM_S, sK + st * TILE);
-                    score_main(TM_B + (c & 1) * 128, sR + (c % NR) * TILE);
+                    score_pair(it + 1);
                     if (!(ok = mbar_wait(bar.ext_full, (it + 1) & 1, abort_flag, wait_ns))) break;
                     tc_fence_after_sync();
-                    score_ext(TM_S, sKX + st * EXT);
-                    score_ext(TM_B + (c & 1) * 128, sRX + (c % NR) * EXT);
+                    score_pair_ext(it + 1);
                     mma_commit(bar.s_full);
-                    mma_commit(bar.k_empty + st);
-                    mma_commit(bar.r_empty + c % NR);
+                    mma_commit(bar.pair_empty + (it + 1) % NP);
                 }
                 if (!(ok = mbar_wait(bar.p_full, it & 1, abort_flag, wait_ns))) break;
                 const int st = it % NS;
@@ -486,13 +503,13 @@ __global__ void __launch_bounds__(256, 1)
                 mma_commit(bar.o_done);
                 mma_commit(bar.v_empty + st);
                 if (it + 2 < T) {
-                    // Biases of tile it+2: key tile it+2 and table chunk it+3.  Their
-                    // TMEM columns hold P until this PV has completed.
+                    // Biases of tile it+2: pair it+2 (key tile it+2, chunk it+3).
+                    // Their TMEM columns hold P until this PV has completed.
                     if (!(ok = mbar_wait(bar.o_done, it & 1, abort_flag, wait_ns))) break;
-                    if (!(ok = wait_k(it + 2) && wait_r(it + 3))) break;
+                    if (!(ok = wait_pair(it + 2))) break;
                     tc_fence_after_sync();
-                    bias_mma(TM_BK, sK + ((it + 2) % NS) * TILE);
-                    bias_mma(TM_BR, sR + ((it + 3) % NR) * TILE);
+                    bias_mma(TM_BK, pair_k(it + 2));
+                    bias_mma(TM_BR, pair_r(it + 2));
                     mma_commit(bar.bias_full);
                 }
             }
@@ -510,14 +527,16 @@ __global__ void __launch_bounds__(256, 1)
         const int i = i0 + row;
         const uint32_t lane_off = (uint32_t)(wq * 32) << 16;
         const uint32_t tS = tmem + lane_off + TM_S;
-        const uint32_t tB = tmem + lane_off + TM_B;
+        const uint32_t tB = tmem + lane_off;
         const uint32_t tO = tmem + lane_off + TM_O;
         const uint32_t skew = smem_u32(smem + OFF_SKEW) + (uint32_t)row * SKEW_STRIDE * 4;
         // Key y of a 32-key piece sits at column (31 - lane + y) of the two
         // staged window chunks.
         const uint32_t skew_rd = skew + (uint32_t)(31 - lane) * 4;
-        const uint32_t sKX = smem_u32(smem + OFF_KEXT);
-        const uint32_t sRX = smem_u32(smem + OFF_REXT);
+        const uint32_t sPX = smem_u32(smem + OFF_PEXT);
+        // bias rows of pair t: keys first for even t, the chunk first for odd t
+        auto pext_k = [&](int t) { return sPX + (t % NP) * EXT2 + ((t & 1) ? BM * 16 : 0); };
+        auto pext_r = [&](int t) { return sPX + (t % NP) * EXT2 + ((t & 1) ? 0 : BM * 16); };
 
         // ---- one-time operands: [u ; v] tile, ones column, zeroed ext tiles ----
         {
@@ -537,8 +556,8 @@ __global__ void __launch_bounds__(256, 1)
             *reinterpret_cast<uint4 *>(smem + OFF_AEXT + row * 16) =
                 make_uint4(0x3f803f80u, 0u, 0u, 0u);
             *reinterpret_cast<uint4 *>(smem + OFF_AEXT + 2048 + row * 16) = make_uint4(0, 0, 0, 0);
-            for (int o = row * 16; o < (NS + NR) * EXT; o += 128 * 16)
-                *reinterpret_cast<uint4 *>(smem + OFF_KEXT + o) = make_uint4(0, 0, 0, 0);
+            for (int o = row * 16; o < NP * EXT2 + EXT; o += 128 * 16)
+                *reinterpret_cast<uint4 *>(smem + OFF_PEXT + o) = make_uint4(0, 0, 0, 0);
             fence_proxy_async_smem();
             mbar_arrive(bar.prep);
         }
@@ -574,7 +593,7 @@ __global__ void __launch_bounds__(256, 1)
             return true;
         };
 
-        bool ok = convert(0, sKX, sRX, sRX + (1 % NR) * EXT);
+        bool ok = convert(0, pext_k(0), pext_r(0), smem_u32(smem + OFF_R0EXT));
 
         const uint64_t sl2x2 = pack2(p.scale_log2, p.scale_log2);
         float m_ref = -INFINITY;  // running max (scaled, log2 units), lazily updated
@@ -590,19 +609,23 @@ __global__ void __launch_bounds__(256, 1)
             // ---- gather: x[jj] = S[row][jj] + window[row][jj + 127 - row] -------
             // Window columns of this warp: [96-32wq, 96-32wq+160) of the virtual
             // 256-column window (five 32-column chunks); table chunk it sits in
-            // TMEM slot it&1, chunk it+1 in the other.  Each window chunk c goes
+            // the even- or odd-chunk TMEM slot by its parity, chunk it+1 in the
+            // other.  Each window chunk c goes
             // once through a 3-slot shared-memory ring (slot c % 3); key y of
             // piece pc is ring column (32*pc + 31 - lane + y), which for pc = 2
             // wraps from slot 2 to slot 0 when y > lane.
-            const uint32_t wbase = (uint32_t)((it & 1) * 128 + 96 - 32 * wq);
+            // window column w of this tile in TMEM: chunk it (w < 128) or it+1
+            const uint32_t slot0 = (it & 1) ? TM_CC : TM_CA, slot1 = (it & 1) ? TM_CA : TM_CC;
+            const uint32_t wbase = (uint32_t)(96 - 32 * wq);
+            auto wcol = [&](uint32_t w) { return w < 128u ? slot0 + w : slot1 + (w - 128u); };
             uint32_t bku = 0, bkv = 0, bru = 0, brv = 0;  // next tile's bias values
             float x[BN];
             float mx[8];  // 8 independent running-max chains over the gathered scores
 #pragma unroll
             for (int a = 0; a < 8; ++a) mx[a] = -INFINITY;
             uint32_t wa[32], wb[32], s[32];
-            tmem_ld32(tB + (wbase & 255u), wa);
-            tmem_ld32(tB + ((wbase + 32u) & 255u), wb);
+            tmem_ld32(tB + wcol(wbase), wa);
+            tmem_ld32(tB + wcol(wbase + 32u), wb);
             tmem_ld32(tS, s);
             tmem_wait_ld();
             reg_fence(wa);
@@ -620,7 +643,7 @@ __global__ void __launch_bounds__(256, 1)
                 // Next window chunk and next S piece are loaded while this piece
                 // is read from the ring.
                 if (pc + 1 < BN / 32) {
-                    tmem_ld32(tB + ((wbase + 32u * (pc + 2)) & 255u), wa);
+                    tmem_ld32(tB + wcol(wbase + 32u * (pc + 2)), wa);
                     tmem_ld32(tS + 32 * (pc + 1), wb);
                 }
                 if (pc + 1 == BN / 32 && it + 1 < T) {
@@ -671,10 +694,7 @@ __global__ void __launch_bounds__(256, 1)
             mbar_arrive(bar.s_free);
 
             // ---- biases of the next tile (key tile it+1, table chunk it+2) -------
-            if (it + 1 < T) {
-                const int st = (it + 1) % NS, c = it + 2;
-                convert_store(bku, brv, sKX + st * EXT, sRX + (c % NR) * EXT);
-            }
+            if (it + 1 < T) convert_store(bku, brv, pext_k(it + 1), pext_r(it + 1));
 
             // ---- mask (keys after the query, keys past K), tile max --------------
             const bool need_mask = (j0 + BN - 1 > i0 + p.M) || (j0 + BN > p.K);
