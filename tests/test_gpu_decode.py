@@ -101,6 +101,6 @@ def test_evaluation_speed_shapes(L, M):
     scale = 1.0 / math.sqrt(64)
     out, lse = run_gpu(case, M, scale)
     want, want_lse = run_oracle(case, M, scale)
-    tol = TOL if L <= 3 else 2e-2  # the tensor-core path rounds P to bf16
+    tol = TOL if L <= 6 else 2e-2  # the tensor-core path (L > 6) rounds P to bf16
     compare(out.float().cpu().numpy(), want, tol, 1e-2, what=f"window L={L} M={M}")
     compare(lse.cpu().numpy(), want_lse, 2e-2, what=f"lse window L={L} M={M}")
