@@ -111,7 +111,8 @@ size_t txl_relattn_workspace_size(int B, int H, int L, int dh, int n_splits);
  *   cores instead, all arithmetic in fp32 (no bf16 rounding of P); n_splits
  *   then counts key ranges per (b, h), each a whole number of 32-key chunks,
  *   at most one per 128 keys (larger requests are capped, ranges that would
- *   hold no key are dropped).
+ *   hold no key are dropped); up to 8 ranges of a head run as one thread-block
+ *   cluster and merge in distributed shared memory, needing no workspace.
  * dtype TXL_F32: every tensor is fp32 and the arithmetic is fp32 on the CUDA
  *   cores (no TF32).  dh must be 64.
  * M >= 0, L >= 1, r_rows >= K, B >= 1, H >= 1.

@@ -74,7 +74,8 @@ def attn(**kw):
     (dict(dh=32), UNSUPPORTED),
     (dict(q=16 + 2), MISALIGNED),
     (dict(r=8), MISALIGNED),
-    (dict(n_splits=2, M=1000, r_rows=1004), WORKSPACE),
+    (dict(n_splits=2, M=1000, L=16, r_rows=1016), WORKSPACE),   # tensor-core path
+    (dict(n_splits=12, M=2000, r_rows=2004), WORKSPACE),         # decode, beyond a cluster
     (dict(dtype=txl.F32, n_splits=2), UNSUPPORTED),
     (dict(dtype=txl.F32, k=2), MISALIGNED),
 ])

@@ -9,6 +9,7 @@ namespace txl {
 // Short-segment (decode) kernel: L <= kDecodeMaxL queries per (batch, head);
 // the keys are split into n_splits ranges of whole 32-key chunks.
 constexpr int kDecodeMaxL = 6;
+constexpr int kDecodeMaxCluster = 8;  // portable cluster size
 
 struct DecodeParams {
     int B, H, M, L, K;
@@ -26,6 +27,8 @@ struct DecodeParams {
     float *lse;               // [B][H][L] natural log or null
     float *part_o;            // [n_splits][B*H*L][64]   (n_splits > 1)
     float *part_lse;          // [n_splits][B*H*L], log2 domain
+    int cluster;              // 1: the n_splits ranges of a head are one thread-block
+                              // cluster and merge in distributed shared memory
     unsigned int *status;     // device status word
     unsigned long long wait_ns;
 };

@@ -52,7 +52,9 @@ constexpr int RING = NSTG * STAGE;              // per warp
 constexpr int OFF_BAR = WARPS * RING;
 constexpr int OFF_MERGE = OFF_BAR + WARPS * NSTG * 8;
 constexpr int MERGE_BYTES = WARPS * LMAX * (2 + DH) * 4;
-constexpr int OFF_FLAG = OFF_MERGE + MERGE_BYTES;
+constexpr int OFF_RES = OFF_MERGE + MERGE_BYTES;   // block result per row: o[64], lse
+constexpr int RES_BYTES = LMAX * (DH + 1) * 4;
+constexpr int OFF_FLAG = OFF_RES + RES_BYTES;
 constexpr int SMEM_BYTES = OFF_FLAG + 16;
 
 static_assert(STAGE % 16 == 0 && RING % 16 == 0, "bulk copies need 16-byte aligned stages");
@@ -101,6 +103,45 @@ __device__ __forceinline__ uint64_t mul2(uint64_t a, uint64_t b)
     uint64_t d;
     asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
     return d;
+}
+
+// Thread-block cluster: the key ranges of one head run as one cluster and merge
+// through distributed shared memory.
+__device__ __forceinline__ uint32_t cluster_rank()
+{
+    uint32_t r;
+    asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+    return r;
+}
+
+// Every thread of every block of the cluster: arrive (release) and wait (acquire).
+__device__ __forceinline__ void cluster_sync()
+{
+    asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::
+                     : "memory");
+}
+
+// Address of the same shared-memory location in block `rank` of the cluster.
+__device__ __forceinline__ uint32_t cluster_addr(uint32_t addr, uint32_t rank)
+{
+    uint32_t r;
+    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(addr), "r"(rank));
+    return r;
+}
+
+__device__ __forceinline__ float ld_cluster_f32(uint32_t addr)
+{
+    float v;
+    asm volatile("ld.shared::cluster.f32 %0, [%1];" : "=f"(v) : "r"(addr) : "memory");
+    return v;
+}
+
+__device__ __forceinline__ float2 ld_cluster_f32x2(uint32_t addr)
+{
+    float2 v;
+    asm volatile("ld.shared::cluster.v2.f32 {%0, %1}, [%2];" : "=f"(v.x), "=f"(v.y) : "r"(addr)
+                 : "memory");
+    return v;
 }
 
 // bf16 pair (dims 2c, 2c+1) as an fp32 pair.
@@ -359,11 +400,53 @@ __global__ void __launch_bounds__(WARPS * 32) relattn_decode_kernel(const Decode
             reinterpret_cast<__nv_bfloat162 *>(p.out + row * DH)[lane] =
                 __floats2bfloat162_rn(o0 * inv, o1 * inv);
             if (p.lse && lane == 0) p.lse[row] = lse2 * 0.69314718055994531f;
+        } else if (p.cluster) {
+            // this key range's normalised partial stays in shared memory
+            reinterpret_cast<float2 *>(smem + OFF_RES)[i * (DH / 2) + lane] =
+                make_float2(o0 * inv, o1 * inv);
+            if (lane == 0) reinterpret_cast<float *>(smem + OFF_RES)[LMAX * DH + i] = lse2;
         } else {
             const size_t prow = (size_t)split * p.B * p.H * L + row;
             reinterpret_cast<float2 *>(p.part_o + prow * DH)[lane] = make_float2(o0 * inv, o1 * inv);
             if (lane == 0) p.part_lse[prow] = lse2;
         }
+    }
+    if (p.cluster) {
+        // The key ranges of this head are the blocks of one cluster (rank =
+        // range): block 0 merges their partials through distributed shared
+        // memory, out = sum_r 2^(lse_r - max) o_r / sum_r 2^(lse_r - max).
+        // Every block reaches both cluster barriers (no early exits above).
+        cluster_sync();
+        if (cluster_rank() == 0) {
+            const uint32_t res = smem_u32(smem + OFF_RES);
+            for (int i = warp; i < L; i += WARPS) {
+                const uint32_t a_lse = res + (uint32_t)(LMAX * DH + i) * 4;
+                const uint32_t a_o = res + (uint32_t)(i * DH + 2 * lane) * 4;
+                float mx = -INFINITY;
+                for (int r = 0; r < p.n_splits; ++r)
+                    mx = fmaxf(mx, ld_cluster_f32(cluster_addr(a_lse, (uint32_t)r)));
+                float wsum = 0.f, c0 = 0.f, c1 = 0.f;
+                if (mx != -INFINITY) {
+                    for (int r = 0; r < p.n_splits; ++r) {
+                        const float lr = ld_cluster_f32(cluster_addr(a_lse, (uint32_t)r));
+                        if (lr == -INFINITY) continue;  // a range without keys
+                        const float w = ex2f(lr - mx);
+                        const float2 o = ld_cluster_f32x2(cluster_addr(a_o, (uint32_t)r));
+                        wsum += w;
+                        c0 = fmaf(w, o.x, c0);
+                        c1 = fmaf(w, o.y, c1);
+                    }
+                }
+                const float inv = (wsum > 0.f) ? 1.f / wsum : 0.f;
+                const size_t row = (size_t)bh * L + i;
+                reinterpret_cast<__nv_bfloat162 *>(p.out + row * DH)[lane] =
+                    __floats2bfloat162_rn(c0 * inv, c1 * inv);
+                if (p.lse && lane == 0)
+                    p.lse[row] = (wsum > 0.f) ? (mx + __log2f(wsum)) * 0.69314718055994531f
+                                              : -INFINITY;
+            }
+        }
+        cluster_sync();  // block 0 has read the others' shared memory
     }
 }
 
@@ -389,8 +472,25 @@ cudaError_t launch_l(const DecodeParams &p, cudaStream_t s)
 {
     const long long blocks = (long long)p.B * p.H * p.n_splits;
     if (blocks <= 0 || blocks > 0x7fffffffLL) return cudaErrorInvalidValue;
-    relattn_decode_kernel<L><<<(unsigned)blocks, WARPS * 32, SMEM_BYTES, s>>>(p);
-    return cudaGetLastError();
+    if (!p.cluster) {
+        relattn_decode_kernel<L><<<(unsigned)blocks, WARPS * 32, SMEM_BYTES, s>>>(p);
+        return cudaGetLastError();
+    }
+    // one cluster of n_splits blocks per (batch, head)
+    if (p.n_splits < 2 || p.n_splits > kDecodeMaxCluster) return cudaErrorInvalidValue;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)blocks, 1, 1);
+    cfg.blockDim = dim3(WARPS * 32, 1, 1);
+    cfg.dynamicSmemBytes = SMEM_BYTES;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = (unsigned)p.n_splits;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, relattn_decode_kernel<L>, p);
 }
 
 // Instances L = 1 .. kDecodeMaxL, indexed by L - 1.

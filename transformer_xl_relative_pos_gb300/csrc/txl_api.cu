@@ -122,8 +122,9 @@ int auto_splits(int units, int n_key_tiles)
     return s < 1 ? 1 : s;
 }
 
-// Short segments (L <= 8): split-K decode kernel on the CUDA cores, then the
-// log-sum-exp merge of the key ranges when there are several.
+// Short segments (L <= kDecodeMaxL): split-K decode kernel on the CUDA cores.
+// Up to kDecodeMaxCluster key ranges of a head merge inside their thread-block
+// cluster; more go through the workspace and the log-sum-exp merge kernel.
 int relattn_decode(const void *q, const void *k, const void *v, const void *r, int r_rows,
                    const void *u, const void *v_bias, void *out, float *lse, int B, int H, int M,
                    int L, float scale, int n_splits, void *workspace, size_t workspace_bytes,
@@ -134,22 +135,28 @@ int relattn_decode(const void *q, const void *k, const void *v, const void *r, i
     // At most one split per 128 keys (four 32-key chunks), and only splits that
     // own keys.
     const int max_splits = (int)((K + 127) / 128);
+    // Up to kDecodeMaxCluster key ranges of a head run as one thread-block
+    // cluster and merge in distributed shared memory; more need the workspace
+    // for their partial results and a merge kernel.
+    const int max_cluster = txl::kDecodeMaxCluster;
     int splits = n_splits;
     if (splits == 0) {
         // One wave of resident blocks: each block streams its key range
         // through its warps' copy rings, so long ranges amortise the first
         // copies' latency, and a second, partly filled wave would cost a full
-        // block time.  No more key ranges than the workspace holds.
+        // block time.  At most a cluster's worth of ranges: merging in the
+        // cluster beat more ranges merged through the workspace even where
+        // those would fill more SMs (one sequence of 16 heads, M = 3800: 8.4 us
+        // with 8 ranges, 9.0 us with 19).
         const long long slots = (long long)sm_count() * txl::decode_blocks_per_sm(L);
-        splits = (int)std::max<long long>(1, std::min<long long>(slots / BH, max_splits));
-        while (splits > 1 && (!workspace || !aligned(workspace, 256) ||
-                              workspace_bytes < workspace_bytes_for(B, H, L, 64, splits)))
-            --splits;
+        splits = (int)std::max<long long>(
+            1, std::min<long long>(std::min<long long>(slots / BH, max_splits), max_cluster));
     }
     if (splits > max_splits) splits = max_splits;
     // Drop splits that would own no keys once ranges are rounded to chunks.
     while (splits > 1 && (long long)(splits - 1) * txl::decode_span((int)K, splits) >= K) --splits;
-    if (splits > 1) {
+    const bool cluster = splits >= 2 && splits <= max_cluster;
+    if (splits > 1 && !cluster) {
         if (!workspace || workspace_bytes < workspace_bytes_for(B, H, L, 64, splits))
             return TXL_ERR_WORKSPACE;
         if (!aligned(workspace, 256)) return TXL_ERR_MISALIGNED;
@@ -171,6 +178,7 @@ int relattn_decode(const void *q, const void *k, const void *v, const void *r, i
     p.r_rows = r_rows;
     p.r_off = r_rows - (int)K;
     p.n_splits = splits;
+    p.cluster = cluster ? 1 : 0;
     p.scale_log2 = scale * 1.4426950408889634f;
     p.q = static_cast<const __nv_bfloat16 *>(q);
     p.k = static_cast<const __nv_bfloat16 *>(k);
@@ -180,7 +188,7 @@ int relattn_decode(const void *q, const void *k, const void *v, const void *r, i
     p.vb = static_cast<const __nv_bfloat16 *>(v_bias);
     p.out = static_cast<__nv_bfloat16 *>(out);
     p.lse = lse;
-    if (splits > 1) {
+    if (splits > 1 && !cluster) {
         const size_t rows = (size_t)BH * L;
         size_t off = (size_t)splits * rows * 64 * sizeof(float);
         off = (off + 255) & ~(size_t)255;
@@ -190,7 +198,7 @@ int relattn_decode(const void *q, const void *k, const void *v, const void *r, i
     }
     cudaError_t err = txl::launch_relattn_decode(p, s);
     if (err != cudaSuccess) return TXL_ERR_CUDA;
-    if (splits > 1) {
+    if (splits > 1 && !cluster) {
         err = txl::launch_relattn_combine(p.part_o, p.part_lse, p.out, lse, splits,
                                           (int)(BH * L), s);
         if (err != cudaSuccess) return TXL_ERR_CUDA;
