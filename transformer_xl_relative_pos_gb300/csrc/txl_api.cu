@@ -1,7 +1,8 @@
 // C-ABI entry points declared in include/txl.h: argument validation, TMA
 // descriptor construction, launch configuration and the device status word.
-// All arithmetic happens in the kernels (relattn_tc.cu, relattn_f32.cu,
-// relpos.cu, mem.cu); this file only checks and dispatches.
+// All arithmetic happens in the kernels (relattn_tc.cu, relattn_decode.cu,
+// relattn_combine.cu, relattn_f32.cu, relpos.cu, mem.cu); this file only
+// checks and dispatches.
 #include <algorithm>
 #include <cstdio>
 #include <cstring>
