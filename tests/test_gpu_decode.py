@@ -48,11 +48,12 @@ def test_decode_matches_oracle(L, M):
 
 
 @pytest.mark.parametrize("n_splits,workspace", [(1, False), (0, False), (3, True), (7, True),
-                                                (40, True)])
+                                                (8, False), (9, True), (40, True)])
 def test_decode_key_ranges(n_splits, workspace):
     # One block per head for all keys, the automatic choice without a
-    # workspace (no split possible), explicit splits, and more splits than
-    # 128-key chunks (capped).
+    # workspace, explicit splits merged inside a thread-block cluster (up to 8,
+    # no workspace needed) or through the workspace (9 and more), and more
+    # splits than 128-key chunks (capped).
     B, H, L, M = 2, 2, 3, 1500
     case = heads_case(B, H, L, M, seed=77 + n_splits)
     check(case, M, n_splits=n_splits, workspace=workspace, what=f"splits {n_splits}")
