@@ -425,6 +425,9 @@ def run_ours(args, world, rank, local):
     flops_step = w.flops()
     value = flops_step * K * world / (t_ms * 1e-3) / 1e12
     tokens = w.B * w.L * K * world / (t_ms * 1e-3)
+    # "useful" work: only the scores a query may see (j <= M + i), i.e.
+    # L*M + L(L+1)/2 of the L*K pairs per head
+    visible = (w.L * w.M + w.L * (w.L + 1) // 2) / (w.L * (w.M + w.L))
 
     # ---- end to end through the public API with host buffers ----------------
     e2e = None
@@ -517,6 +520,7 @@ def run_ours(args, world, rank, local):
                    "launch": f"CUDA graph of {chunk} steps x {reps} replays"},
         "tokens_per_s": tokens,
         "pct_bf16_peak": 100.0 * value / pk["bf16_tflops"],
+        "useful_tflops": value * visible,
         "attn_us": attn_ms * 1e3,
         "clocks": clocks,
         "e2e": e2e,
