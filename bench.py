@@ -91,6 +91,9 @@ def parse_args():
     ap.add_argument("--decode", action="store_true",
                     help="time decode-shaped calls (a few new tokens against a long memory) "
                          "and their HBM bandwidth, instead of the headline step")
+    ap.add_argument("--configs", action="store_true",
+                    help="time one attention call of every bf16 workload shape, instead of the "
+                         "headline step")
     ap.add_argument("--shapes", nargs="*", default=None,
                     help="with --decode: B,L,M triples (default: the long-memory decode set)")
     ap.add_argument("--calls", type=int, default=10,
@@ -630,6 +633,29 @@ def run_decode(args):
             "path": "decode kernel" if L <= 6 else "tensor-core kernel"}}), flush=True)
 
 
+def run_configs(args):
+    """Graph-replayed attention calls of every bf16 workload shape (random
+    operands, rotating input sets larger than L2): TFLOP/s, fraction of the
+    bf16 peak and HBM bandwidth per shape."""
+    import torch
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    pk = peaks()
+    for name, w in txl_inputs.WORKLOADS.items():
+        if w.dtype != "bf16" or name.startswith("c5"):
+            continue  # c5 is the stack; its attention call is c2's shape
+        K = w.M + w.L
+        nbytes = 2 * (2 * w.B * w.H * w.L * 64 + 2 * w.B * w.H * K * 64 + w.H * K * 64)
+        n_sets = max(1, min(3, -(-3 * 126 * 2 ** 20 // nbytes)))
+        us = attn_call_us(w.B, w.H, w.L, w.M, reps=args.calls, per=30, n_sets=n_sets)
+        tflops = w.flops() / (us * 1e-6) / 1e12
+        print(json.dumps({"config": {
+            "workload": name, "B": w.B, "H": w.H, "L": w.L, "M": w.M, "dtype": "bf16",
+            "us_per_call": us, "tflops": tflops, "pct_bf16_peak": 100.0 * tflops / pk["bf16_tflops"],
+            "achieved_gbs": nbytes / (us * 1e-6) / 1e9, "hbm_frac": nbytes / (us * 1e-6) / 1e9 / pk["hbm_gbs"],
+            "input_sets": n_sets}}), flush=True)
+
+
 def run_stack(args):
     """Per-segment time of the streaming stack on the 12-layer, 16-segment
     workload (B=16, H=8, L=M=512, d=512), memories full, with and without the
@@ -674,6 +700,9 @@ def main():
         return
     if args.decode:
         run_decode(args)
+        return
+    if args.configs:
+        run_configs(args)
         return
     world, rank, local = dist_setup(args)
     if args.impl == "reference":
