@@ -51,8 +51,8 @@ import txl_inputs  # noqa: E402
 PROFILED_TRAFFIC = {
     "workload": "c3_word_large_L128_M1600",
     "sources": ("relattn_tc.cu", "ptx.cuh", "kernels.h"),
-    "sha256": "12c5e7c622f4ad5a73dcad9bb0143bc3dc3456078d5696609a51511ba3ca3f72",
-    "bytes_per_launch": 121081600 + 2525952,
+    "sha256": "e51616e453c3ecd35576a6c9d5bd5bd6630d75341b316055df6e6b90ff387c91",
+    "bytes_per_launch": 121106944 + 2579200,
 }
 
 

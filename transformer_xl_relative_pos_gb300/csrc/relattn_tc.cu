@@ -381,6 +381,31 @@ __global__ void __launch_bounds__(256, 1)
                 if (it + 1 < T && !(ok = load_pair(it + 1))) break;
                 if (!(ok = load_v(it))) break;
             }
+            if (ok) {
+                // The block that will most likely take this SM next (one block
+                // per SM, launched in index order): pull its first q, key,
+                // value tiles and table chunks into L2 so that its start does
+                // not wait on HBM.
+                uint32_t nsm;
+                asm("mov.u32 %0, %%nsmid;" : "=r"(nsm));
+                int nw = (int)blockIdx.x + (int)nsm;
+                if (nw < (int)gridDim.x) {
+                    const int n_split = nw % p.n_splits;
+                    nw /= p.n_splits;
+                    const int n_qt = nw % p.n_qtiles;
+                    const int n_bh = nw / p.n_qtiles;
+                    const int n_i0 = n_qt * BM;
+                    const int n_jmax = min(p.K - 1, p.M + n_i0 + min(BM, p.L - n_i0) - 1);
+                    const int n_per = (n_jmax / BN + 1 + p.n_splits - 1) / p.n_splits;
+                    const int n_tb = n_split * n_per;
+                    const int n_rbase = p.L - BM - n_i0 + p.r_off + n_tb * BN;
+                    tma_prefetch_3d(&tm_q, 0, n_i0, n_bh);
+                    tma_prefetch_3d(&tm_k, 0, n_tb * BN, n_bh);
+                    tma_prefetch_3d(&tm_v, 0, n_tb * BN, n_bh);
+                    tma_prefetch_3d(&tm_r, 0, n_rbase, n_bh % p.H);
+                    tma_prefetch_3d(&tm_r, 0, n_rbase + BN, n_bh % p.H);
+                }
+            }
             if (!ok) {
                 fail(p, abort_flag);
                 // Drain: let every copy this thread started land before the block
@@ -454,15 +479,19 @@ __global__ void __launch_bounds__(256, 1)
                 mma_commit(bar.bias_full);
             }
             // Scores of tile 0: pair 0 (S and chunk 1), chunk 0 into the even slot.
-            if (ok) ok = mbar_wait(bar.ext_full, 0, abort_flag, wait_ns);
+            // The main K-steps go right behind the bias MMAs; only the two bias
+            // K-steps wait for the softmax warps' conversion.
             if (ok) {
-                tc_fence_after_sync();
                 score_pair(0);
-                score_pair_ext(0);
 #pragma unroll
                 for (int kk = 0; kk < DH / 16; ++kk)
                     mma_bf16_ss(tmem + TM_CA, sdesc_sw128(sQ + kk * 32), sdesc_sw128(sR0 + kk * 32),
                                 ID_N128, kk);
+                ok = mbar_wait(bar.ext_full, 0, abort_flag, wait_ns);
+            }
+            if (ok) {
+                tc_fence_after_sync();
+                score_pair_ext(0);
                 mma_bf16_ss(tmem + TM_CA, d_aext, sdesc_ext(sR0X), ID_N128, 1);
                 mma_commit(bar.s_full);
                 mma_commit(bar.pair_empty);
