@@ -361,16 +361,18 @@ __global__ void __launch_bounds__(256, 1)
                 vc = t + 1;
                 return true;
             };
-            mbar_arrive_expect_tx(bar.q_full, TILE);
-            tma_load_3d(smem + OFF_Q, &tm_q, bar.q_full, 0, i0, bh);
+            // The first biases need pair 0 and chunk 0, q only the scores after
+            // them: copies in that order, then the L2 prefetches.
+            ok = load_pair(0);
             mbar_arrive_expect_tx(bar.r0_full, TILE);
             tma_load_3d_hint(smem + OFF_R0, &tm_r, bar.r0_full, 0, r_base, h, pol_keep);
+            mbar_arrive_expect_tx(bar.q_full, TILE);
+            tma_load_3d(smem + OFF_Q, &tm_q, bar.q_full, 0, i0, bh);
             for (int c = 0; c < min(PF, T); ++c) {
                 tma_prefetch_3d(&tm_k, 0, (t_begin + c) * BN, bh);
                 tma_prefetch_3d(&tm_v, 0, (t_begin + c) * BN, bh);
                 tma_prefetch_3d(&tm_r, 0, r_base + (c + 1) * BN, h);
             }
-            ok = load_pair(0);
             for (int it = 0; it < T && ok; ++it) {
                 const int t = t_begin + it;
                 if (it + PF < T) {
@@ -467,9 +469,9 @@ __global__ void __launch_bounds__(256, 1)
                 return mbar_wait(bar.pair_full + t % NP, (t / NP) & 1, abort_flag, wait_ns);
             };
 
-            bool ok = mbar_wait(bar.prep, 0, abort_flag, wait_ns) &&
-                      mbar_wait(bar.q_full, 0, abort_flag, wait_ns);
-            // Prologue: biases of pair 0 (key tile 0, chunk 1) and of chunk 0.
+            // Prologue: biases of pair 0 (key tile 0, chunk 1) and of chunk 0
+            // (they need the [u ; v] tile, not q).
+            bool ok = mbar_wait(bar.prep, 0, abort_flag, wait_ns);
             if (ok) ok = wait_pair(0) && mbar_wait(bar.r0_full, 0, abort_flag, wait_ns);
             if (ok) {
                 tc_fence_after_sync();
@@ -481,7 +483,9 @@ __global__ void __launch_bounds__(256, 1)
             // Scores of tile 0: pair 0 (S and chunk 1), chunk 0 into the even slot.
             // The main K-steps go right behind the bias MMAs; only the two bias
             // K-steps wait for the softmax warps' conversion.
+            if (ok) ok = mbar_wait(bar.q_full, 0, abort_flag, wait_ns);
             if (ok) {
+                tc_fence_after_sync();
                 score_pair(0);
 #pragma unroll
                 for (int kk = 0; kk < DH / 16; ++kk)
