@@ -51,8 +51,8 @@ import txl_inputs  # noqa: E402
 PROFILED_TRAFFIC = {
     "workload": "c3_word_large_L128_M1600",
     "sources": ("relattn_tc.cu", "ptx.cuh", "kernels.h"),
-    "sha256": "e51616e453c3ecd35576a6c9d5bd5bd6630d75341b316055df6e6b90ff387c91",
-    "bytes_per_launch": 121106944 + 2579200,
+    "sha256": "2a366df086e48b87c46e7976438c5b36849f6464343b68d1e82dafc35e15ec49",
+    "bytes_per_launch": 121106688 + 2542336,
 }
 
 
