@@ -257,11 +257,15 @@ __global__ void __launch_bounds__(256, 1)
     const int lane = threadIdx.x & 31;
 
     // ---- work of this block: (b*H + h, query tile, key split) -----------------
+    // Query tiles go last-first over the grid: later tiles see more keys (the
+    // causal edge), so the longest blocks start first and the shorter ones
+    // fill the last wave.
     int wid = blockIdx.x;
     const int split = wid % p.n_splits;
     wid /= p.n_splits;
-    const int qt = wid % p.n_qtiles;
-    const int bh = wid / p.n_qtiles;
+    const int n_bh = p.B * p.H;
+    const int qt = p.n_qtiles - 1 - wid / n_bh;
+    const int bh = wid % n_bh;
     const int h = bh % p.H;
     const int i0 = qt * BM;
     const int rows_valid = min(BM, p.L - i0);
@@ -394,18 +398,18 @@ __global__ void __launch_bounds__(256, 1)
                 if (nw < (int)gridDim.x) {
                     const int n_split = nw % p.n_splits;
                     nw /= p.n_splits;
-                    const int n_qt = nw % p.n_qtiles;
-                    const int n_bh = nw / p.n_qtiles;
+                    const int n_qt = p.n_qtiles - 1 - nw / n_bh;
+                    const int nx_bh = nw % n_bh;
                     const int n_i0 = n_qt * BM;
                     const int n_jmax = min(p.K - 1, p.M + n_i0 + min(BM, p.L - n_i0) - 1);
                     const int n_per = (n_jmax / BN + 1 + p.n_splits - 1) / p.n_splits;
                     const int n_tb = n_split * n_per;
                     const int n_rbase = p.L - BM - n_i0 + p.r_off + n_tb * BN;
-                    tma_prefetch_3d(&tm_q, 0, n_i0, n_bh);
-                    tma_prefetch_3d(&tm_k, 0, n_tb * BN, n_bh);
-                    tma_prefetch_3d(&tm_v, 0, n_tb * BN, n_bh);
-                    tma_prefetch_3d(&tm_r, 0, n_rbase, n_bh % p.H);
-                    tma_prefetch_3d(&tm_r, 0, n_rbase + BN, n_bh % p.H);
+                    tma_prefetch_3d(&tm_q, 0, n_i0, nx_bh);
+                    tma_prefetch_3d(&tm_k, 0, n_tb * BN, nx_bh);
+                    tma_prefetch_3d(&tm_v, 0, n_tb * BN, nx_bh);
+                    tma_prefetch_3d(&tm_r, 0, n_rbase, nx_bh % p.H);
+                    tma_prefetch_3d(&tm_r, 0, n_rbase + BN, nx_bh % p.H);
                 }
             }
             if (!ok) {
