@@ -51,8 +51,8 @@ import txl_inputs  # noqa: E402
 PROFILED_TRAFFIC = {
     "workload": "c3_word_large_L128_M1600",
     "sources": ("relattn_tc.cu", "ptx.cuh", "kernels.h"),
-    "sha256": "2a366df086e48b87c46e7976438c5b36849f6464343b68d1e82dafc35e15ec49",
-    "bytes_per_launch": 121106688 + 2542336,
+    "sha256": "5a973654892192a6f00ea2abcc8addb581f1a096b3609df596c9535df53cb40c",
+    "bytes_per_launch": 121076480 + 2540288,
 }
 
 
