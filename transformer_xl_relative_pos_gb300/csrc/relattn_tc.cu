@@ -28,7 +28,9 @@
 // The bias terms u.k_j and v.r_rho are exact in fp32: q enters the MMA as
 // given, and the biases come from small MMAs [K tile | table chunk] x [u ; v]^T
 // whose fp32 results the softmax warps split into bf16 hi + lo pairs; a fifth
-// MMA K-step multiplies a column of ones by those pairs.
+// MMA K-step multiplies a column of ones by those pairs.  The same pairs carry
+// the causal mask: a hidden key (j > i + M, or j >= K) always meets a table row
+// past the end of r, whose pair is (-inf, 0), so its score comes out -inf.
 //
 // P goes from the softmax registers to TMEM (tcgen05.st) and the PV product
 // takes its A operand from there.
@@ -39,7 +41,7 @@
 //   warp 1      MMA issuer (one thread)
 //   warp 2      TMEM allocator
 //   warps 4..7  softmax: thread = query row.  Per tile: gather S + shifted
-//               window, mask, running max (lazy rescale), exp2, P (bf16) to
+//               window, running max (lazy rescale), exp2, P (bf16) to
 //               TMEM; convert the next tile's biases; finally O / l.
 //
 // Every barrier wait is bounded: on time-out the block records an error in the
@@ -599,11 +601,22 @@ __global__ void __launch_bounds__(256, 1)
             mbar_arrive(bar.prep);
         }
 
+        // The causal mask lives in the table biases.  A key j is hidden from
+        // query i exactly when its distance M + i - j is negative (j > i + M, and
+        // every key past K), i.e. when the window reads a table row past the end
+        // of r.  TMA fills those rows with zeros, and their bias becomes
+        // (hi, lo) = (-inf, 0), so the score MMA writes -inf there and the
+        // softmax needs no mask of its own.  Table row of this thread in
+        // chunk c, relative to the end of r: rmask + c*BN (masked when >= 0).
+        const int rmask = r_base + row - (p.K + p.r_off);
+        auto r_bias = [&](uint32_t rv, int c) {
+            return (rmask + c * BN >= 0) ? 0x0000FF80u : split_bf16(__uint_as_float(rv));
+        };
         // Second half of a bias conversion: (hi, lo) pairs of already loaded
-        // fp32 k.u and v.r values into the ext tiles.
-        auto convert_store = [&](uint32_t ku, uint32_t rv, uint32_t kext, uint32_t rext) {
+        // fp32 k.u and v.r values (table chunk c) into the ext tiles.
+        auto convert_store = [&](uint32_t ku, uint32_t rv, int c, uint32_t kext, uint32_t rext) {
             st_shared_b32(kext + row * 16, split_bf16(__uint_as_float(ku)));
-            st_shared_b32(rext + row * 16, split_bf16(__uint_as_float(rv)));
+            st_shared_b32(rext + row * 16, r_bias(rv, c));
             fence_proxy_async_smem();
             tc_fence_before_sync();
             mbar_arrive(bar.ext_full);
@@ -622,8 +635,8 @@ __global__ void __launch_bounds__(256, 1)
             asm volatile("tcgen05.wait::ld.sync.aligned;"
                          : "+r"(ku), "+r"(kv), "+r"(ru), "+r"(rv), "+r"(r2u), "+r"(r2v)::"memory");
             st_shared_b32(kext + row * 16, split_bf16(__uint_as_float(ku)));
-            st_shared_b32(rext + row * 16, split_bf16(__uint_as_float(rv)));
-            if (rext2) st_shared_b32(rext2 + row * 16, split_bf16(__uint_as_float(r2v)));
+            st_shared_b32(rext + row * 16, r_bias(rv, 1));
+            if (rext2) st_shared_b32(rext2 + row * 16, r_bias(r2v, 0));
             fence_proxy_async_smem();
             tc_fence_before_sync();
             mbar_arrive(bar.ext_full);
@@ -638,7 +651,6 @@ __global__ void __launch_bounds__(256, 1)
         const uint32_t tP = tmem + lane_off + TM_P;
 
         for (int it = 0; it < T && ok; ++it) {
-            const int j0 = (t_begin + it) * BN;
             ok = __all_sync(0xffffffffu, mbar_wait(bar.s_full, it & 1, abort_flag, wait_ns));
             if (!ok) break;
             tc_fence_after_sync();
@@ -731,25 +743,9 @@ __global__ void __launch_bounds__(256, 1)
             mbar_arrive(bar.s_free);
 
             // ---- biases of the next tile (key tile it+1, table chunk it+2) -------
-            if (it + 1 < T) convert_store(bku, brv, pext_k(it + 1), pext_r(it + 1));
+            if (it + 1 < T) convert_store(bku, brv, it + 2, pext_k(it + 1), pext_r(it + 1));
 
-            // ---- mask (keys after the query, keys past K), tile max --------------
-            const bool need_mask = (j0 + BN - 1 > i0 + p.M) || (j0 + BN > p.K);
-            if (need_mask) {
-                const int jlim = min(i + p.M, p.K - 1) - j0;  // last visible key (tile-local)
-#pragma unroll
-                for (int a = 0; a < 8; ++a) mx[a] = -INFINITY;
-#pragma unroll
-                for (int jj = 0; jj < BN; ++jj)
-                    if (jj > jlim) x[jj] = -INFINITY;
-#pragma unroll
-                for (int pc = 0; pc < BN / 32; ++pc)
-#pragma unroll
-                    for (int a = 0; a < 8; ++a) {
-                        mx[a] = max3f(mx[a], x[32 * pc + 4 * a], x[32 * pc + 4 * a + 1]);
-                        mx[a] = max3f(mx[a], x[32 * pc + 4 * a + 2], x[32 * pc + 4 * a + 3]);
-                    }
-            }
+            // ---- tile max (masked keys hold -inf) ----------------------------------
             float mt = max3f(max3f(mx[0], mx[1], mx[2]), max3f(mx[3], mx[4], mx[5]),
                              fmaxf(mx[6], mx[7]));
             mt *= p.scale_log2;  // scores scale by a positive constant
