@@ -706,17 +706,20 @@ __global__ void __launch_bounds__(256, 1)
                     }
                 }
                 const uint32_t rd = skew_rd + (uint32_t)((pc % 3) * 128);
+                float wv[32];
                 if (pc % 3 == 2) {
 #pragma unroll
-                    for (int y = 0; y < 32; ++y) {
-                        const uint32_t a = rd + y * 4 - ((y > lane) ? 384u : 0u);
-                        x[32 * pc + y] = __uint_as_float(s[y]) + ld_shared_f32(a);
-                    }
+                    for (int y = 0; y < 32; ++y)
+                        wv[y] = ld_shared_f32(rd + y * 4 - ((y > lane) ? 384u : 0u));
                 } else {
 #pragma unroll
-                    for (int y = 0; y < 32; ++y)
-                        x[32 * pc + y] = __uint_as_float(s[y]) + ld_shared_f32(rd + y * 4);
+                    for (int y = 0; y < 32; ++y) wv[y] = ld_shared_f32(rd + y * 4);
                 }
+#pragma unroll
+                for (int k = 0; k < 16; ++k)
+                    unpack2(add2(pack2(__uint_as_float(s[2 * k]), __uint_as_float(s[2 * k + 1])),
+                                 pack2(wv[2 * k], wv[2 * k + 1])),
+                            x[32 * pc + 2 * k], x[32 * pc + 2 * k + 1]);
 #pragma unroll
                 for (int a = 0; a < 8; ++a) {
                     mx[a] = max3f(mx[a], x[32 * pc + 4 * a], x[32 * pc + 4 * a + 1]);
