@@ -51,8 +51,8 @@ import txl_inputs  # noqa: E402
 PROFILED_TRAFFIC = {
     "workload": "c3_word_large_L128_M1600",
     "sources": ("relattn_tc.cu", "ptx.cuh", "kernels.h"),
-    "sha256": "5a973654892192a6f00ea2abcc8addb581f1a096b3609df596c9535df53cb40c",
-    "bytes_per_launch": 121076480 + 2540288,
+    "sha256": "a7b1496112f5ed656ca45896b82b45d80349332c8ad14e8d9989da9fb8ea7cce",
+    "bytes_per_launch": 121077248 + 2568448,
 }
 
 
