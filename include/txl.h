@@ -84,6 +84,29 @@ int txl_rel_pos_emb(void *R, int K, int d_model, int dtype, void *stream);
  */
 size_t txl_relattn_workspace_size(int B, int H, int L, int dh, int n_splits);
 
+/* Kernels txl_relattn_fwd may run (reported by txl_relattn_plan). */
+typedef enum {
+    TXL_KERNEL_TC = 1,     /* bf16: tensor cores (tcgen05, TMEM, TMA), 128-row query tiles */
+    TXL_KERNEL_DECODE = 2, /* bf16, L <= 6: split-K kernel on the CUDA cores */
+    TXL_KERNEL_F32 = 3     /* fp32: CUDA cores */
+} txl_kernel;
+
+/*
+ * txl_relattn_plan - the kernel and the split txl_relattn_fwd would use for a
+ * call with these arguments and a workspace of `workspace_bytes` bytes (0 = no
+ * workspace; a non-zero size stands for a 256-byte aligned workspace).  Host
+ * arithmetic plus cached device attributes of the current device; launches
+ * nothing.
+ *   *kernel  a txl_kernel value
+ *   *splits  key ranges per query tile (TXL_KERNEL_TC) or per (b, h)
+ *            (TXL_KERNEL_DECODE); 1 for TXL_KERNEL_F32
+ * Returns the status the call would return for its sizes (TXL_ERR_WORKSPACE
+ * when the split needs more workspace than given), or TXL_ERR_INVALID_ARG for
+ * NULL outputs.
+ */
+int txl_relattn_plan(int B, int H, int M, int L, int r_rows, int dh, int dtype, int n_splits,
+                     size_t workspace_bytes, int *kernel, int *splits);
+
 /*
  * txl_relattn_fwd - forward relative-position attention of one layer over the
  * extended context (§3.2 recurrence, §3.3 score and N-layer summary,
@@ -107,9 +130,13 @@ size_t txl_relattn_workspace_size(int B, int H, int L, int dh, int n_splits);
  * dtype TXL_BF16: q, k, v, r, u, v_bias and out are bf16; scores, softmax and
  *   accumulation are fp32 on the tensor cores (tcgen05).  dh must be 64; q, k,
  *   v and r must be 16-byte aligned.  Segments of L <= 6 queries (decoding a
- *   few new tokens against a long memory) take a split-K kernel on the CUDA
- *   cores instead, all arithmetic in fp32 (no bf16 rounding of P); n_splits
- *   then counts key ranges per (b, h), each a whole number of 32-key chunks,
+ *   few new tokens against a long memory) can take a split-K kernel on the CUDA
+ *   cores instead, all arithmetic in fp32 (no bf16 rounding of P): always when
+ *   n_splits >= 1, and with n_splits = 0 when its estimated time is below the
+ *   tensor-core kernel's (short memories, several sequences; one sequence
+ *   against a long memory goes to the tensor cores from L of about 4 or 5 on;
+ *   txl_relattn_plan tells which).  For this kernel n_splits
+ *   counts key ranges per (b, h), each a whole number of 32-key chunks,
  *   at most one per 128 keys (larger requests are capped, ranges that would
  *   hold no key are dropped); up to 8 ranges of a head run as one thread-block
  *   cluster and merge in distributed shared memory, needing no workspace.

@@ -7,6 +7,7 @@ import os
 import re
 
 import pytest
+import torch
 
 import transformer_xl_relative_pos_gb300 as txl
 
@@ -48,6 +49,36 @@ def test_workspace_size_arithmetic():
     o = 3 * rows * 64 * 4
     o = (o + 255) // 256 * 256
     assert txl.workspace_size(16, 16, 128, 64, 3) == o + 3 * rows * 4
+
+
+def test_relattn_plan_validation_and_routing():
+    # Host arithmetic only.  Without a GPU the SM count is taken as GB300's 152.
+    k, n = ctypes.c_int(0), ctypes.c_int(0)
+    plan = txl.lib().txl_relattn_plan
+    assert plan(1, 16, 100, 4, 104, 64, txl.BF16, 0, 0, None, ctypes.byref(n)) == INVALID
+    assert plan(1, 16, 100, 4, 103, 64, txl.BF16, 0, 0, ctypes.byref(k), ctypes.byref(n)) == SHAPE
+    assert plan(1, 16, 100, 4, 104, 32, txl.BF16, 0, 0, ctypes.byref(k), ctypes.byref(n)) == UNSUPPORTED
+    assert plan(1, 16, 100, 0, 100, 64, txl.BF16, 0, 0, ctypes.byref(k), ctypes.byref(n)) == INVALID
+    assert plan(1, 16, 100, 4, 104, 64, 7, 0, 0, ctypes.byref(k), ctypes.byref(n)) == INVALID
+    assert plan(1, 1, 16, 16, 32, 64, txl.F32, 2, 0, ctypes.byref(k), ctypes.byref(n)) == UNSUPPORTED
+    assert txl.relattn_plan(1, 1, 16, 16, torch.float32) == ("f32", 1)
+    ws = 1 << 30
+    # Segments past six queries always take the tensor cores; the headline shape
+    # (256 query tiles on 152 SMs) is not split.
+    assert txl.relattn_plan(16, 16, 1600, 128, workspace_bytes=ws) == ("tc", 1)
+    assert txl.relattn_plan(8, 16, 3800, 7, workspace_bytes=ws)[0] == "tc"
+    # An explicit split of a short segment counts decode key ranges.
+    assert txl.relattn_plan(8, 16, 3800, 6, n_splits=3, workspace_bytes=ws) == ("decode", 3)
+    # The automatic choice for short segments follows the two kernels' estimates.
+    assert txl.relattn_plan(8, 16, 3800, 1, workspace_bytes=ws)[0] == "decode"
+    assert txl.relattn_plan(2, 16, 800, 6, workspace_bytes=ws)[0] == "decode"
+    assert txl.relattn_plan(1, 16, 3800, 6, workspace_bytes=ws)[0] == "tc"
+    # Without a workspace the tensor-core kernel cannot split one sequence's
+    # keys, and the decode kernel (which merges inside a cluster) is cheaper.
+    assert txl.relattn_plan(1, 16, 3800, 6, workspace_bytes=0)[0] == "decode"
+    # An explicit tensor-core split needs its workspace.
+    assert plan(16, 16, 1600, 128, 1728, 64, txl.BF16, 4, 0, ctypes.byref(k),
+                ctypes.byref(n)) == WORKSPACE
 
 
 L = txl.lib

@@ -105,3 +105,35 @@ def test_evaluation_speed_shapes(L, M):
     tol = TOL if L <= 6 else 2e-2  # the tensor-core path (L > 6) rounds P to bf16
     compare(out.float().cpu().numpy(), want, tol, 1e-2, what=f"window L={L} M={M}")
     compare(lse.cpu().numpy(), want_lse, 2e-2, what=f"lse window L={L} M={M}")
+
+
+# Which kernel takes a short segment is the library's estimate (n_splits = 0):
+# one sequence of 16 heads against a long memory goes to the tensor cores from
+# about four queries on; several sequences or short memories stay on the decode
+# kernel; an explicit split always means the decode kernel.  Both routes keep
+# the same tolerances.
+@pytest.mark.parametrize("B,L,M,want", [(1, 4, 8000, "tc"), (1, 5, 3800, "tc"), (1, 6, 3800, "tc"),
+                                        (1, 3, 12000, "tc"), (2, 6, 800, "decode"),
+                                        (8, 1, 3800, "decode"), (1, 6, 1600, "decode")])
+def test_short_segment_routing(B, L, M, want):
+    H = 16
+    ws_bytes = max(txl.workspace_size(B, H, L, 64, 64), 256)
+    kernel, splits = txl.relattn_plan(B, H, M, L, workspace_bytes=ws_bytes)
+    assert kernel == want, (B, L, M, kernel, splits)
+    assert txl.relattn_plan(B, H, M, L, n_splits=2, workspace_bytes=ws_bytes) == ("decode", 2)
+    case = heads_case(B, H, L, M, seed=4000 + 31 * L + M)
+    d = dev()
+    t = {k: v.to(d).contiguous() for k, v in case.items()}
+    ws = torch.empty(ws_bytes, dtype=torch.uint8, device=d)
+    scale = 1.0 / math.sqrt(64)
+    out, lse = txl.relattn_fwd(t["q"], t["k"], t["v"], t["r"], t["u"], t["v_bias"], M, scale,
+                               lse=True, workspace=ws)
+    torch.cuda.synchronize()
+    assert txl.device_status() == 0
+    bh = list(range(0, B * H, 3))  # every third head keeps the oracle quick
+    want_o, want_lse = run_oracle(case, M, scale, bh=bh)
+    got, got_lse = out.float().cpu().numpy(), lse.cpu().numpy()
+    for p in bh:
+        b, h = divmod(p, H)
+        compare(got[b, h], want_o[b, h], TOL, TOL_RMS, what=f"{kernel} B={B} L={L} M={M} h={h}")
+        compare(got_lse[b, h], want_lse[b, h], TOL_LSE, what=f"lse {kernel} L={L} h={h}")

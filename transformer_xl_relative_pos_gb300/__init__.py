@@ -12,6 +12,7 @@ N-layer summary, Appendix B reversed table and shift):
 
   rel_pos_emb     sinusoid table R in Appendix B's reversed row order
   relattn_fwd     fused relative-position attention over [memory ; segment]
+  relattn_plan    which kernel and key split relattn_fwd would use
   mem_concat      extended context [SG(m) o h] from the ring-buffer memory
   mem_update      advance the memory to the newest M states
 """
@@ -32,6 +33,7 @@ from ._lib import (  # noqa: F401
     rel_pos_emb,
     relattn_fwd,
     relattn_fwd_noalloc,
+    relattn_plan,
     set_wait_limit_ns,
     status_string,
     version,

@@ -58,6 +58,9 @@ def lib():
                 "txl_version": (_c_int, []),
                 "txl_rel_pos_emb": (_c_int, [_c_p, _c_int, _c_int, _c_int, _c_p]),
                 "txl_relattn_workspace_size": (_c_size, [_c_int, _c_int, _c_int, _c_int, _c_int]),
+                "txl_relattn_plan": (_c_int, [_c_int, _c_int, _c_int, _c_int, _c_int, _c_int, _c_int,
+                                              _c_int, _c_size, ctypes.POINTER(_c_int),
+                                              ctypes.POINTER(_c_int)]),
                 "txl_relattn_fwd": (_c_int, [_c_p, _c_p, _c_p, _c_p, _c_int, _c_p, _c_p, _c_p, _c_p,
                                              _c_int, _c_int, _c_int, _c_int, _c_int, _c_float,
                                              _c_int, _c_int, _c_p, _c_size, _c_p]),
@@ -132,6 +135,21 @@ def rel_pos_emb(K: int, d_model: int, dtype=torch.float32, device=None, out=None
 
 def workspace_size(B: int, H: int, L: int, dh: int, n_splits: int) -> int:
     return int(lib().txl_relattn_workspace_size(int(B), int(H), int(L), int(dh), int(n_splits)))
+
+
+KERNELS = {1: "tc", 2: "decode", 3: "f32"}
+
+
+def relattn_plan(B: int, H: int, M: int, L: int, dtype=torch.bfloat16, *, r_rows: int | None = None,
+                 dh: int = 64, n_splits: int = 0, workspace_bytes: int = 0):
+    """(kernel, splits) that relattn_fwd would use for these sizes: kernel is
+    "tc", "decode" or "f32".  Raises TxlError for sizes the call would reject."""
+    kernel, splits = _c_int(0), _c_int(0)
+    _check(lib().txl_relattn_plan(int(B), int(H), int(M), int(L),
+                                  int(r_rows if r_rows is not None else M + L), int(dh),
+                                  _code(dtype), int(n_splits), int(workspace_bytes),
+                                  ctypes.byref(kernel), ctypes.byref(splits)), "txl_relattn_plan")
+    return KERNELS[kernel.value], splits.value
 
 
 def relattn_fwd(q, k, v, r, u, v_bias, M: int, scale: float, *, out=None, lse=None,

@@ -91,11 +91,11 @@ int sm_count()
 {
     static int n[kMaxDevices] = {};
     int dev = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return 148;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return 152;
     if (!n[dev]) {
         int v = 0;
         if (cudaDeviceGetAttribute(&v, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || v <= 0)
-            v = 148;
+            v = 152;  // GB300
         n[dev] = v;
     }
     return n[dev];
@@ -118,6 +118,13 @@ size_t workspace_bytes_for(int B, int H, int L, int dh, int n_splits)
 // the merge kernel (about one tile).  The s with the least estimated time wins
 // (B=8 H=16 L=128 M=3800, 128 blocks on 152 SMs: 55.5 us unsplit against
 // 69.7 us with 2 splits), keeping >= 4 key tiles per split.
+double tc_wave_cost(long long units, int n_key_tiles, int s)
+{
+    const int sms = sm_count();
+    const long long waves = (units * s + sms - 1) / sms;
+    return (double)waves * ((n_key_tiles + s - 1) / s + 1.5) + (s > 1 ? 1.0 : 0.0);
+}
+
 int auto_splits(int units, int n_key_tiles)
 {
     const int sms = sm_count();
@@ -126,14 +133,102 @@ int auto_splits(int units, int n_key_tiles)
     int best = 1;
     double best_cost = 0.0;
     for (int s = 1; s <= max_s; ++s) {
-        const long long waves = ((long long)units * s + sms - 1) / sms;
-        const double cost = (double)waves * ((n_key_tiles + s - 1) / s + 1.5) + (s > 1 ? 1.0 : 0.0);
+        const double cost = tc_wave_cost(units, n_key_tiles, s);
         if (s == 1 || cost < best_cost) {
             best = s;
             best_cost = cost;
         }
     }
     return best;
+}
+
+// Estimated device times (microseconds, GB300) that choose between the two
+// bf16 kernels for short segments when the library picks the split.  The
+// tensor-core kernel costs about the same for any L <= 128 (every block
+// multiplies whole 128-row tiles): the wave model above at 1.6 us per tile-time.
+// The decode kernel reads k, v and the table once (at about 6.1 TB/s, with a
+// 2 us floor for small calls) and its arithmetic grows with the number of
+// queries; each query past the first adds ~27%, plus ~5.5 us of fixed cost.
+// Fitted to graph-replayed times of both kernels on H = 16, L = 1..6,
+// M = 800..3800, B = 1..64 (the model picks the faster one on 20 of 21 shapes;
+// on the other its pick is 2% slower).  With one sequence of 16 heads and M = 3800
+// the tensor-core kernel takes 14.6 us at L = 6 against 20.0 us; with two
+// sequences and M = 800 at L = 6 the decode kernel wins, 11.4 against 14.9 us.
+constexpr double kTcTileUs = 1.6;
+
+double decode_cost_us(long long B, long long H, long long K, int L, long long r_rows)
+{
+    const double bytes = 2.0 * (2.0 * B * H * K * 64 + (double)H * r_rows * 64 + 2.0 * B * H * L * 64);
+    return std::max(bytes / 6.1e6, 2.0) * (1.0 + 0.27 * (L - 1)) + 5.5;
+}
+
+// Key splits of the tensor-core kernel for one call: the caller's n_splits,
+// or the automatic choice when that is 0, limited to 1 when there is no usable
+// workspace (have_ws: non-NULL and 256-byte aligned) big enough for the
+// partial results.
+int tc_splits(int B, int H, int L, int dh, int n_qtiles, int n_key_tiles, int n_splits,
+              bool have_ws, size_t workspace_bytes)
+{
+    int splits = n_splits;
+    if (splits == 0) {
+        const long long units = std::min<long long>((long long)B * H * n_qtiles, 1 << 30);
+        splits = auto_splits((int)units, n_key_tiles);
+        if (splits > 1 && (!have_ws || workspace_bytes < workspace_bytes_for(B, H, L, dh, splits)))
+            splits = 1;
+    }
+    if (splits > n_key_tiles) splits = n_key_tiles;
+    return splits;
+}
+
+// Key ranges per (b, h) of the decode kernel: the caller's n_splits or the
+// automatic choice, capped at one per 128 keys, without ranges that own no key.
+int decode_splits(long long BH, long long K, int L, int n_splits)
+{
+    // At most one split per 128 keys (four 32-key chunks), and only splits that
+    // own keys.
+    const int max_splits = (int)((K + 127) / 128);
+    int splits = n_splits;
+    if (splits == 0) {
+        // One wave of resident blocks: each block streams its key range
+        // through its warps' copy rings, so long ranges amortise the first
+        // copies' latency, and a second, partly filled wave would cost a full
+        // block time.  At most a cluster's worth of ranges: merging in the
+        // cluster beat more ranges merged through the workspace even where
+        // those would fill more SMs (one sequence of 16 heads, M = 3800: 8.4 us
+        // with 8 ranges, 9.0 us with 19).
+        const long long slots = (long long)sm_count() * txl::decode_blocks_per_sm(L);
+        splits = (int)std::max<long long>(
+            1, std::min<long long>(std::min<long long>(slots / BH, max_splits),
+                                   txl::kDecodeMaxCluster));
+    }
+    if (splits > max_splits) splits = max_splits;
+    // Drop splits that would own no keys once ranges are rounded to chunks.
+    while (splits > 1 && (long long)(splits - 1) * txl::decode_span((int)K, splits) >= K) --splits;
+    return splits;
+}
+
+// Which bf16 kernel a call runs: the decode kernel for segments of at most
+// kDecodeMaxL queries when the caller fixed the split (n_splits >= 1: the
+// split then counts decode key ranges), when the call is small, or when its
+// estimate is the lower one.
+bool use_decode(int B, int H, int M, int L, int r_rows, int n_splits, bool have_ws,
+                size_t workspace_bytes)
+{
+    if (L > txl::kDecodeMaxL) return false;
+    if (n_splits != 0) return true;
+    const long long K = (long long)M + L;
+    const double dec_us = decode_cost_us(B, H, K, L, r_rows);
+    // Calls the decode kernel finishes in about 12 us stay on it: at that size
+    // the two kernels differ by a few microseconds either way, and its launch
+    // encodes no tensor maps on the host.
+    if (dec_us < 12.0) return true;
+    const int n_qtiles = (L + txl::kTcBM - 1) / txl::kTcBM;
+    const int jmax_all = (int)std::min<long long>(K - 1, (long long)M + L - 1);
+    const int n_key_tiles = jmax_all / txl::kTcBN + 1;
+    const int s = tc_splits(B, H, L, 64, n_qtiles, n_key_tiles, 0, have_ws, workspace_bytes);
+    const long long units = (long long)B * H * n_qtiles;
+    const double tc_us = tc_wave_cost(units, n_key_tiles, s) * kTcTileUs;
+    return dec_us <= tc_us;
 }
 
 // Short segments (L <= kDecodeMaxL): split-K decode kernel on the CUDA cores.
@@ -146,30 +241,11 @@ int relattn_decode(const void *q, const void *k, const void *v, const void *r, i
 {
     const long long K = (long long)M + L;
     const long long BH = (long long)B * H;
-    // At most one split per 128 keys (four 32-key chunks), and only splits that
-    // own keys.
-    const int max_splits = (int)((K + 127) / 128);
     // Up to kDecodeMaxCluster key ranges of a head run as one thread-block
     // cluster and merge in distributed shared memory; more need the workspace
     // for their partial results and a merge kernel.
-    const int max_cluster = txl::kDecodeMaxCluster;
-    int splits = n_splits;
-    if (splits == 0) {
-        // One wave of resident blocks: each block streams its key range
-        // through its warps' copy rings, so long ranges amortise the first
-        // copies' latency, and a second, partly filled wave would cost a full
-        // block time.  At most a cluster's worth of ranges: merging in the
-        // cluster beat more ranges merged through the workspace even where
-        // those would fill more SMs (one sequence of 16 heads, M = 3800: 8.4 us
-        // with 8 ranges, 9.0 us with 19).
-        const long long slots = (long long)sm_count() * txl::decode_blocks_per_sm(L);
-        splits = (int)std::max<long long>(
-            1, std::min<long long>(std::min<long long>(slots / BH, max_splits), max_cluster));
-    }
-    if (splits > max_splits) splits = max_splits;
-    // Drop splits that would own no keys once ranges are rounded to chunks.
-    while (splits > 1 && (long long)(splits - 1) * txl::decode_span((int)K, splits) >= K) --splits;
-    const bool cluster = splits >= 2 && splits <= max_cluster;
+    const int splits = decode_splits(BH, K, L, n_splits);
+    const bool cluster = splits >= 2 && splits <= txl::kDecodeMaxCluster;
     if (splits > 1 && !cluster) {
         if (!workspace || workspace_bytes < workspace_bytes_for(B, H, L, 64, splits))
             return TXL_ERR_WORKSPACE;
@@ -263,6 +339,44 @@ size_t txl_relattn_workspace_size(int B, int H, int L, int dh, int n_splits)
     return workspace_bytes_for(B, H, L, dh, n_splits);
 }
 
+int txl_relattn_plan(int B, int H, int M, int L, int r_rows, int dh, int dtype, int n_splits,
+                     size_t workspace_bytes, int *kernel, int *splits)
+{
+    if (!kernel || !splits) return TXL_ERR_INVALID_ARG;
+    if (B < 1 || H < 1 || M < 0 || L < 1 || dh < 1 || n_splits < 0) return TXL_ERR_INVALID_ARG;
+    if (dtype != TXL_F32 && dtype != TXL_BF16) return TXL_ERR_INVALID_ARG;
+    const long long K = (long long)M + L;
+    if (K > 0x7fffffffLL / 2 || r_rows < K) return TXL_ERR_SHAPE;
+    if (dh != 64) return TXL_ERR_UNSUPPORTED;
+    if (dtype == TXL_F32) {
+        if (n_splits > 1) return TXL_ERR_UNSUPPORTED;
+        *kernel = TXL_KERNEL_F32;
+        *splits = 1;
+        return TXL_OK;
+    }
+    const long long BH = (long long)B * H;
+    if (BH * L > 0x7fffffffLL || BH > 0x7fffffffLL / 64) return TXL_ERR_UNSUPPORTED;
+    const bool have_ws = workspace_bytes > 0;
+    int n = 1;
+    if (use_decode(B, H, M, L, r_rows, n_splits, have_ws, workspace_bytes)) {
+        n = decode_splits(BH, K, L, n_splits);
+        if (n > txl::kDecodeMaxCluster && workspace_bytes < workspace_bytes_for(B, H, L, 64, n))
+            return TXL_ERR_WORKSPACE;
+        if (BH * n > 0x7fffffffLL) return TXL_ERR_UNSUPPORTED;
+        *kernel = TXL_KERNEL_DECODE;
+    } else {
+        const int n_qtiles = (L + txl::kTcBM - 1) / txl::kTcBM;
+        const int jmax_all = (int)std::min<long long>(K - 1, (long long)M + L - 1);
+        const int n_key_tiles = jmax_all / txl::kTcBN + 1;
+        n = tc_splits(B, H, L, dh, n_qtiles, n_key_tiles, n_splits, have_ws, workspace_bytes);
+        if (n > 1 && workspace_bytes < workspace_bytes_for(B, H, L, dh, n)) return TXL_ERR_WORKSPACE;
+        if (BH * n_qtiles * n > 0x7fffffffLL) return TXL_ERR_UNSUPPORTED;
+        *kernel = TXL_KERNEL_TC;
+    }
+    *splits = n;
+    return TXL_OK;
+}
+
 int txl_relattn_fwd(const void *q, const void *k, const void *v, const void *r, int r_rows,
                     const void *u, const void *v_bias, void *out, float *lse, int B, int H,
                     int M, int L, int dh, float scale, int dtype, int n_splits,
@@ -307,21 +421,15 @@ int txl_relattn_fwd(const void *q, const void *k, const void *v, const void *r, 
     if (lse && !aligned(lse, 4)) return TXL_ERR_MISALIGNED;
     const long long BH = (long long)B * H;
     if (BH * L > 0x7fffffffLL || BH > 0x7fffffffLL / 64) return TXL_ERR_UNSUPPORTED;
-    if (L <= txl::kDecodeMaxL)
+    const bool have_ws = workspace && aligned(workspace, 256);
+    if (use_decode(B, H, M, L, r_rows, n_splits, have_ws, workspace_bytes))
         return relattn_decode(q, k, v, r, r_rows, u, v_bias, out, lse, B, H, M, L, scale, n_splits,
                               workspace, workspace_bytes, s);
     const int n_qtiles = (L + txl::kTcBM - 1) / txl::kTcBM;
     const int jmax_all = (int)std::min<long long>(K - 1, (long long)M + L - 1);
     const int n_key_tiles = jmax_all / txl::kTcBN + 1;
-    int splits = n_splits;
-    if (splits == 0) {
-        splits = auto_splits((int)std::min<long long>(BH * n_qtiles, 1 << 30), n_key_tiles);
-        if (splits > 1 && (!workspace ||
-                           workspace_bytes < workspace_bytes_for(B, H, L, dh, splits) ||
-                           !aligned(workspace, 256)))
-            splits = 1;
-    }
-    if (splits > n_key_tiles) splits = n_key_tiles;
+    const int splits =
+        tc_splits(B, H, L, dh, n_qtiles, n_key_tiles, n_splits, have_ws, workspace_bytes);
     if (splits > 1) {
         if (!workspace || workspace_bytes < workspace_bytes_for(B, H, L, dh, splits))
             return TXL_ERR_WORKSPACE;
