@@ -695,16 +695,6 @@ __global__ void __launch_bounds__(256, 1)
                     tmem_ld32(tB + wcol(wbase + 32u * (pc + 2)), wa);
                     tmem_ld32(tS + 32 * (pc + 1), wb);
                 }
-                if (pc + 1 == BN / 32 && it + 1 < T) {
-                    // The next tile's biases: their TMEM loads overlap this piece.
-                    ok = __all_sync(0xffffffffu, mbar_wait(bar.bias_full, (it + 1) & 1, abort_flag,
-                                                           wait_ns));
-                    if (ok) {
-                        tc_fence_after_sync();
-                        tmem_ld_x2(tmem + lane_off + TM_BK, bku, bkv);
-                        tmem_ld_x2(tmem + lane_off + TM_BR, bru, brv);
-                    }
-                }
                 const uint32_t rd = skew_rd + (uint32_t)((pc % 3) * 128);
                 float wv[32];
                 if (pc % 3 == 2) {
@@ -739,14 +729,24 @@ __global__ void __launch_bounds__(256, 1)
                     for (int e = 0; e < 32; ++e) s[e] = wb[e];
                 }
             }
-            if (!ok) break;
-            asm volatile("tcgen05.wait::ld.sync.aligned;"
-                         : "+r"(bku), "+r"(bkv), "+r"(bru), "+r"(brv)::"memory");
             tc_fence_before_sync();
             mbar_arrive(bar.s_free);
 
             // ---- biases of the next tile (key tile it+1, table chunk it+2) -------
-            if (it + 1 < T) convert_store(bku, brv, it + 2, pext_k(it + 1), pext_r(it + 1));
+            // Read before this tile's P overwrites their columns; by now the MMA
+            // warp has computed them (after the previous tile's PV), so the wait
+            // is rarely a wait.
+            if (it + 1 < T) {
+                ok = __all_sync(0xffffffffu, mbar_wait(bar.bias_full, (it + 1) & 1, abort_flag,
+                                                       wait_ns));
+                if (!ok) break;
+                tc_fence_after_sync();
+                tmem_ld_x2(tmem + lane_off + TM_BK, bku, bkv);
+                tmem_ld_x2(tmem + lane_off + TM_BR, bru, brv);
+                asm volatile("tcgen05.wait::ld.sync.aligned;"
+                             : "+r"(bku), "+r"(bkv), "+r"(bru), "+r"(brv)::"memory");
+                convert_store(bku, brv, it + 2, pext_k(it + 1), pext_r(it + 1));
+            }
 
             // ---- tile max (masked keys hold -inf) ----------------------------------
             float mt = max3f(max3f(mx[0], mx[1], mx[2]), max3f(mx[3], mx[4], mx[5]),
