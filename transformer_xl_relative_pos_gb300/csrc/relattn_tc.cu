@@ -764,12 +764,17 @@ __global__ void __launch_bounds__(256, 1)
             }
             const float mu = (m_ref == -INFINITY) ? 0.f : m_ref;
 
-            // PV of the previous tile must be done: it reads P and writes O.
+            // PV of the previous tile must be done: it reads P and writes O.  Before
+            // any tile but the last this is already known: the MMA warp issues the
+            // next tile's bias products only after that PV has completed, and their
+            // commit (bias_full, waited for above) covers every earlier MMA.
             if (it > 0) {
-                ok = __all_sync(0xffffffffu,
-                                mbar_wait(bar.o_done, (it - 1) & 1, abort_flag, wait_ns));
-                if (!ok) break;
-                tc_fence_after_sync();
+                if (it + 1 == T) {
+                    ok = __all_sync(0xffffffffu,
+                                    mbar_wait(bar.o_done, (it - 1) & 1, abort_flag, wait_ns));
+                    if (!ok) break;
+                    tc_fence_after_sync();
+                }
                 if (__any_sync(0xffffffffu, resc)) {
 #pragma unroll
                     for (int half = 0; half < 2; ++half) {
