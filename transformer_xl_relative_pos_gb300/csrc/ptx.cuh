@@ -102,6 +102,20 @@ __device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity,
     }
 }
 
+// The same bound, polling with plain try_wait (no suspend hint): for a thread
+// on the critical path that should resume as soon as the phase completes.
+__device__ __forceinline__ bool mbar_wait_poll(uint64_t *bar, uint32_t parity,
+                                               const volatile int *abort_flag, uint64_t limit_ns)
+{
+    if (mbar_try_wait(bar, parity)) return true;
+    const uint64_t t0 = globaltimer_ns();
+    while (true) {
+        if (mbar_try_wait(bar, parity)) return true;
+        if (*abort_flag) return false;
+        if (globaltimer_ns() - t0 > limit_ns) return false;
+    }
+}
+
 // ---------------------------------------------------------------------------
 // TMA
 // ---------------------------------------------------------------------------

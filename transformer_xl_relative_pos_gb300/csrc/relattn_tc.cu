@@ -517,20 +517,20 @@ __global__ void __launch_bounds__(256, 1)
                 }
             }
             for (int it = 0; it < T && ok; ++it) {
-                if (!(ok = mbar_wait(bar.s_free, it & 1, abort_flag, wait_ns))) break;
+                if (!(ok = mbar_wait_poll(bar.s_free, it & 1, abort_flag, wait_ns))) break;
                 if (it + 1 < T) {
                     // Scores of tile it+1: pair it+1, whose chunk it+2 goes into
                     // the slot chunk it just left.  The bias K-step waits for the
                     // softmax warps' conversion; the main ones need not.
                     tc_fence_after_sync();
                     score_pair(it + 1);
-                    if (!(ok = mbar_wait(bar.ext_full, (it + 1) & 1, abort_flag, wait_ns))) break;
+                    if (!(ok = mbar_wait_poll(bar.ext_full, (it + 1) & 1, abort_flag, wait_ns))) break;
                     tc_fence_after_sync();
                     score_pair_ext(it + 1);
                     mma_commit(bar.s_full);
                     mma_commit(bar.pair_empty + (it + 1) % NP);
                 }
-                if (!(ok = mbar_wait(bar.p_full, it & 1, abort_flag, wait_ns))) break;
+                if (!(ok = mbar_wait_poll(bar.p_full, it & 1, abort_flag, wait_ns))) break;
                 const int st = it % NS;
                 if (!(ok = mbar_wait(bar.v_full + st, (it / NS) & 1, abort_flag, wait_ns))) break;
                 tc_fence_after_sync();
