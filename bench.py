@@ -51,8 +51,8 @@ import txl_inputs  # noqa: E402
 PROFILED_TRAFFIC = {
     "workload": "c3_word_large_L128_M1600",
     "sources": ("relattn_tc.cu", "ptx.cuh", "kernels.h"),
-    "sha256": "a7b1496112f5ed656ca45896b82b45d80349332c8ad14e8d9989da9fb8ea7cce",
-    "bytes_per_launch": 121077248 + 2568448,
+    "sha256": "df823f679bf0a2032b158d6ee03518bbdcd7edb041f5adc549f88f528f0910ed",
+    "bytes_per_launch": 121081088 + 2561792,
 }
 
 
