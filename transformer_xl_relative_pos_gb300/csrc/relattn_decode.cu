@@ -311,8 +311,10 @@ __global__ void __launch_bounds__(WARPS * 32) relattn_decode_kernel(const Decode
             float mx = s;
 #pragma unroll
             for (int o = 16; o > 0; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+            // No branch for a query that has seen no visible key yet (m_new = -inf):
+            // the selects below then give sc = 0 and pj = 0, which leave l and acc at
+            // zero, and without control flow the L queries' chains interleave.
             const float m_new = fmaxf(m[i], mx);
-            if (m_new == -INFINITY) continue;  // nothing visible yet (warp-uniform)
             const float sc = (m[i] == -INFINITY) ? 0.f : ex2f(m[i] - m_new);
             const float pj = (s == -INFINITY) ? 0.f : ex2f(s - m_new);
             float sum = pj;
