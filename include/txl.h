@@ -133,9 +133,8 @@ int txl_relattn_plan(int B, int H, int M, int L, int r_rows, int dh, int dtype, 
  *   few new tokens against a long memory) can take a split-K kernel on the CUDA
  *   cores instead, all arithmetic in fp32 (no bf16 rounding of P): always when
  *   n_splits >= 1, and with n_splits = 0 when its estimated time is below the
- *   tensor-core kernel's (short memories, several sequences; one sequence
- *   against a long memory goes to the tensor cores from L of about 4 or 5 on;
- *   txl_relattn_plan tells which).  For this kernel n_splits
+ *   tensor-core kernel's (which takes one sequence against a long memory
+ *   from L of about 4 or 5 on; txl_relattn_plan tells which).  For this kernel n_splits
  *   counts key ranges per (b, h), each a whole number of 32-key chunks,
  *   at most one per 128 keys (larger requests are capped, ranges that would
  *   hold no key are dropped); up to 8 ranges of a head run as one thread-block

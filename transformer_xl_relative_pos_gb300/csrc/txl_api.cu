@@ -145,21 +145,21 @@ int auto_splits(int units, int n_key_tiles)
 // Estimated device times (microseconds, GB300) that choose between the two
 // bf16 kernels for short segments when the library picks the split.  The
 // tensor-core kernel costs about the same for any L <= 128 (every block
-// multiplies whole 128-row tiles): the wave model above at 1.6 us per tile-time.
-// The decode kernel reads k, v and the table once (at about 6.1 TB/s, with a
-// 2 us floor for small calls) and its arithmetic grows with the number of
-// queries; each query past the first adds ~27%, plus ~5.5 us of fixed cost.
-// Fitted to graph-replayed times of both kernels on H = 16, L = 1..6,
-// M = 800..3800, B = 1..64 (the model picks the faster one on 20 of 21 shapes;
-// on the other its pick is 2% slower).  With one sequence of 16 heads and M = 3800
-// the tensor-core kernel takes 14.6 us at L = 6 against 20.0 us; with two
-// sequences and M = 800 at L = 6 the decode kernel wins, 11.4 against 14.9 us.
-constexpr double kTcTileUs = 1.6;
+// multiplies whole 128-row tiles): the wave model above at 1.67 us per
+// tile-time.  The decode kernel reads k, v and the table once (at about
+// 6.5 TB/s, with a 2.5 us floor for small calls), each query past the first
+// adds ~18% to that, plus ~6.5 us of fixed cost.  Fitted to graph-replayed
+// times of both kernels forced on 28 shapes (H = 16, L = 1..6, M = 800..12000,
+// B = 1..64): the pick is the faster kernel on all of them.  The tensor cores
+// win only for one sequence against a long memory (M = 3800, L = 6: 14.9
+// against 17.3 us; M = 8000, L = 4: 18.5 against 21.4 us); with more sequences
+// the decode kernel wins (eight sequences, M = 3800, L = 6: 46.6 against 48.5 us).
+constexpr double kTcTileUs = 1.67;
 
 double decode_cost_us(long long B, long long H, long long K, int L, long long r_rows)
 {
     const double bytes = 2.0 * (2.0 * B * H * K * 64 + (double)H * r_rows * 64 + 2.0 * B * H * L * 64);
-    return std::max(bytes / 6.1e6, 2.0) * (1.0 + 0.27 * (L - 1)) + 5.5;
+    return std::max(bytes / 6.5e6, 2.5) * (1.0 + 0.18 * (L - 1)) + 6.5;
 }
 
 // Key splits of the tensor-core kernel for one call: the caller's n_splits,
