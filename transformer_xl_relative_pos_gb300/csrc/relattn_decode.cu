@@ -59,6 +59,14 @@ constexpr int SMEM_BYTES = OFF_FLAG + 16;
 
 static_assert(STAGE % 16 == 0 && RING % 16 == 0, "bulk copies need 16-byte aligned stages");
 
+// Maximum of v over the warp in one instruction (sm_100 family).
+__device__ __forceinline__ float warp_max(float v)
+{
+    float r;
+    asm("redux.sync.max.f32 %0, %1, 0xffffffff;" : "=f"(r) : "f"(v));
+    return r;
+}
+
 __device__ __forceinline__ float ex2f(float x)
 {
     float y;
@@ -243,8 +251,9 @@ __global__ void __launch_bounds__(WARPS * 32) relattn_decode_kernel(const Decode
         }
     }
 
-    // running max (log2 units) and sum per row; this group's partial output of
-    // dimensions 8 sub .. 8 sub + 7 (four pairs) per row
+    // running max (log2 units, warp-uniform) and this lane's part of the sum per
+    // row (summed over the warp once, after the keys); this group's partial
+    // output of dimensions 8 sub .. 8 sub + 7 (four pairs) per row
     float m[L], l[L];
     uint64_t acc[L][4];
 #pragma unroll
@@ -308,20 +317,15 @@ __global__ void __launch_bounds__(WARPS * 32) relattn_decode_kernel(const Decode
             const int j = j0 + lane;
             if (j >= k_end || j > p.M + i) s = -INFINITY;
             // ---- online softmax over the warp's 32 keys --------------------------
-            float mx = s;
-#pragma unroll
-            for (int o = 16; o > 0; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+            const float mx = warp_max(s);
             // No branch for a query that has seen no visible key yet (m_new = -inf):
             // the selects below then give sc = 0 and pj = 0, which leave l and acc at
             // zero, and without control flow the L queries' chains interleave.
             const float m_new = fmaxf(m[i], mx);
             const float sc = (m[i] == -INFINITY) ? 0.f : ex2f(m[i] - m_new);
             const float pj = (s == -INFINITY) ? 0.f : ex2f(s - m_new);
-            float sum = pj;
-#pragma unroll
-            for (int o = 16; o > 0; o >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, o);
             m[i] = m_new;
-            l[i] = l[i] * sc + sum;
+            l[i] = l[i] * sc + pj;
             const uint64_t sc2 = pack2(sc, sc);
 #pragma unroll
             for (int c = 0; c < 4; ++c) acc[i][c] = mul2(acc[i][c], sc2);
@@ -352,6 +356,8 @@ __global__ void __launch_bounds__(WARPS * 32) relattn_decode_kernel(const Decode
     float o8[L][8];
 #pragma unroll
     for (int i = 0; i < L; ++i) {
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) l[i] += __shfl_xor_sync(0xffffffffu, l[i], o);
 #pragma unroll
         for (int c = 0; c < 4; ++c) unpack2(acc[i][c], o8[i][2 * c], o8[i][2 * c + 1]);
 #pragma unroll
