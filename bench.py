@@ -51,7 +51,7 @@ import txl_inputs  # noqa: E402
 PROFILED_TRAFFIC = {
     "workload": "c3_word_large_L128_M1600",
     "sources": ("relattn_tc.cu", "ptx.cuh", "kernels.h"),
-    "sha256": "df823f679bf0a2032b158d6ee03518bbdcd7edb041f5adc549f88f528f0910ed",
+    "sha256": "74d59f5edb74e83aa638f12a11a7ba8b713534eecddd9c96913c005cf3086344",
     "bytes_per_launch": 121081088 + 2561792,
 }
 

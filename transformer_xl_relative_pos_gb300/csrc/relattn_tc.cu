@@ -41,8 +41,8 @@
 //   warp 1      MMA issuer (one thread)
 //   warp 2      TMEM allocator
 //   warps 4..7  softmax: thread = query row.  Per tile: gather S + shifted
-//               window, running max (lazy rescale), exp2, P (bf16) to
-//               TMEM; convert the next tile's biases; finally O / l.
+//               window, release S, convert the next tile's biases, running
+//               max (lazy rescale), exp2, P (bf16) to TMEM; finally O / l.
 //
 // Every barrier wait is bounded: on time-out the block records an error in the
 // device status word, raises a block-wide abort flag, drains its own in-flight
