@@ -41,7 +41,7 @@ extern "C" {
 typedef enum {
     TXL_OK = 0,
     TXL_ERR_INVALID_ARG = -1, /* null pointer, negative size, bad dtype code */
-    TXL_ERR_UNSUPPORTED = -2, /* a shape or dtype this build has no kernel for */
+    TXL_ERR_UNSUPPORTED = -2, /* a shape or dtype the library has no kernel for */
     TXL_ERR_MISALIGNED = -3,  /* a pointer breaks the stated alignment */
     TXL_ERR_SHAPE = -4,       /* sizes inconsistent with each other */
     TXL_ERR_CUDA = -5,        /* a CUDA runtime or driver call failed */
