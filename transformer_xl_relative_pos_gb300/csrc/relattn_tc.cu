@@ -64,7 +64,7 @@ constexpr int EXT = 4096;              // bias-column tile: 128 rows x 16 bytes,
                                        // 2 KB of zeros for K columns 8..15
 constexpr int EXT2 = 8192;             // the same for a pair: 256 rows, then 4 KB of zeros
 constexpr int PAIR = 2 * TILE;
-constexpr int SKEW_STRIDE = 100;       // floats per skew row: a 3 x 32 ring + 4 pad
+constexpr int SKEW_STRIDE = 132;       // floats per skew row: a 4 x 32 ring + 4 pad
                                        // (stride = 4 mod 32: conflict-free both ways)
 
 // TMEM columns
@@ -84,12 +84,15 @@ constexpr uint32_t TM_COLS = 512;
 constexpr int OFF_Q = 0;
 constexpr int OFF_PAIR = OFF_Q + TILE;            // NP pair stages
 constexpr int OFF_V = OFF_PAIR + NP * PAIR;       // NS stages
-constexpr int OFF_R0 = OFF_V + NS * TILE;         // table chunk 0 (first tile only)
-constexpr int OFF_UB = OFF_R0 + TILE;             // [u ; v ; 0 x 14] 16 x 128 bytes, swizzled
+constexpr int OFF_UB = OFF_V + NS * TILE;         // [u ; v ; 0 x 14] 16 x 128 bytes, swizzled
 constexpr int OFF_AEXT = OFF_UB + 2048;           // ones column: rows [1, 1, 0 x 6]
 constexpr int OFF_PEXT = OFF_AEXT + EXT;          // NP pair tiles of (hi, lo) of k.u / v.r
 constexpr int OFF_R0EXT = OFF_PEXT + NP * EXT2;   // (hi, lo) of v.r of chunk 0
 constexpr int OFF_SKEW = OFF_R0EXT + EXT;         // 128 rows x SKEW_STRIDE floats
+// Table chunk 0 of the first tile shares the skew buffer's bytes: the MMAs that
+// read it complete before s_full of the first tile, and the softmax warps write
+// the skew buffer only after that.
+constexpr int OFF_R0 = OFF_SKEW;
 constexpr int OFF_BAR = OFF_SKEW + BM * SKEW_STRIDE * 4;
 constexpr int N_BAR = 1 + 2 * NP + 2 * NS + 1 + 8;
 constexpr int OFF_MISC = OFF_BAR + N_BAR * 8;
@@ -97,7 +100,8 @@ constexpr int SMEM_USED = OFF_MISC + 16;
 constexpr int SMEM_BYTES = SMEM_USED + 1024;      // slack for the manual alignment
 
 static_assert(SMEM_BYTES <= 232448, "shared memory budget exceeded");
-static_assert(OFF_UB % 1024 == 0, "swizzled tiles need 1024-byte alignment");
+static_assert(OFF_UB % 1024 == 0 && OFF_R0 % 1024 == 0, "swizzled tiles need 1024-byte alignment");
+static_assert(OFF_R0 + TILE <= OFF_SKEW + BM * SKEW_STRIDE * 4, "chunk 0 must fit the skew buffer");
 
 struct Bars {
     uint64_t *q_full;
@@ -660,9 +664,11 @@ __global__ void __launch_bounds__(256, 1)
             // 256-column window (five 32-column chunks); table chunk it sits in
             // the even- or odd-chunk TMEM slot by its parity, chunk it+1 in the
             // other.  Each window chunk c goes
-            // once through a 3-slot shared-memory ring (slot c % 3); key y of
-            // piece pc is ring column (32*pc + 31 - lane + y), which for pc = 2
-            // wraps from slot 2 to slot 0 when y > lane.
+            // once through a 4-slot shared-memory ring (slot c % 4); key y of
+            // piece pc is ring column (32*pc + 31 - lane + y), which for pc = 3
+            // wraps from slot 3 to slot 0 when y > lane.  Chunk 4 of a tile is
+            // chunk 0 of the next (the same 32 columns of table chunk it+1), and
+            // it lands in slot 0: only a block's first tile loads chunk 0.
             // window column w of this tile in TMEM: chunk it (w < 128) or it+1
             const uint32_t slot0 = (it & 1) ? TM_CC : TM_CA, slot1 = (it & 1) ? TM_CA : TM_CC;
             const uint32_t wbase = (uint32_t)(96 - 32 * wq);
@@ -673,16 +679,20 @@ __global__ void __launch_bounds__(256, 1)
 #pragma unroll
             for (int a = 0; a < 8; ++a) mx[a] = -INFINITY;
             uint32_t wa[32], wb[32], s[32];
-            tmem_ld32(tB + wcol(wbase), wa);
+            if (it == 0) {
+                tmem_ld32(tB + wcol(wbase), wa);
+                tmem_wait_ld();
+                reg_fence(wa);
+#pragma unroll
+                for (int c = 0; c < 8; ++c)
+                    st_shared_v4(skew + c * 16, wa[4 * c], wa[4 * c + 1], wa[4 * c + 2],
+                                 wa[4 * c + 3]);
+            }
             tmem_ld32(tB + wcol(wbase + 32u), wb);
             tmem_ld32(tS, s);
             tmem_wait_ld();
-            reg_fence(wa);
             reg_fence(wb);
             reg_fence(s);
-#pragma unroll
-            for (int c = 0; c < 8; ++c)
-                st_shared_v4(skew + c * 16, wa[4 * c], wa[4 * c + 1], wa[4 * c + 2], wa[4 * c + 3]);
 #pragma unroll
             for (int c = 0; c < 8; ++c)
                 st_shared_v4(skew + 128 + c * 16, wb[4 * c], wb[4 * c + 1], wb[4 * c + 2],
@@ -695,12 +705,12 @@ __global__ void __launch_bounds__(256, 1)
                     tmem_ld32(tB + wcol(wbase + 32u * (pc + 2)), wa);
                     tmem_ld32(tS + 32 * (pc + 1), wb);
                 }
-                const uint32_t rd = skew_rd + (uint32_t)((pc % 3) * 128);
+                const uint32_t rd = skew_rd + (uint32_t)(pc * 128);
                 float wv[32];
-                if (pc % 3 == 2) {
+                if (pc == 3) {
 #pragma unroll
                     for (int y = 0; y < 32; ++y)
-                        wv[y] = ld_shared_f32(rd + y * 4 - ((y > lane) ? 384u : 0u));
+                        wv[y] = ld_shared_f32(rd + y * 4 - ((y > lane) ? 512u : 0u));
                 } else {
 #pragma unroll
                     for (int y = 0; y < 32; ++y) wv[y] = ld_shared_f32(rd + y * 4);
@@ -719,8 +729,9 @@ __global__ void __launch_bounds__(256, 1)
                     tmem_wait_ld();
                     reg_fence(wa);
                     reg_fence(wb);
-                    // chunk pc+2 replaces chunk pc-1, which no later piece reads
-                    const uint32_t slot = skew + (uint32_t)(((pc + 2) % 3) * 128);
+                    // chunk pc+2 into slot (pc+2) % 4: empty, or (chunk 4) the slot of
+                    // chunk 0, which no later piece of this tile reads
+                    const uint32_t slot = skew + (uint32_t)(((pc + 2) % 4) * 128);
 #pragma unroll
                     for (int c = 0; c < 8; ++c)
                         st_shared_v4(slot + c * 16, wa[4 * c], wa[4 * c + 1], wa[4 * c + 2],
