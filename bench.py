@@ -51,8 +51,8 @@ import txl_inputs  # noqa: E402
 PROFILED_TRAFFIC = {
     "workload": "c3_word_large_L128_M1600",
     "sources": ("relattn_tc.cu", "ptx.cuh", "kernels.h"),
-    "sha256": "74d59f5edb74e83aa638f12a11a7ba8b713534eecddd9c96913c005cf3086344",
-    "bytes_per_launch": 121081088 + 2561792,
+    "sha256": "2a461321da6dec8339007a82cde17ee91f65fe73d8dd63d4f82debb69db6ac58",
+    "bytes_per_launch": 121071360 + 2636288,
 }
 
 
