@@ -51,8 +51,8 @@ import txl_inputs  # noqa: E402
 PROFILED_TRAFFIC = {
     "workload": "c3_word_large_L128_M1600",
     "sources": ("relattn_tc.cu", "ptx.cuh", "kernels.h"),
-    "sha256": "2a461321da6dec8339007a82cde17ee91f65fe73d8dd63d4f82debb69db6ac58",
-    "bytes_per_launch": 121071360 + 2636288,
+    "sha256": "1299e3274fb067a55ca10e4156aeebe10099a4923d5cc6258957421294eb4121",
+    "bytes_per_launch": 121081600 + 2305024,
 }
 
 
