@@ -57,7 +57,7 @@ using namespace ptx;
 
 constexpr int BM = kTcBM, BN = kTcBN, DH = kTcDH;
 constexpr int NP = 2;                  // pair stages [key tile t, table chunk t+1]
-constexpr int NS = 3;                  // V ring stages
+constexpr int NS = 2;                  // V ring stages
 constexpr int PF = 2;                  // L2 prefetch distance (tiles)
 constexpr int TILE = BM * DH * 2;      // 16384 bytes: 128 rows x 128 bytes
 constexpr int EXT = 4096;              // bias-column tile: 128 rows x 16 bytes, then
