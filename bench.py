@@ -51,8 +51,8 @@ import txl_inputs  # noqa: E402
 PROFILED_TRAFFIC = {
     "workload": "c3_word_large_L128_M1600",
     "sources": ("relattn_tc.cu", "ptx.cuh", "kernels.h"),
-    "sha256": "1299e3274fb067a55ca10e4156aeebe10099a4923d5cc6258957421294eb4121",
-    "bytes_per_launch": 121081600 + 2305024,
+    "sha256": "718faf4db13841ca2b315f4bdad07e22c0c7a2f07835fc699c2e75da18ca31b5",
+    "bytes_per_launch": 121107712 + 2742016,
 }
 
 
