@@ -146,3 +146,45 @@ def test_python_binding_rejects_host_tensors():
     q = torch.zeros(1, 1, 4, 64, dtype=torch.bfloat16)
     with pytest.raises(ValueError, match="CUDA tensor"):
         txl.relattn_fwd(q, q, q, q[0], q[0, 0, :1], q[0, 0, :1], 0, 0.125, out=q)
+
+
+def _span(K, n):
+    # keys of one decode key range: a whole number of 32-key chunks
+    return ((K + n - 1) // n + 31) // 32 * 32
+
+
+@pytest.mark.parametrize("B,H", [(1, 1), (1, 16), (2, 3), (8, 16), (64, 16)])
+@pytest.mark.parametrize("M,L", [(0, 1), (1, 1), (127, 1), (300, 3), (3799, 1), (3800, 6), (511, 7),
+                                 (512, 512), (1600, 128), (3800, 128), (5000, 130)])
+@pytest.mark.parametrize("n_splits", [0, 1, 2, 5, 9, 40])
+def test_plan_splits_are_valid(B, H, M, L, n_splits):
+    # Host logic only.  Whatever the request, the split the library picks must be
+    # realisable: every decode key range owns keys (ranges of whole 32-key
+    # chunks, at most one per 128 keys), tensor-core splits never exceed the
+    # key tiles, and a split that needs partials needs the workspace.
+    K = M + L
+    ws = 1 << 34
+    kernel, splits = txl.relattn_plan(B, H, M, L, n_splits=n_splits, workspace_bytes=ws)
+    assert splits >= 1
+    if kernel == "decode":
+        assert L <= 6
+        assert splits <= max(1, (K + 127) // 128)
+        assert (splits - 1) * _span(K, splits) < K
+        if n_splits:
+            assert splits <= n_splits
+    else:
+        assert kernel == "tc"
+        n_key_tiles = min(K - 1, M + L - 1) // 128 + 1
+        assert splits <= n_key_tiles
+        if n_splits:
+            assert splits == min(n_splits, n_key_tiles)
+        assert L > 6 or n_splits == 0, "an explicit split of a short segment means the decode kernel"
+    if splits > 8 or (kernel == "tc" and splits > 1):
+        # partials in the workspace: without one the call must refuse
+        k, n = ctypes.c_int(0), ctypes.c_int(0)
+        rc = txl.lib().txl_relattn_plan(B, H, M, L, K, 64, txl.BF16, n_splits, 0,
+                                        ctypes.byref(k), ctypes.byref(n))
+        if n_splits:
+            assert rc == WORKSPACE
+        else:
+            assert rc == OK  # the automatic choice falls back to a split that fits
