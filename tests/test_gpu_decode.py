@@ -137,3 +137,20 @@ def test_short_segment_routing(B, L, M, want):
         b, h = divmod(p, H)
         compare(got[b, h], want_o[b, h], TOL, TOL_RMS, what=f"{kernel} B={B} L={L} M={M} h={h}")
         compare(got_lse[b, h], want_lse[b, h], TOL_LSE, what=f"lse {kernel} L={L} h={h}")
+
+
+@pytest.mark.parametrize("B,H,M,L", [(1, 16, 3800, 1), (8, 16, 3800, 2), (2, 3, 300, 3), (64, 16, 3800, 6),
+                                     (1, 16, 8000, 4), (16, 16, 1600, 128), (8, 16, 3800, 128)])
+@pytest.mark.parametrize("n_splits", [0, 3, 9])
+def test_plan_on_device_is_realisable(B, H, M, L, n_splits):
+    # The split chosen with this device's occupancy (not the host fallback):
+    # decode ranges own keys and stay within one per 128 keys, tensor-core
+    # splits within the key tiles.
+    K = M + L
+    kernel, splits = txl.relattn_plan(B, H, M, L, n_splits=n_splits, workspace_bytes=1 << 34)
+    assert splits >= 1
+    if kernel == "decode":
+        span = ((K + splits - 1) // splits + 31) // 32 * 32
+        assert splits <= max(1, (K + 127) // 128) and (splits - 1) * span < K
+    else:
+        assert splits <= min(K - 1, M + L - 1) // 128 + 1
