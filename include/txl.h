@@ -178,10 +178,13 @@ int txl_relattn_fwd(const void *q, const void *k, const void *v, const void *r, 
  * device array of TXL_NOALLOC_SCRATCH_BYTES that every GPU which loads the
  * library holds until the process exits.  The call itself allocates nothing
  * (no cudaMalloc, cudaFree or allocating library routine).
- *   - n_splits > 1 whose partial results need more than the scratch
- *     (txl_relattn_workspace_size(B, H, L, dh, n_splits) bytes) returns
- *     TXL_ERR_WORKSPACE and launches nothing; n_splits = 0 chooses a split
- *     that fits (or none).
+ *   - A split whose partial results need more than the scratch returns
+ *     TXL_ERR_WORKSPACE and launches nothing.  What counts is the split the
+ *     call runs, as txl_relattn_plan reports it for workspace_bytes =
+ *     TXL_NOALLOC_SCRATCH_BYTES: requests above the key-tile count are capped
+ *     first, and decode key ranges merged inside a thread-block cluster need
+ *     no scratch; otherwise it needs txl_relattn_workspace_size(B, H, L, dh,
+ *     splits) bytes.  n_splits = 0 chooses a split that fits (or none).
  *   - Every call shares the array and leaves its partial results in it; calls
  *     that may run at the same time on the GPU (other streams, or other host
  *     threads without ordering) race on it and must be serialised by the

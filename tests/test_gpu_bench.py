@@ -26,7 +26,10 @@ def test_bench_line_contract_and_end_to_end_leg():
         assert key in line, key
     assert line["value"] > 0 and line["n_gpus"] == 1 and line["device_status"] == 0
     assert line["config"]["workload"] == "c3_word_large_L128_M1600"
-    assert line["gpu_launches"] >= 3 * line["steps"]
+    # per step: the attention (plus a merge when its key range is split) and the
+    # memory update; the table is built once per layer, outside the step
+    assert line["gpu_launches"] >= 2 * line["steps"]
+    assert line["rel_pos_emb_us"] > 0
     roof = line["roofline"]
     assert roof["kernel"] == "relattn_fwd_tc_kernel" and 0 < roof["frac"] and roof["peak"] > 0
     e2e = line["e2e"]

@@ -58,10 +58,10 @@ extern "C" int txl_relattn_fwd_noalloc(const void *q, const void *k, const void 
                                        int M, int L, int dh, float scale, int dtype,
                                        int n_splits, void *stream)
 {
-    // A split the built-in scratch cannot hold is refused before anything runs.
-    if (n_splits > 1 && B >= 1 && H >= 1 && L >= 1 && dh >= 1 &&
-        txl_relattn_workspace_size(B, H, L, dh, n_splits) > (size_t)TXL_NOALLOC_SCRATCH_BYTES)
-        return TXL_ERR_WORKSPACE;
+    // txl_relattn_fwd sizes the split it will actually run (decode key ranges
+    // merged inside a thread-block cluster need no scratch; requests above the
+    // key-tile count are capped) against the scratch and refuses, before
+    // anything is launched, a split whose partial results do not fit.
     int status = TXL_OK;
     void *scratch = scratch_address(&status);
     if (!scratch) return status;

@@ -38,7 +38,9 @@
 // Warp roles (256 threads):
 //   warp 0      TMA producer: q tile once, then K, V and table chunks through
 //               shared-memory rings, with L2 prefetches further ahead
-//   warp 1      MMA issuer (one thread)
+//   warp 1      MMA issuer: the whole warp follows the schedule (barrier
+//               waits, descriptors) so that its values stay warp-uniform, and one
+//               elected lane issues each group of MMAs and commits
 //   warp 2      TMEM allocator
 //   warps 4..7  softmax: thread = query row.  Per tile: gather S + shifted
 //               window, release S, convert the next tile's biases, running
@@ -436,131 +438,147 @@ __global__ void __launch_bounds__(256, 1)
         }
     } else if (warp == 1) {
         // ===================== MMA issuer =======================================
-        if (lane == 0) {
+        // Descriptors are computed once as 64-bit bases; an offset of b bytes
+        // adds b / 16.  Every lane waits on the barriers (votes keep the warp
+        // converged) and one elected lane issues.
+        {
             constexpr uint32_t ID_N128 = idesc_bf16_f32(128, 128, false);
             constexpr uint32_t ID_N256 = idesc_bf16_f32(128, 256, false);
             constexpr uint32_t ID_N16 = idesc_bf16_f32(128, 16, false);
             constexpr uint32_t ID_O = idesc_bf16_f32(128, 64, true);
-            const uint32_t sQ = smem_u32(smem + OFF_Q);
-            const uint32_t sPair = smem_u32(smem + OFF_PAIR);
-            const uint32_t sV = smem_u32(smem + OFF_V);
-            const uint32_t sR0 = smem_u32(smem + OFF_R0);
-            const uint32_t sUB = smem_u32(smem + OFF_UB);
-            const uint32_t sAX = smem_u32(smem + OFF_AEXT);
-            const uint32_t sPX = smem_u32(smem + OFF_PEXT);
-            const uint32_t sR0X = smem_u32(smem + OFF_R0EXT);
-            const uint64_t d_aext = sdesc_ext(sAX);
-
-            // [tile rows] x [u ; v]^T into a 16-column TMEM region.
-            auto bias_mma = [&](uint32_t tcol, uint32_t a_tile) {
-#pragma unroll
-                for (int kk = 0; kk < DH / 16; ++kk)
-                    mma_bf16_ss(tmem + tcol, sdesc_sw128(a_tile + kk * 32),
-                                sdesc_sw128(sUB + kk * 32), ID_N16, kk);
+            const uint64_t dQ = sdesc_sw128(smem_u32(smem + OFF_Q));
+            const uint64_t dPair = sdesc_sw128(smem_u32(smem + OFF_PAIR));
+            const uint64_t dV = sdesc_sw128(smem_u32(smem + OFF_V));
+            const uint64_t dR0 = sdesc_sw128(smem_u32(smem + OFF_R0));
+            const uint64_t dUB = sdesc_sw128(smem_u32(smem + OFF_UB));
+            const uint64_t d_aext = sdesc_ext(smem_u32(smem + OFF_AEXT));
+            const uint64_t dPX = sdesc_ext2(smem_u32(smem + OFF_PEXT));
+            const uint64_t dR0X = sdesc_ext(smem_u32(smem + OFF_R0EXT));
+            auto elect = []() -> bool {
+                uint32_t el;
+                asm volatile("{\n\t.reg .pred P;\n\telect.sync _|P, 0xffffffff;\n\tselp.u32 %0, 1, 0, P;\n\t}"
+                             : "=r"(el));
+                return el != 0;
             };
-            auto pair_k = [&](int t) { return sPair + (t % NP) * PAIR + ((t & 1) ? TILE : 0); };
-            auto pair_r = [&](int t) { return sPair + (t % NP) * PAIR + ((t & 1) ? 0 : TILE); };
-            // Pair t times q: S of tile t and table chunk t+1 in one N = 256 MMA
-            // per K-step (results on [S | odd slot] or [even slot | S]), then
-            // the ext K-step adding both halves' bias pairs.
+            auto W = [&](uint64_t *bar, int par) {
+                return __all_sync(0xffffffffu, mbar_wait(bar, par, abort_flag, wait_ns));
+            };
+            auto WP = [&](uint64_t *bar, int par) {
+                return __all_sync(0xffffffffu, mbar_wait_poll(bar, par, abort_flag, wait_ns));
+            };
+            // descriptor offsets are added in 16-byte units
+            auto bias_mma = [&](uint32_t tcol, uint64_t a_tile) {
+                if (elect()) {
+#pragma unroll
+                    for (int kk = 0; kk < DH / 16; ++kk)
+                        mma_bf16_ss(tmem + tcol, a_tile + kk * 2, dUB + kk * 2, ID_N16, kk);
+                }
+                __syncwarp();
+            };
+            auto pair_k = [&](int t) { return dPair + (uint64_t)(((t % NP) * PAIR + ((t & 1) ? TILE : 0)) >> 4); };
+            auto pair_r = [&](int t) { return dPair + (uint64_t)(((t % NP) * PAIR + ((t & 1) ? 0 : TILE)) >> 4); };
             auto score_pair = [&](int t) {
                 const uint32_t dcol = (t & 1) ? TM_CA : TM_S;
-                const uint32_t b = sPair + (t % NP) * PAIR;
+                const uint64_t bb = dPair + (uint64_t)(((t % NP) * PAIR) >> 4);
+                if (elect()) {
 #pragma unroll
-                for (int kk = 0; kk < DH / 16; ++kk)
-                    mma_bf16_ss(tmem + dcol, sdesc_sw128(sQ + kk * 32), sdesc_sw128(b + kk * 32),
-                                ID_N256, kk);
+                    for (int kk = 0; kk < DH / 16; ++kk)
+                        mma_bf16_ss(tmem + dcol, dQ + kk * 2, bb + kk * 2, ID_N256, kk);
+                }
+                __syncwarp();
             };
             auto score_pair_ext = [&](int t) {
                 const uint32_t dcol = (t & 1) ? TM_CA : TM_S;
-                mma_bf16_ss(tmem + dcol, d_aext, sdesc_ext2(sPX + (t % NP) * EXT2), ID_N256, 1);
+                const uint64_t bx = dPX + (uint64_t)(((t % NP) * EXT2) >> 4);
+                if (elect()) {
+                    mma_bf16_ss(tmem + dcol, d_aext, bx, ID_N256, 1);
+                    mma_commit(bar.s_full);
+                    mma_commit(bar.pair_empty + t % NP);
+                }
+                __syncwarp();
             };
-            auto wait_pair = [&](int t) {
-                return mbar_wait(bar.pair_full + t % NP, (t / NP) & 1, abort_flag, wait_ns);
+            auto commit1 = [&](uint64_t *b1) {
+                if (elect()) mma_commit(b1);
+                __syncwarp();
             };
+            auto wait_pair = [&](int t) { return W(bar.pair_full + t % NP, (t / NP) & 1); };
 
-            // Prologue: biases of pair 0 (key tile 0, chunk 1) and of chunk 0
-            // (they need the [u ; v] tile, not q).
-            bool ok = mbar_wait(bar.prep, 0, abort_flag, wait_ns);
-            if (ok) ok = wait_pair(0) && mbar_wait(bar.r0_full, 0, abort_flag, wait_ns);
+            bool ok = W(bar.prep, 0);
+            if (ok) ok = wait_pair(0) && W(bar.r0_full, 0);
             if (ok) {
                 tc_fence_after_sync();
                 bias_mma(TM_BK, pair_k(0));
                 bias_mma(TM_BR, pair_r(0));
-                bias_mma(TM_BR2, sR0);
-                mma_commit(bar.bias_full);
+                bias_mma(TM_BR2, dR0);
+                commit1(bar.bias_full);
             }
-            // Scores of tile 0: pair 0 (S and chunk 1), chunk 0 into the even slot.
-            // The main K-steps go right behind the bias MMAs; only the two bias
-            // K-steps wait for the softmax warps' conversion.
-            if (ok) ok = mbar_wait(bar.q_full, 0, abort_flag, wait_ns);
+            if (ok) ok = W(bar.q_full, 0);
             if (ok) {
                 tc_fence_after_sync();
                 score_pair(0);
+                if (elect()) {
 #pragma unroll
-                for (int kk = 0; kk < DH / 16; ++kk)
-                    mma_bf16_ss(tmem + TM_CA, sdesc_sw128(sQ + kk * 32), sdesc_sw128(sR0 + kk * 32),
-                                ID_N128, kk);
-                ok = mbar_wait(bar.ext_full, 0, abort_flag, wait_ns);
+                    for (int kk = 0; kk < DH / 16; ++kk)
+                        mma_bf16_ss(tmem + TM_CA, dQ + kk * 2, dR0 + kk * 2, ID_N128, kk);
+                }
+                __syncwarp();
+                ok = W(bar.ext_full, 0);
             }
             if (ok) {
                 tc_fence_after_sync();
-                score_pair_ext(0);
-                mma_bf16_ss(tmem + TM_CA, d_aext, sdesc_ext(sR0X), ID_N128, 1);
-                mma_commit(bar.s_full);
-                mma_commit(bar.pair_empty);
+                if (elect()) {
+                    mma_bf16_ss(tmem + TM_S, d_aext, dPX, ID_N256, 1);
+                    mma_bf16_ss(tmem + TM_CA, d_aext, dR0X, ID_N128, 1);
+                    mma_commit(bar.s_full);
+                    mma_commit(bar.pair_empty);
+                }
+                __syncwarp();
             }
-            // Biases of tile 1: pair 1 (key tile 1, chunk 2).
             if (ok && T > 1) {
                 ok = wait_pair(1);
                 if (ok) {
                     tc_fence_after_sync();
                     bias_mma(TM_BK, pair_k(1));
                     bias_mma(TM_BR, pair_r(1));
-                    mma_commit(bar.bias_full);
+                    commit1(bar.bias_full);
                 }
             }
             for (int it = 0; it < T && ok; ++it) {
-                if (!(ok = mbar_wait_poll(bar.s_free, it & 1, abort_flag, wait_ns))) break;
+                if (!(ok = WP(bar.s_free, it & 1))) break;
                 if (it + 1 < T) {
-                    // Scores of tile it+1: pair it+1, whose chunk it+2 goes into
-                    // the slot chunk it just left.  The bias K-step waits for the
-                    // softmax warps' conversion; the main ones need not.
                     tc_fence_after_sync();
                     score_pair(it + 1);
-                    if (!(ok = mbar_wait_poll(bar.ext_full, (it + 1) & 1, abort_flag, wait_ns))) break;
+                    if (!(ok = WP(bar.ext_full, (it + 1) & 1))) break;
                     tc_fence_after_sync();
                     score_pair_ext(it + 1);
-                    mma_commit(bar.s_full);
-                    mma_commit(bar.pair_empty + (it + 1) % NP);
                 }
-                if (!(ok = mbar_wait_poll(bar.p_full, it & 1, abort_flag, wait_ns))) break;
+                if (!(ok = WP(bar.p_full, it & 1))) break;
                 const int st = it % NS;
-                if (!(ok = mbar_wait(bar.v_full + st, (it / NS) & 1, abort_flag, wait_ns))) break;
+                if (!(ok = W(bar.v_full + st, (it / NS) & 1))) break;
                 tc_fence_after_sync();
-                const uint32_t vb = sV + st * TILE;
+                const uint64_t vb = dV + (uint64_t)((st * TILE) >> 4);
+                if (elect()) {
 #pragma unroll
-                for (int kk = 0; kk < BN / 16; ++kk)
-                    mma_bf16_ts(tmem + TM_O, tmem + TM_P + 8 * kk, sdesc_sw128(vb + kk * 2048), ID_O,
-                                (it > 0 || kk > 0) ? 1u : 0u);
-                mma_commit(bar.o_done);
-                mma_commit(bar.v_empty + st);
+                    for (int kk = 0; kk < BN / 16; ++kk)
+                        mma_bf16_ts(tmem + TM_O, tmem + TM_P + 8 * kk, vb + kk * (2048 >> 4), ID_O,
+                                    (it > 0 || kk > 0) ? 1u : 0u);
+                    mma_commit(bar.o_done);
+                    mma_commit(bar.v_empty + st);
+                }
+                __syncwarp();
                 if (it + 2 < T) {
-                    // Biases of tile it+2: pair it+2 (key tile it+2, chunk it+3).
-                    // Their TMEM columns hold P until this PV has completed.
-                    if (!(ok = mbar_wait(bar.o_done, it & 1, abort_flag, wait_ns))) break;
+                    if (!(ok = W(bar.o_done, it & 1))) break;
                     if (!(ok = wait_pair(it + 2))) break;
                     tc_fence_after_sync();
                     bias_mma(TM_BK, pair_k(it + 2));
                     bias_mma(TM_BR, pair_r(it + 2));
-                    mma_commit(bar.bias_full);
+                    commit1(bar.bias_full);
                 }
             }
-            // Every MMA issued above completes before TMEM is released.
-            mma_commit(bar.drain);
+            commit1(bar.drain);
             const int zero = 0;
             mbar_wait(bar.drain, 0, &zero, wait_ns);
-            if (!ok) fail(p, abort_flag);
+            if (!ok && lane == 0) fail(p, abort_flag);
         }
     } else if (warp >= 4) {
         // ===================== softmax warps ====================================

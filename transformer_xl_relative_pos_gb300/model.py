@@ -103,6 +103,11 @@ class XLStack:
         self.mems = None
         self.states = None
         self._r_cache = {}
+        # When set to a list, each eager segment appends, per layer, the layer's
+        # input h, its memory, the attention operands (q, k, v, r, M), the
+        # attention output a [B, H, L, dh] and the layer's output h' (all on the
+        # device): what a per-layer check of the stack needs.
+        self.taps = None
 
     def reset(self, B: int):
         self._graphs = {}
@@ -196,12 +201,16 @@ class XLStack:
                 ext = txl.mem_concat(self.mems[n], st, h)
                 k = project_heads(ext, lay["W_kE"], self.H)
                 v = project_heads(ext, lay["W_v"], self.H)
-            a = txl.relattn_fwd(q, k, v, self._r(n, M_cur + L), self.u, self.v_bias, M_cur,
-                                self.scale)
-            a = a.transpose(1, 2).reshape(B, L, -1)
+            r = self._r(n, M_cur + L)
+            a_heads = txl.relattn_fwd(q, k, v, r, self.u, self.v_bias, M_cur, self.scale)
+            a = a_heads.transpose(1, 2).reshape(B, L, -1)
             o = layer_norm((a @ lay["W_o"].t()).float() + lay["b_o"].float() + h.float())
             f = torch.relu(o.to(self.dtype) @ lay["W_1"].t() + lay["b_1"])
             h_next = layer_norm(o + (f @ lay["W_2"].t()).float() + lay["b_2"].float())
+            if self.taps is not None:
+                mem_now = txl.mem_concat(self.mems[n], st, h[:, :0])
+                self.taps.append({"h": h, "mem": mem_now, "q": q, "k": k, "v": v, "r": r,
+                                  "M": M_cur, "a": a_heads, "h_out": h_next.to(self.dtype)})
             txl.mem_update(self.mems[n], st, h)
             if self.cache_kv:
                 txl.mem_update(self.kmems[n], ks, k_new)
