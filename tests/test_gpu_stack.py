@@ -19,7 +19,8 @@ import torch
 
 import oracle
 import txl_inputs
-from parity import compare, dev
+from parity import TOL_BF16, TOL_BF16_RMS, compare, dev
+import transformer_xl_relative_pos_gb300 as txl
 from transformer_xl_relative_pos_gb300.model import XLStack
 
 pytestmark = pytest.mark.gpu
@@ -57,14 +58,99 @@ def test_small_stack_memory_fill_and_wrap(cache_kv):
                             dtype="bf16", seed=41, d_ff=256, n_layer=3, n_seg=5, vocab=base.vocab)
     h_gpu, h_or, stack, mems = run_stack(w, cache_kv=cache_kv)
     assert all(m.shape[1] == 100 for m in mems)
+    # three layers: sqrt(3) times the one-layer bound (below) is 4.5e-2
     compare(h_gpu, h_or, 6e-2, 1.5e-2, what=f"small stack cache_kv={cache_kv}")
 
 
-def test_c5_stack12_last_segment():
+# Bounds of the stack checks.  The stack keeps its states in bf16 between layers
+# (the workload's element type), so a layer's output carries up to half a bf16
+# ulp of its magnitude: 2^-9 * 2^ceil(log2 max|h|), 0.0156 for the LayerNorm
+# outputs here (|h| < 8).  Inside a layer the other bf16 rounding points (the
+# attention output, the Linear outputs, o rounded for the feed-forward input)
+# reach the output through weights ~N(0, 0.02) (a gain of about 0.02 * sqrt(fan-in)
+# ~ 0.45 per matmul) and the LayerNorm's division by a standard deviation near 1:
+# at most about 1e-2 on the largest outputs.  One layer: half an output ulp + 1e-2.
+# Through N layers the residual stream carries each layer's error forward with a
+# gain near 1 (LayerNorm of o + f, both O(1)); independent roundings add like a
+# random walk, so N = 12 layers stay within 1e-1 at the maximum (sqrt(12) times
+# the one-layer bound is 9e-2) and 2e-2 in rms (12 times the one-layer rms bound).
+LAYER_INTERNAL = 1e-2
+LAYER_RMS = 5e-3
+
+
+def half_ulp_bf16(x):
+    m = float(np.abs(x).max())
+    return 2.0 ** -9 * 2.0 ** math.ceil(math.log2(m)) if m > 0 else 0.0
+
+
+@pytest.fixture(scope="module")
+def c5_last_segment():
+    """The 12-layer, 16-segment stream; the last segment runs with taps on every
+    layer (input, memory, attention operands and output, layer output)."""
     w = txl_inputs.WORKLOADS["c5_stack12_L512_M512"]
-    h_gpu, h_or, stack, mems = run_stack(w)
+    params = txl_inputs.draw_stack(w)
+    stack = XLStack(params, w.H, w.M, dev(), torch.bfloat16)
+    tokens = params["tokens"]
+    for s in range(tokens.shape[0] - 1):
+        stack.segment(tokens[s])
+    mems = [m.double().cpu().numpy() for m in stack.memories()]
+    stack.taps = []
+    h_gpu = stack.segment(tokens[-1]).double().cpu().numpy()
+    torch.cuda.synchronize()
+    assert txl.device_status() == 0
+    taps = [{k: (v.double().cpu().numpy() if torch.is_tensor(v) else v) for k, v in tp.items()}
+            for tp in stack.taps]
+    layers64 = [{k: rounded(v) for k, v in lay.items()} for lay in params["layers"]]
+    return {"w": w, "params": params, "mems": mems, "h_gpu": h_gpu, "taps": taps,
+            "layers64": layers64, "u": rounded(params["u"]), "v_bias": rounded(params["v_bias"])}
+
+
+def test_c5_stack12_attention_of_every_layer(c5_last_segment):
+    # Kernel parity inside the stream, at the stated tolerance: each layer's
+    # attention output of the last segment against the fp64 oracle on that
+    # layer's own bf16 q, k, v and table (§3.3 summary, one layer at a time).
+    c = c5_last_segment
+    w = c["w"]
+    assert len(c["taps"]) == 12
+    for n, tp in enumerate(c["taps"]):
+        K = tp["k"].shape[2]
+        assert tp["M"] == w.M and K == w.M + w.L
+        rel = oracle.distance_table(tp["r"][:, -K:])
+        want, _ = oracle.relattn(tp["q"], tp["k"], tp["v"], rel, c["u"], c["v_bias"], tp["M"],
+                                 w.L, 1.0 / math.sqrt(w.dh))
+        compare(tp["a"], want, TOL_BF16, TOL_BF16_RMS, what=f"c5 layer {n} attention")
+
+
+def test_c5_stack12_every_layer_step(c5_last_segment):
+    # Each layer of the last segment against the oracle's layer (§3.3 summary:
+    # attention, Linear + residual + LayerNorm, feed-forward) run in fp64 on the
+    # GPU layer's own bf16 input and memory; bound: half an output ulp plus the
+    # propagated internal rounding (see the bounds above).
+    c = c5_last_segment
+    w = c["w"]
+    for n, tp in enumerate(c["taps"]):
+        want = oracle.layer_forward(tp["h"], tp["mem"], c["layers64"][n], c["u"], c["v_bias"],
+                                    w.H, 1.0 / math.sqrt(w.dh))
+        bound = half_ulp_bf16(want) + LAYER_INTERNAL
+        err = np.abs(tp["h_out"] - want)
+        assert float(err.max()) <= bound, f"layer {n}: max |err| {err.max():.3e} > {bound:.3e}"
+        assert math.sqrt(float((err ** 2).mean())) <= LAYER_RMS, f"layer {n}: rms"
+        if n + 1 < len(c["taps"]):  # the next layer reads exactly this output
+            assert np.array_equal(c["taps"][n + 1]["h"], tp["h_out"])
+
+
+def test_c5_stack12_last_segment(c5_last_segment):
+    # The whole stream against the oracle's explicit recomputation of the last
+    # segment from the stored memories (§3.2 recurrence, §3.3 summary); bound
+    # from the one-layer bound compounded over 12 layers (see above).
+    c = c5_last_segment
+    w = c["w"]
+    mems = c["mems"]
     assert len(mems) == 12 and all(m.shape == (w.B, w.M, w.d_model) for m in mems)
-    compare(h_gpu, h_or, 1e-1, 2e-2, what="c5 top layer")
+    h_or, _ = oracle.segment_forward(c["params"]["tokens"][-1].numpy(), rounded(c["params"]["emb"]),
+                                     c["layers64"], mems, c["u"], c["v_bias"], w.H, w.M,
+                                     1.0 / math.sqrt(w.dh))
+    compare(c["h_gpu"], h_or, 1e-1, 2e-2, what="c5 top layer")
 
 
 def test_cached_kv_rings_match_projected_memory():
