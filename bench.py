@@ -30,9 +30,10 @@ after the timed region.
 
 End to end (the line's ``e2e``): the recurrent evaluation through the public
 API from pinned host buffers: each step copies in the new segment's q, k, v
-and hidden states, extends the device-resident k/v memory rings
-(txl_mem_concat), computes the table, attends over all K keys, advances the
-rings (txl_mem_update) and reads the output back; host clock around the steps.
+and hidden states, appends k and v behind the device-resident memory windows
+(txl_kv_window_append), attends over all K keys read in place from those
+windows (txl_relattn_fwd_strided), advances the windows and the hidden-state
+ring (txl_mem_update) and reads the output back; host clock around the steps.
 
 ``--impl reference`` times the fp64 CPU oracle instead (the reference arm).
 """
@@ -82,7 +83,6 @@ def profiled_traffic(workload_name: str):
 
 METRIC = "rel-attn fwd TFLOP/s + tokens/s at L=128,M=1600; % of GB300 bf16 TC peak"
 N_SETS = 3
-RING_PERIOD = 25        # M / gcd(M, L) segments bring the ring head back to 0
 GRAPH_CHUNK = 1500      # steps per graph when K is large (multiple of 3 * 25)
 
 
@@ -315,6 +315,176 @@ def build_operands(w, dev, rank=0):
     return {"q": q, "k": k, "v": v, "r": r, "u": u, "v_bias": vb, "h": h_seg, "mem": mem}
 
 
+def run_e2e(w, dev, hs, r, u, vb, scale, ws, flops_step, n_steps):
+    """End to end through the API, as a recurrent evaluation runs it (§3.2).
+
+    The memory's projected keys and values stay on the device between segments,
+    each in a window of a larger buffer (txl_kv_window_append / _advance), so
+    the attention reads [memory ; segment] in place (txl_relattn_fwd_strided):
+    nothing is concatenated.  Each step copies in, from pinned host buffers,
+    only what is new (the segment's q, k, v and hidden states, one copy of one
+    buffer), appends the segment to the k and v windows, attends over all
+    K = M + L keys, advances the windows and the hidden-state memory ring
+    (txl_mem_update), and reads the output back.  Two different host segments
+    alternate.  The copies of step n+1 run on a copy stream while step n's
+    kernels run (two device input sets), and each result is read back on a
+    third stream.  Once the memories are full the device work of a step is
+    replayed from a CUDA graph: the windows (capacity M + 25 L) and the ring
+    both repeat their positions every 25 steps, so one graph per step of that
+    cycle and input set is captured in step order.  After the timed steps the
+    last output is checked against an attention over [memory ; segment] built
+    on the host from the known segment sequence."""
+    import torch
+    import transformer_xl_relative_pos_gb300 as txl
+    B, H, BH, L_, M_, dh_ = w.B, w.H, w.B * w.H, w.L, w.M, w.dh
+    cyc = M_ // math.gcd(M_, L_)          # ring positions of the hidden-state memory
+    C = M_ + cyc * L_                     # window capacity: the same cycle (>= 2M + L)
+    assert C >= 2 * M_ + L_
+    g = torch.Generator().manual_seed(123)
+    # the segment's q, k, v [B, H, L, 64] and hidden states [B, L, d]: set 0 as
+    # drawn for the step, set 1 a second, different segment
+    segs = [{"q": hs["q"].cpu(), "k": hs["k"][:, :, M_:].cpu(), "v": hs["v"][:, :, M_:].cpu(),
+             "h": hs["h"].cpu()}]
+    segs.append({k2: (t.float() + 0.25 * torch.randn(t.shape, generator=g)).to(t.dtype)
+                 for k2, t in segs[0].items()})
+    layout, off = {}, 0
+    for k2, t in segs[0].items():
+        nb = t.numel() * t.element_size()
+        layout[k2] = (off, nb, t.dtype, tuple(t.shape))
+        off += (nb + 255) // 256 * 256
+    h2d = off
+
+    def views(flat):
+        return {k2: flat[o:o + nb].view(dt).view(sh) for k2, (o, nb, dt, sh) in layout.items()}
+
+    host_flat = [torch.empty(h2d, dtype=torch.uint8).pin_memory() for _ in range(2)]
+    for j in range(2):
+        for k2, t in views(host_flat[j]).items():
+            t.copy_(segs[j][k2].contiguous())
+    outs_h = [torch.empty(hs["out"].shape, dtype=hs["out"].dtype).pin_memory() for _ in range(2)]
+    d2h = outs_h[0].numel() * outs_h[0].element_size()
+    dev_flat = [torch.empty(h2d, dtype=torch.uint8, device=dev) for _ in range(2)]
+    dev_in = [views(f) for f in dev_flat]
+    dev_out = [torch.empty_like(hs["out"]) for _ in range(2)]
+    kbuf = torch.empty(BH, C, dh_, dtype=torch.bfloat16, device=dev)
+    vbuf = torch.empty_like(kbuf)
+    h_ring = torch.empty_like(hs["mem"])
+    k_win, v_win = txl.KVWindow(0, 0, C, M_), txl.KVWindow(0, 0, C, M_)
+    h_st = txl.MemState(0, 0, M_)
+    copy_s, comp_s, back_s = torch.cuda.Stream(), torch.cuda.Stream(), torch.cuda.Stream()
+    in_free = [torch.cuda.Event() for _ in range(2)]    # step's kernels done with its inputs
+    in_ready = [torch.cuda.Event() for _ in range(2)]   # step's inputs copied
+    out_ready = [torch.cuda.Event() for _ in range(2)]  # step's output written
+    out_read = [torch.cuda.Event() for _ in range(2)]   # step's output read back
+    for e in in_free + out_read:
+        e.record(comp_s)
+
+    def device_work(b):
+        x = dev_in[b]
+        m_cur = k_win.fill
+        k_new = x["k"].view(BH, L_, dh_)
+        v_new = x["v"].view(BH, L_, dh_)
+        txl.kv_window_append(kbuf, k_win, k_new)
+        txl.kv_window_append(vbuf, v_win, v_new)
+        txl.relattn_fwd(x["q"], txl.kv_window_view(kbuf, k_win, L_, B, H),
+                        txl.kv_window_view(vbuf, v_win, L_, B, H), r, u, vb, m_cur, scale,
+                        out=dev_out[b], workspace=ws)
+        txl.kv_window_advance(k_win, L_)
+        txl.kv_window_advance(v_win, L_)
+        txl.mem_update(h_ring, h_st, x["h"])
+
+    graphs = {}  # step index within the cycle -> captured device work
+
+    def e2e_step(i, cycle=None):
+        b = i % 2
+        with torch.cuda.stream(copy_s):
+            copy_s.wait_event(in_free[b])
+            dev_flat[b].copy_(host_flat[b], non_blocking=True)
+            in_ready[b].record(copy_s)
+        with torch.cuda.stream(comp_s):
+            comp_s.wait_event(in_ready[b])
+            comp_s.wait_event(out_read[b])
+            if cycle is None:
+                device_work(b)
+            else:
+                graphs[i % cycle].replay()
+            in_free[b].record(comp_s)
+            out_ready[b].record(comp_s)
+        with torch.cuda.stream(back_s):
+            back_s.wait_event(out_ready[b])
+            outs_h[b].copy_(dev_out[b], non_blocking=True)
+            out_read[b].record(back_s)
+
+    def drain():
+        for s_ in (copy_s, comp_s, back_s):
+            s_.synchronize()
+
+    # Fill the memories from the host, and run eagerly until the windows have
+    # moved back to their buffers' front once: from then on their positions
+    # repeat every 25 steps (before, while M / L is not a whole number, they
+    # follow a different sequence).  Then capture one graph per step of the
+    # cycle, in step order (the host-side window and ring states advance as the
+    # eager calls advance them).
+    i, moved_back = 0, False
+    while i < -(-M_ // L_) + 3 or not moved_back:
+        full = k_win.fill == M_
+        e2e_step(i)
+        moved_back = moved_back or (full and k_win.start == L_)  # appended at the front
+        i += 1
+        assert i < 10 * cyc, "the windows never moved back"
+    e2e_step(i)
+    n_fill = i + 1
+    drain()
+    assert k_win.fill == M_ and v_win.fill == M_ and h_st.fill == M_
+    cycle = 2 * cyc  # positions x the two input sets
+    cap_s = torch.cuda.Stream()
+    cap_s.wait_stream(comp_s)
+    for i in range(n_fill, n_fill + cycle):
+        g_ = torch.cuda.CUDAGraph()
+        with torch.cuda.stream(cap_s):
+            with torch.cuda.graph(g_, stream=cap_s):
+                device_work(i % 2)
+        graphs[i % cycle] = g_
+    comp_s.wait_stream(cap_s)
+    for i in range(n_fill, n_fill + 3):
+        e2e_step(i, cycle)
+    drain()
+    base_i = n_fill + 3
+    t0 = time.perf_counter()
+    for i in range(n_steps):
+        e2e_step(base_i + i, cycle)
+    drain()
+    t_e2e = time.perf_counter() - t0
+    # Check the last step independently: its memory is the newest M rows of the
+    # k, v stream of all earlier segments (set (i % 2) at step i), its segment
+    # the last one; attention over [memory ; segment] concatenated here.
+    last = base_i + n_steps - 1
+    need = -(-M_ // L_)
+    kv = {}
+    for name in ("k", "v"):
+        hist = torch.cat([segs[i % 2][name] for i in range(last - need, last)], dim=2)
+        kv[name] = torch.cat([hist[:, :, -M_:], segs[last % 2][name]], dim=2).to(dev)
+    want = txl.relattn_fwd(segs[last % 2]["q"].to(dev), kv["k"], kv["v"], r, u, vb, M_, scale,
+                           workspace=ws)
+    torch.cuda.synchronize()
+    assert torch.equal(dev_out[last % 2], want), "replayed step differs from the direct attention"
+    assert torch.equal(outs_h[last % 2], want.cpu()), "host copy of the output differs"
+    assert txl.device_status() == 0
+    return {"value": flops_step * n_steps / t_e2e / 1e12, "unit": "TFLOP/s",
+            "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+            "steps": n_steps, "ms_per_step": 1e3 * t_e2e / n_steps,
+            "inputs": "per step from pinned host memory: the segment's q, k, v [B, H, L, 64] and "
+                      "hidden states [B, L, d_model], two different segments alternating; the "
+                      "memory's k, v (M rows) stay on the device in windows filled from the host "
+                      "by earlier steps",
+            "device_work": "kv_window_append (k, v) + relattn_fwd over K = M + L keys read in "
+                           "place (strided) + kv_window_advance + mem_update (h), replayed from "
+                           "one CUDA graph per step of the 25-step cycle; the last output checked "
+                           "equal to an attention over [memory ; segment] rebuilt on the host",
+            "timing": "host clock around all steps (copies on their own streams), synchronized "
+                      "on both sides"}
+
+
 def run_ours(args, world, rank, local):
     import torch
     import transformer_xl_relative_pos_gb300 as txl
@@ -451,142 +621,7 @@ def run_ours(args, world, rank, local):
     # ---- end to end through the public API with host buffers ----------------
     e2e = None
     if rank == 0 and args.e2e_steps > 0:
-        # End to end through the API, as a recurrent evaluation runs it (§3.2):
-        # the memory's projected keys and values stay on the device in rings
-        # between segments, and each step copies in, from pinned host buffers,
-        # only what is new: the segment's q, k, v and hidden states.  On the
-        # device the step builds the extended keys and values ([memory ;
-        # segment], txl_mem_concat), attends over all K = M + L of them, and
-        # advances the k, v and hidden-state rings (txl_mem_update); the output
-        # goes back to the host.  The inputs travel as one copy (one pinned
-        # buffer holding the four tensors).  The copies of step n+1 run on a copy
-        # stream while step n's kernels run (two device input sets), and each
-        # result is read back on a third stream.  Once the rings are full, the
-        # device work of a step is replayed from a CUDA graph: the rings advance
-        # by L rows a step, so their positions repeat every M / gcd(M, L) steps,
-        # and one graph per step of that cycle (times the two input sets) is
-        # captured in step order.  Every memory row the timed steps attend to
-        # came from the host in an earlier step.
-        hs = sets[0]
-        BH, L_, M_, dh_ = w.B * w.H, w.L, w.M, w.dh
-        seg = {"q": hs["q"], "k": hs["k"][:, :, M_:], "v": hs["v"][:, :, M_:], "h": hs["h"]}
-        layout, off = {}, 0
-        for k2, t in seg.items():
-            nb = t.numel() * t.element_size()
-            layout[k2] = (off, nb, t.dtype, tuple(t.shape))
-            off += (nb + 255) // 256 * 256
-        h2d = off
-        host_flat = torch.empty(h2d, dtype=torch.uint8).pin_memory()
-
-        def views(flat):
-            return {k2: flat[o:o + nb].view(dt).view(sh) for k2, (o, nb, dt, sh) in layout.items()}
-
-        for k2, t in views(host_flat).items():
-            t.copy_(seg[k2].cpu())
-        outs_h = [torch.empty(hs["out"].shape, dtype=hs["out"].dtype).pin_memory() for _ in range(2)]
-        d2h = outs_h[0].numel() * outs_h[0].element_size()
-        dev_flat = [torch.empty(h2d, dtype=torch.uint8, device=dev) for _ in range(2)]
-        dev_in = [views(f) for f in dev_flat]
-        dev_out = [torch.empty_like(hs["out"]) for _ in range(2)]
-        k_ring = torch.empty(BH, M_, dh_, dtype=torch.bfloat16, device=dev)
-        v_ring = torch.empty_like(k_ring)
-        h_ring = torch.empty_like(hs["mem"])
-        k_st, v_st, h_st = (txl.MemState(0, 0, M_), txl.MemState(0, 0, M_), txl.MemState(0, 0, M_))
-        k_ext = [torch.empty(BH, M_ + L_, dh_, dtype=torch.bfloat16, device=dev) for _ in range(2)]
-        v_ext = [torch.empty_like(k_ext[0]) for _ in range(2)]
-        copy_s, comp_s, back_s = torch.cuda.Stream(), torch.cuda.Stream(), torch.cuda.Stream()
-        in_free = [torch.cuda.Event() for _ in range(2)]    # step's kernels done with its inputs
-        in_ready = [torch.cuda.Event() for _ in range(2)]   # step's inputs copied
-        out_ready = [torch.cuda.Event() for _ in range(2)]  # step's output written
-        out_read = [torch.cuda.Event() for _ in range(2)]   # step's output read back
-        for e in in_free + out_read:
-            e.record(comp_s)
-
-        def device_work(b):
-            x = dev_in[b]
-            m_cur = k_st.fill
-            k_new = x["k"].view(BH, L_, dh_)
-            v_new = x["v"].view(BH, L_, dh_)
-            full = m_cur == M_
-            kx = txl.mem_concat(k_ring, k_st, k_new, out=k_ext[b] if full else None)
-            vx = txl.mem_concat(v_ring, v_st, v_new, out=v_ext[b] if full else None)
-            txl.relattn_fwd(x["q"], kx.view(w.B, w.H, m_cur + L_, dh_),
-                            vx.view(w.B, w.H, m_cur + L_, dh_), r, u, vb, m_cur, scale,
-                            out=dev_out[b], workspace=ws)
-            txl.mem_update(k_ring, k_st, k_new)
-            txl.mem_update(v_ring, v_st, v_new)
-            txl.mem_update(h_ring, h_st, x["h"])
-
-        graphs = {}  # step index within the ring cycle -> captured device work
-
-        def e2e_step(i, cycle=None):
-            b = i % 2
-            with torch.cuda.stream(copy_s):
-                copy_s.wait_event(in_free[b])
-                dev_flat[b].copy_(host_flat, non_blocking=True)
-                in_ready[b].record(copy_s)
-            with torch.cuda.stream(comp_s):
-                comp_s.wait_event(in_ready[b])
-                comp_s.wait_event(out_read[b])
-                if cycle is None:
-                    device_work(b)
-                else:
-                    graphs[i % cycle].replay()
-                in_free[b].record(comp_s)
-                out_ready[b].record(comp_s)
-            with torch.cuda.stream(back_s):
-                back_s.wait_event(out_ready[b])
-                outs_h[b].copy_(dev_out[b], non_blocking=True)
-                out_read[b].record(back_s)
-
-        def drain():
-            for s_ in (copy_s, comp_s, back_s):
-                s_.synchronize()
-
-        # Fill the rings from the host (M / L segments), then a few full steps
-        # (eager).  The same segment comes in every step, so once the rings are
-        # full every step's output is the same: the graph-replayed steps are
-        # checked against the last eager one bit for bit.
-        n_fill = -(-M_ // L_) + 3
-        for i in range(n_fill):
-            e2e_step(i)
-        drain()
-        assert k_st.fill == M_ and v_st.fill == M_ and h_st.fill == M_
-        want = dev_out[(n_fill - 1) % 2].clone()
-        cycle = 2 * (M_ // math.gcd(M_, L_))  # ring positions x the two input sets
-        cap_s = torch.cuda.Stream()
-        cap_s.wait_stream(comp_s)
-        for i in range(n_fill, n_fill + cycle):  # in step order: the host ring states advance
-            g_ = torch.cuda.CUDAGraph()
-            with torch.cuda.stream(cap_s):
-                with torch.cuda.graph(g_, stream=cap_s):
-                    device_work(i % 2)
-            graphs[i % cycle] = g_
-        comp_s.wait_stream(cap_s)
-        for i in range(n_fill, n_fill + 3):
-            e2e_step(i, cycle)
-        drain()
-        base_i = n_fill + 3
-        t0 = time.perf_counter()
-        for i in range(args.e2e_steps):
-            e2e_step(base_i + i, cycle)
-        drain()
-        t_e2e = time.perf_counter() - t0
-        last = (base_i + args.e2e_steps - 1) % 2
-        assert torch.equal(dev_out[last], want), "graph-replayed step differs from the eager one"
-        assert torch.equal(outs_h[last], want.cpu()), "host copy of the output differs"
-        assert txl.device_status() == 0
-        e2e = {"value": flops_step * args.e2e_steps / t_e2e / 1e12, "unit": "TFLOP/s",
-               "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
-               "steps": args.e2e_steps, "ms_per_step": 1e3 * t_e2e / args.e2e_steps,
-               "inputs": "per step from pinned host memory: the segment's q, k, v [B, H, L, 64] and "
-                         "hidden states [B, L, d_model]; the memory's k, v (M rows) stay on the "
-                         "device in rings filled from the host by earlier steps",
-               "device_work": "mem_concat (k, v) + relattn_fwd over K = M + L keys + "
-                              "mem_update (k, v, h), replayed from one CUDA graph per step of the "
-                              "rings' cycle; outputs checked equal to an eager step",
-               "timing": "host clock around all steps (copies on their own streams), synchronized "
-                         "on both sides"}
+        e2e = run_e2e(w, dev, sets[0], r, u, vb, scale, ws, flops_step, args.e2e_steps)
 
     if rank != 0:
         return
@@ -699,11 +734,11 @@ def run_table9(args):
                 "note": "one attention layer; the paper's ratio is for the whole model"}}), flush=True)
 
 
-# Decode steps (one to six new tokens against a long memory), H = 16 heads of
+# Decode steps (one to eight new tokens against a long memory), H = 16 heads of
 # 64: the memory lengths of the long-memory evaluation (M = 1600 and 3800).
-DECODE_SHAPES = [(8, 1, 3800), (8, 2, 3800), (8, 3, 3800), (8, 4, 3800), (8, 5, 3800), (8, 6, 3800),
-                 (16, 1, 1600), (16, 6, 1600), (64, 1, 3800), (64, 6, 3800), (1, 1, 3800), (1, 6, 3800),
-                 (2, 6, 800)]
+DECODE_SHAPES = [(8, L, 3800) for L in range(1, 9)] + [
+    (16, 1, 1600), (16, 6, 1600), (16, 8, 1600), (64, 1, 3800), (64, 6, 3800), (64, 8, 3800),
+    (1, 1, 3800), (1, 6, 3800), (1, 8, 12000), (2, 6, 800)]
 
 
 def run_decode(args):
@@ -727,7 +762,8 @@ def run_decode(args):
             "B": B, "H": H, "L": L, "M": M, "dtype": "bf16", "us_per_call": us,
             "algorithmic_bytes": nbytes, "achieved_gbs": gbs, "peak_gbs": pk["hbm_gbs"],
             "hbm_frac": gbs / pk["hbm_gbs"], "input_sets": n_sets,
-            "path": {"decode": "decode kernel", "tc": "tensor-core kernel"}[kernel],
+            "path": {"decode": "decode kernel (CUDA cores)", "decode_mma": "decode kernel (warp MMAs)",
+                     "tc": "tensor-core kernel"}[kernel],
             "splits": splits}}), flush=True)
 
 
@@ -770,24 +806,32 @@ def run_stack(args):
     w = txl_inputs.WORKLOADS["c5_stack12_L512_M512"]
     params = txl_inputs.draw_stack(w)
     tokens = params["tokens"].to(dev)
+    n_seg = tokens.shape[0]
     for graphs, cache_kv in ((False, True), (False, False), (True, True), (True, False)):
         stack = XLStack(params, w.H, w.M, dev, torch.bfloat16, cache_kv=cache_kv, graphs=graphs)
-        n_warm = 3  # memories are full after the first segment (L = M); graph captured in the third
+        # Memories are full after the first segment (L = M); with graphs one is
+        # captured per distinct ring and window position, from the third segment
+        # on (one position for the rings, two for the windows of capacity
+        # M + 2L): the warm-up covers them all, so no capture falls in the
+        # timed segments.  Segments cycle through the workload's 16.
+        n_warm = 3 + 4
         for s_ in range(n_warm):
-            stack.segment(tokens[s_])
+            stack.segment(tokens[s_ % n_seg])
         torch.cuda.synchronize()
+        n_graphs = len(stack._graphs)
         e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         e0.record()
-        n_timed = tokens.shape[0] - n_warm
-        for s_ in range(n_warm, tokens.shape[0]):
-            stack.segment(tokens[s_])
+        n_timed = n_seg
+        for s_ in range(n_warm, n_warm + n_timed):
+            stack.segment(tokens[s_ % n_seg])
         e1.record()
         torch.cuda.synchronize()
+        assert len(stack._graphs) == n_graphs, "a graph was captured inside the timed segments"
         ms = e0.elapsed_time(e1) / n_timed
         print(json.dumps({"stack": {
             "workload": w.name, "layers": len(params["layers"]), "B": w.B, "H": w.H, "L": w.L,
             "M": w.M, "d_model": w.d_model, "cache_kv": cache_kv, "cuda_graphs": graphs,
-            "segments_timed": n_timed,
+            "graphs": n_graphs, "segments_timed": n_timed,
             "ms_per_segment": ms, "tokens_per_s": w.B * w.L / (ms * 1e-3)}}), flush=True)
 
 

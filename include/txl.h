@@ -46,7 +46,8 @@ typedef enum {
     TXL_ERR_SHAPE = -4,       /* sizes inconsistent with each other */
     TXL_ERR_CUDA = -5,        /* a CUDA runtime or driver call failed */
     TXL_ERR_TIMEOUT = -6,     /* a kernel gave up waiting on an on-chip barrier */
-    TXL_ERR_WORKSPACE = -7    /* workspace missing or too small for the request */
+    TXL_ERR_WORKSPACE = -7,   /* workspace missing or too small for the request */
+    TXL_ERR_INDEX = -8        /* a device-side index check failed (debug builds only) */
 } txl_status;
 
 typedef enum {
@@ -87,8 +88,9 @@ size_t txl_relattn_workspace_size(int B, int H, int L, int dh, int n_splits);
 /* Kernels txl_relattn_fwd may run (reported by txl_relattn_plan). */
 typedef enum {
     TXL_KERNEL_TC = 1,     /* bf16: tensor cores (tcgen05, TMEM, TMA), 128-row query tiles */
-    TXL_KERNEL_DECODE = 2, /* bf16, L <= 6: split-K kernel on the CUDA cores */
-    TXL_KERNEL_F32 = 3     /* fp32: CUDA cores */
+    TXL_KERNEL_DECODE = 2, /* bf16, L = 1: split-K decode kernel on the CUDA cores, fp32 */
+    TXL_KERNEL_F32 = 3,    /* fp32: CUDA cores */
+    TXL_KERNEL_DECODE_MMA = 4 /* bf16, 2 <= L <= 8: split-K decode kernel, warp-level tensor-core MMAs */
 } txl_kernel;
 
 /*
@@ -99,7 +101,7 @@ typedef enum {
  * nothing.
  *   *kernel  a txl_kernel value
  *   *splits  key ranges per query tile (TXL_KERNEL_TC) or per (b, h)
- *            (TXL_KERNEL_DECODE); 1 for TXL_KERNEL_F32
+ *            (TXL_KERNEL_DECODE, TXL_KERNEL_DECODE_MMA); 1 for TXL_KERNEL_F32
  * Returns the status the call would return for its sizes (TXL_ERR_WORKSPACE
  * when the split needs more workspace than given), or TXL_ERR_INVALID_ARG for
  * NULL outputs.
@@ -129,12 +131,12 @@ int txl_relattn_plan(int B, int H, int M, int L, int r_rows, int dh, int dtype, 
  *   out [B][H][L][dh]        lse [B][H][L] fp32, natural log (may be NULL)
  * dtype TXL_BF16: q, k, v, r, u, v_bias and out are bf16; scores, softmax and
  *   accumulation are fp32 on the tensor cores (tcgen05).  dh must be 64; q, k,
- *   v and r must be 16-byte aligned.  Segments of L <= 6 queries (decoding a
- *   few new tokens against a long memory) can take a split-K kernel on the CUDA
- *   cores instead, all arithmetic in fp32 (no bf16 rounding of P): always when
- *   n_splits >= 1, and with n_splits = 0 when its estimated time is below the
- *   tensor-core kernel's (which takes one sequence against a long memory
- *   from L of about 4 or 5 on; txl_relattn_plan tells which).  For this kernel n_splits
+ *   v and r must be 16-byte aligned.  Segments of L <= 8 queries (decoding a
+ *   few new tokens against a long memory) always take a split-K decode kernel
+ *   instead: from L = 2 on the tensor cores' warp-level MMAs with q + u, q + v
+ *   and P each carried as a bf16 pair (value and residual), for L = 1 the CUDA
+ *   cores in fp32; either way the error before the output's bf16 rounding is
+ *   far below that rounding (txl_relattn_plan tells which kernel).  For it n_splits
  *   counts key ranges per (b, h), each a whole number of 32-key chunks,
  *   at most one per 128 keys (larger requests are capped, ranges that would
  *   hold no key are dropped); up to 8 ranges of a head run as one thread-block
@@ -158,6 +160,31 @@ int txl_relattn_fwd(const void *q, const void *k, const void *v, const void *r, 
                     const void *u, const void *v_bias, void *out, float *lse, int B, int H,
                     int M, int L, int dh, float scale, int dtype, int n_splits,
                     void *workspace, size_t workspace_bytes, void *stream);
+
+/*
+ * txl_relattn_fwd_strided - txl_relattn_fwd with the (b, h) planes of k and v
+ * kv_stride elements apart instead of K * dh, so that the K = M + L keys of each
+ * plane can be a window of a larger buffer (the memory of §3.2 kept in place,
+ * the segment's rows written behind it; see txl_kv_window below) and nothing
+ * has to be concatenated before the call.
+ *
+ *   k, v  plane p = b*H + h starts at k + p * kv_stride (elements); within a
+ *         plane the K rows of dh elements are contiguous, memory rows first.
+ *         Only those K rows of each plane are read.
+ *   kv_stride >= K * dh and a multiple of 8 (16 bytes of bf16: every plane
+ *         starts 16-byte aligned when k and v do).
+ * Everything else (q, r, u, v_bias, out, lse, n_splits, workspace, the
+ * kernels, results and errors) is as for txl_relattn_fwd, which is this call
+ * with kv_stride = K * dh.
+ * Errors: those of txl_relattn_fwd; TXL_ERR_INVALID_ARG for kv_stride < 1,
+ * TXL_ERR_SHAPE for kv_stride < K * dh, TXL_ERR_MISALIGNED for a kv_stride not
+ * a multiple of 8.
+ */
+int txl_relattn_fwd_strided(const void *q, const void *k, const void *v, long long kv_stride,
+                            const void *r, int r_rows, const void *u, const void *v_bias,
+                            void *out, float *lse, int B, int H, int M, int L, int dh,
+                            float scale, int dtype, int n_splits, void *workspace,
+                            size_t workspace_bytes, void *stream);
 
 /*
  * TXL_NOALLOC_SCRATCH_BYTES - size of the scratch array built into the library
@@ -241,9 +268,60 @@ int txl_mem_update(void *mem, txl_mem_state *st, const void *h_new, int B, int L
                    int dtype, void *stream);
 
 /*
+ * A memory of §3.2 ("a predefined length-M old hidden states spanning
+ * (possibly) multiple segments") kept as a contiguous window of a larger
+ * buffer, one window per plane (e.g. the projected keys or values of each
+ * (batch, head)), so that [memory ; segment] is read in place by
+ * txl_relattn_fwd_strided.
+ *
+ *   buf   [planes][capacity][d] on the device, owned by the caller.
+ *   txl_kv_window lives in HOST memory and is owned by the caller:
+ *     start     row of the oldest memory row in every plane
+ *     fill      memory rows held (0..M)
+ *     capacity  rows per plane of buf; at least 2 * M + L for segments of L rows
+ *     M         memory length
+ * Initialise with {0, 0, capacity, M}.  Per segment:
+ *   txl_kv_window_append  puts the segment's L rows behind the memory rows;
+ *                         afterwards rows [start, start + fill + L) of every
+ *                         plane are [memory ; segment] (K = fill + L keys, at a
+ *                         plane stride of capacity * d elements);
+ *   (attention over that window)
+ *   txl_kv_window_advance keeps the newest M rows as the memory (host only).
+ */
+typedef struct {
+    int start;
+    int fill;
+    int capacity;
+    int M;
+} txl_kv_window;
+
+/*
+ * txl_kv_window_append - copy seg [planes][L][d] into rows start + fill ..
+ * start + fill + L - 1 of every plane.  When those rows would run past the
+ * buffer's end, the fill memory rows are first copied to rows 0 .. fill - 1 and
+ * start becomes 0 (with capacity >= 2M + L the two ranges never overlap).
+ * Same dtype and 16-byte rules as txl_mem_update.  Updates w->start on the host.
+ * Errors: TXL_ERR_INVALID_ARG (bad state, sizes, pointers or dtype),
+ * TXL_ERR_SHAPE (capacity < 2M + L), TXL_ERR_MISALIGNED, TXL_ERR_CUDA; *w is
+ * unchanged on error.
+ */
+int txl_kv_window_append(void *buf, txl_kv_window *w, const void *seg, int planes, int L, int d,
+                         int dtype, void *stream);
+
+/*
+ * txl_kv_window_advance - after attending to a segment of L rows appended by
+ * txl_kv_window_append: the memory becomes the newest min(fill + L, M) rows of
+ * [memory ; segment] (§3.2, the summary's m^n_tau).  Host arithmetic only.
+ * Errors: TXL_ERR_INVALID_ARG (bad state, L < 0), TXL_ERR_SHAPE (the window
+ * would run past the buffer: the segment was not appended).
+ */
+int txl_kv_window_advance(txl_kv_window *w, int L);
+
+/*
  * txl_device_status - synchronise `stream`, then read and clear the device
- * status word in which kernels record barrier time-outs.  Returns TXL_OK,
- * TXL_ERR_TIMEOUT or TXL_ERR_CUDA.
+ * status word in which kernels record barrier time-outs (and, in a debug
+ * build, failed index checks).  Returns TXL_OK, TXL_ERR_TIMEOUT (a time-out was
+ * recorded), TXL_ERR_INDEX (only failed index checks were) or TXL_ERR_CUDA.
  */
 int txl_device_status(void *stream);
 
@@ -262,6 +340,23 @@ uint64_t txl_set_wait_limit_ns(uint64_t ns);
  * (TXL_ERR_TIMEOUT when the path works).
  */
 int txl_debug_wait_timeout(uint64_t ns, void *stream);
+
+/*
+ * Debug build.  A library compiled with -DTXL_DEBUG checks, inside its kernels,
+ * the index arithmetic of the hot path (work split of each block, every row of
+ * the shared-memory ring that applies the Appendix B shift, TMEM columns of the
+ * table chunks, output rows, decode key and table ranges, memory ring slots and
+ * window rows).  A failed check records TXL_ERR_INDEX in the device status word
+ * and the kernel goes on: nothing traps.  Release builds compile the checks
+ * away.
+ *
+ * txl_debug_checks - 1 in a debug build, 0 otherwise.
+ * txl_debug_index_probe - launch one small kernel that fails one check on
+ *   purpose, then return txl_device_status(stream): TXL_ERR_INDEX in a debug
+ *   build (the reporting path works), TXL_OK in a release build.
+ */
+int txl_debug_checks(void);
+int txl_debug_index_probe(void *stream);
 
 #ifdef __cplusplus
 }

@@ -63,19 +63,20 @@ def test_relattn_plan_validation_and_routing():
     assert plan(1, 1, 16, 16, 32, 64, txl.F32, 2, 0, ctypes.byref(k), ctypes.byref(n)) == UNSUPPORTED
     assert txl.relattn_plan(1, 1, 16, 16, torch.float32) == ("f32", 1)
     ws = 1 << 30
-    # Segments past six queries always take the tensor cores; the headline shape
+    # Segments past eight queries take the tensor cores; the headline shape
     # (256 query tiles on 152 SMs) is not split.
     assert txl.relattn_plan(16, 16, 1600, 128, workspace_bytes=ws) == ("tc", 1)
-    assert txl.relattn_plan(8, 16, 3800, 7, workspace_bytes=ws)[0] == "tc"
-    # An explicit split of a short segment counts decode key ranges.
-    assert txl.relattn_plan(8, 16, 3800, 6, n_splits=3, workspace_bytes=ws) == ("decode", 3)
-    # The automatic choice for short segments follows the two kernels' estimates.
-    assert txl.relattn_plan(8, 16, 3800, 1, workspace_bytes=ws)[0] == "decode"
-    assert txl.relattn_plan(2, 16, 800, 6, workspace_bytes=ws)[0] == "decode"
-    assert txl.relattn_plan(1, 16, 3800, 6, workspace_bytes=ws)[0] == "tc"
-    # Without a workspace the tensor-core kernel cannot split one sequence's
-    # keys, and the decode kernel (which merges inside a cluster) is cheaper.
-    assert txl.relattn_plan(1, 16, 3800, 6, workspace_bytes=0)[0] == "decode"
+    assert txl.relattn_plan(8, 16, 3800, 9, workspace_bytes=ws)[0] == "tc"
+    assert txl.relattn_plan(1, 16, 3800, 9, workspace_bytes=0)[0] == "tc"
+    # Up to eight queries always a decode kernel, whatever the batch, memory
+    # or workspace (one query on the CUDA cores, more on warp MMAs); an explicit
+    # split counts its key ranges.
+    assert txl.relattn_plan(8, 16, 3800, 6, n_splits=3, workspace_bytes=ws) == ("decode_mma", 3)
+    assert txl.relattn_plan(8, 16, 3800, 1, n_splits=3, workspace_bytes=ws) == ("decode", 3)
+    for B, M, L in [(8, 3800, 1), (2, 800, 6), (1, 3800, 6), (1, 12000, 8), (64, 3800, 8), (1, 5, 2)]:
+        want = "decode" if L == 1 else "decode_mma"
+        assert txl.relattn_plan(B, 16, M, L, workspace_bytes=ws)[0] == want
+        assert txl.relattn_plan(B, 16, M, L, workspace_bytes=0)[0] == want
     # An explicit tensor-core split needs its workspace.
     assert plan(16, 16, 1600, 128, 1728, 64, txl.BF16, 4, 0, ctypes.byref(k),
                 ctypes.byref(n)) == WORKSPACE
@@ -155,7 +156,8 @@ def _span(K, n):
 
 @pytest.mark.parametrize("B,H", [(1, 1), (1, 16), (2, 3), (8, 16), (64, 16)])
 @pytest.mark.parametrize("M,L", [(0, 1), (1, 1), (127, 1), (300, 3), (3799, 1), (3800, 6), (511, 7),
-                                 (512, 512), (1600, 128), (3800, 128), (5000, 130)])
+                                 (4000, 8), (700, 9), (512, 512), (1600, 128), (3800, 128),
+                                 (5000, 130)])
 @pytest.mark.parametrize("n_splits", [0, 1, 2, 5, 9, 40])
 def test_plan_splits_are_valid(B, H, M, L, n_splits):
     # Host logic only.  Whatever the request, the split the library picks must be
@@ -166,8 +168,8 @@ def test_plan_splits_are_valid(B, H, M, L, n_splits):
     ws = 1 << 34
     kernel, splits = txl.relattn_plan(B, H, M, L, n_splits=n_splits, workspace_bytes=ws)
     assert splits >= 1
-    if kernel == "decode":
-        assert L <= 6
+    if kernel.startswith("decode"):
+        assert L <= 8 and (kernel == "decode") == (L == 1)
         assert splits <= max(1, (K + 127) // 128)
         assert (splits - 1) * _span(K, splits) < K
         if n_splits:
@@ -178,7 +180,7 @@ def test_plan_splits_are_valid(B, H, M, L, n_splits):
         assert splits <= n_key_tiles
         if n_splits:
             assert splits == min(n_splits, n_key_tiles)
-        assert L > 6 or n_splits == 0, "an explicit split of a short segment means the decode kernel"
+        assert L > 8, "every segment of up to eight queries takes the decode kernel"
     if splits > 8 or (kernel == "tc" and splits > 1):
         # partials in the workspace: without one the call must refuse
         k, n = ctypes.c_int(0), ctypes.c_int(0)
@@ -188,3 +190,66 @@ def test_plan_splits_are_valid(B, H, M, L, n_splits):
             assert rc == WORKSPACE
         else:
             assert rc == OK  # the automatic choice falls back to a split that fits
+
+
+def attn_strided(kv_stride, **kw):
+    a = dict(q=16, k=16, v=16, r=16, r_rows=8, u=16, vb=16, out=16, lse=None, B=1, H=1, M=4, L=4,
+             dh=64, scale=0.125, dtype=txl.BF16, n_splits=1, ws=None, ws_bytes=0)
+    a.update(kw)
+    return L().txl_relattn_fwd_strided(a["q"], a["k"], a["v"], kv_stride, a["r"], a["r_rows"],
+                                       a["u"], a["vb"], a["out"], a["lse"], a["B"], a["H"],
+                                       a["M"], a["L"], a["dh"], a["scale"], a["dtype"],
+                                       a["n_splits"], a["ws"], a["ws_bytes"], None)
+
+
+@pytest.mark.parametrize("kv_stride,kw,want", [
+    (0, {}, INVALID),                 # no plane stride given
+    (8 * 64 - 8, {}, SHAPE),          # planes closer than K rows
+    (8 * 64 + 4, {}, MISALIGNED),     # a plane would not start 16-byte aligned
+    (8 * 64, dict(q=None), INVALID),  # the dense call's own checks still apply
+    (8 * 64, dict(r_rows=7), SHAPE),
+    (8 * 64, dict(dh=32), UNSUPPORTED),
+    (4096, dict(n_splits=2, M=1000, L=16, r_rows=1016), SHAPE),
+    (1016 * 64, dict(n_splits=2, M=1000, L=16, r_rows=1016), WORKSPACE),
+])
+def test_relattn_strided_validation(kv_stride, kw, want):
+    assert attn_strided(kv_stride, **kw) == want
+
+
+def test_kv_window_state_follows_the_memory():
+    # Host arithmetic of the window (no kernel runs here): after each segment the
+    # window holds the newest min(total, M) rows, and the rows of [memory ;
+    # segment] it exposes stay inside the buffer.
+    M, L, C = 100, 32, 2 * 100 + 32
+    w = txl.KVWindow(0, 0, C, M)
+    total = 0
+    for _ in range(30):
+        # what txl_kv_window_append does to the state: compaction when the
+        # segment would not fit behind the memory
+        if w.start + w.fill + L > C:
+            w.start = 0
+        assert w.start + w.fill + L <= C
+        txl.kv_window_advance(w, L)
+        total += L
+        assert w.fill == min(total, M)
+        assert 0 <= w.start and w.start + w.fill <= C
+
+
+def test_kv_window_validation():
+    w = txl.KVWindow(0, 0, 100, 50)
+    # capacity below 2M + L
+    assert L().txl_kv_window_append(16, ctypes.byref(w), 16, 4, 8, 64, txl.BF16, None) == SHAPE
+    # a state whose window runs past the buffer, fill above M, negative start
+    for bad in (txl.KVWindow(190, 20, 200, 50), txl.KVWindow(0, 60, 200, 50),
+                txl.KVWindow(-1, 0, 200, 50)):
+        assert L().txl_kv_window_append(16, ctypes.byref(bad), 16, 4, 8, 64, txl.BF16,
+                                        None) == INVALID
+        assert L().txl_kv_window_advance(ctypes.byref(bad), 8) == INVALID
+    w = txl.KVWindow(0, 0, 200, 50)
+    assert L().txl_kv_window_append(16, ctypes.byref(w), 16, 4, 8, 6, txl.BF16, None) == MISALIGNED
+    assert L().txl_kv_window_append(16, ctypes.byref(w), 16, 4, 8, 64, 7, None) == INVALID
+    # L = 0 appends nothing; advancing past the buffer's end is refused
+    assert L().txl_kv_window_append(None, ctypes.byref(w), None, 4, 0, 64, txl.BF16, None) == OK
+    w = txl.KVWindow(150, 50, 200, 50)
+    assert L().txl_kv_window_advance(ctypes.byref(w), 8) == SHAPE
+    assert (w.start, w.fill) == (150, 50)

@@ -3,13 +3,15 @@
 Generation feeds one or a few new tokens per step and attends to a long cached
 memory ("Transformer-XL: Attentive Language Models Beyond a Fixed-Length
 Context", §3.2 recurrence with a longer memory at evaluation, §3.3 score,
-Appendix B reversed table).  txl_relattn_fwd takes such calls (bf16, L <= 6)
-through a split-K kernel on the CUDA cores: q + u and q + v in fp32, scores,
-softmax and P.V in fp32, so the output differs from the exact value only by
-its bf16 rounding (2^-9 relative) and fp32 sums.  Tolerances: max |err| <= 1e-2
-on O(1) outputs, rms(err)/rms(out) <= 4e-3, log-sum-exp <= 1e-3.  L = 7 and 8
-check the hand-over to the tensor-core kernel (whose P is bf16) under the same
-tolerances.
+Appendix B reversed table).  txl_relattn_fwd takes every such call (bf16,
+L <= 8) through a split-K decode kernel: for L >= 2 warp-level tensor-core
+MMAs with q + u, q + v and the probabilities each carried as a bf16 value plus
+its bf16 residual (about 2^-17 relative), fp32 accumulation and softmax; for
+L = 1 fp32 arithmetic on the CUDA cores.  Either way the output differs from
+the exact value by its bf16 rounding (2^-9 relative) and fp32 sums.
+Tolerances: max |err| <= 1e-2 on O(1) outputs, rms(err)/rms(out) <= 4e-3,
+log-sum-exp <= 1e-3.  L = 9 checks the hand-over to the 128-row tensor-core
+kernel under the same tolerances.
 """
 
 import math
@@ -37,9 +39,9 @@ def check(case, M, n_splits=0, workspace=True, what=""):
     return out
 
 
-# Query counts of the decode kernel (1..6) and past it, memories that end
-# inside, at and just past a 128-key block, and none.
-@pytest.mark.parametrize("L", [1, 2, 3, 4, 6, 7, 8])
+# Query counts of the two decode kernels (1; 2..8) and past them, memories that
+# end inside, at and just past a 128-key block, and none.
+@pytest.mark.parametrize("L", [1, 2, 3, 4, 5, 6, 7, 8, 9])
 @pytest.mark.parametrize("M", [0, 1, 127, 128, 300, 2000])
 def test_decode_matches_oracle(L, M):
     B, H = 2, 3
@@ -59,10 +61,11 @@ def test_decode_key_ranges(n_splits, workspace):
     check(case, M, n_splits=n_splits, workspace=workspace, what=f"splits {n_splits}")
 
 
-@pytest.mark.parametrize("L,n_splits", [(6, 1), (6, 5), (4, 0)])
-def test_decode_six_queries_key_ranges(L, n_splits):
-    # The largest decode segment, whose table window is 37 rows per 32-key
-    # chunk, over one and several key ranges.
+@pytest.mark.parametrize("L,n_splits", [(6, 1), (6, 5), (4, 0), (8, 1), (8, 3), (8, 11), (1, 11)])
+def test_decode_long_segments_key_ranges(L, n_splits):
+    # The largest decode segments (eight queries: a table window of 39 of the 40
+    # rows a chunk copies), over one key range, ranges merged in a cluster and
+    # through the workspace.
     B, H, M = 2, 3, 1100
     case = heads_case(B, H, L, M, seed=300 + 7 * L + n_splits)
     check(case, M, n_splits=n_splits, workspace=n_splits != 1, what=f"L={L} splits {n_splits}")
@@ -76,12 +79,14 @@ def test_decode_longer_table_and_sharp_scores():
     check(case, M, what="long table, sharp")
 
 
-def test_decode_full_memory_sampled():
-    # The long-memory evaluation shape (M = 3800) with one new token for a
-    # batch of 8 x 16 heads; every head is checked against the oracle.
-    B, H, L, M = 8, 16, 1, 3800
-    case = heads_case(B, H, L, M, seed=11)
-    check(case, M, what="M=3800 L=1")
+@pytest.mark.parametrize("L", [1, 4, 8])
+def test_decode_full_memory(L):
+    # The long-memory evaluation shape (M = 3800) with one, four and eight new
+    # tokens for a batch of 8 x 16 heads, in the launch the library picks;
+    # every head is checked against the oracle.
+    B, H, M = 8, 16, 3800
+    case = heads_case(B, H, L, M, seed=11 + L)
+    check(case, M, what=f"M=3800 L={L}")
 
 
 def test_decode_repeatable():
@@ -102,25 +107,26 @@ def test_evaluation_speed_shapes(L, M):
     scale = 1.0 / math.sqrt(64)
     out, lse = run_gpu(case, M, scale)
     want, want_lse = run_oracle(case, M, scale)
-    tol = TOL if L <= 6 else 2e-2  # the tensor-core path (L > 6) rounds P to bf16
+    tol = TOL if L <= 8 else 2e-2  # the 128-row tensor-core kernel (L > 8) rounds P to bf16
     compare(out.float().cpu().numpy(), want, tol, 1e-2, what=f"window L={L} M={M}")
     compare(lse.cpu().numpy(), want_lse, 2e-2, what=f"lse window L={L} M={M}")
 
 
-# Which kernel takes a short segment is the library's estimate (n_splits = 0):
-# one sequence of 16 heads against a long memory goes to the tensor cores from
-# four or five queries on; several sequences or short memories stay on the
-# decode kernel; an explicit split always means the decode kernel.  Both routes keep
-# the same tolerances.
-@pytest.mark.parametrize("B,L,M,want", [(1, 4, 8000, "tc"), (1, 5, 3800, "tc"), (1, 6, 3800, "tc"),
-                                        (8, 6, 3800, "decode"), (2, 6, 800, "decode"),
-                                        (8, 1, 3800, "decode"), (1, 6, 1600, "decode")])
+# Every segment of up to eight queries takes a decode kernel (one query the
+# CUDA-core one, more the warp-MMA one), one sequence or many, short memory or
+# long, with or without a workspace; nine queries take the 128-row tensor-core
+# kernel.  An explicit split counts decode key ranges.
+@pytest.mark.parametrize("B,L,M,want", [(1, 4, 8000, "decode_mma"), (1, 6, 3800, "decode_mma"),
+                                        (8, 6, 3800, "decode_mma"), (2, 8, 800, "decode_mma"),
+                                        (8, 1, 3800, "decode"), (1, 9, 1600, "tc")])
 def test_short_segment_routing(B, L, M, want):
     H = 16
     ws_bytes = max(txl.workspace_size(B, H, L, 64, 64), 256)
     kernel, splits = txl.relattn_plan(B, H, M, L, workspace_bytes=ws_bytes)
     assert kernel == want, (B, L, M, kernel, splits)
-    assert txl.relattn_plan(B, H, M, L, n_splits=2, workspace_bytes=ws_bytes) == ("decode", 2)
+    if want != "tc":
+        assert txl.relattn_plan(B, H, M, L, n_splits=2, workspace_bytes=ws_bytes) == (want, 2)
+        assert txl.relattn_plan(B, H, M, L, workspace_bytes=0)[0] == want
     case = heads_case(B, H, L, M, seed=4000 + 31 * L + M)
     d = dev()
     t = {k: v.to(d).contiguous() for k, v in case.items()}
@@ -140,7 +146,8 @@ def test_short_segment_routing(B, L, M, want):
 
 
 @pytest.mark.parametrize("B,H,M,L", [(1, 16, 3800, 1), (8, 16, 3800, 2), (2, 3, 300, 3), (64, 16, 3800, 6),
-                                     (1, 16, 8000, 4), (16, 16, 1600, 128), (8, 16, 3800, 128)])
+                                     (1, 16, 8000, 4), (4, 16, 12000, 8), (16, 16, 1600, 128),
+                                     (8, 16, 3800, 128)])
 @pytest.mark.parametrize("n_splits", [0, 3, 9])
 def test_plan_on_device_is_realisable(B, H, M, L, n_splits):
     # The split chosen with this device's occupancy (not the host fallback):
@@ -149,7 +156,7 @@ def test_plan_on_device_is_realisable(B, H, M, L, n_splits):
     K = M + L
     kernel, splits = txl.relattn_plan(B, H, M, L, n_splits=n_splits, workspace_bytes=1 << 34)
     assert splits >= 1
-    if kernel == "decode":
+    if kernel.startswith("decode"):
         span = ((K + splits - 1) // splits + 31) // 32 * 32
         assert splits <= max(1, (K + 127) // 128) and (splits - 1) * span < K
     else:

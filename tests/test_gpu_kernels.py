@@ -73,6 +73,7 @@ def test_memory_ring_matches_oracle(M, L, n_seg, dtype):
         assert st.head == ((s + 1) * L) % M if M else st.head == 0
     empty = torch.empty(B, 0, d, dtype=dtype, device=dev())
     np.testing.assert_array_equal(txl.mem_concat(mem, st, empty).double().cpu().numpy(), ref)
+    assert txl.device_status() == 0
 
 
 # ---------------------------------------------------------------------------

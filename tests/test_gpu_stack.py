@@ -153,39 +153,42 @@ def test_c5_stack12_last_segment(c5_last_segment):
     compare(c["h_gpu"], h_or, 1e-1, 2e-2, what="c5 top layer")
 
 
-def test_cached_kv_rings_match_projected_memory():
-    # After the memories have filled and wrapped, each layer's key and value
-    # rings hold the projections of that layer's hidden-state memory.
-    from transformer_xl_relative_pos_gb300 import _lib as txl
+def test_cached_kv_windows_match_projected_memory():
+    # After the memories have filled and the windows have moved back to their
+    # buffers' front at least once, each layer's key and value windows hold the
+    # projections of that layer's hidden-state memory.
     from transformer_xl_relative_pos_gb300.model import project_heads
     base = txl_inputs.WORKLOADS["c5_stack12_L512_M512"]
     w = txl_inputs.Workload("ring_stack", B=2, H=2, dh=64, L=48, M=100, d_model=128,
-                            dtype="bf16", seed=43, d_ff=256, n_layer=3, n_seg=4, vocab=base.vocab)
+                            dtype="bf16", seed=43, d_ff=256, n_layer=3, n_seg=9, vocab=base.vocab)
     params = txl_inputs.draw_stack(w)
     stack = XLStack(params, w.H, w.M, dev(), torch.bfloat16, cache_kv=True)
+    starts = set()
     for s in range(w.n_seg):
         stack.segment(params["tokens"][s])
+        starts.add(stack.kv_windows[0][0].start)
+    assert 0 in starts and len(starts) > 2
     for n, (mem, lay) in enumerate(zip(stack.memories(), stack.layers)):
-        ks, vs = stack.kv_states[n]
-        empty = torch.empty(w.B * w.H, 0, w.dh, dtype=torch.bfloat16, device=dev())
-        k_ring = txl.mem_concat(stack.kmems[n], ks, empty).view(w.B, w.H, -1, w.dh)
-        v_ring = txl.mem_concat(stack.vmems[n], vs, empty).view(w.B, w.H, -1, w.dh)
+        kw, vw = stack.kv_windows[n]
+        assert kw.fill == vw.fill == w.M
+        k_win = stack.kbufs[n][:, kw.start:kw.start + kw.fill].reshape(w.B, w.H, -1, w.dh)
+        v_win = stack.vbufs[n][:, vw.start:vw.start + vw.fill].reshape(w.B, w.H, -1, w.dh)
         k_mem = project_heads(mem, lay["W_kE"], w.H)
         v_mem = project_heads(mem, lay["W_v"], w.H)
         # the same bf16 products, possibly summed in another order by the GEMM
-        compare(k_ring.float().cpu().numpy(), k_mem.float().cpu().numpy(), 5e-3, what=f"k ring {n}")
-        compare(v_ring.float().cpu().numpy(), v_mem.float().cpu().numpy(), 5e-3, what=f"v ring {n}")
+        compare(k_win.float().cpu().numpy(), k_mem.float().cpu().numpy(), 5e-3, what=f"k window {n}")
+        compare(v_win.float().cpu().numpy(), v_mem.float().cpu().numpy(), 5e-3, what=f"v window {n}")
 
 
 @pytest.mark.parametrize("L,M,cache_kv", [(64, 64, False), (64, 128, True), (48, 80, False)])
 def test_graph_replayed_stack_matches_eager(L, M, cache_kv):
     # Once the memories are full the stack replays each segment from a CUDA
-    # graph per ring position (one when L is a multiple of M, M / gcd(M, L)
-    # otherwise); every segment's output and the final memories must equal the
-    # eager stack's bit for bit (same kernels, same order, same operands).
+    # graph per position of its rings (and windows); every segment's output and
+    # the final memories must equal the eager stack's bit for bit (same
+    # kernels, same order, same operands).
     base = txl_inputs.WORKLOADS["c5_stack12_L512_M512"]
     w = txl_inputs.Workload("graph_stack", B=2, H=2, dh=64, L=L, M=M, d_model=128,
-                            dtype="bf16", seed=43, d_ff=256, n_layer=2, n_seg=9, vocab=base.vocab)
+                            dtype="bf16", seed=43, d_ff=256, n_layer=2, n_seg=10, vocab=base.vocab)
     params = txl_inputs.draw_stack(w)
     eager = XLStack(params, w.H, w.M, dev(), torch.bfloat16, cache_kv=cache_kv)
     graphed = XLStack(params, w.H, w.M, dev(), torch.bfloat16, cache_kv=cache_kv, graphs=True)
@@ -194,8 +197,46 @@ def test_graph_replayed_stack_matches_eager(L, M, cache_kv):
         got = graphed.segment(params["tokens"][s]).clone()
         torch.cuda.synchronize()
         assert torch.equal(got, want), f"segment {s}"
-    assert len(graphed._graphs) == M // math.gcd(M, L)
+    # one graph per combination of ring heads and window starts: the ring heads
+    # repeat every M / gcd(M, L) segments, the windows' starts (0, L, ..., C - M - L)
+    # every (C - M - L) / L + 1, a multiple of that
+    expected = M // math.gcd(M, L)
+    if cache_kv:
+        C = graphed.kv_windows[0][0].capacity
+        expected = (C - M - L) // L + 1
+        assert expected % (M // math.gcd(M, L)) == 0
+    assert len(graphed._graphs) == expected
     for a, b in zip(eager.memories(), graphed.memories()):
         assert torch.equal(a, b)
-    for sa, sb in zip(eager._rings(), graphed._rings()):
-        assert (sa.head, sa.fill) == (sb.head, sb.fill)
+    for sa, sb in zip(eager._host_states(), graphed._host_states()):
+        assert XLStack._snap(sa) == XLStack._snap(sb)
+
+
+@pytest.mark.parametrize("cache_kv,graphs", [(False, False), (True, False), (True, True)])
+def test_checkpoint_resume_is_exact(cache_kv, graphs):
+    # 16 segments straight against 8, a checkpoint to host memory, a fresh stack
+    # restored from it, and 8 more: every output and the final memories equal the
+    # straight run's bit for bit (§3.2: the memory is all the stream carries).
+    base = txl_inputs.WORKLOADS["c5_stack12_L512_M512"]
+    w = txl_inputs.Workload("ckpt_stack", B=2, H=2, dh=64, L=48, M=100, d_model=128,
+                            dtype="bf16", seed=47, d_ff=256, n_layer=3, n_seg=16, vocab=base.vocab)
+    params = txl_inputs.draw_stack(w)
+    tokens = params["tokens"]
+    straight = XLStack(params, w.H, w.M, dev(), torch.bfloat16, cache_kv=cache_kv, graphs=graphs)
+    want = [straight.segment(tokens[s]).clone() for s in range(16)]
+    first = XLStack(params, w.H, w.M, dev(), torch.bfloat16, cache_kv=cache_kv, graphs=graphs)
+    for s in range(8):
+        assert torch.equal(first.segment(tokens[s]), want[s])
+    ck = first.checkpoint()
+    assert all(not t.is_cuda for t in ck["mems"])
+    del first
+    second = XLStack(params, w.H, w.M, dev(), torch.bfloat16, cache_kv=cache_kv, graphs=graphs)
+    second.restore(ck)
+    for s in range(8, 16):
+        got = second.segment(tokens[s]).clone()
+        torch.cuda.synchronize()
+        assert torch.equal(got, want[s]), f"segment {s}"
+    for a, b in zip(straight.memories(), second.memories()):
+        assert torch.equal(a, b)
+    for sa, sb in zip(straight._host_states(), second._host_states()):
+        assert XLStack._snap(sa) == XLStack._snap(sb)

@@ -32,9 +32,10 @@ def _operands(case):
 
 
 # (B, H, L, M, n_splits, kernel): a tensor-core split, the automatic choice, and
-# a decode call with more key ranges than one thread-block cluster merges, so
-# that its partials go through the scratch and the merge kernel.
-CASES = [(2, 3, 130, 900, 3, "tc"), (2, 3, 130, 900, 0, "tc"), (2, 3, 3, 2000, 12, "decode")]
+# decode calls (both kernels) with more key ranges than one thread-block cluster
+# merges, so that their partials go through the scratch and the merge kernel.
+CASES = [(2, 3, 130, 900, 3, "tc"), (2, 3, 130, 900, 0, "tc"), (2, 3, 3, 2000, 12, "decode_mma"),
+         (2, 3, 1, 2000, 12, "decode")]
 
 
 @pytest.mark.parametrize("B,H,L,M,n_splits,kernel", CASES)

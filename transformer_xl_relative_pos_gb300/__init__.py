@@ -15,6 +15,8 @@ N-layer summary, Appendix B reversed table and shift):
   relattn_plan    which kernel and key split relattn_fwd would use
   mem_concat      extended context [SG(m) o h] from the ring-buffer memory
   mem_update      advance the memory to the newest M states
+  kv_window_*     a memory kept as a window of a larger buffer, read in place
+                  by relattn_fwd (k, v as strided views)
 """
 
 from __future__ import annotations
@@ -22,10 +24,16 @@ from __future__ import annotations
 from ._lib import (  # noqa: F401
     F32,
     BF16,
+    KVWindow,
     MemState,
     TxlError,
+    debug_checks,
+    debug_index_probe,
     debug_wait_timeout,
     device_status,
+    kv_window_advance,
+    kv_window_append,
+    kv_window_view,
     lib,
     lib_path,
     mem_concat,

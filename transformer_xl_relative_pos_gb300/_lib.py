@@ -28,6 +28,18 @@ class TxlError(RuntimeError):
         self.status = status
 
 
+class KVWindow(ctypes.Structure):
+    """txl_kv_window: host-side state of a memory kept as a contiguous window of
+    a larger buffer [planes, capacity, d] (capacity >= 2 M + L)."""
+
+    _fields_ = [("start", ctypes.c_int), ("fill", ctypes.c_int), ("capacity", ctypes.c_int),
+                ("M", ctypes.c_int)]
+
+    def __repr__(self):
+        return (f"KVWindow(start={self.start}, fill={self.fill}, capacity={self.capacity}, "
+                f"M={self.M})")
+
+
 class MemState(ctypes.Structure):
     """txl_mem_state: host-side ring-buffer state of one layer's memory."""
 
@@ -37,19 +49,28 @@ class MemState(ctypes.Structure):
         return f"MemState(head={self.head}, fill={self.fill}, capacity={self.capacity})"
 
 
+def _debug() -> bool:
+    return os.environ.get("TXL_DEBUG_LIB") == "1"
+
+
 def lib_path() -> str:
-    return _build.LIB_PATH
+    return _build.DEBUG_LIB_PATH if _debug() else _build.LIB_PATH
 
 
 def lib():
-    """Load ``libtxl_gb300.so``; build it first when the sources are newer.
+    """Load ``libtxl_gb300.so`` (with TXL_DEBUG_LIB=1 in the environment: the
+    debug build ``libtxl_gb300_debug.so``); build it first when the sources are
+    newer.
 
     Raises if it cannot be built or loaded: nothing falls back to another
     implementation."""
     global _lib
     with _lock:
         if _lib is None:
-            path = _build.build() if os.environ.get("TXL_NO_BUILD") != "1" else _build.LIB_PATH
+            if os.environ.get("TXL_NO_BUILD") == "1":
+                path = lib_path()
+            else:
+                path = _build.build(debug=_debug())
             if not os.path.exists(path):
                 raise TxlError(-5, f"CUDA library missing: {path}")
             L = ctypes.CDLL(path)
@@ -64,6 +85,13 @@ def lib():
                 "txl_relattn_fwd": (_c_int, [_c_p, _c_p, _c_p, _c_p, _c_int, _c_p, _c_p, _c_p, _c_p,
                                              _c_int, _c_int, _c_int, _c_int, _c_int, _c_float,
                                              _c_int, _c_int, _c_p, _c_size, _c_p]),
+                "txl_relattn_fwd_strided": (_c_int, [_c_p, _c_p, _c_p, ctypes.c_longlong, _c_p,
+                                                     _c_int, _c_p, _c_p, _c_p, _c_p, _c_int, _c_int,
+                                                     _c_int, _c_int, _c_int, _c_float, _c_int,
+                                                     _c_int, _c_p, _c_size, _c_p]),
+                "txl_kv_window_append": (_c_int, [_c_p, ctypes.POINTER(KVWindow), _c_p, _c_int,
+                                                  _c_int, _c_int, _c_int, _c_p]),
+                "txl_kv_window_advance": (_c_int, [ctypes.POINTER(KVWindow), _c_int]),
                 "txl_relattn_fwd_noalloc": (_c_int, [_c_p, _c_p, _c_p, _c_p, _c_int, _c_p, _c_p,
                                                      _c_p, _c_p, _c_int, _c_int, _c_int, _c_int,
                                                      _c_int, _c_float, _c_int, _c_int, _c_p]),
@@ -74,6 +102,8 @@ def lib():
                 "txl_device_status": (_c_int, [_c_p]),
                 "txl_set_wait_limit_ns": (_c_u64, [_c_u64]),
                 "txl_debug_wait_timeout": (_c_int, [_c_u64, _c_p]),
+                "txl_debug_checks": (_c_int, []),
+                "txl_debug_index_probe": (_c_int, [_c_p]),
             }
             for name, (res, args) in sig.items():
                 fn = getattr(L, name)
@@ -137,13 +167,14 @@ def workspace_size(B: int, H: int, L: int, dh: int, n_splits: int) -> int:
     return int(lib().txl_relattn_workspace_size(int(B), int(H), int(L), int(dh), int(n_splits)))
 
 
-KERNELS = {1: "tc", 2: "decode", 3: "f32"}
+KERNELS = {1: "tc", 2: "decode", 3: "f32", 4: "decode_mma"}
 
 
 def relattn_plan(B: int, H: int, M: int, L: int, dtype=torch.bfloat16, *, r_rows: int | None = None,
                  dh: int = 64, n_splits: int = 0, workspace_bytes: int = 0):
     """(kernel, splits) that relattn_fwd would use for these sizes: kernel is
-    "tc", "decode" or "f32".  Raises TxlError for sizes the call would reject."""
+    "tc", "decode" (one query, CUDA cores), "decode_mma" (2 to 8 queries,
+    warp MMAs) or "f32".  Raises TxlError for sizes the call would reject."""
     kernel, splits = _c_int(0), _c_int(0)
     _check(lib().txl_relattn_plan(int(B), int(H), int(M), int(L),
                                   int(r_rows if r_rows is not None else M + L), int(dh),
@@ -152,15 +183,36 @@ def relattn_plan(B: int, H: int, M: int, L: int, dtype=torch.bfloat16, *, r_rows
     return KERNELS[kernel.value], splits.value
 
 
+def _kv_plane_stride(k, v):
+    """0 for dense k, v; else the element stride between (b, h) planes when k and
+    v are windows [B, H, K, dh] of larger buffers (rows contiguous within a plane,
+    planes equally spaced)."""
+    if k.is_contiguous() and v.is_contiguous():
+        return 0
+    B, H, K, dh = k.shape
+    for t, name in ((k, "k"), (v, "v")):
+        if not t.is_cuda:
+            raise ValueError(f"{name} must be a CUDA tensor (the library takes device pointers)")
+        st = t.stride()
+        if st[3] != 1 or st[2] != dh or st[0] != H * st[1]:
+            raise ValueError(f"{name}: rows of a plane must be contiguous and planes equally "
+                             f"spaced (strides {st})")
+    if k.stride() != v.stride():
+        raise ValueError("k and v must have the same strides")
+    return int(k.stride(1))
+
+
 def relattn_fwd(q, k, v, r, u, v_bias, M: int, scale: float, *, out=None, lse=None,
                 n_splits: int = 0, workspace=None, stream=None):
     """Relative-position attention of one layer.
 
     q [B,H,L,dh]; k, v [B,H,M+L,dh] (memory rows first); r [H,r_rows,dh] in the
     reversed order (row rho = W_kR R_{r_rows-1-rho}); u, v_bias [H,dh].  All
-    bf16 (tensor-core path) or all fp32 (CUDA-core path).  ``lse``: True to
-    return log-sum-exp [B,H,L] (fp32), or a tensor to fill.  Returns ``out``
-    or ``(out, lse)``."""
+    bf16 (tensor-core path) or all fp32 (CUDA-core path).  k and v may be
+    windows of larger buffers (e.g. ``kv_window_view``): rows contiguous, the
+    (b, h) planes equally spaced; they then go through txl_relattn_fwd_strided.
+    ``lse``: True to return log-sum-exp [B,H,L] (fp32), or a tensor to fill.
+    Returns ``out`` or ``(out, lse)``."""
     B, H, L, dh = q.shape
     dt = q.dtype
     code = _code(dt)
@@ -173,12 +225,23 @@ def relattn_fwd(q, k, v, r, u, v_bias, M: int, scale: float, *, out=None, lse=No
     ws_ptr, ws_bytes = None, 0
     if workspace is not None:
         ws_ptr, ws_bytes = _dev(workspace, "workspace"), workspace.numel() * workspace.element_size()
-    rc = lib().txl_relattn_fwd(
-        _dev(q, "q", dt), _dev(k, "k", dt), _dev(v, "v", dt), _dev(r, "r", dt), int(r.shape[1]),
-        _dev(u, "u", dt), _dev(v_bias, "v_bias", dt), _dev(out, "out", dt), lse_ptr,
-        int(B), int(H), int(M), int(L), int(dh), float(scale), code, int(n_splits),
-        ws_ptr, int(ws_bytes), _stream(q, stream))
-    _check(rc, "txl_relattn_fwd")
+    kv_stride = _kv_plane_stride(k, v)
+    if kv_stride == 0:
+        rc = lib().txl_relattn_fwd(
+            _dev(q, "q", dt), _dev(k, "k", dt), _dev(v, "v", dt), _dev(r, "r", dt),
+            int(r.shape[1]), _dev(u, "u", dt), _dev(v_bias, "v_bias", dt), _dev(out, "out", dt),
+            lse_ptr, int(B), int(H), int(M), int(L), int(dh), float(scale), code, int(n_splits),
+            ws_ptr, int(ws_bytes), _stream(q, stream))
+        _check(rc, "txl_relattn_fwd")
+    else:
+        if k.dtype != dt or v.dtype != dt:
+            raise ValueError(f"k and v must be {dt}")
+        rc = lib().txl_relattn_fwd_strided(
+            _dev(q, "q", dt), k.data_ptr(), v.data_ptr(), kv_stride, _dev(r, "r", dt),
+            int(r.shape[1]), _dev(u, "u", dt), _dev(v_bias, "v_bias", dt), _dev(out, "out", dt),
+            lse_ptr, int(B), int(H), int(M), int(L), int(dh), float(scale), code, int(n_splits),
+            ws_ptr, int(ws_bytes), _stream(q, stream))
+        _check(rc, "txl_relattn_fwd_strided")
     return (out, lse) if want_lse else out
 
 
@@ -233,6 +296,33 @@ def mem_update(mem, state: MemState, h_new, stream=None):
     return state
 
 
+def kv_window_append(buf, state: KVWindow, seg, stream=None):
+    """Append seg [planes, L, d] behind the memory rows of the window kept in buf
+    [planes, capacity, d] (moving the memory to the buffer's front first when the
+    rows would not fit); updates ``state.start`` in place."""
+    P, L, d = seg.shape
+    if buf.shape[0] != P or buf.shape[2] != d or buf.shape[1] != state.capacity:
+        raise ValueError("buf must be [planes, capacity, d] matching seg and the state")
+    _check(lib().txl_kv_window_append(_dev(buf, "buf", seg.dtype), ctypes.byref(state),
+                                      _dev(seg, "seg") if seg.numel() else None, int(P), int(L),
+                                      int(d), _code(seg.dtype), _stream(seg, stream)),
+           "txl_kv_window_append")
+    return state
+
+
+def kv_window_advance(state: KVWindow, L: int):
+    """After attending to the appended segment of L rows: keep the newest M rows."""
+    _check(lib().txl_kv_window_advance(ctypes.byref(state), int(L)), "txl_kv_window_advance")
+    return state
+
+
+def kv_window_view(buf, state: KVWindow, L: int, B: int, H: int):
+    """The window [memory ; segment] of buf [B*H, capacity, d] as a [B, H, fill+L, d]
+    view (no copy), for relattn_fwd."""
+    d = buf.shape[2]
+    return buf.view(B, H, state.capacity, d)[:, :, state.start:state.start + state.fill + L]
+
+
 def device_status(stream=None) -> int:
     """Synchronise and return (and clear) the kernels' device status word."""
     return int(lib().txl_device_status(_stream(None, stream)))
@@ -244,3 +334,14 @@ def set_wait_limit_ns(ns: int) -> int:
 
 def debug_wait_timeout(ns: int, stream=None) -> int:
     return int(lib().txl_debug_wait_timeout(int(ns), _stream(None, stream)))
+
+
+def debug_checks() -> bool:
+    """True when the loaded library is the debug build (device-side index checks)."""
+    return bool(lib().txl_debug_checks())
+
+
+def debug_index_probe(stream=None) -> int:
+    """Fail one device-side index check on purpose; returns the status then read
+    (TXL_ERR_INDEX = -8 in the debug build, 0 in a release build)."""
+    return int(lib().txl_debug_index_probe(_stream(None, stream)))

@@ -3,6 +3,8 @@
 Each translation unit compiles in parallel to an object file under
 ``_build/``; the objects link into a shared library next to this file.  A
 rebuild happens only when a source or header is newer than the library.
+``build(debug=True)`` builds ``libtxl_gb300_debug.so`` (objects under
+``_build_debug/``) with -DTXL_DEBUG: the kernels' device-side index checks.
 """
 
 from __future__ import annotations
@@ -18,11 +20,14 @@ CSRC = os.path.join(PKG, "csrc")
 INCLUDE = os.path.join(ROOT, "include")
 BUILD_DIR = os.path.join(PKG, "_build")
 LIB_PATH = os.path.join(PKG, "libtxl_gb300.so")
+DEBUG_BUILD_DIR = os.path.join(PKG, "_build_debug")
+DEBUG_LIB_PATH = os.path.join(PKG, "libtxl_gb300_debug.so")
 
 SOURCES = ["txl_api.cu", "relattn_tc.cu", "relattn_combine.cu", "relattn_decode.cu",
-           "relattn_f32.cu", "relpos.cu", "mem.cu", "relattn_noalloc.cu"]
+           "relattn_decode_mma.cu", "relattn_f32.cu", "relpos.cu", "mem.cu", "relattn_noalloc.cu"]
 HEADERS = [os.path.join(CSRC, "kernels.h"), os.path.join(CSRC, "decode.h"),
-           os.path.join(CSRC, "ptx.cuh"), os.path.join(INCLUDE, "txl.h")]
+           os.path.join(CSRC, "decode_common.cuh"), os.path.join(CSRC, "ptx.cuh"),
+           os.path.join(INCLUDE, "txl.h")]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 
@@ -37,25 +42,28 @@ def _cuda_lib_dir(nvcc: str) -> str:
     return os.path.join(os.path.dirname(os.path.dirname(os.path.realpath(nvcc))), "lib64")
 
 
-def _stale() -> bool:
-    if not os.path.exists(LIB_PATH):
+def _stale(lib_path: str) -> bool:
+    if not os.path.exists(lib_path):
         return True
-    t = os.path.getmtime(LIB_PATH)
+    t = os.path.getmtime(lib_path)
     deps = [os.path.join(CSRC, s) for s in SOURCES] + HEADERS + [os.path.abspath(__file__)]
     return any(os.path.getmtime(p) > t for p in deps)
 
 
-def build(force: bool = False, verbose: bool = False) -> str:
-    """Compile (if needed) and return the path of ``libtxl_gb300.so``."""
-    if not force and not _stale():
-        return LIB_PATH
+def build(force: bool = False, verbose: bool = False, debug: bool = False) -> str:
+    """Compile (if needed) and return the path of ``libtxl_gb300.so`` (with
+    ``debug``: ``libtxl_gb300_debug.so``, built with -DTXL_DEBUG)."""
+    lib_path = DEBUG_LIB_PATH if debug else LIB_PATH
+    build_dir = DEBUG_BUILD_DIR if debug else BUILD_DIR
+    if not force and not _stale(lib_path):
+        return lib_path
     nvcc = _nvcc()
-    os.makedirs(BUILD_DIR, exist_ok=True)
+    os.makedirs(build_dir, exist_ok=True)
     common = ARCH + ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC",
-                     "-I", INCLUDE, "-I", CSRC]
+                     "-I", INCLUDE, "-I", CSRC] + (["-DTXL_DEBUG"] if debug else [])
 
     def compile_one(src: str) -> str:
-        obj = os.path.join(BUILD_DIR, src.replace(".cu", ".o"))
+        obj = os.path.join(build_dir, src.replace(".cu", ".o"))
         cmd = [nvcc] + common + ["-c", os.path.join(CSRC, src), "-o", obj]
         if verbose:
             print(" ".join(cmd), flush=True)
@@ -66,7 +74,7 @@ def build(force: bool = False, verbose: bool = False) -> str:
 
     with concurrent.futures.ThreadPoolExecutor(max_workers=len(SOURCES)) as ex:
         objs = list(ex.map(compile_one, SOURCES))
-    tmp = LIB_PATH + f".tmp{os.getpid()}"
+    tmp = lib_path + f".tmp{os.getpid()}"
     libdir = _cuda_lib_dir(nvcc)
     cmd = [nvcc] + ARCH + ["-shared", "-o", tmp] + objs + [
         "-cudart", "shared", "-L", libdir, "-Xlinker", f"-rpath,{libdir}"]
@@ -75,8 +83,8 @@ def build(force: bool = False, verbose: bool = False) -> str:
     r = subprocess.run(cmd, capture_output=True, text=True)
     if r.returncode != 0:
         raise RuntimeError(f"link failed:\n{r.stdout}\n{r.stderr}")
-    os.replace(tmp, LIB_PATH)
-    return LIB_PATH
+    os.replace(tmp, lib_path)
+    return lib_path
 
 
 if __name__ == "__main__":

@@ -6,20 +6,29 @@
 
 namespace txl {
 
-// Short-segment (decode) kernel: L <= kDecodeMaxL queries per (batch, head);
-// the keys are split into n_splits ranges of whole 32-key chunks.
-constexpr int kDecodeMaxL = 6;
+// Short-segment (decode) kernels: L <= kDecodeMaxL queries per (batch, head);
+// the keys are split into n_splits ranges of whole 32-key chunks.  The
+// tensor-core kernel takes every L up to kDecodeMaxL, the CUDA-core kernel up
+// to kDecodeFmaMaxL.
+constexpr int kDecodeMaxL = 8;
+constexpr int kDecodeFmaMaxL = 6;
 constexpr int kDecodeMaxCluster = 8;  // portable cluster size
+// Tensor maps of the tensor-core kernel: k and v [B*H planes][K][64] read in
+// boxes of 32 rows, the table [H][r_rows][64] in boxes of 40 rows (the 32 + L - 1
+// rows one chunk needs); bf16, 128-byte swizzle.
+constexpr int kDecodeMmaKeyBox = 32;
+constexpr int kDecodeMmaTableBox = 40;
 
 struct DecodeParams {
     int B, H, M, L, K;
     int r_rows;         // table rows per head (>= K)
     int r_off;          // r_rows - K
     int n_splits;       // key ranges per (batch, head); > 1 writes partials
+    long long kv_stride;  // elements between consecutive (b, h) planes of k and v
     float scale_log2;   // scale * log2(e)
     const __nv_bfloat16 *q;   // [B][H][L][64]
-    const __nv_bfloat16 *k;   // [B][H][K][64]
-    const __nv_bfloat16 *v;   // [B][H][K][64]
+    const __nv_bfloat16 *k;   // [B*H planes, kv_stride apart][K][64]
+    const __nv_bfloat16 *v;   // [B*H planes, kv_stride apart][K][64]
     const __nv_bfloat16 *r;   // [H][r_rows][64]
     const __nv_bfloat16 *u;   // [H][64]
     const __nv_bfloat16 *vb;  // [H][64]
@@ -40,8 +49,13 @@ __host__ __device__ inline int decode_span(int K, int n_splits)
     return ((K + n_splits - 1) / n_splits + 31) / 32 * 32;
 }
 int decode_chunk_keys();                // 32
-int decode_blocks_per_sm(int L);        // resident decode blocks per SM for L queries
-
+// CUDA-core kernel (L <= kDecodeFmaMaxL): resident blocks per SM, launch.
+int decode_blocks_per_sm(int L);
 cudaError_t launch_relattn_decode(const DecodeParams &p, cudaStream_t s);
+// Tensor-core kernel (L <= kDecodeMaxL): resident blocks per SM, launch.
+int decode_mma_blocks_per_sm(int L);
+cudaError_t launch_relattn_decode_mma(const CUtensorMap &tm_k, const CUtensorMap &tm_v,
+                                      const CUtensorMap &tm_r, const DecodeParams &p,
+                                      cudaStream_t s);
 
 } // namespace txl

@@ -8,6 +8,24 @@
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 
+// Bits of the device status word (read and cleared by txl_device_status).
+#define TXL_STATUS_TIMEOUT 1u  // a bounded barrier wait gave up
+#define TXL_STATUS_INDEX 2u    // a device-side index check failed (TXL_DEBUG builds)
+
+// Device-side index checks of the debug build (compiled with -DTXL_DEBUG): a
+// failed check records TXL_STATUS_INDEX in the status word and the kernel goes
+// on (no trap); release builds compile the checks away.
+#ifdef TXL_DEBUG
+#define TXL_CHECK(cond, status)                                                   \
+    do {                                                                          \
+        if (!(cond)) atomicOr((status), TXL_STATUS_INDEX);                        \
+    } while (0)
+#else
+#define TXL_CHECK(cond, status) \
+    do {                        \
+    } while (0)
+#endif
+
 namespace txl {
 
 // Tile shape of the tensor-core attention kernel.
@@ -46,6 +64,7 @@ struct F32Params {
     const float *q, *k, *v, *r, *u, *vb;
     float *out, *lse;
     int B, H, M, L, K, r_rows;
+    long long kv_stride;  // elements between consecutive (b, h) planes of k and v
     float scale;
 };
 
@@ -53,12 +72,23 @@ cudaError_t launch_relattn_f32(const F32Params &p, cudaStream_t s);
 
 cudaError_t launch_rel_pos_emb(void *R, int K, int d_model, bool bf16, cudaStream_t s);
 
+// Rows [src_row0, src_row0 + rows) of every plane of src into rows
+// [dst_row0, ...) of the same plane of dst (planes rows apart by the strides,
+// in 16-byte units); row_vec = row bytes / 16.  The row ranges of one plane must
+// not overlap.
+cudaError_t launch_rows_copy(uint4 *dst, long long dst_plane_vec, int dst_row0, const uint4 *src,
+                             long long src_plane_vec, int src_row0, int planes, int rows,
+                             int row_vec, unsigned int *status, cudaStream_t s);
+
 // Row copies for the segment memory; row_vec = row bytes / 16.
 cudaError_t launch_mem_concat(uint4 *ext, const uint4 *mem, const uint4 *h_new, int B,
-                              int fill, int head, int cap, int L, int row_vec, cudaStream_t s);
+                              int fill, int head, int cap, int L, int row_vec,
+                              unsigned int *status, cudaStream_t s);
 cudaError_t launch_mem_write(uint4 *mem, const uint4 *h_new, int B, int L, int first_row,
-                             int head, int cap, int row_vec, cudaStream_t s);
+                             int head, int cap, int row_vec, unsigned int *status, cudaStream_t s);
 
 cudaError_t launch_wait_probe(unsigned int *status, unsigned long long wait_ns, cudaStream_t s);
+// One thread fails one index check (a no-op in release builds).
+cudaError_t launch_index_probe(unsigned int *status, cudaStream_t s);
 
 } // namespace txl

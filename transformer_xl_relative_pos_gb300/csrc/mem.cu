@@ -30,7 +30,8 @@ __global__ void __launch_bounds__(kThreads) mem_concat_kernel(uint4 *__restrict_
                                                               const uint4 *__restrict__ mem,
                                                               const uint4 *__restrict__ h_new,
                                                               int fill, int head, int cap, int L,
-                                                              int row_vec, int shift)
+                                                              int row_vec, int shift,
+                                                              unsigned int *status)
 {
     const int rows = fill + L;
     const int total = rows * row_vec;  // vectors of this batch row
@@ -44,9 +45,11 @@ __global__ void __launch_bounds__(kThreads) mem_concat_kernel(uint4 *__restrict_
         const int t = row_of(i, row_vec, shift);
         const int c = i - t * row_vec;
         const uint4 *src;
+        TXL_CHECK(t >= 0 && t < rows && c >= 0 && c < row_vec, status);
         if (t < fill) {
             int slot = head - fill + t;
             slot += (slot < 0) ? cap : 0;
+            TXL_CHECK(slot >= 0 && slot < cap, status);
             src = mem + (b * cap + slot) * row_vec + c;
         } else {
             src = h_new + (b * L + (t - fill)) * row_vec + c;
@@ -64,7 +67,8 @@ __global__ void __launch_bounds__(kThreads) mem_concat_kernel(uint4 *__restrict_
 __global__ void __launch_bounds__(kThreads) mem_write_kernel(uint4 *__restrict__ mem,
                                                              const uint4 *__restrict__ h_new,
                                                              int L, int first_row, int head,
-                                                             int cap, int row_vec, int shift)
+                                                             int cap, int row_vec, int shift,
+                                                             unsigned int *status)
 {
     const int total = (L - first_row) * row_vec;  // vectors of this batch row
     const long long b = blockIdx.y;
@@ -79,12 +83,50 @@ __global__ void __launch_bounds__(kThreads) mem_write_kernel(uint4 *__restrict__
         const int r = row_of(i, row_vec, shift);
         const int c = i - r * row_vec;
         const int l = first_row + r;
+        TXL_CHECK(l >= 0 && l < L && (head + l) % cap < cap, status);
         v[k] = __ldcs(h_new + (b * L + l) * row_vec + c);
         dst[k] = (b * cap + (head + l) % cap) * row_vec + c;
     }
 #pragma unroll
     for (int k = 0; k < kVecPerThread; ++k)
         if (dst[k] >= 0) mem[dst[k]] = v[k];
+}
+
+// dst[p][dst_row0 + r] = src[p][src_row0 + r] for r in [0, rows), planes p
+// dst_plane / src_plane vectors apart: the k / v window of a memory kept in a
+// larger buffer (compaction to the buffer's front, the segment's rows behind
+// the memory's).
+__global__ void __launch_bounds__(kThreads) rows_copy_kernel(uint4 *__restrict__ dst,
+                                                             long long dst_plane, int dst_row0,
+                                                             const uint4 *__restrict__ src,
+                                                             long long src_plane, int src_row0,
+                                                             int rows, int row_vec, int shift,
+                                                             unsigned int *status)
+{
+    const int total = rows * row_vec;  // vectors of this plane
+    const long long pl = blockIdx.y;
+    const int base = blockIdx.x * kThreads * kVecPerThread + threadIdx.x;
+    uint4 v[kVecPerThread];
+#pragma unroll
+    for (int k = 0; k < kVecPerThread; ++k) {
+        const int i = base + k * kThreads;
+        if (i < total) {
+            const int r = row_of(i, row_vec, shift);
+            // both rows inside their planes
+            TXL_CHECK((long long)(src_row0 + r + 1) * row_vec <= src_plane &&
+                          (long long)(dst_row0 + r + 1) * row_vec <= dst_plane,
+                      status);
+            v[k] = __ldcs(src + pl * src_plane + (long long)(src_row0 + r) * row_vec + (i - r * row_vec));
+        }
+    }
+#pragma unroll
+    for (int k = 0; k < kVecPerThread; ++k) {
+        const int i = base + k * kThreads;
+        if (i < total) {
+            const int r = row_of(i, row_vec, shift);
+            dst[pl * dst_plane + (long long)(dst_row0 + r) * row_vec + (i - r * row_vec)] = v[k];
+        }
+    }
 }
 
 int shift_of(int row_vec)
@@ -98,26 +140,42 @@ int shift_of(int row_vec)
 } // namespace
 
 cudaError_t launch_mem_concat(uint4 *ext, const uint4 *mem, const uint4 *h_new, int B,
-                              int fill, int head, int cap, int L, int row_vec, cudaStream_t s)
+                              int fill, int head, int cap, int L, int row_vec,
+                              unsigned int *status, cudaStream_t s)
 {
     const long long total = (long long)(fill + L) * row_vec;
     if (total == 0 || B == 0) return cudaSuccess;
     if (B > 65535 || total > 0x7fffffffLL - kThreads * kVecPerThread) return cudaErrorInvalidValue;
     const unsigned blocks = (unsigned)((total + kThreads * kVecPerThread - 1) / (kThreads * kVecPerThread));
     mem_concat_kernel<<<dim3(blocks, B), kThreads, 0, s>>>(ext, mem, h_new, fill, head, cap, L,
-                                                           row_vec, shift_of(row_vec));
+                                                           row_vec, shift_of(row_vec), status);
     return cudaGetLastError();
 }
 
 cudaError_t launch_mem_write(uint4 *mem, const uint4 *h_new, int B, int L, int first_row,
-                             int head, int cap, int row_vec, cudaStream_t s)
+                             int head, int cap, int row_vec, unsigned int *status, cudaStream_t s)
 {
     const long long total = (long long)(L - first_row) * row_vec;
     if (total <= 0 || B == 0) return cudaSuccess;
     if (B > 65535 || total > 0x7fffffffLL - kThreads * kVecPerThread) return cudaErrorInvalidValue;
     const unsigned blocks = (unsigned)((total + kThreads * kVecPerThread - 1) / (kThreads * kVecPerThread));
     mem_write_kernel<<<dim3(blocks, B), kThreads, 0, s>>>(mem, h_new, L, first_row, head, cap,
-                                                          row_vec, shift_of(row_vec));
+                                                          row_vec, shift_of(row_vec), status);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_rows_copy(uint4 *dst, long long dst_plane_vec, int dst_row0, const uint4 *src,
+                             long long src_plane_vec, int src_row0, int planes, int rows,
+                             int row_vec, unsigned int *status, cudaStream_t s)
+{
+    const long long total = (long long)rows * row_vec;
+    if (total <= 0 || planes == 0) return cudaSuccess;
+    if (planes > 65535 || total > 0x7fffffffLL - kThreads * kVecPerThread)
+        return cudaErrorInvalidValue;
+    const unsigned blocks = (unsigned)((total + kThreads * kVecPerThread - 1) / (kThreads * kVecPerThread));
+    rows_copy_kernel<<<dim3(blocks, planes), kThreads, 0, s>>>(
+        dst, dst_plane_vec, dst_row0, src, src_plane_vec, src_row0, rows, row_vec, shift_of(row_vec),
+        status);
     return cudaGetLastError();
 }
 

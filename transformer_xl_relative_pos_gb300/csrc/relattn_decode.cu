@@ -26,9 +26,7 @@
 // and the block writes the output, or its key range's normalised partial and
 // log2-sum-exp for the merge kernel.  The per-key work grows with L while the
 // bytes do not: from L = 7 on the tensor-core kernel is the faster path.
-#include "kernels.h"
-#include "decode.h"
-#include "ptx.cuh"
+#include "decode_common.cuh"
 
 #include <utility>
 
@@ -36,25 +34,20 @@ namespace txl {
 namespace {
 
 using namespace ptx;
+using namespace decode;
 
-constexpr int DH = kTcDH;         // 64
-constexpr int WARPS = 4;          // warps per block
-constexpr int GK = 32;            // keys per chunk
-constexpr int LMAX = kDecodeMaxL;
+constexpr int FMAX = kDecodeFmaMaxL;  // longest segment this kernel takes
 constexpr int NSTG = 2;           // ring stages per warp
-constexpr int ROWB = DH * 2;      // bytes of one bf16 row
-constexpr int RROWS = GK + LMAX - 1;
+constexpr int RROWS = GK + FMAX - 1;
 constexpr int ST_K = 0;                         // stage layout: 32 k rows,
 constexpr int ST_V = ST_K + GK * ROWB;          // 32 v rows,
-constexpr int ST_R = ST_V + GK * ROWB;          // up to 34 table rows
-constexpr int STAGE = ST_R + RROWS * ROWB;      // 12544 bytes
+constexpr int ST_R = ST_V + GK * ROWB;          // up to 37 table rows
+constexpr int STAGE = ST_R + RROWS * ROWB;      // 12928 bytes
 constexpr int RING = NSTG * STAGE;              // per warp
 constexpr int OFF_BAR = WARPS * RING;
-constexpr int OFF_MERGE = OFF_BAR + WARPS * NSTG * 8;
-constexpr int MERGE_BYTES = WARPS * LMAX * (2 + DH) * 4;
-constexpr int OFF_RES = OFF_MERGE + MERGE_BYTES;   // block result per row: o[64], lse
-constexpr int RES_BYTES = LMAX * (DH + 1) * 4;
-constexpr int OFF_FLAG = OFF_RES + RES_BYTES;
+constexpr int OFF_MERGE = OFF_BAR + WARPS * NSTG * 8;   // WarpRec per warp
+constexpr int OFF_RES = OFF_MERGE + WARPS * (int)sizeof(WarpRec);   // BlockRes
+constexpr int OFF_FLAG = OFF_RES + (int)sizeof(BlockRes);
 constexpr int SMEM_BYTES = OFF_FLAG + 16;
 
 static_assert(STAGE % 16 == 0 && RING % 16 == 0, "bulk copies need 16-byte aligned stages");
@@ -65,13 +58,6 @@ __device__ __forceinline__ float warp_max(float v)
     float r;
     asm("redux.sync.max.f32 %0, %1, 0xffffffff;" : "=f"(r) : "f"(v));
     return r;
-}
-
-__device__ __forceinline__ float ex2f(float x)
-{
-    float y;
-    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
-    return y;
 }
 
 __device__ __forceinline__ uint4 ld_shared_v4(uint32_t addr)
@@ -111,45 +97,6 @@ __device__ __forceinline__ uint64_t mul2(uint64_t a, uint64_t b)
     uint64_t d;
     asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
     return d;
-}
-
-// Thread-block cluster: the key ranges of one head run as one cluster and merge
-// through distributed shared memory.
-__device__ __forceinline__ uint32_t cluster_rank()
-{
-    uint32_t r;
-    asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
-    return r;
-}
-
-// Every thread of every block of the cluster: arrive (release) and wait (acquire).
-__device__ __forceinline__ void cluster_sync()
-{
-    asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::
-                     : "memory");
-}
-
-// Address of the same shared-memory location in block `rank` of the cluster.
-__device__ __forceinline__ uint32_t cluster_addr(uint32_t addr, uint32_t rank)
-{
-    uint32_t r;
-    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(addr), "r"(rank));
-    return r;
-}
-
-__device__ __forceinline__ float ld_cluster_f32(uint32_t addr)
-{
-    float v;
-    asm volatile("ld.shared::cluster.f32 %0, [%1];" : "=f"(v) : "r"(addr) : "memory");
-    return v;
-}
-
-__device__ __forceinline__ float2 ld_cluster_f32x2(uint32_t addr)
-{
-    float2 v;
-    asm volatile("ld.shared::cluster.v2.f32 {%0, %1}, [%2];" : "=f"(v.x), "=f"(v.y) : "r"(addr)
-                 : "memory");
-    return v;
 }
 
 // bf16 pair (dims 2c, 2c+1) as an fp32 pair.
@@ -194,9 +141,10 @@ __global__ void __launch_bounds__(WARPS * 32) relattn_decode_kernel(const Decode
     const int k_begin = split * span, k_end = min(K, k_begin + span);
     const int n_chunks = (k_end > k_begin) ? (k_end - k_begin + GK - 1) / GK : 0;
     const int n_mine = (n_chunks > warp) ? (n_chunks - warp + WARPS - 1) / WARPS : 0;
+    TXL_CHECK(k_begin >= 0 && k_end <= K && bh < p.B * p.H && split < p.n_splits, p.status);
 
-    const uint8_t *kg = reinterpret_cast<const uint8_t *>(p.k) + (size_t)bh * K * ROWB;
-    const uint8_t *vg = reinterpret_cast<const uint8_t *>(p.v) + (size_t)bh * K * ROWB;
+    const uint8_t *kg = reinterpret_cast<const uint8_t *>(p.k) + (size_t)bh * p.kv_stride * 2;
+    const uint8_t *vg = reinterpret_cast<const uint8_t *>(p.v) + (size_t)bh * p.kv_stride * 2;
     const uint8_t *rg = reinterpret_cast<const uint8_t *>(p.r) + ((size_t)h * p.r_rows + p.r_off) * ROWB;
     uint8_t *ring = smem + warp * RING;
     uint64_t *bars = reinterpret_cast<uint64_t *>(smem + OFF_BAR) + warp * NSTG;
@@ -223,6 +171,10 @@ __global__ void __launch_bounds__(WARPS * 32) relattn_decode_kernel(const Decode
         uint8_t *stg = ring + (n % NSTG) * STAGE;
         const int rows = min(GK, k_end - j0);
         const int rrows = min(min(GK + L - 1, K - j0), k_end - j0 + L - 1);
+        // key rows of this block's range; table rows inside the table
+        TXL_CHECK(j0 >= k_begin && rows > 0 && j0 + rows <= k_end && rrows >= rows &&
+                      rrows <= GK + L - 1 && p.r_off + j0 + rrows <= p.r_rows,
+                  p.status);
         mbar_arrive_expect_tx(bars + n % NSTG, (uint32_t)(2 * rows + rrows) * ROWB);
         bulk_load_hint(stg + ST_K, kg + (size_t)j0 * ROWB, rows * ROWB, bars + n % NSTG, pol_stream);
         bulk_load_hint(stg + ST_V, vg + (size_t)j0 * ROWB, rows * ROWB, bars + n % NSTG, pol_stream);
@@ -367,95 +319,23 @@ __global__ void __launch_bounds__(WARPS * 32) relattn_decode_kernel(const Decode
         }
     }
 
-    // ---- merge the block's warps: w = 2^(m_w - max), out = sum w a / sum w l ----
-    float *sm_m = reinterpret_cast<float *>(smem + OFF_MERGE);   // [WARPS][LMAX]
-    float *sm_l = sm_m + WARPS * LMAX;                             // [WARPS][LMAX]
-    float *sm_a = sm_l + WARPS * LMAX;                             // [WARPS][LMAX][64]
+    // ---- this warp's record for the block merge ---------------------------------
+    WarpRec *mine = reinterpret_cast<WarpRec *>(smem + OFF_MERGE) + warp;
 #pragma unroll
     for (int i = 0; i < L; ++i) {
         if (lane == 0) {
-            sm_m[warp * LMAX + i] = m[i];
-            sm_l[warp * LMAX + i] = l[i];
+            mine->m[i] = m[i];
+            mine->l[i] = l[i];
         }
         if (g == 0) {
-            float4 *dst = reinterpret_cast<float4 *>(sm_a + (warp * LMAX + i) * DH + 8 * sub);
+            float4 *dst = reinterpret_cast<float4 *>(mine->a[i] + 8 * sub);
             dst[0] = make_float4(o8[i][0], o8[i][1], o8[i][2], o8[i][3]);
             dst[1] = make_float4(o8[i][4], o8[i][5], o8[i][6], o8[i][7]);
         }
     }
-    __syncthreads();
-    for (int i = warp; i < L; i += WARPS) {
-        float mx = -INFINITY;
-#pragma unroll
-        for (int w = 0; w < WARPS; ++w) mx = fmaxf(mx, sm_m[w * LMAX + i]);
-        float ls = 0.f, o0 = 0.f, o1 = 0.f;
-        if (mx != -INFINITY) {
-#pragma unroll
-            for (int w = 0; w < WARPS; ++w) {
-                const float mw = sm_m[w * LMAX + i];
-                if (mw == -INFINITY) continue;
-                const float sw = ex2f(mw - mx);
-                ls += sw * sm_l[w * LMAX + i];
-                const float2 aw = reinterpret_cast<const float2 *>(sm_a + (w * LMAX + i) * DH)[lane];
-                o0 = fmaf(sw, aw.x, o0);
-                o1 = fmaf(sw, aw.y, o1);
-            }
-        }
-        const float inv = (ls > 0.f) ? 1.f / ls : 0.f;
-        const float lse2 = (ls > 0.f) ? mx + __log2f(ls) : -INFINITY;
-        const size_t row = (size_t)bh * L + i;
-        if (p.n_splits == 1) {
-            reinterpret_cast<__nv_bfloat162 *>(p.out + row * DH)[lane] =
-                __floats2bfloat162_rn(o0 * inv, o1 * inv);
-            if (p.lse && lane == 0) p.lse[row] = lse2 * 0.69314718055994531f;
-        } else if (p.cluster) {
-            // this key range's normalised partial stays in shared memory
-            reinterpret_cast<float2 *>(smem + OFF_RES)[i * (DH / 2) + lane] =
-                make_float2(o0 * inv, o1 * inv);
-            if (lane == 0) reinterpret_cast<float *>(smem + OFF_RES)[LMAX * DH + i] = lse2;
-        } else {
-            const size_t prow = (size_t)split * p.B * p.H * L + row;
-            reinterpret_cast<float2 *>(p.part_o + prow * DH)[lane] = make_float2(o0 * inv, o1 * inv);
-            if (lane == 0) p.part_lse[prow] = lse2;
-        }
-    }
-    if (p.cluster) {
-        // The key ranges of this head are the blocks of one cluster (rank =
-        // range): block 0 merges their partials through distributed shared
-        // memory, out = sum_r 2^(lse_r - max) o_r / sum_r 2^(lse_r - max).
-        // Every block reaches both cluster barriers (no early exits above).
-        cluster_sync();
-        if (cluster_rank() == 0) {
-            const uint32_t res = smem_u32(smem + OFF_RES);
-            for (int i = warp; i < L; i += WARPS) {
-                const uint32_t a_lse = res + (uint32_t)(LMAX * DH + i) * 4;
-                const uint32_t a_o = res + (uint32_t)(i * DH + 2 * lane) * 4;
-                float mx = -INFINITY;
-                for (int r = 0; r < p.n_splits; ++r)
-                    mx = fmaxf(mx, ld_cluster_f32(cluster_addr(a_lse, (uint32_t)r)));
-                float wsum = 0.f, c0 = 0.f, c1 = 0.f;
-                if (mx != -INFINITY) {
-                    for (int r = 0; r < p.n_splits; ++r) {
-                        const float lr = ld_cluster_f32(cluster_addr(a_lse, (uint32_t)r));
-                        if (lr == -INFINITY) continue;  // a range without keys
-                        const float w = ex2f(lr - mx);
-                        const float2 o = ld_cluster_f32x2(cluster_addr(a_o, (uint32_t)r));
-                        wsum += w;
-                        c0 = fmaf(w, o.x, c0);
-                        c1 = fmaf(w, o.y, c1);
-                    }
-                }
-                const float inv = (wsum > 0.f) ? 1.f / wsum : 0.f;
-                const size_t row = (size_t)bh * L + i;
-                reinterpret_cast<__nv_bfloat162 *>(p.out + row * DH)[lane] =
-                    __floats2bfloat162_rn(c0 * inv, c1 * inv);
-                if (p.lse && lane == 0)
-                    p.lse[row] = (wsum > 0.f) ? (mx + __log2f(wsum)) * 0.69314718055994531f
-                                              : -INFINITY;
-            }
-        }
-        cluster_sync();  // block 0 has read the others' shared memory
-    }
+    const uint8_t *const merge = smem + OFF_MERGE;
+    const auto rec = [merge](int w) { return reinterpret_cast<const WarpRec *>(merge) + w; };
+    finish_block<L>(rec, reinterpret_cast<BlockRes *>(smem + OFF_RES), p, bh, split, warp, lane);
 }
 
 template <int L>
@@ -501,7 +381,7 @@ cudaError_t launch_l(const DecodeParams &p, cudaStream_t s)
     return cudaLaunchKernelEx(&cfg, relattn_decode_kernel<L>, p);
 }
 
-// Instances L = 1 .. kDecodeMaxL, indexed by L - 1.
+// Instances L = 1 .. FMAX, indexed by L - 1.
 template <int... I>
 struct Table {
     static constexpr cudaError_t (*set_smem[])() = {set_smem_l<I + 1>...};
@@ -510,7 +390,7 @@ struct Table {
 };
 template <int... I>
 Table<I...> make_table(std::integer_sequence<int, I...>);
-using Inst = decltype(make_table(std::make_integer_sequence<int, kDecodeMaxL>{}));
+using Inst = decltype(make_table(std::make_integer_sequence<int, FMAX>{}));
 
 // The dynamic shared-memory attribute of every instance, once per device.
 cudaError_t ensure_smem_attr()
@@ -520,7 +400,7 @@ cudaError_t ensure_smem_attr()
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return e;
     if (dev >= 0 && dev < 64 && done[dev]) return cudaSuccess;
-    for (int l = 0; l < kDecodeMaxL; ++l)
+    for (int l = 0; l < FMAX; ++l)
         if ((e = Inst::set_smem[l]()) != cudaSuccess) return e;
     if (dev >= 0 && dev < 64) done[dev] = true;
     return cudaSuccess;
@@ -532,15 +412,15 @@ int decode_chunk_keys() { return GK; }
 
 int decode_blocks_per_sm(int L)
 {
-    static int cache[kDecodeMaxL + 1] = {};  // per query count; one device per process
-    if (L < 1 || L > kDecodeMaxL) return 1;
+    static int cache[FMAX + 1] = {};  // per query count; one device per process
+    if (L < 1 || L > FMAX) return 1;
     if (!cache[L]) cache[L] = (ensure_smem_attr() == cudaSuccess) ? Inst::blocks[L - 1]() : 1;
     return cache[L];
 }
 
 cudaError_t launch_relattn_decode(const DecodeParams &p, cudaStream_t s)
 {
-    if (p.L < 1 || p.L > kDecodeMaxL) return cudaErrorInvalidValue;
+    if (p.L < 1 || p.L > FMAX) return cudaErrorInvalidValue;
     const cudaError_t e = ensure_smem_attr();
     if (e != cudaSuccess) return e;
     return Inst::launch[p.L - 1](p, s);

@@ -42,8 +42,8 @@ __global__ void __launch_bounds__(ROWS)
     // Keys visible to the last row of this block.
     const int last_row = min(p.L - 1, row0 + ROWS - 1);
     const int jend = min(K, p.M + last_row + 1);
-    const float *kbase = p.k + (size_t)bh * K * DH;
-    const float *vbase = p.v + (size_t)bh * K * DH;
+    const float *kbase = p.k + (size_t)bh * p.kv_stride;
+    const float *vbase = p.v + (size_t)bh * p.kv_stride;
     const float *rbase = p.r + (size_t)h * p.r_rows * DH;
 
     for (int j0 = 0; j0 < jend; j0 += KT) {

@@ -282,6 +282,10 @@ __global__ void __launch_bounds__(256, 1)
     const int per_split = (n_tiles_all + p.n_splits - 1) / p.n_splits;
     const int t_begin = split * per_split;
     const int T = min(n_tiles_all, t_begin + per_split) - t_begin;
+    // (a split past the last tile is empty: T <= 0, handled below)
+    TXL_CHECK(split < p.n_splits && qt >= 0 && qt < p.n_qtiles && bh < n_bh && t_begin >= 0 &&
+                  T <= per_split && rows_valid > 0,
+              p.status);
 
     if (T <= 0) {
         // An empty key split (only with n_splits > 1): contribute nothing.
@@ -724,6 +728,11 @@ __global__ void __launch_bounds__(256, 1)
                     tmem_ld32(tS + 32 * (pc + 1), wb);
                 }
                 const uint32_t rd = skew_rd + (uint32_t)(pc * 128);
+                // every skewed read stays inside this row's 4 x 32-float ring
+                TXL_CHECK(pc == 3 ? (rd + 4u * (lane + 1) - 512u >= skew || lane == 31) &&
+                                        rd + 4u * lane < skew + 512u
+                                  : rd + 124u < skew + 512u,
+                          p.status);
                 float wv[32];
                 if (pc == 3) {
 #pragma unroll
@@ -750,6 +759,7 @@ __global__ void __launch_bounds__(256, 1)
                     // chunk pc+2 into slot (pc+2) % 4: empty, or (chunk 4) the slot of
                     // chunk 0, which no later piece of this tile reads
                     const uint32_t slot = skew + (uint32_t)(((pc + 2) % 4) * 128);
+                    TXL_CHECK(wcol(wbase + 32u * (pc + 2)) + 32u <= TM_O, p.status);
 #pragma unroll
                     for (int c = 0; c < 8; ++c)
                         st_shared_v4(slot + c * 16, wa[4 * c], wa[4 * c + 1], wa[4 * c + 2],
@@ -865,6 +875,7 @@ __global__ void __launch_bounds__(256, 1)
             const float lse2 = (l_sum > 0.f) ? m_ref + __log2f(l_sum) : -INFINITY;
             if (row < rows_valid) {
                 const size_t orow = (size_t)bh * p.L + i;
+                TXL_CHECK(i < p.L && orow < (size_t)p.B * p.H * p.L, p.status);
                 if (p.n_splits == 1) {
                     uint4 *dst = reinterpret_cast<uint4 *>(p.out + orow * DH);
 #pragma unroll
@@ -902,6 +913,13 @@ __global__ void __launch_bounds__(256, 1)
         tc_fence_after_sync();
         tmem_dealloc(tmem, TM_COLS);
     }
+}
+
+// One thread fails one index check: tests that the debug build reports it (a
+// no-op in release builds, where the checks compile away).
+__global__ void index_probe_kernel(unsigned int *status)
+{
+    if (threadIdx.x == 0) TXL_CHECK(status == nullptr, status);
 }
 
 // Waits on a barrier nothing will complete; the bounded wait must give up and
@@ -943,6 +961,12 @@ cudaError_t launch_relattn_tc(const CUtensorMap &tm_q, const CUtensorMap &tm_k,
     const long long blocks = (long long)p.B * p.H * p.n_qtiles * p.n_splits;
     if (blocks <= 0 || blocks > 0x7fffffffLL) return cudaErrorInvalidValue;
     relattn_fwd_tc_kernel<<<(unsigned)blocks, 256, SMEM_BYTES, s>>>(tm_q, tm_k, tm_v, tm_r, p);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_index_probe(unsigned int *status, cudaStream_t s)
+{
+    index_probe_kernel<<<1, 32, 0, s>>>(status);
     return cudaGetLastError();
 }
 

@@ -70,14 +70,16 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn()
     return fn;
 }
 
-// 3-D bf16 view [outer][rows][64] with a 64 x 128 box and 128-byte swizzle.
+// 3-D bf16 view [outer][rows][64] with a 64 x box_rows box and 128-byte
+// swizzle; planes plane_elems elements apart (rows * 64 when dense).
 bool make_map(CUtensorMap *map, const void *base, long long rows, long long outer,
-              unsigned box_rows = 128)
+              unsigned box_rows = 128, long long plane_elems = 0)
 {
     auto fn = encode_fn();
     if (!fn) return false;
+    if (plane_elems == 0) plane_elems = rows * 64;
     const cuuint64_t dims[3] = {64, (cuuint64_t)rows, (cuuint64_t)outer};
-    const cuuint64_t strides[2] = {64 * 2, (cuuint64_t)rows * 64 * 2};
+    const cuuint64_t strides[2] = {64 * 2, (cuuint64_t)plane_elems * 2};
     const cuuint32_t box[3] = {64, box_rows, 1};
     const cuuint32_t estr[3] = {1, 1, 1};
     CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void *>(base), dims,
@@ -142,26 +144,6 @@ int auto_splits(int units, int n_key_tiles)
     return best;
 }
 
-// Estimated device times (microseconds, GB300) that choose between the two
-// bf16 kernels for short segments when the library picks the split.  The
-// tensor-core kernel costs about the same for any L <= 128 (every block
-// multiplies whole 128-row tiles): the wave model above at 1.67 us per
-// tile-time.  The decode kernel reads k, v and the table once (at about
-// 6.5 TB/s, with a 2.5 us floor for small calls), each query past the first
-// adds ~18% to that, plus ~6.5 us of fixed cost.  Fitted to graph-replayed
-// times of both kernels forced on 28 shapes (H = 16, L = 1..6, M = 800..12000,
-// B = 1..64): the pick is the faster kernel on all of them.  The tensor cores
-// win only for one sequence against a long memory (M = 3800, L = 6: 14.9
-// against 17.3 us; M = 8000, L = 4: 18.5 against 21.4 us); with more sequences
-// the decode kernel wins (eight sequences, M = 3800, L = 6: 46.6 against 48.5 us).
-constexpr double kTcTileUs = 1.67;
-
-double decode_cost_us(long long B, long long H, long long K, int L, long long r_rows)
-{
-    const double bytes = 2.0 * (2.0 * B * H * K * 64 + (double)H * r_rows * 64 + 2.0 * B * H * L * 64);
-    return std::max(bytes / 6.5e6, 2.5) * (1.0 + 0.18 * (L - 1)) + 6.5;
-}
-
 // Key splits of the tensor-core kernel for one call: the caller's n_splits,
 // or the automatic choice when that is 0, limited to 1 when there is no usable
 // workspace (have_ws: non-NULL and 256-byte aligned) big enough for the
@@ -180,6 +162,20 @@ int tc_splits(int B, int H, int L, int dh, int n_qtiles, int n_key_tiles, int n_
     return splits;
 }
 
+// Which decode kernel a segment of L queries runs: the tensor-core one from
+// kDecodeMmaFromL queries on, the CUDA-core one below.  One query is the CUDA-core
+// kernel's best case (eight sequences of 16 heads against M = 3800: 22.2 against
+// 23.5 us); from two on the tensor-core kernel is faster (24.3 against 23.6 us)
+// and its time hardly grows with L (23.6 to 24.8 us for L = 2..7, where the
+// CUDA-core kernel goes to 44.9 us at L = 6).
+constexpr int kDecodeMmaFromL = 2;
+bool decode_on_mma(int L) { return L >= kDecodeMmaFromL || L > txl::kDecodeFmaMaxL; }
+
+int decode_blocks(int L)
+{
+    return decode_on_mma(L) ? txl::decode_mma_blocks_per_sm(L) : txl::decode_blocks_per_sm(L);
+}
+
 // Key ranges per (b, h) of the decode kernel: the caller's n_splits or the
 // automatic choice, capped at one per 128 keys, without ranges that own no key.
 int decode_splits(long long BH, long long K, int L, int n_splits)
@@ -196,7 +192,7 @@ int decode_splits(long long BH, long long K, int L, int n_splits)
         // cluster beat more ranges merged through the workspace even where
         // those would fill more SMs (one sequence of 16 heads, M = 3800: 8.4 us
         // with 8 ranges, 9.0 us with 19).
-        const long long slots = (long long)sm_count() * txl::decode_blocks_per_sm(L);
+        const long long slots = (long long)sm_count() * decode_blocks(L);
         splits = (int)std::max<long long>(
             1, std::min<long long>(std::min<long long>(slots / BH, max_splits),
                                    txl::kDecodeMaxCluster));
@@ -207,37 +203,23 @@ int decode_splits(long long BH, long long K, int L, int n_splits)
     return splits;
 }
 
-// Which bf16 kernel a call runs: the decode kernel for segments of at most
-// kDecodeMaxL queries when the caller fixed the split (n_splits >= 1: the
-// split then counts decode key ranges), when the call is small, or when its
-// estimate is the lower one.
-bool use_decode(int B, int H, int M, int L, int r_rows, int n_splits, bool have_ws,
-                size_t workspace_bytes)
-{
-    if (L > txl::kDecodeMaxL) return false;
-    if (n_splits != 0) return true;
-    const long long K = (long long)M + L;
-    const double dec_us = decode_cost_us(B, H, K, L, r_rows);
-    // Calls the decode kernel finishes in about 12 us stay on it: at that size
-    // the two kernels differ by a few microseconds either way, and its launch
-    // encodes no tensor maps on the host.
-    if (dec_us < 12.0) return true;
-    const int n_qtiles = (L + txl::kTcBM - 1) / txl::kTcBM;
-    const int jmax_all = (int)std::min<long long>(K - 1, (long long)M + L - 1);
-    const int n_key_tiles = jmax_all / txl::kTcBN + 1;
-    const int s = tc_splits(B, H, L, 64, n_qtiles, n_key_tiles, 0, have_ws, workspace_bytes);
-    const long long units = (long long)B * H * n_qtiles;
-    const double tc_us = tc_wave_cost(units, n_key_tiles, s) * kTcTileUs;
-    return dec_us <= tc_us;
-}
+// Which bf16 kernel a call runs: the decode kernel for every segment of at
+// most kDecodeMaxL queries.  Forced both ways on 48 shapes (H = 16, B = 1, 2,
+// 4, L = 2, 4, 6, 8, M = 800 to 12000, graph-replayed), the decode kernel was
+// the faster one on all of them, by 1.19x (one sequence, M = 8000, L = 8:
+// 14.7 against 17.5 us) to 2.2x; with eight sequences against M = 3800 it
+// takes 24 us for any L from 2 to 7, the tensor-core kernel 44 us (that kernel
+// multiplies whole 128-row query tiles, 16x the rows of an eight-query segment).
+bool use_decode(int L) { return L <= txl::kDecodeMaxL; }
 
-// Short segments (L <= kDecodeMaxL): split-K decode kernel on the CUDA cores.
+// Short segments (L <= kDecodeMaxL): split-K decode kernel, on the tensor
+// cores (warp MMAs) or the CUDA cores.
 // Up to kDecodeMaxCluster key ranges of a head merge inside their thread-block
 // cluster; more go through the workspace and the log-sum-exp merge kernel.
-int relattn_decode(const void *q, const void *k, const void *v, const void *r, int r_rows,
-                   const void *u, const void *v_bias, void *out, float *lse, int B, int H, int M,
-                   int L, float scale, int n_splits, void *workspace, size_t workspace_bytes,
-                   cudaStream_t s)
+int relattn_decode(const void *q, const void *k, const void *v, long long kv_stride,
+                   const void *r, int r_rows, const void *u, const void *v_bias, void *out,
+                   float *lse, int B, int H, int M, int L, float scale, int n_splits,
+                   void *workspace, size_t workspace_bytes, cudaStream_t s)
 {
     const long long K = (long long)M + L;
     const long long BH = (long long)B * H;
@@ -268,6 +250,7 @@ int relattn_decode(const void *q, const void *k, const void *v, const void *r, i
     p.r_rows = r_rows;
     p.r_off = r_rows - (int)K;
     p.n_splits = splits;
+    p.kv_stride = kv_stride;
     p.cluster = cluster ? 1 : 0;
     p.scale_log2 = scale * 1.4426950408889634f;
     p.q = static_cast<const __nv_bfloat16 *>(q);
@@ -286,7 +269,17 @@ int relattn_decode(const void *q, const void *k, const void *v, const void *r, i
         p.part_lse = reinterpret_cast<float *>(static_cast<char *>(workspace) + off);
         p.lse = nullptr;
     }
-    cudaError_t err = txl::launch_relattn_decode(p, s);
+    cudaError_t err;
+    if (decode_on_mma(L)) {
+        CUtensorMap tk, tv, tr;
+        if (!make_map(&tk, k, K, BH, txl::kDecodeMmaKeyBox, kv_stride) ||
+            !make_map(&tv, v, K, BH, txl::kDecodeMmaKeyBox, kv_stride) ||
+            !make_map(&tr, r, r_rows, H, txl::kDecodeMmaTableBox))
+            return TXL_ERR_CUDA;
+        err = txl::launch_relattn_decode_mma(tk, tv, tr, p, s);
+    } else {
+        err = txl::launch_relattn_decode(p, s);
+    }
     if (err != cudaSuccess) return TXL_ERR_CUDA;
     if (splits > 1 && !cluster) {
         err = txl::launch_relattn_combine(p.part_o, p.part_lse, p.out, lse, splits,
@@ -311,6 +304,7 @@ const char *txl_status_string(int status)
     case TXL_ERR_CUDA: return "CUDA error";
     case TXL_ERR_TIMEOUT: return "kernel barrier wait timed out";
     case TXL_ERR_WORKSPACE: return "workspace missing or too small";
+    case TXL_ERR_INDEX: return "a device-side index check failed";
     default: return "unknown status";
     }
 }
@@ -358,12 +352,12 @@ int txl_relattn_plan(int B, int H, int M, int L, int r_rows, int dh, int dtype, 
     if (BH * L > 0x7fffffffLL || BH > 0x7fffffffLL / 64) return TXL_ERR_UNSUPPORTED;
     const bool have_ws = workspace_bytes > 0;
     int n = 1;
-    if (use_decode(B, H, M, L, r_rows, n_splits, have_ws, workspace_bytes)) {
+    if (use_decode(L)) {
         n = decode_splits(BH, K, L, n_splits);
         if (n > txl::kDecodeMaxCluster && workspace_bytes < workspace_bytes_for(B, H, L, 64, n))
             return TXL_ERR_WORKSPACE;
         if (BH * n > 0x7fffffffLL) return TXL_ERR_UNSUPPORTED;
-        *kernel = TXL_KERNEL_DECODE;
+        *kernel = decode_on_mma(L) ? TXL_KERNEL_DECODE_MMA : TXL_KERNEL_DECODE;
     } else {
         const int n_qtiles = (L + txl::kTcBM - 1) / txl::kTcBM;
         const int jmax_all = (int)std::min<long long>(K - 1, (long long)M + L - 1);
@@ -377,10 +371,15 @@ int txl_relattn_plan(int B, int H, int M, int L, int r_rows, int dh, int dtype, 
     return TXL_OK;
 }
 
-int txl_relattn_fwd(const void *q, const void *k, const void *v, const void *r, int r_rows,
-                    const void *u, const void *v_bias, void *out, float *lse, int B, int H,
-                    int M, int L, int dh, float scale, int dtype, int n_splits,
-                    void *workspace, size_t workspace_bytes, void *stream)
+} // extern "C"
+
+namespace {
+
+// txl_relattn_fwd with k and v planes kv_stride elements apart (0: dense).
+int relattn_impl(const void *q, const void *k, const void *v, long long kv_stride,
+                 const void *r, int r_rows, const void *u, const void *v_bias, void *out,
+                 float *lse, int B, int H, int M, int L, int dh, float scale, int dtype,
+                 int n_splits, void *workspace, size_t workspace_bytes, void *stream)
 {
     if (!q || !k || !v || !r || !u || !v_bias || !out) return TXL_ERR_INVALID_ARG;
     if (B < 1 || H < 1 || M < 0 || L < 1 || dh < 1 || n_splits < 0) return TXL_ERR_INVALID_ARG;
@@ -389,6 +388,9 @@ int txl_relattn_fwd(const void *q, const void *k, const void *v, const void *r, 
     const long long K = (long long)M + L;
     if (K > 0x7fffffffLL / 2 || r_rows < K) return TXL_ERR_SHAPE;
     if (dh != 64) return TXL_ERR_UNSUPPORTED;
+    if (kv_stride == 0) kv_stride = K * dh;
+    if (kv_stride < K * dh) return TXL_ERR_SHAPE;
+    if (kv_stride % 8 != 0) return TXL_ERR_MISALIGNED;
     cudaStream_t s = as_stream(stream);
 
     if (dtype == TXL_F32) {
@@ -411,6 +413,7 @@ int txl_relattn_fwd(const void *q, const void *k, const void *v, const void *r, 
         p.L = L;
         p.K = (int)K;
         p.r_rows = r_rows;
+        p.kv_stride = kv_stride;
         p.scale = scale;
         return cuda_status(txl::launch_relattn_f32(p, s));
     }
@@ -422,9 +425,9 @@ int txl_relattn_fwd(const void *q, const void *k, const void *v, const void *r, 
     const long long BH = (long long)B * H;
     if (BH * L > 0x7fffffffLL || BH > 0x7fffffffLL / 64) return TXL_ERR_UNSUPPORTED;
     const bool have_ws = workspace && aligned(workspace, 256);
-    if (use_decode(B, H, M, L, r_rows, n_splits, have_ws, workspace_bytes))
-        return relattn_decode(q, k, v, r, r_rows, u, v_bias, out, lse, B, H, M, L, scale, n_splits,
-                              workspace, workspace_bytes, s);
+    if (use_decode(L))
+        return relattn_decode(q, k, v, kv_stride, r, r_rows, u, v_bias, out, lse, B, H, M, L,
+                              scale, n_splits, workspace, workspace_bytes, s);
     const int n_qtiles = (L + txl::kTcBM - 1) / txl::kTcBM;
     const int jmax_all = (int)std::min<long long>(K - 1, (long long)M + L - 1);
     const int n_key_tiles = jmax_all / txl::kTcBN + 1;
@@ -438,8 +441,8 @@ int txl_relattn_fwd(const void *q, const void *k, const void *v, const void *r, 
     if (BH * n_qtiles * splits > 0x7fffffffLL) return TXL_ERR_UNSUPPORTED;
 
     CUtensorMap tq, tk, tv, tr;
-    if (!make_map(&tq, q, L, BH) || !make_map(&tk, k, K, BH) || !make_map(&tv, v, K, BH) ||
-        !make_map(&tr, r, r_rows, H))
+    if (!make_map(&tq, q, L, BH) || !make_map(&tk, k, K, BH, 128, kv_stride) ||
+        !make_map(&tv, v, K, BH, 128, kv_stride) || !make_map(&tr, r, r_rows, H))
         return TXL_ERR_CUDA;
 
     cudaError_t err;
@@ -480,6 +483,84 @@ int txl_relattn_fwd(const void *q, const void *k, const void *v, const void *r, 
     return TXL_OK;
 }
 
+bool window_ok(const txl_kv_window *w)
+{
+    return w && w->M >= 0 && w->fill >= 0 && w->fill <= w->M && w->start >= 0 &&
+           w->capacity >= 0 && (long long)w->start + w->fill <= w->capacity;
+}
+
+} // namespace
+
+extern "C" {
+
+int txl_relattn_fwd(const void *q, const void *k, const void *v, const void *r, int r_rows,
+                    const void *u, const void *v_bias, void *out, float *lse, int B, int H,
+                    int M, int L, int dh, float scale, int dtype, int n_splits,
+                    void *workspace, size_t workspace_bytes, void *stream)
+{
+    return relattn_impl(q, k, v, 0, r, r_rows, u, v_bias, out, lse, B, H, M, L, dh, scale, dtype,
+                        n_splits, workspace, workspace_bytes, stream);
+}
+
+int txl_relattn_fwd_strided(const void *q, const void *k, const void *v, long long kv_stride,
+                            const void *r, int r_rows, const void *u, const void *v_bias,
+                            void *out, float *lse, int B, int H, int M, int L, int dh,
+                            float scale, int dtype, int n_splits, void *workspace,
+                            size_t workspace_bytes, void *stream)
+{
+    if (kv_stride < 1) return TXL_ERR_INVALID_ARG;
+    return relattn_impl(q, k, v, kv_stride, r, r_rows, u, v_bias, out, lse, B, H, M, L, dh,
+                        scale, dtype, n_splits, workspace, workspace_bytes, stream);
+}
+
+int txl_kv_window_append(void *buf, txl_kv_window *w, const void *seg, int planes, int L, int d,
+                         int dtype, void *stream)
+{
+    if (!window_ok(w) || planes < 1 || L < 0 || d < 1) return TXL_ERR_INVALID_ARG;
+    if (dtype != TXL_F32 && dtype != TXL_BF16) return TXL_ERR_INVALID_ARG;
+    if ((long long)w->capacity < 2LL * w->M + L) return TXL_ERR_SHAPE;
+    if (L == 0) return TXL_OK;
+    if (!buf || !seg) return TXL_ERR_INVALID_ARG;
+    const size_t esz = dtype == TXL_F32 ? 4 : 2;
+    if (((size_t)d * esz) % 16 != 0) return TXL_ERR_MISALIGNED;
+    if (!aligned(buf, 16) || !aligned(seg, 16)) return TXL_ERR_MISALIGNED;
+    const int row_vec = (int)((size_t)d * esz / 16);
+    const long long plane = (long long)w->capacity * row_vec;
+    cudaStream_t s = as_stream(stream);
+    cudaError_t serr;
+    unsigned int *status = status_word(&serr);
+    if (!status) return TXL_ERR_CUDA;
+    int start = w->start;
+    if ((long long)start + w->fill + L > w->capacity) {
+        // Move the memory rows to the buffer's front.  With capacity >= 2M + L the
+        // window starts at row >= M >= fill here, so the two ranges are disjoint.
+        if (w->fill > 0) {
+            cudaError_t e = txl::launch_rows_copy(static_cast<uint4 *>(buf), plane, 0,
+                                                  static_cast<const uint4 *>(buf), plane, start,
+                                                  planes, w->fill, row_vec, status, s);
+            if (e != cudaSuccess) return TXL_ERR_CUDA;
+        }
+        start = 0;
+    }
+    cudaError_t e = txl::launch_rows_copy(static_cast<uint4 *>(buf), plane, start + w->fill,
+                                          static_cast<const uint4 *>(seg), (long long)L * row_vec,
+                                          0, planes, L, row_vec, status, s);
+    if (e != cudaSuccess) return TXL_ERR_CUDA;
+    w->start = start;
+    return TXL_OK;
+}
+
+int txl_kv_window_advance(txl_kv_window *w, int L)
+{
+    if (!window_ok(w) || L < 0) return TXL_ERR_INVALID_ARG;
+    const long long total = (long long)w->fill + L;
+    if ((long long)w->start + total > w->capacity) return TXL_ERR_SHAPE;
+    const int keep = (int)std::min<long long>(total, w->M);
+    w->start = (int)(w->start + total - keep);
+    w->fill = keep;
+    return TXL_OK;
+}
+
 int txl_mem_concat(void *ext, const void *mem, const txl_mem_state *st, const void *h_new,
                    int B, int L, int d, int dtype, void *stream)
 {
@@ -495,10 +576,13 @@ int txl_mem_concat(void *ext, const void *mem, const txl_mem_state *st, const vo
     if (!aligned(ext, 16) || (h_new && !aligned(h_new, 16)) || (mem && !aligned(mem, 16)))
         return TXL_ERR_MISALIGNED;
     const int row_vec = (int)((size_t)d * esz / 16);
+    cudaError_t serr;
+    unsigned int *status = status_word(&serr);
+    if (!status) return TXL_ERR_CUDA;
     return cuda_status(txl::launch_mem_concat(
         static_cast<uint4 *>(ext), static_cast<const uint4 *>(mem),
         static_cast<const uint4 *>(h_new), B, st->fill, st->head, st->capacity, L, row_vec,
-        as_stream(stream)));
+        status, as_stream(stream)));
 }
 
 int txl_mem_update(void *mem, txl_mem_state *st, const void *h_new, int B, int L, int d,
@@ -517,9 +601,12 @@ int txl_mem_update(void *mem, txl_mem_state *st, const void *h_new, int B, int L
     const int row_vec = (int)((size_t)d * esz / 16);
     const int cap = st->capacity;
     const int first = L > cap ? L - cap : 0;  // older rows would be overwritten anyway
+    cudaError_t serr;
+    unsigned int *status = status_word(&serr);
+    if (!status) return TXL_ERR_CUDA;
     cudaError_t e = txl::launch_mem_write(static_cast<uint4 *>(mem),
                                           static_cast<const uint4 *>(h_new), B, L, first,
-                                          st->head, cap, row_vec, as_stream(stream));
+                                          st->head, cap, row_vec, status, as_stream(stream));
     if (e != cudaSuccess) return TXL_ERR_CUDA;
     st->head = (int)(((long long)st->head + L) % cap);
     st->fill = (int)std::min<long long>((long long)st->fill + L, cap);
@@ -538,9 +625,28 @@ int txl_device_status(void *stream)
         const unsigned int zero = 0;
         if (cudaMemcpy(w, &zero, sizeof(zero), cudaMemcpyHostToDevice) != cudaSuccess)
             return TXL_ERR_CUDA;
-        return TXL_ERR_TIMEOUT;
+        return (v & TXL_STATUS_TIMEOUT) ? TXL_ERR_TIMEOUT : TXL_ERR_INDEX;
     }
     return TXL_OK;
+}
+
+int txl_debug_checks(void)
+{
+#ifdef TXL_DEBUG
+    return 1;
+#else
+    return 0;
+#endif
+}
+
+int txl_debug_index_probe(void *stream)
+{
+    cudaError_t err;
+    unsigned int *w = status_word(&err);
+    if (!w) return TXL_ERR_CUDA;
+    err = txl::launch_index_probe(w, as_stream(stream));
+    if (err != cudaSuccess) return TXL_ERR_CUDA;
+    return txl_device_status(stream);
 }
 
 int txl_debug_wait_timeout(uint64_t ns, void *stream)

@@ -10,26 +10,24 @@
                                                            residual, LayerNorm)
 and the memory of each layer advances to the newest M states of its input
 (§3.2)                                                  -> mem_update (kernel).
-With ``cache_kv`` the stack also keeps, per layer, rings of the memory's
-projected keys and values: the memory rows and W_kE, W_v do not change at
-evaluation, so k and v of the memory are the ones projected when those states
-were the segment, and each segment projects only its own L rows (2·M·d²
-multiply-adds saved per layer and projection); the rings are the same kernels
-on a [B·H, M, d_head] view.  The attention takes k and v as one contiguous
-tensor, so the rings are copied out every segment: replayed from CUDA graphs
-the cached stack is slightly faster than re-projecting the memory (the saved
-multiply-adds outweigh the copies), launched eagerly it is slower (four more
-launches per layer), so it is off by default.
+With ``cache_kv`` the stack also keeps, per layer, the memory's projected keys
+and values: the memory rows and W_kE, W_v do not change at evaluation, so k and
+v of the memory are the ones projected when those states were the segment, and
+each segment projects only its own L rows (2·M·d² multiply-adds saved per layer
+and projection).  They live in windows of larger buffers [B·H, capacity, d_head]
+(txl_kv_window_append / _advance): the segment's rows are written behind the
+memory's and the attention reads [memory ; segment] in place, with no copy of
+the memory per segment.
 The relative table r = W_kR R is built from rel_pos_emb (kernel) and one matmul
 and is cached per (layer, K): R has no parameters and W_kR is fixed at
 evaluation.
 
 With ``graphs`` the stack replays each segment from a CUDA graph once the
 memories are full: every launch of a segment then has fixed shapes and
-pointers, and the ring heads come back to the same positions every
-M / gcd(M, L) segments, so one graph per ring position covers the stream (one
-graph when L is a multiple of M).  The host-side ring states advance exactly
-as the eager calls advance them.
+pointers, and the ring heads and window starts come back to the same positions
+periodically (every M / gcd(M, L) segments for the rings), so one graph per
+combination of positions covers the stream.  A capture records the states the
+eager calls leave behind, and a replay sets the host-side states to them.
 
 Torch is used here for the dense projections, LayerNorm and the feed-forward
 only; the attention, the positional table and the memory run in the CUDA
@@ -115,13 +113,59 @@ class XLStack:
         self.mems = [torch.zeros(B, self.M, self.d, dtype=self.dtype, device=self.device)
                      for _ in self.layers]
         self.states = [txl.MemState(0, 0, self.M) for _ in self.layers]
-        # projected memory: [B*H, M, dh] rings of k and v per layer, each with its
-        # own ring state (they advance exactly as the hidden-state ring)
-        ring = lambda: torch.zeros(B * self.H, self.M, self.dh, dtype=self.dtype, device=self.device)
-        self.kmems = [ring() for _ in self.layers] if self.cache_kv else None
-        self.vmems = [ring() for _ in self.layers] if self.cache_kv else None
-        self.kv_states = ([(txl.MemState(0, 0, self.M), txl.MemState(0, 0, self.M))
-                           for _ in self.layers] if self.cache_kv else None)
+        # projected memory: k and v of each layer in windows of [B*H, C, dh]
+        # buffers; capacity C = M + n*L with n the smallest multiple of the ring
+        # period M / gcd(M, L) that keeps C >= 2M + L (window positions then
+        # repeat with the rings')
+        self.kbufs = self.vbufs = self.kv_windows = None
+        self._kv_L = None
+
+    def _kv_reset(self, B: int, L: int):
+        period = self.M // math.gcd(self.M, L) if self.M > 0 else 1
+        n = period * max(1, -(-(self.M + L) // (period * L)))
+        C = self.M + n * L
+        buf = lambda: torch.zeros(B * self.H, C, self.dh, dtype=self.dtype, device=self.device)
+        self.kbufs = [buf() for _ in self.layers]
+        self.vbufs = [buf() for _ in self.layers]
+        self.kv_windows = [(txl.KVWindow(0, 0, C, self.M), txl.KVWindow(0, 0, C, self.M))
+                           for _ in self.layers]
+        self._kv_L = L
+        self._graphs = {}
+        self._full_segments = 0
+
+    def checkpoint(self) -> dict:
+        """Host copy of everything the stream carries from one segment to the
+        next (§3.2: the memory of each layer; with cache_kv also the windows of
+        projected keys and values), with the host-side ring and window states.
+        ``restore`` on a fresh stack continues the stream exactly."""
+        if self.mems is None:
+            raise RuntimeError("checkpoint: no segment has run yet")
+        torch.cuda.synchronize(self.device)
+        ck = {"mems": [m.cpu() for m in self.mems],
+              "states": [self._snap(st) for st in self.states], "kv": None}
+        if self.cache_kv and self.kbufs is not None:
+            ck["kv"] = {"L": self._kv_L, "k": [b.cpu() for b in self.kbufs],
+                        "v": [b.cpu() for b in self.vbufs],
+                        "windows": [(self._snap(a), self._snap(b)) for a, b in self.kv_windows]}
+        return ck
+
+    def restore(self, ck: dict):
+        """Load a ``checkpoint`` (same parameters, shapes and options)."""
+        B = ck["mems"][0].shape[0]
+        self.reset(B)
+        for mem, saved, st, snap in zip(self.mems, ck["mems"], self.states, ck["states"]):
+            mem.copy_(saved)
+            self._restore(st, snap)
+        if ck["kv"] is not None:
+            if not self.cache_kv:
+                raise ValueError("restore: the checkpoint holds key/value windows")
+            self._kv_reset(B, ck["kv"]["L"])
+            for buf, saved in zip(self.kbufs + self.vbufs, ck["kv"]["k"] + ck["kv"]["v"]):
+                buf.copy_(saved)
+            for (kw, vw), (ks, vs) in zip(self.kv_windows, ck["kv"]["windows"]):
+                self._restore(kw, ks)
+                self._restore(vw, vs)
+        torch.cuda.synchronize(self.device)
 
     def memories(self):
         """Each layer's memory in logical order (oldest first), [B, fill, d]."""
@@ -140,11 +184,21 @@ class XLStack:
                                                  self.H).to(self.dtype)
         return self._r_cache[key]
 
-    def _rings(self):
-        rings = list(self.states)
-        if self.cache_kv:
-            rings += [s for pair in self.kv_states for s in pair]
-        return rings
+    def _host_states(self):
+        """Every host-side memory state a segment advances (rings, windows)."""
+        sts = list(self.states)
+        if self.cache_kv and self.kv_windows is not None:
+            sts += [w for pair in self.kv_windows for w in pair]
+        return sts
+
+    @staticmethod
+    def _snap(st):
+        return tuple(getattr(st, f) for f, _ in st._fields_)
+
+    @staticmethod
+    def _restore(st, snap):
+        for (f, _), v in zip(st._fields_, snap):
+            setattr(st, f, v)
 
     def segment(self, tokens: torch.Tensor) -> torch.Tensor:
         """One segment [B, L] -> the top layer's states [B, L, d].  With graphs
@@ -153,6 +207,8 @@ class XLStack:
         B, L = tokens.shape
         if self.mems is None or self.mems[0].shape[0] != B:
             self.reset(B)
+        if self.cache_kv and (self.kbufs is None or self._kv_L != L):
+            self._kv_reset(B, L)
         full = self.M > 0 and self.states[0].fill == self.M
         # capture only after one eager segment at full memory (warm-up of the
         # library's and torch's lazily set-up state for these shapes)
@@ -160,9 +216,9 @@ class XLStack:
             if full:
                 self._full_segments += 1
             return self._segment(tokens.to(self.device))
-        key = self.states[0].head
+        sts = self._host_states()
+        key = tuple(self._snap(st) for st in sts)
         if key not in self._graphs:
-            saved = [(st.head, st.fill) for st in self._rings()]
             tok = torch.empty(B, L, dtype=torch.long, device=self.device)
             tok.copy_(tokens)
             graph = torch.cuda.CUDAGraph()
@@ -170,17 +226,18 @@ class XLStack:
                 self._pool = torch.cuda.graph_pool_handle()
             with torch.cuda.graph(graph, pool=self._pool):
                 out = self._segment(tok)
-            # capture recorded the launches without running them: put the ring
-            # states back; the replay below runs the segment
-            for st, (head, fill) in zip(self._rings(), saved):
-                st.head, st.fill = head, fill
-            self._graphs[key] = (graph, tok, out)
-        graph, tok, out = self._graphs[key]
+            # capture recorded the launches without running them: keep the
+            # states the calls left behind for every replay, put the current
+            # ones back; the replay below runs the segment
+            after = [self._snap(st) for st in sts]
+            for st, snap in zip(sts, key):
+                self._restore(st, snap)
+            self._graphs[key] = (graph, tok, out, after)
+        graph, tok, out, after = self._graphs[key]
         tok.copy_(tokens)
         graph.replay()
-        for st in self._rings():  # what the eager mem_update calls do on the host
-            st.fill = min(st.fill + L, st.capacity)
-            st.head = (st.head + L) % st.capacity
+        for st, snap in zip(sts, after):
+            self._restore(st, snap)
         return out
 
     def _segment(self, tokens: torch.Tensor) -> torch.Tensor:
@@ -191,12 +248,15 @@ class XLStack:
             M_cur = st.fill
             q = project_heads(h, lay["W_q"], self.H)
             if self.cache_kv:
-                # only the segment's rows are projected; the memory's come from the rings
-                ks, vs = self.kv_states[n]
+                # only the segment's rows are projected, written behind the
+                # memory's in the windows; attention reads both in place
+                kw, vw = self.kv_windows[n]
                 k_new = project_heads(h, lay["W_kE"], self.H).view(B * self.H, L, self.dh)
                 v_new = project_heads(h, lay["W_v"], self.H).view(B * self.H, L, self.dh)
-                k = txl.mem_concat(self.kmems[n], ks, k_new).view(B, self.H, M_cur + L, self.dh)
-                v = txl.mem_concat(self.vmems[n], vs, v_new).view(B, self.H, M_cur + L, self.dh)
+                txl.kv_window_append(self.kbufs[n], kw, k_new)
+                txl.kv_window_append(self.vbufs[n], vw, v_new)
+                k = txl.kv_window_view(self.kbufs[n], kw, L, B, self.H)
+                v = txl.kv_window_view(self.vbufs[n], vw, L, B, self.H)
             else:
                 ext = txl.mem_concat(self.mems[n], st, h)
                 k = project_heads(ext, lay["W_kE"], self.H)
@@ -213,7 +273,7 @@ class XLStack:
                                   "M": M_cur, "a": a_heads, "h_out": h_next.to(self.dtype)})
             txl.mem_update(self.mems[n], st, h)
             if self.cache_kv:
-                txl.mem_update(self.kmems[n], ks, k_new)
-                txl.mem_update(self.vmems[n], vs, v_new)
+                txl.kv_window_advance(kw, L)
+                txl.kv_window_advance(vw, L)
             h = h_next.to(self.dtype)
         return h
