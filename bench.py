@@ -109,7 +109,9 @@ def parse_args():
     ap.add_argument("--shapes", nargs="*", default=None,
                     help="with --decode: B,L,M triples (default: the long-memory decode set)")
     ap.add_argument("--calls", type=int, default=10,
-                    help="with --decode: graph replays timed per shape (30 calls each)")
+                    help="with --decode or --configs: graph replays timed per shape (30 calls each)")
+    ap.add_argument("--workload", nargs="*", default=None,
+                    help="with --configs: only these workloads (names as in txl_inputs.WORKLOADS)")
     return ap.parse_args()
 
 
@@ -778,6 +780,8 @@ def run_configs(args):
     for name, w in txl_inputs.WORKLOADS.items():
         if w.dtype != "bf16" or name.startswith("c5"):
             continue  # c5 is the stack; its attention call is c2's shape
+        if args.workload and name not in args.workload:
+            continue
         K = w.M + w.L
         nbytes = 2 * (2 * w.B * w.H * w.L * 64 + 2 * w.B * w.H * K * 64 + w.H * K * 64)
         n_sets = max(1, min(3, -(-3 * 126 * 2 ** 20 // nbytes)))

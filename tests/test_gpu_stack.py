@@ -166,13 +166,11 @@ def test_cached_kv_windows_match_projected_memory():
     starts = set()
     for s in range(w.n_seg):
         stack.segment(params["tokens"][s])
-        starts.add(stack.kv_windows[0][0].start)
+        starts.add(stack.kv_windows[0].start)
     assert 0 in starts and len(starts) > 2
     for n, (mem, lay) in enumerate(zip(stack.memories(), stack.layers)):
-        kw, vw = stack.kv_windows[n]
-        assert kw.fill == vw.fill == w.M
-        k_win = stack.kbufs[n][:, kw.start:kw.start + kw.fill].reshape(w.B, w.H, -1, w.dh)
-        v_win = stack.vbufs[n][:, vw.start:vw.start + vw.fill].reshape(w.B, w.H, -1, w.dh)
+        assert stack.kv_windows[n].fill == w.M
+        k_win, v_win = stack.kv_memory(n)
         k_mem = project_heads(mem, lay["W_kE"], w.H)
         v_mem = project_heads(mem, lay["W_v"], w.H)
         # the same bf16 products, possibly summed in another order by the GEMM
@@ -202,7 +200,7 @@ def test_graph_replayed_stack_matches_eager(L, M, cache_kv):
     # every (C - M - L) / L + 1, a multiple of that
     expected = M // math.gcd(M, L)
     if cache_kv:
-        C = graphed.kv_windows[0][0].capacity
+        C = graphed.kv_windows[0].capacity
         expected = (C - M - L) // L + 1
         assert expected % (M // math.gcd(M, L)) == 0
     assert len(graphed._graphs) == expected

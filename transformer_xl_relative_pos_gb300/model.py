@@ -3,7 +3,8 @@
 "Transformer-XL: Attentive Language Models Beyond a Fixed-Length Context",
 §3.3 N-layer summary, for n = 1..N:
     h~  = [SG(m^{n-1}) o h^{n-1}]                      -> mem_concat (kernel)
-    q, k, v = h W_q^T, h~ W_kE^T, h~ W_v^T             -> torch matmul
+    q, k, v = h W_q^T, h~ W_kE^T, h~ W_v^T             -> torch matmul (one
+                                                           GEMM per operand set)
     a   = Masked-Softmax(A) v                           -> relattn_fwd (kernel)
     o   = LayerNorm(Linear(a) + h^{n-1})                -> torch
     h^n = Positionwise-Feed-Forward(o)                  -> torch (ReLU MLP,
@@ -14,10 +15,11 @@ With ``cache_kv`` the stack also keeps, per layer, the memory's projected keys
 and values: the memory rows and W_kE, W_v do not change at evaluation, so k and
 v of the memory are the ones projected when those states were the segment, and
 each segment projects only its own L rows (2·M·d² multiply-adds saved per layer
-and projection).  They live in windows of larger buffers [B·H, capacity, d_head]
-(txl_kv_window_append / _advance): the segment's rows are written behind the
-memory's and the attention reads [memory ; segment] in place, with no copy of
-the memory per segment.
+and projection); q, k and v of the segment come from one GEMM.  Keys and values
+of a layer live in one window of a buffer [2·B·H, capacity, d_head] (the keys'
+planes, then the values'; txl_kv_window_append / _advance): the segment's rows
+are written behind the memory's and the attention reads [memory ; segment] in
+place, with no copy of the memory per segment.
 The relative table r = W_kR R is built from rel_pos_emb (kernel) and one matmul
 and is cached per (layer, K): R has no parameters and W_kR is fixed at
 evaluation.
@@ -50,6 +52,14 @@ def project_heads(x: torch.Tensor, W: torch.Tensor, H: int) -> torch.Tensor:
     B, T, _ = x.shape
     y = x @ W.t()
     return y.view(B, T, H, -1).transpose(1, 2).contiguous()
+
+
+def project_stacked(x: torch.Tensor, W: torch.Tensor, n: int, H: int) -> torch.Tensor:
+    """x [B, T, d] times W^T for W = [W_1; ...; W_n] (each [H*dh, d]) in one
+    GEMM -> contiguous [n, B, H, T, dh] (operand i at index i)."""
+    B, T, _ = x.shape
+    y = x @ W.t()
+    return y.view(B, T, n, H, -1).permute(2, 0, 3, 1, 4).contiguous()
 
 
 def rel_table_heads(R_rev: torch.Tensor, W_kR: torch.Tensor, H: int) -> torch.Tensor:
@@ -95,6 +105,11 @@ class XLStack:
         self.u = to(params["u"])
         self.v_bias = to(params["v_bias"])
         self.layers = [{k: to(v) for k, v in lay.items()} for lay in params["layers"]]
+        for lay in self.layers:
+            # stacked projection weights: q, k, v of the segment (cached k/v) or
+            # k, v of the extended context (re-projection) in one GEMM
+            lay["W_qkv"] = torch.cat([lay["W_q"], lay["W_kE"], lay["W_v"]]).contiguous()
+            lay["W_kv"] = torch.cat([lay["W_kE"], lay["W_v"]]).contiguous()
         self.d = self.emb.shape[1]
         self.dh = self.u.shape[1]
         self.scale = 1.0 / math.sqrt(self.dh)
@@ -113,22 +128,20 @@ class XLStack:
         self.mems = [torch.zeros(B, self.M, self.d, dtype=self.dtype, device=self.device)
                      for _ in self.layers]
         self.states = [txl.MemState(0, 0, self.M) for _ in self.layers]
-        # projected memory: k and v of each layer in windows of [B*H, C, dh]
-        # buffers; capacity C = M + n*L with n the smallest multiple of the ring
-        # period M / gcd(M, L) that keeps C >= 2M + L (window positions then
-        # repeat with the rings')
-        self.kbufs = self.vbufs = self.kv_windows = None
+        # projected memory: k and v of each layer in one window of a
+        # [2*B*H, C, dh] buffer; capacity C = M + n*L with n the smallest
+        # multiple of the ring period M / gcd(M, L) that keeps C >= 2M + L
+        # (window positions then repeat with the rings')
+        self.kvbufs = self.kv_windows = None
         self._kv_L = None
 
     def _kv_reset(self, B: int, L: int):
         period = self.M // math.gcd(self.M, L) if self.M > 0 else 1
         n = period * max(1, -(-(self.M + L) // (period * L)))
         C = self.M + n * L
-        buf = lambda: torch.zeros(B * self.H, C, self.dh, dtype=self.dtype, device=self.device)
-        self.kbufs = [buf() for _ in self.layers]
-        self.vbufs = [buf() for _ in self.layers]
-        self.kv_windows = [(txl.KVWindow(0, 0, C, self.M), txl.KVWindow(0, 0, C, self.M))
-                           for _ in self.layers]
+        self.kvbufs = [torch.zeros(2 * B * self.H, C, self.dh, dtype=self.dtype, device=self.device)
+                       for _ in self.layers]
+        self.kv_windows = [txl.KVWindow(0, 0, C, self.M) for _ in self.layers]
         self._kv_L = L
         self._graphs = {}
         self._full_segments = 0
@@ -143,10 +156,9 @@ class XLStack:
         torch.cuda.synchronize(self.device)
         ck = {"mems": [m.cpu() for m in self.mems],
               "states": [self._snap(st) for st in self.states], "kv": None}
-        if self.cache_kv and self.kbufs is not None:
-            ck["kv"] = {"L": self._kv_L, "k": [b.cpu() for b in self.kbufs],
-                        "v": [b.cpu() for b in self.vbufs],
-                        "windows": [(self._snap(a), self._snap(b)) for a, b in self.kv_windows]}
+        if self.cache_kv and self.kvbufs is not None:
+            ck["kv"] = {"L": self._kv_L, "bufs": [b.cpu() for b in self.kvbufs],
+                        "windows": [self._snap(w) for w in self.kv_windows]}
         return ck
 
     def restore(self, ck: dict):
@@ -160,11 +172,10 @@ class XLStack:
             if not self.cache_kv:
                 raise ValueError("restore: the checkpoint holds key/value windows")
             self._kv_reset(B, ck["kv"]["L"])
-            for buf, saved in zip(self.kbufs + self.vbufs, ck["kv"]["k"] + ck["kv"]["v"]):
+            for buf, saved in zip(self.kvbufs, ck["kv"]["bufs"]):
                 buf.copy_(saved)
-            for (kw, vw), (ks, vs) in zip(self.kv_windows, ck["kv"]["windows"]):
-                self._restore(kw, ks)
-                self._restore(vw, vs)
+            for w, snap in zip(self.kv_windows, ck["kv"]["windows"]):
+                self._restore(w, snap)
         torch.cuda.synchronize(self.device)
 
     def memories(self):
@@ -175,6 +186,14 @@ class XLStack:
             empty = torch.empty(B, 0, self.d, dtype=self.dtype, device=self.device)
             out.append(txl.mem_concat(mem, st, empty))
         return out
+
+    def kv_memory(self, n: int):
+        """Layer n's cached projected memory (cache_kv): keys and values
+        [B, H, fill, dh], views into its window buffer."""
+        w = self.kv_windows[n]
+        kv = self.kvbufs[n][:, w.start:w.start + w.fill]
+        kv = kv.view(2, -1, self.H, w.fill, self.dh)
+        return kv[0], kv[1]
 
     def _r(self, n: int, K: int) -> torch.Tensor:
         key = (n, K)
@@ -188,7 +207,7 @@ class XLStack:
         """Every host-side memory state a segment advances (rings, windows)."""
         sts = list(self.states)
         if self.cache_kv and self.kv_windows is not None:
-            sts += [w for pair in self.kv_windows for w in pair]
+            sts += self.kv_windows
         return sts
 
     @staticmethod
@@ -207,7 +226,7 @@ class XLStack:
         B, L = tokens.shape
         if self.mems is None or self.mems[0].shape[0] != B:
             self.reset(B)
-        if self.cache_kv and (self.kbufs is None or self._kv_L != L):
+        if self.cache_kv and (self.kvbufs is None or self._kv_L != L):
             self._kv_reset(B, L)
         full = self.M > 0 and self.states[0].fill == self.M
         # capture only after one eager segment at full memory (warm-up of the
@@ -246,21 +265,22 @@ class XLStack:
         for n, lay in enumerate(self.layers):
             st = self.states[n]
             M_cur = st.fill
-            q = project_heads(h, lay["W_q"], self.H)
             if self.cache_kv:
-                # only the segment's rows are projected, written behind the
-                # memory's in the windows; attention reads both in place
-                kw, vw = self.kv_windows[n]
-                k_new = project_heads(h, lay["W_kE"], self.H).view(B * self.H, L, self.dh)
-                v_new = project_heads(h, lay["W_v"], self.H).view(B * self.H, L, self.dh)
-                txl.kv_window_append(self.kbufs[n], kw, k_new)
-                txl.kv_window_append(self.vbufs[n], vw, v_new)
-                k = txl.kv_window_view(self.kbufs[n], kw, L, B, self.H)
-                v = txl.kv_window_view(self.vbufs[n], vw, L, B, self.H)
+                # only the segment's rows are projected (q, k, v in one GEMM);
+                # k and v are written behind the memory's in the window and the
+                # attention reads both in place
+                kw = self.kv_windows[n]
+                qkv = project_stacked(h, lay["W_qkv"], 3, self.H)
+                q = qkv[0]
+                txl.kv_window_append(self.kvbufs[n], kw, qkv[1:].view(2 * B * self.H, L, self.dh))
+                kv = txl.kv_window_view(self.kvbufs[n], kw, L, 2 * B, self.H)
+                kv = kv.view(2, B, self.H, -1, self.dh)
+                k, v = kv[0], kv[1]
             else:
+                q = project_heads(h, lay["W_q"], self.H)
                 ext = txl.mem_concat(self.mems[n], st, h)
-                k = project_heads(ext, lay["W_kE"], self.H)
-                v = project_heads(ext, lay["W_v"], self.H)
+                kv = project_stacked(ext, lay["W_kv"], 2, self.H)
+                k, v = kv[0], kv[1]
             r = self._r(n, M_cur + L)
             a_heads = txl.relattn_fwd(q, k, v, r, self.u, self.v_bias, M_cur, self.scale)
             a = a_heads.transpose(1, 2).reshape(B, L, -1)
@@ -274,6 +294,5 @@ class XLStack:
             txl.mem_update(self.mems[n], st, h)
             if self.cache_kv:
                 txl.kv_window_advance(kw, L)
-                txl.kv_window_advance(vw, L)
             h = h_next.to(self.dtype)
         return h
