@@ -64,8 +64,8 @@ import txl_inputs  # noqa: E402
 PROFILED_TRAFFIC = {
     "workload": "c3_word_large_L128_M1600",
     "sources": ("relattn_tc.cu", "ptx.cuh", "kernels.h"),
-    "sha256": "718faf4db13841ca2b315f4bdad07e22c0c7a2f07835fc699c2e75da18ca31b5",
-    "bytes_per_launch": 121107712 + 2742016,
+    "sha256": "10af1cd26231feb98175aa8b69ea255436175eeed89233452dbd7c85e0294582",
+    "bytes_per_launch": 121095424 + 2810880,
 }
 
 
