@@ -110,7 +110,7 @@ __device__ __forceinline__ uint32_t split_bf16x2(float x0, float x1, uint32_t &r
 }
 
 template <int L>
-__global__ void __launch_bounds__(WARPS * 32)
+__global__ void __launch_bounds__(WARPS * 32, 2)
     relattn_decode_mma_kernel(const __grid_constant__ CUtensorMap tm_k,
                               const __grid_constant__ CUtensorMap tm_v,
                               const __grid_constant__ CUtensorMap tm_r, const DecodeParams p)
