@@ -73,7 +73,8 @@ def test_small_stack_memory_fill_and_wrap(cache_kv):
 # Through N layers the residual stream carries each layer's error forward with a
 # gain near 1 (LayerNorm of o + f, both O(1)); independent roundings add like a
 # random walk, so N = 12 layers stay within 1e-1 at the maximum (sqrt(12) times
-# the one-layer bound is 9e-2) and 2e-2 in rms (12 times the one-layer rms bound).
+# the one-layer bound is 9e-2) and 2e-2 in rms (sqrt(12) times the one-layer rms
+# bound is 1.7e-2).
 LAYER_INTERNAL = 1e-2
 LAYER_RMS = 5e-3
 
