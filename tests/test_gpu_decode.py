@@ -89,6 +89,23 @@ def test_decode_full_memory(L):
     check(case, M, what=f"M=3800 L={L}")
 
 
+@pytest.mark.parametrize("B,L,M", [(32, 4, 3800), (64, 6, 3800), (24, 1, 3800), (48, 8, 1600)])
+def test_decode_large_batch_sampled_heads(B, L, M):
+    # Many sequences: one key range per head and several waves of blocks; every
+    # 29th head (of B x 16) is checked against the oracle.
+    H = 16
+    case = heads_case(B, H, L, M, seed=6000 + B + L)
+    scale = 1.0 / math.sqrt(64)
+    out, lse = run_gpu(case, M, scale)
+    bh = list(range(0, B * H, 29))
+    want_o, want_lse = run_oracle(case, M, scale, bh=bh)
+    got, got_lse = out.float().cpu().numpy(), lse.cpu().numpy()
+    for p in bh:
+        b, h = divmod(p, H)
+        compare(got[b, h], want_o[b, h], TOL, TOL_RMS, what=f"B={B} L={L} M={M} b={b} h={h}")
+        compare(got_lse[b, h], want_lse[b, h], TOL_LSE, what=f"lse B={B} L={L} b={b} h={h}")
+
+
 def test_decode_repeatable():
     B, H, L, M = 2, 2, 3, 2000
     case = heads_case(B, H, L, M, seed=9)

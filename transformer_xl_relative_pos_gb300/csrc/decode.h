@@ -8,10 +8,10 @@ namespace txl {
 
 // Short-segment (decode) kernels: L <= kDecodeMaxL queries per (batch, head);
 // the keys are split into n_splits ranges of whole 32-key chunks.  The
-// tensor-core kernel takes every L up to kDecodeMaxL, the CUDA-core kernel up
-// to kDecodeFmaMaxL.
+// CUDA-core kernel takes L <= kDecodeFmaMaxL (one query: its per-key arithmetic
+// grows with L), the warp-MMA kernel the rest.
 constexpr int kDecodeMaxL = 8;
-constexpr int kDecodeFmaMaxL = 6;
+constexpr int kDecodeFmaMaxL = 1;
 constexpr int kDecodeMaxCluster = 8;  // portable cluster size
 // Tensor maps of the tensor-core kernel: k and v [B*H planes][K][64] read in
 // boxes of 32 rows, the table [H][r_rows][64] in boxes of 40 rows (the 32 + L - 1

@@ -1,6 +1,6 @@
-// Relative-position attention for short segments (L <= 6 queries) against a
-// long memory: the decode pattern of generation, one or a few new tokens per
-// step attending to the cached M states ("Transformer-XL: Attentive Language
+// Relative-position attention for one new query (L = 1; the kernel is written
+// for any small L) against a long memory: the decode pattern of generation,
+// one new token per step attending to the cached M states ("Transformer-XL: Attentive Language
 // Models Beyond a Fixed-Length Context", §3.2 recurrence and evaluation with a
 // long memory, §3.3 score, Appendix B reversed table).
 //
@@ -25,7 +25,8 @@
 // block's warps merge their partial results
 // and the block writes the output, or its key range's normalised partial and
 // log2-sum-exp for the merge kernel.  The per-key work grows with L while the
-// bytes do not: from L = 7 on the tensor-core kernel is the faster path.
+// bytes do not: from L = 2 on the warp-MMA kernel (relattn_decode_mma.cu) is
+// the faster path, so only L = 1 is instantiated.
 #include "decode_common.cuh"
 
 #include <utility>

@@ -162,14 +162,13 @@ int tc_splits(int B, int H, int L, int dh, int n_qtiles, int n_key_tiles, int n_
     return splits;
 }
 
-// Which decode kernel a segment of L queries runs: the tensor-core one from
-// kDecodeMmaFromL queries on, the CUDA-core one below.  One query is the CUDA-core
-// kernel's best case (eight sequences of 16 heads against M = 3800: 22.2 against
-// 23.5 us); from two on the tensor-core kernel is faster (24.3 against 23.6 us)
-// and its time hardly grows with L (23.6 to 24.8 us for L = 2..7, where the
-// CUDA-core kernel goes to 44.9 us at L = 6).
-constexpr int kDecodeMmaFromL = 2;
-bool decode_on_mma(int L) { return L >= kDecodeMmaFromL || L > txl::kDecodeFmaMaxL; }
+// Which decode kernel a segment of L queries runs: the CUDA-core one for
+// L <= kDecodeFmaMaxL (one query), the warp-MMA one above.  One query is the
+// CUDA-core kernel's best case (eight sequences of 16 heads against M = 3800:
+// 22.2 against 23.5 us); from two on the warp-MMA kernel is faster (24.3
+// against 23.6 us) and its time hardly grows with L (23.6 to 24.8 us for
+// L = 2..7, where the CUDA-core kernel went to 44.9 us at L = 6).
+bool decode_on_mma(int L) { return L > txl::kDecodeFmaMaxL; }
 
 int decode_blocks(int L)
 {
