@@ -504,26 +504,43 @@ def run_ours(args, world, rank, local):
             "q": base["q"].clone(), "k": base["k"].clone(), "v": base["v"].clone(),
             "h": base["h"].clone(), "mem": base["mem"].clone(),
             "out": torch.empty_like(base["q"]),
+            "out2": torch.empty_like(base["q"]),  # for steps of the second chain
             "st": txl.MemState(0, w.M, w.M),
         })
     r, u, vb = base["r"], base["u"], base["v_bias"]
     del base
     torch.cuda.synchronize()
 
-    # The memory update of a step is independent of its attention (it reads the
-    # segment's h and writes the ring; the attention reads q, k, v and r), so it
-    # runs on a second stream forked before the attention: its blocks take the
-    # SMs that the attention's last wave leaves idle.  Captured into the step
-    # graph as a fork and a join.
+    # Consecutive steps are independent batches (rotating input sets), so the
+    # step graph runs them as two chains of attentions on two streams, steps
+    # alternating: one step's first wave of blocks takes the SMs the other's
+    # last wave leaves idle (256 blocks on 152 SMs).  The memory update of a step
+    # is independent of its attention (it reads the segment's h and writes the
+    # ring; the attention reads q, k, v and r) and runs on a third stream.  Each
+    # step is forked from the launching stream; the graph joins every chain at
+    # its end.  A dependent chain of calls (one layer's attention feeding the
+    # next) gets none of this overlap: the line also reports the same steps on
+    # one stream ("one_stream").
+    chains = [torch.cuda.Stream(dev), torch.cuda.Stream(dev)]
+    ws2 = torch.empty_like(ws)  # the second chain's split-key scratch
     side = torch.cuda.Stream(dev)
     forks = [torch.cuda.Event() for _ in range(N_SETS)]
 
-    def step(i):
+    def step(i, streams=2):
         s = sets[i % N_SETS]
         fork = forks[i % N_SETS]
-        fork.record(torch.cuda.current_stream(dev))
-        txl.relattn_fwd(s["q"], s["k"], s["v"], r, u, vb, w.M, scale, out=s["out"], workspace=ws)
+        main = torch.cuda.current_stream(dev)
+        fork.record(main)
+        att = chains[i % 2] if streams == 2 else main
+        att.wait_event(fork)
         side.wait_event(fork)
+        # each chain writes its own outputs (steps i and i + 3 share an input
+        # set and may run at the same time on the two chains)
+        second = streams == 2 and i % 2 == 1
+        out = s["out2"] if second else s["out"]
+        with torch.cuda.stream(att):
+            txl.relattn_fwd(s["q"], s["k"], s["v"], r, u, vb, w.M, scale, out=out,
+                            workspace=ws2 if second else ws)
         with torch.cuda.stream(side):
             txl.mem_update(s["mem"], s["st"], s["h"])
 
@@ -534,7 +551,8 @@ def run_ours(args, world, rank, local):
 
     for i in range(max(args.warmup, 3)):
         step(i)
-    torch.cuda.current_stream(dev).wait_stream(side)
+    for s_ in chains + [side]:
+        torch.cuda.current_stream(dev).wait_stream(s_)
     torch.cuda.synchronize()
     assert txl.device_status() == 0
 
@@ -545,20 +563,22 @@ def run_ours(args, world, rank, local):
         chunk = GRAPH_CHUNK
         reps = max(1, round(K / GRAPH_CHUNK))
         K = chunk * reps
-    def capture():
+    def capture(streams):
         g = torch.cuda.CUDAGraph()
         cap_stream = torch.cuda.Stream(dev)
         cap_stream.wait_stream(torch.cuda.current_stream(dev))
-        side.wait_stream(cap_stream)
+        for s_ in chains + [side]:
+            s_.wait_stream(cap_stream)
         with torch.cuda.stream(cap_stream):
             with torch.cuda.graph(g, stream=cap_stream):
                 for i in range(chunk):
-                    step(i)
-                cap_stream.wait_stream(side)  # join the memory updates
+                    step(i, streams)
+                for s_ in (chains if streams == 2 else []) + [side]:
+                    cap_stream.wait_stream(s_)  # join every chain
         torch.cuda.current_stream(dev).wait_stream(cap_stream)
         return g
 
-    g = capture()
+    g = capture(2)
     g.replay()  # untimed replay: graph upload and warm caches
     torch.cuda.synchronize()
 
@@ -608,6 +628,20 @@ def run_ours(args, world, rank, local):
     attn_ms = a_.elapsed_time(b_) / n_attn
     del ga
 
+    # The same K steps on one stream (each step's attention after the previous
+    # one's), timed the same way: what a chain of dependent calls gets.
+    g1 = capture(1)
+    g1.replay()
+    torch.cuda.synchronize()
+    a_, b_ = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    a_.record(stream)
+    for _ in range(reps):
+        g1.replay()
+    b_.record(stream)
+    torch.cuda.synchronize()
+    one_ms = max_over_ranks(a_.elapsed_time(b_), world)
+    del g1
+
     # The sinusoid table kernel, per layer (outside the step): graph-replayed.
     R_buf = torch.empty(w.K, w.d_model, dtype=torch.float32, device=dev)
     gr = torch.cuda.CUDAGraph()
@@ -630,6 +664,9 @@ def run_ours(args, world, rank, local):
 
     flops_step = w.flops()
     value = flops_step * K * world / (t_ms * 1e-3) / 1e12
+    one_stream = {"ms_per_step": one_ms / K,
+                  "value": flops_step * K * world / (one_ms * 1e-3) / 1e12, "unit": "TFLOP/s",
+                  "note": "the same steps with every attention on one stream, one after another"}
     tokens = w.B * w.L * K * world / (t_ms * 1e-3)
     # "useful" work: only the scores a query may see (j <= M + i), i.e.
     # L*M + L(L+1)/2 of the L*K pairs per head
@@ -662,15 +699,18 @@ def run_ours(args, world, rank, local):
         "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
         "config": {"workload": w.name, "B": w.B, "H": w.H, "L": w.L, "M": w.M, "K": w.K,
                    "dh": w.dh, "d_model": w.d_model,
-                   "step": "relattn_fwd + mem_update, the memory update on a second stream "
-                           "concurrent with the attention (table R and r built once per layer, "
-                           "outside the step)",
+                   "step": "relattn_fwd + mem_update over one batch (table R and r built once "
+                           "per layer, outside the step)",
+                   "streams": "steps are independent batches: their attentions alternate between "
+                              "two streams (one step's first wave fills the SMs the other's last "
+                              "wave leaves idle), memory updates on a third",
                    "l2": f"{N_SETS} rotating input sets (>2x L2 of traffic between reuses)",
                    "launch": f"CUDA graph of {chunk} steps x {reps} replays"},
         "tokens_per_s": tokens,
         "pct_bf16_peak": 100.0 * value / pk["bf16_tflops"],
         "useful_tflops": value * visible,
         "attn_us": attn_ms * 1e3,
+        "one_stream": one_stream,
         "rel_pos_emb_us": relpos_us,
         "clocks": clocks,
         "e2e": e2e,

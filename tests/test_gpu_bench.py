@@ -30,6 +30,10 @@ def test_bench_line_contract_and_end_to_end_leg():
     # memory update; the table is built once per layer, outside the step
     assert line["gpu_launches"] >= 2 * line["steps"]
     assert line["rel_pos_emb_us"] > 0
+    # the same steps with all attentions on one stream are reported beside the
+    # two-chain figure (consecutive steps are independent batches)
+    one = line["one_stream"]
+    assert one["value"] > 0 and one["ms_per_step"] > 0
     roof = line["roofline"]
     assert roof["kernel"] == "relattn_fwd_tc_kernel" and 0 < roof["frac"] and roof["peak"] > 0
     e2e = line["e2e"]
