@@ -106,6 +106,15 @@ def test_decode_large_batch_sampled_heads(B, L, M):
         compare(got_lse[b, h], want_lse[b, h], TOL_LSE, what=f"lse B={B} L={L} b={b} h={h}")
 
 
+@pytest.mark.parametrize("L,M", [(8, 12000), (3, 20000), (1, 20000)])
+def test_decode_very_long_memory(L, M):
+    # One sequence against a memory far past the evaluation lengths: hundreds of
+    # 32-key chunks per key range.
+    B, H = 1, 4
+    case = heads_case(B, H, L, M, seed=7000 + L)
+    check(case, M, what=f"long memory L={L} M={M}")
+
+
 def test_decode_repeatable():
     B, H, L, M = 2, 2, 3, 2000
     case = heads_case(B, H, L, M, seed=9)

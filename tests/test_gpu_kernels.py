@@ -167,6 +167,20 @@ def test_relattn_bf16_merge_is_repeatable():
         assert torch.equal(a, run_gpu(case, M, 0.125, n_splits=5, want_lse=False))
 
 
+@pytest.mark.parametrize("L,M,n_splits", [(128, 8000, 0), (200, 8000, 5), (130, 12000, 1)])
+def test_relattn_bf16_long_memory(L, M, n_splits):
+    # Long memories (the evaluation of §3.2 with M in the thousands): 64 to 95 key
+    # tiles per query tile, over one block, the automatic split and an explicit
+    # one merged through the workspace.
+    B, H = 1, 2
+    case = heads_case(B, H, L, M, seed=800 + M // 1000 + L)
+    out, lse = run_gpu(case, M, 0.125, n_splits=n_splits)
+    want, want_lse = run_oracle(case, M, 0.125)
+    what = f"long memory L={L} M={M} splits {n_splits}"
+    compare(out.float().cpu().numpy(), want, TOL_BF16, TOL_BF16_RMS, what=what)
+    compare(lse.cpu().numpy(), want_lse, TOL_BF16, what="lse " + what)
+
+
 def test_relattn_bf16_longer_table():
     # A table built for a longer memory: only its last K rows are used.
     B, H, L, M = 1, 2, 128, 200
