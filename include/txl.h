@@ -318,6 +318,36 @@ int txl_kv_window_append(void *buf, txl_kv_window *w, const void *seg, int plane
 int txl_kv_window_advance(txl_kv_window *w, int L);
 
 /*
+ * txl_qkv_project - one layer's projections for a segment, written where the
+ * attention reads them, with the memory update in the same launch ("Transformer-XL:
+ * Attentive Language Models Beyond a Fixed-Length Context", §3.3 N-layer
+ * summary: q = h W_q^T and k, v = h~ W_kE^T, h~ W_v^T, of which only the
+ * segment's rows are new when the memory's k and v are kept in a window; §3.2:
+ * the memory takes the newest states).  One GEMM, Y = h W^T over the stacked
+ * weights, on the tensor cores (bf16 in, fp32 accumulate, bf16 out), whose
+ * epilogue writes
+ *   q      [B][H][L][dh]                               (when q != NULL)
+ *   k, v   rows start + fill .. start + fill + L - 1 of the window planes of
+ *          kv_buf: keys in planes 0 .. B*H-1, values in planes B*H .. 2*B*H-1
+ *          ([2*B*H][capacity][dh], plane = b*H + h), exactly as
+ *          txl_kv_window_append would place them (moving the memory rows to
+ *          the buffer's front first when needed; updates kv_win->start)
+ *   mem    the memory ring [B][capacity][d_model] advanced as txl_mem_update
+ *          would (when mem != NULL; updates *mem_st)
+ * h [B][L][d_model]; w [n_out * H * dh][d_model] with n_out = 3 (rows W_q,
+ * W_kE, W_v, head-major inside each) when q != NULL, else 2 (W_kE, W_v).
+ * All bf16, dense, 16-byte aligned; dh must be 64 and d_model a multiple of 8.
+ * The caller owns every buffer and both states (host memory).  Asynchronous on
+ * `stream`.  Errors: TXL_ERR_INVALID_ARG (NULL h, w, kv_buf or kv_win, bad
+ * sizes or states, mem without mem_st), TXL_ERR_UNSUPPORTED (dh != 64),
+ * TXL_ERR_SHAPE (window capacity < 2M + L, ring row width), TXL_ERR_MISALIGNED,
+ * TXL_ERR_CUDA; the states are unchanged on error.
+ */
+int txl_qkv_project(const void *h, const void *w, int B, int L, int d_model, int H, int dh,
+                    void *q, void *kv_buf, txl_kv_window *kv_win, void *mem,
+                    txl_mem_state *mem_st, void *stream);
+
+/*
  * txl_device_status - synchronise `stream`, then read and clear the device
  * status word in which kernels record barrier time-outs (and, in a debug
  * build, failed index checks).  Returns TXL_OK, TXL_ERR_TIMEOUT (a time-out was

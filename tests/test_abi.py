@@ -253,3 +253,31 @@ def test_kv_window_validation():
     w = txl.KVWindow(150, 50, 200, 50)
     assert L().txl_kv_window_advance(ctypes.byref(w), 8) == SHAPE
     assert (w.start, w.fill) == (150, 50)
+
+
+def test_qkv_project_validation():
+    # Host checks only (every case is refused or a no-op before any launch).
+    w = txl.KVWindow(0, 0, 200, 50)
+    st = txl.MemState(0, 0, 50)
+    f = L().txl_qkv_project
+    # null h / w / kv_buf / window, bad sizes, mem without its state
+    assert f(None, 16, 2, 8, 64, 2, 64, 16, 16, ctypes.byref(w), None, None, None) == INVALID
+    assert f(16, None, 2, 8, 64, 2, 64, 16, 16, ctypes.byref(w), None, None, None) == INVALID
+    assert f(16, 16, 2, 8, 64, 2, 64, 16, None, ctypes.byref(w), None, None, None) == INVALID
+    assert f(16, 16, 2, 8, 64, 2, 64, 16, 16, None, None, None, None) == INVALID
+    assert f(16, 16, 0, 8, 64, 2, 64, 16, 16, ctypes.byref(w), None, None, None) == INVALID
+    assert f(16, 16, 2, 8, 64, 2, 64, 16, 16, ctypes.byref(w), 16, None, None) == INVALID
+    bad_st = txl.MemState(60, 0, 50)
+    assert f(16, 16, 2, 8, 64, 2, 64, 16, 16, ctypes.byref(w), 16, ctypes.byref(bad_st),
+             None) == INVALID
+    assert f(16, 16, 2, 8, 64, 2, 64, 16, 16, ctypes.byref(txl.KVWindow(190, 20, 200, 50)), None,
+             None, None) == INVALID
+    # head width other than 64, window capacity below 2M + L, unaligned width / pointers
+    assert f(16, 16, 2, 8, 64, 2, 32, 16, 16, ctypes.byref(w), None, None, None) == UNSUPPORTED
+    assert f(16, 16, 2, 120, 64, 2, 64, 16, 16, ctypes.byref(w), None, None, None) == SHAPE
+    assert f(16, 16, 2, 8, 60, 2, 64, 16, 16, ctypes.byref(w), None, None, None) == MISALIGNED
+    assert f(8, 16, 2, 8, 64, 2, 64, 16, 16, ctypes.byref(w), None, None, None) == MISALIGNED
+    assert f(16, 16, 2, 8, 64, 2, 64, 8, 16, ctypes.byref(w), None, None, None) == MISALIGNED
+    # an empty segment changes nothing
+    assert f(16, 16, 2, 0, 64, 2, 64, 16, 16, ctypes.byref(w), 16, ctypes.byref(st), None) == OK
+    assert (w.start, w.fill, st.head, st.fill) == (0, 0, 0, 0)

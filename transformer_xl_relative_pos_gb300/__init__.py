@@ -17,6 +17,8 @@ N-layer summary, Appendix B reversed table and shift):
   mem_update      advance the memory to the newest M states
   kv_window_*     a memory kept as a window of a larger buffer, read in place
                   by relattn_fwd (k, v as strided views)
+  qkv_project     one layer's q, k, v projections written into q and the k / v
+                  window, with the memory update, in one launch
 """
 
 from __future__ import annotations
@@ -38,6 +40,7 @@ from ._lib import (  # noqa: F401
     lib_path,
     mem_concat,
     mem_update,
+    qkv_project,
     rel_pos_emb,
     relattn_fwd,
     relattn_fwd_noalloc,

@@ -92,6 +92,9 @@ def lib():
                 "txl_kv_window_append": (_c_int, [_c_p, ctypes.POINTER(KVWindow), _c_p, _c_int,
                                                   _c_int, _c_int, _c_int, _c_p]),
                 "txl_kv_window_advance": (_c_int, [ctypes.POINTER(KVWindow), _c_int]),
+                "txl_qkv_project": (_c_int, [_c_p, _c_p, _c_int, _c_int, _c_int, _c_int, _c_int,
+                                             _c_p, _c_p, ctypes.POINTER(KVWindow), _c_p,
+                                             ctypes.POINTER(MemState), _c_p]),
                 "txl_relattn_fwd_noalloc": (_c_int, [_c_p, _c_p, _c_p, _c_p, _c_int, _c_p, _c_p,
                                                      _c_p, _c_p, _c_int, _c_int, _c_int, _c_int,
                                                      _c_int, _c_float, _c_int, _c_int, _c_p]),
@@ -307,6 +310,37 @@ def kv_window_append(buf, state: KVWindow, seg, stream=None):
                                       _dev(seg, "seg") if seg.numel() else None, int(P), int(L),
                                       int(d), _code(seg.dtype), _stream(seg, stream)),
            "txl_kv_window_append")
+    return state
+
+
+def qkv_project(h, w, kv_buf, state: KVWindow, q=None, mem=None, mem_state: MemState | None = None,
+                stream=None):
+    """One layer's projections of the segment h [B, L, d_model] (bf16) by the
+    stacked weights w [n_out*H*64, d_model] (W_q, W_kE, W_v rows when q is given,
+    else W_kE, W_v): q into q [B, H, L, 64], k and v into the window rows behind
+    the memory of kv_buf [2*B*H, capacity, 64] (keys' planes, then values'),
+    and, when mem is given, h into the memory ring mem [B, capacity, d_model].
+    Updates ``state.start`` and ``mem_state`` in place, as kv_window_append and
+    mem_update do."""
+    B, L, d = h.shape
+    n_out = 3 if q is not None else 2
+    if w.shape[1] != d or w.shape[0] % (n_out * 64):
+        raise ValueError("w must be [n_out * H * 64, d_model]")
+    H = w.shape[0] // (n_out * 64)
+    if kv_buf.shape != (2 * B * H, state.capacity, 64):
+        raise ValueError("kv_buf must be [2 * B * H, capacity, 64]")
+    if q is not None and tuple(q.shape) != (B, H, L, 64):
+        raise ValueError("q must be [B, H, L, 64]")
+    if (mem is None) != (mem_state is None):
+        raise ValueError("mem and mem_state go together")
+    _check(lib().txl_qkv_project(_dev(h, "h", torch.bfloat16), _dev(w, "w", torch.bfloat16),
+                                 int(B), int(L), int(d), int(H), 64,
+                                 _dev(q, "q", torch.bfloat16) if q is not None else None,
+                                 _dev(kv_buf, "kv_buf", torch.bfloat16), ctypes.byref(state),
+                                 _dev(mem, "mem", torch.bfloat16) if mem is not None else None,
+                                 ctypes.byref(mem_state) if mem_state is not None else None,
+                                 _stream(h, stream)),
+           "txl_qkv_project")
     return state
 
 

@@ -24,7 +24,8 @@ DEBUG_BUILD_DIR = os.path.join(PKG, "_build_debug")
 DEBUG_LIB_PATH = os.path.join(PKG, "libtxl_gb300_debug.so")
 
 SOURCES = ["txl_api.cu", "relattn_tc.cu", "relattn_combine.cu", "relattn_decode.cu",
-           "relattn_decode_mma.cu", "relattn_f32.cu", "relpos.cu", "mem.cu", "relattn_noalloc.cu"]
+           "relattn_decode_mma.cu", "relattn_f32.cu", "relpos.cu", "mem.cu", "relattn_noalloc.cu",
+           "project.cu"]
 HEADERS = [os.path.join(CSRC, "kernels.h"), os.path.join(CSRC, "decode.h"),
            os.path.join(CSRC, "decode_common.cuh"), os.path.join(CSRC, "ptx.cuh"),
            os.path.join(INCLUDE, "txl.h")]

@@ -87,6 +87,26 @@ cudaError_t launch_mem_concat(uint4 *ext, const uint4 *mem, const uint4 *h_new, 
 cudaError_t launch_mem_write(uint4 *mem, const uint4 *h_new, int B, int L, int first_row,
                              int head, int cap, int row_vec, unsigned int *status, cudaStream_t s);
 
+// Projection of a segment's states h [M = B*L][K] by stacked weights [N][K]
+// (N = n_out * H * 64; outputs in order, e.g. q, k, v), written per head: output
+// o, head hd, batch b, segment row l goes to out[o] + ((b*H + hd) *
+// plane_stride[o] + row0[o] + l) * 64; optionally mem[b][(mem_head + l) mod
+// mem_cap] = h[b][l] for l >= mem_first (the memory update).
+struct ProjParams {
+    int M, N, K, L, B, H, n_out;
+    const __nv_bfloat16 *h;
+    __nv_bfloat16 *out[3];
+    long long plane_stride[3];  // elements
+    int row0[3];
+    __nv_bfloat16 *mem;         // [B][mem_cap][K] or null
+    int mem_cap, mem_head, mem_first;
+    unsigned int *status;
+    unsigned long long wait_ns;
+};
+int project_smem_bytes();
+cudaError_t launch_project(const CUtensorMap &tm_h, const CUtensorMap &tm_w, const ProjParams &p,
+                           cudaStream_t s);
+
 cudaError_t launch_wait_probe(unsigned int *status, unsigned long long wait_ns, cudaStream_t s);
 // One thread fails one index check (a no-op in release builds).
 cudaError_t launch_index_probe(unsigned int *status, cudaStream_t s);

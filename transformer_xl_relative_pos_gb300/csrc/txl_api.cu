@@ -488,6 +488,30 @@ bool window_ok(const txl_kv_window *w)
            w->capacity >= 0 && (long long)w->start + w->fill <= w->capacity;
 }
 
+// 2-D bf16 view [rows][inner] (as 3-D with one plane) read in boxes of
+// 64 columns x box_rows rows with 128-byte swizzle.
+bool make_map_rows(CUtensorMap *map, const void *base, long long inner, long long rows,
+                   unsigned box_rows)
+{
+    auto fn = encode_fn();
+    if (!fn) return false;
+    const cuuint64_t dims[3] = {(cuuint64_t)inner, (cuuint64_t)rows, 1};
+    const cuuint64_t strides[2] = {(cuuint64_t)inner * 2, (cuuint64_t)(inner * rows * 2)};
+    const cuuint32_t box[3] = {64, box_rows, 1};
+    const cuuint32_t estr[3] = {1, 1, 1};
+    CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void *>(base), dims,
+                    strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                    CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                    CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS;
+}
+
+bool mem_state_ok(const txl_mem_state *st)
+{
+    return st && st->capacity >= 0 && st->fill >= 0 && st->fill <= st->capacity && st->head >= 0 &&
+           (st->capacity == 0 ? st->head == 0 : st->head < st->capacity);
+}
+
 } // namespace
 
 extern "C" {
@@ -546,6 +570,92 @@ int txl_kv_window_append(void *buf, txl_kv_window *w, const void *seg, int plane
                                           0, planes, L, row_vec, status, s);
     if (e != cudaSuccess) return TXL_ERR_CUDA;
     w->start = start;
+    return TXL_OK;
+}
+
+int txl_qkv_project(const void *h, const void *w, int B, int L, int d_model, int H, int dh,
+                    void *q, void *kv_buf, txl_kv_window *kv_win, void *mem,
+                    txl_mem_state *mem_st, void *stream)
+{
+    if (!h || !w || !kv_buf || !window_ok(kv_win)) return TXL_ERR_INVALID_ARG;
+    if (B < 1 || L < 0 || d_model < 1 || H < 1 || dh < 1) return TXL_ERR_INVALID_ARG;
+    if (mem && !mem_state_ok(mem_st)) return TXL_ERR_INVALID_ARG;
+    if (dh != 64) return TXL_ERR_UNSUPPORTED;
+    if ((long long)kv_win->capacity < 2LL * kv_win->M + L) return TXL_ERR_SHAPE;
+    if (d_model % 8 != 0) return TXL_ERR_MISALIGNED;
+    for (const void *p : {h, w, (const void *)kv_buf})
+        if (!aligned(p, 16)) return TXL_ERR_MISALIGNED;
+    if ((q && !aligned(q, 16)) || (mem && !aligned(mem, 16))) return TXL_ERR_MISALIGNED;
+    const long long M = (long long)B * L;
+    const int n_out = q ? 3 : 2;
+    const long long N = (long long)n_out * H * 64;
+    if (M > 0x7fffffffLL || N > 0x7fffffffLL || (long long)B * H * 2 > 0x7fffffffLL)
+        return TXL_ERR_UNSUPPORTED;
+    if (L == 0) return TXL_OK;
+    cudaStream_t s = as_stream(stream);
+    cudaError_t serr;
+    unsigned int *status = status_word(&serr);
+    if (!status) return TXL_ERR_CUDA;
+
+    const long long C = kv_win->capacity;
+    const int row_vec = 64 * 2 / 16;
+    int start = kv_win->start;
+    if ((long long)start + kv_win->fill + L > C) {
+        // move the memory rows of every key and value plane to the front, as
+        // txl_kv_window_append does (disjoint ranges since C >= 2M + L)
+        if (kv_win->fill > 0) {
+            cudaError_t e = txl::launch_rows_copy(static_cast<uint4 *>(kv_buf), C * row_vec, 0,
+                                                  static_cast<const uint4 *>(kv_buf), C * row_vec,
+                                                  start, 2 * B * H, kv_win->fill, row_vec, status, s);
+            if (e != cudaSuccess) return TXL_ERR_CUDA;
+        }
+        start = 0;
+    }
+
+    txl::ProjParams p{};
+    p.M = (int)M;
+    p.N = (int)N;
+    p.K = d_model;
+    p.L = L;
+    p.B = B;
+    p.H = H;
+    p.n_out = n_out;
+    p.h = static_cast<const __nv_bfloat16 *>(h);
+    auto *kv = static_cast<__nv_bfloat16 *>(kv_buf);
+    int o = 0;
+    if (q) {
+        p.out[o] = static_cast<__nv_bfloat16 *>(q);
+        p.plane_stride[o] = (long long)L * 64;
+        p.row0[o] = 0;
+        ++o;
+    }
+    for (int kv_i = 0; kv_i < 2; ++kv_i, ++o) {
+        p.out[o] = kv + (size_t)kv_i * B * H * C * 64;
+        p.plane_stride[o] = C * 64;
+        p.row0[o] = start + kv_win->fill;
+    }
+    int new_head = 0, new_fill = 0;
+    if (mem && mem_st->capacity > 0) {
+        const int cap = mem_st->capacity;
+        p.mem = static_cast<__nv_bfloat16 *>(mem);
+        p.mem_cap = cap;
+        p.mem_head = mem_st->head;
+        p.mem_first = L > cap ? L - cap : 0;  // older rows would be overwritten anyway
+        new_head = (int)(((long long)mem_st->head + L) % cap);
+        new_fill = (int)std::min<long long>((long long)mem_st->fill + L, cap);
+    }
+    p.status = status;
+    p.wait_ns = g_wait_ns;
+
+    CUtensorMap tm_h, tm_w;
+    if (!make_map_rows(&tm_h, h, d_model, M, 128) || !make_map_rows(&tm_w, w, d_model, N, 256))
+        return TXL_ERR_CUDA;
+    if (txl::launch_project(tm_h, tm_w, p, s) != cudaSuccess) return TXL_ERR_CUDA;
+    kv_win->start = start;
+    if (p.mem) {
+        mem_st->head = new_head;
+        mem_st->fill = new_fill;
+    }
     return TXL_OK;
 }
 

@@ -15,11 +15,12 @@ With ``cache_kv`` the stack also keeps, per layer, the memory's projected keys
 and values: the memory rows and W_kE, W_v do not change at evaluation, so k and
 v of the memory are the ones projected when those states were the segment, and
 each segment projects only its own L rows (2·M·d² multiply-adds saved per layer
-and projection); q, k and v of the segment come from one GEMM.  Keys and values
-of a layer live in one window of a buffer [2·B·H, capacity, d_head] (the keys'
-planes, then the values'; txl_kv_window_append / _advance): the segment's rows
-are written behind the memory's and the attention reads [memory ; segment] in
-place, with no copy of the memory per segment.
+and projection).  Keys and values of a layer live in one window of a buffer
+[2·B·H, capacity, d_head] (the keys' planes, then the values'): one launch of
+txl_qkv_project computes the segment's q, k and v (one GEMM over the stacked
+weights), writes k and v behind the memory's rows in the window and advances the
+hidden-state memory ring; the attention reads [memory ; segment] in place, with
+no copy of the memory per segment (txl_kv_window_advance after it).
 The relative table r = W_kR R is built from rel_pos_emb (kernel) and one matmul
 and is cached per (layer, K): R has no parameters and W_kR is fixed at
 evaluation.
@@ -265,14 +266,18 @@ class XLStack:
         for n, lay in enumerate(self.layers):
             st = self.states[n]
             M_cur = st.fill
+            mem_now = None
+            if self.taps is not None:  # the memory this layer attends to
+                mem_now = txl.mem_concat(self.mems[n], st, h[:, :0])
             if self.cache_kv:
-                # only the segment's rows are projected (q, k, v in one GEMM);
-                # k and v are written behind the memory's in the window and the
-                # attention reads both in place
+                # only the segment's rows are projected: one launch computes q,
+                # k, v (one GEMM over the stacked weights), writes k and v behind
+                # the memory's rows in the window and advances the memory ring;
+                # the attention reads [memory ; segment] in place
                 kw = self.kv_windows[n]
-                qkv = project_stacked(h, lay["W_qkv"], 3, self.H)
-                q = qkv[0]
-                txl.kv_window_append(self.kvbufs[n], kw, qkv[1:].view(2 * B * self.H, L, self.dh))
+                q = torch.empty(B, self.H, L, self.dh, dtype=self.dtype, device=self.device)
+                txl.qkv_project(h, lay["W_qkv"], self.kvbufs[n], kw, q=q, mem=self.mems[n],
+                                mem_state=st)
                 kv = txl.kv_window_view(self.kvbufs[n], kw, L, 2 * B, self.H)
                 kv = kv.view(2, B, self.H, -1, self.dh)
                 k, v = kv[0], kv[1]
@@ -288,11 +293,11 @@ class XLStack:
             f = torch.relu(o.to(self.dtype) @ lay["W_1"].t() + lay["b_1"])
             h_next = layer_norm(o + (f @ lay["W_2"].t()).float() + lay["b_2"].float())
             if self.taps is not None:
-                mem_now = txl.mem_concat(self.mems[n], st, h[:, :0])
                 self.taps.append({"h": h, "mem": mem_now, "q": q, "k": k, "v": v, "r": r,
                                   "M": M_cur, "a": a_heads, "h_out": h_next.to(self.dtype)})
-            txl.mem_update(self.mems[n], st, h)
             if self.cache_kv:
-                txl.kv_window_advance(kw, L)
+                txl.kv_window_advance(kw, L)  # (the ring advanced in qkv_project)
+            else:
+                txl.mem_update(self.mems[n], st, h)
             h = h_next.to(self.dtype)
         return h
