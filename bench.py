@@ -110,6 +110,9 @@ def parse_args():
                     help="with --decode: B,L,M triples (default: the long-memory decode set)")
     ap.add_argument("--calls", type=int, default=10,
                     help="with --decode or --configs: graph replays timed per shape (30 calls each)")
+    ap.add_argument("--project", action="store_true",
+                    help="time one layer's fused projection (txl_qkv_project) at the 12-layer "
+                         "stream's shape against the unfused calls it replaces")
     ap.add_argument("--workload", nargs="*", default=None,
                     help="with --configs: only these workloads (names as in txl_inputs.WORKLOADS)")
     return ap.parse_args()
@@ -853,6 +856,67 @@ def run_configs(args):
             "tflops_l2_hot": w.flops() / (us_hot * 1e-6) / 1e12}}), flush=True)
 
 
+def run_project(args):
+    """Graph-replayed time of one layer's projections of a segment at the
+    12-layer stream's shape (B=16, L=M=512, d=512, H=8): txl_qkv_project (q, k,
+    v into q and the window, the memory update) against the calls it replaces
+    (torch GEMM + head-major permutation + txl_kv_window_append +
+    txl_mem_update) and against the GEMM alone."""
+    import torch
+    import transformer_xl_relative_pos_gb300 as txl
+    from transformer_xl_relative_pos_gb300.model import project_stacked
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    w_ = txl_inputs.WORKLOADS["c5_stack12_L512_M512"]
+    B, H, L, M, d = w_.B, w_.H, w_.L, w_.M, w_.d_model
+    C = M + 2 * L
+    g = torch.Generator(device=dev).manual_seed(0)
+    h = torch.randn(B, L, d, device=dev, generator=g).to(torch.bfloat16)
+    W = (torch.randn(3 * H * 64, d, device=dev, generator=g) * d ** -0.5).to(torch.bfloat16)
+    kv = torch.zeros(2 * B * H, C, 64, dtype=torch.bfloat16, device=dev)
+    mem = torch.zeros(B, M, d, dtype=torch.bfloat16, device=dev)
+    q = torch.empty(B, H, L, 64, dtype=torch.bfloat16, device=dev)
+
+    def fused():
+        txl.qkv_project(h, W, kv, txl.KVWindow(0, M, C, M), q=q, mem=mem,
+                        mem_state=txl.MemState(0, M, M))
+
+    def unfused():
+        win = txl.KVWindow(0, M, C, M)
+        qkv = project_stacked(h, W, 3, H)
+        txl.kv_window_append(kv, win, qkv[1:].view(2 * B * H, L, 64))
+        txl.mem_update(mem, txl.MemState(0, M, M), h)
+
+    def gemm_only():
+        torch.matmul(h, W.t())
+
+    flops = 2.0 * B * L * 3 * H * 64 * d
+    for name, fn in (("qkv_project", fused), ("unfused", unfused), ("library_gemm_only", gemm_only)):
+        s_ = torch.cuda.Stream(dev)
+        with torch.cuda.stream(s_):
+            for _ in range(3):
+                fn()
+        torch.cuda.synchronize()
+        gr = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(gr, stream=s_):
+            for _ in range(20):
+                fn()
+        gr.replay()
+        torch.cuda.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(s_)
+        with torch.cuda.stream(s_):
+            for _ in range(max(1, args.calls)):
+                gr.replay()
+        e1.record(s_)
+        torch.cuda.synchronize()
+        us = e0.elapsed_time(e1) * 1e3 / (20 * max(1, args.calls))
+        print(json.dumps({"project": {"op": name, "B": B, "L": L, "d_model": d, "H": H,
+                                      "us_per_call": us, "tflops": flops / (us * 1e-6) / 1e12}}),
+              flush=True)
+    assert txl.device_status() == 0
+
+
 def run_stack(args):
     """Per-segment time of the streaming stack on the 12-layer, 16-segment
     workload (B=16, H=8, L=M=512, d=512), memories full, with and without the
@@ -899,6 +963,9 @@ def main():
     args = parse_args()
     if args.stack:
         run_stack(args)
+        return
+    if args.project:
+        run_project(args)
         return
     if args.table9:
         run_table9(args)
