@@ -219,15 +219,15 @@ int project_smem_bytes() { return SMEM_BYTES; }
 cudaError_t launch_project(const CUtensorMap &tm_h, const CUtensorMap &tm_w, const ProjParams &p,
                            cudaStream_t s)
 {
-    static bool attr_set[64] = {};
+    static bool attr_set[64] = {};  // the attribute is set once per device
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return e;
-    if (dev >= 0 && dev < 64 && !attr_set[dev]) {
+    if (dev < 0 || dev >= 64 || !attr_set[dev]) {
         e = cudaFuncSetAttribute(project_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                  SMEM_BYTES);
         if (e != cudaSuccess) return e;
-        attr_set[dev] = true;
+        if (dev >= 0 && dev < 64) attr_set[dev] = true;
     }
     const dim3 grid((unsigned)((p.M + BM - 1) / BM), (unsigned)((p.N + BN - 1) / BN));
     project_kernel<<<grid, 256, SMEM_BYTES, s>>>(tm_h, tm_w, p);
