@@ -10,7 +10,9 @@ Context" (Dai et al.):
   * §3.3, the four-term relative score A^rel (terms (a)-(d));
   * §3.3, the N-layer computational summary (extended context [SG(m) o h],
     masked softmax, Linear + residual + LayerNorm, position-wise feed-forward);
-  * §3.2, the memory of the last M hidden states per layer;
+  * §3.2, the memory of the last M hidden states per layer, and training
+    that backpropagates within a segment (``relattn_bwd``: the chain rule of
+    the forward above, the memory SG(m));
   * Appendix B, the reversed table Q and the left-shift relation between
     B~ = q Q^T and B (used here only as a self-check, never for the result).
 
@@ -67,6 +69,9 @@ def _load():
                                          ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int,
                                          ctypes.c_double, ip, ctypes.c_int, ctypes.c_int]
             lib.txlo_relattn.restype = ctypes.c_int
+            lib.txlo_relattn_bwd.argtypes = [dp] * 13 + [ctypes.c_int] * 5 + [ctypes.c_double,
+                                                                                 ctypes.c_int]
+            lib.txlo_relattn_bwd.restype = ctypes.c_int
             lib.txlo_max_threads.argtypes = []
             lib.txlo_max_threads.restype = ctypes.c_int
             _lib = lib
@@ -144,6 +149,34 @@ def relattn(q, k, v, rel, u, v_bias, M: int, L: int, scale: float,
     if rc != 0:
         raise RuntimeError(f"txlo_relattn failed ({rc})")
     return out, lse
+
+
+def relattn_bwd(q, k, v, rel, u, v_bias, dout, M: int, L: int, scale: float,
+                nthreads: int = 0):
+    """Gradients of :func:`relattn`'s output against ``dout`` (training within a
+    segment, §3.2; the memory rows are SG(m), yet their projected k and v get
+    gradients like the segment's).
+
+    Shapes as :func:`relattn`; dout [B,H,L,dh].  Returns fp64
+    (dq [B,H,L,dh], dk [B,H,M+L,dh], dv [B,H,M+L,dh], drel [H,M+L,dh] by
+    distance, du [H,dh], dvb [H,dh]); drel, du, dvb are summed over the batch.
+    """
+    q, k, v, rel, u, v_bias, dout = (_f64(t) for t in (q, k, v, rel, u, v_bias, dout))
+    B, H, Lq, dh = q.shape
+    K = M + L
+    if Lq != L or k.shape != (B, H, K, dh) or v.shape != (B, H, K, dh) or dout.shape != q.shape:
+        raise ValueError("relattn_bwd: shape mismatch")
+    if rel.shape != (H, K, dh) or u.shape != (H, dh) or v_bias.shape != (H, dh):
+        raise ValueError("relattn_bwd: rel/u/v_bias shape mismatch")
+    dq, dk, dv = np.empty_like(q), np.empty_like(k), np.empty_like(v)
+    drel, du, dvb = np.empty_like(rel), np.empty_like(u), np.empty_like(v_bias)
+    rc = _load().txlo_relattn_bwd(_dp(q), _dp(k), _dp(v), _dp(rel), _dp(u), _dp(v_bias),
+                                  _dp(dout), _dp(dq), _dp(dk), _dp(dv), _dp(drel), _dp(du),
+                                  _dp(dvb), B, H, int(M), int(L), dh, float(scale),
+                                  int(nthreads))
+    if rc != 0:
+        raise RuntimeError(f"txlo_relattn_bwd failed ({rc})")
+    return dq, dk, dv, drel, du, dvb
 
 
 def score_terms(q, k, rel, u, v_bias, M: int, L: int):

@@ -186,3 +186,124 @@ int txlo_max_threads(void)
     return 1;
 #endif
 }
+
+/* ---------------------------------------------------------------------------
+ * Backward of the attention above for one segment (training backpropagates
+ * within a segment, §3.2; the memory is SG(m), so no gradient leaves through
+ * it, but its projected keys and values still receive one).
+ *
+ * With A_ij = scale (a + b + c + d) for a kept pair, P = softmax_j(A), O = P v
+ * and dO the gradient of the output, the chain rule gives, per head:
+ *   dv_j      = sum_i P_ij dO_i
+ *   dP_ij     = dO_i . v_j
+ *   dA_ij     = P_ij (dP_ij - sum_j' P_ij' dP_ij')
+ *   g_ij      = scale dA_ij                      (gradient of a + b + c + d)
+ *   dq_i      = sum_j g_ij (k_j + rel_{M+i-j})   (terms (a), (b))
+ *   dk_j      = sum_i g_ij (q_i + u)             (terms (a), (c))
+ *   du        = sum_ij g_ij k_j                  (term (c))
+ *   dvb       = sum_ij g_ij rel_{M+i-j}          (term (d))
+ *   drel_dlt  = sum_{i - j = dlt - M} g_ij (q_i + vb)   (terms (b), (d))
+ * Masked pairs have P = 0 and contribute nothing.  rel, u, vb are shared by the
+ * batch, so drel, du, dvb are sums over b as well.
+ *
+ * Shapes as txlo_relattn; dout [B][H][L][dh]; outputs dq [B][H][L][dh], dk, dv
+ * [B][H][M+L][dh], drel [H][M+L][dh] (by distance), du, dvb [H][dh].  Heads
+ * run in parallel; the batch loop inside a head is sequential, so the sums over
+ * b need no synchronisation.
+ * ------------------------------------------------------------------------- */
+static void one_head_bwd(const double *q, const double *k, const double *v,
+                         const double *rel, const double *u, const double *vb,
+                         const double *dout, double *dq, double *dk, double *dv,
+                         double *drel, double *du, double *dvb, int M, int L, int dh,
+                         double scale, double *P, double *G)
+{
+    const int K = M + L;
+    for (int i = 0; i < L; ++i) {
+        const double *qi = q + (size_t)i * dh;
+        const double *doi = dout + (size_t)i * dh;
+        /* probabilities of row i */
+        double amax = -INFINITY;
+        for (int j = 0; j < K; ++j) {
+            const int delta = M + i - j;
+            if (delta < 0) { P[j] = -INFINITY; continue; }
+            const double *kj = k + (size_t)j * dh;
+            const double *rd = rel + (size_t)delta * dh;
+            P[j] = scale * (dotd(qi, kj, dh) + dotd(qi, rd, dh) + dotd(u, kj, dh) +
+                            dotd(vb, rd, dh));
+            if (P[j] > amax) amax = P[j];
+        }
+        double sum = 0.0;
+        for (int j = 0; j < K; ++j) {
+            P[j] = (P[j] == -INFINITY) ? 0.0 : exp(P[j] - amax);
+            sum += P[j];
+        }
+        for (int j = 0; j < K; ++j) P[j] /= sum;
+        /* dP and its P-weighted row mean */
+        double mean = 0.0;
+        for (int j = 0; j < K; ++j) {
+            G[j] = (P[j] == 0.0) ? 0.0 : dotd(doi, v + (size_t)j * dh, dh);
+            mean += P[j] * G[j];
+        }
+        for (int j = 0; j < K; ++j) G[j] = scale * P[j] * (G[j] - mean);
+        /* contributions of row i */
+        double *dqi = dq + (size_t)i * dh;
+        for (int j = 0; j < K; ++j) {
+            const int delta = M + i - j;
+            if (delta < 0) continue;
+            const double *kj = k + (size_t)j * dh;
+            const double *rd = rel + (size_t)delta * dh;
+            double *dkj = dk + (size_t)j * dh, *dvj = dv + (size_t)j * dh;
+            double *drd = drel + (size_t)delta * dh;
+            for (int t = 0; t < dh; ++t) {
+                dvj[t] += P[j] * doi[t];
+                dqi[t] += G[j] * (kj[t] + rd[t]);
+                dkj[t] += G[j] * (qi[t] + u[t]);
+                du[t] += G[j] * kj[t];
+                dvb[t] += G[j] * rd[t];
+                drd[t] += G[j] * (qi[t] + vb[t]);
+            }
+        }
+    }
+}
+
+int txlo_relattn_bwd(const double *q, const double *k, const double *v,
+                     const double *rel, const double *u, const double *vb,
+                     const double *dout, double *dq, double *dk, double *dv,
+                     double *drel, double *du, double *dvb, int B, int H, int M, int L,
+                     int dh, double scale, int nthreads)
+{
+    if (B < 0 || H < 1 || M < 0 || L < 1 || dh < 1) return -1;
+    const int K = M + L;
+    for (size_t x = 0; x < (size_t)B * H * L * dh; ++x) dq[x] = 0.0;
+    for (size_t x = 0; x < (size_t)B * H * K * dh; ++x) dk[x] = dv[x] = 0.0;
+    for (size_t x = 0; x < (size_t)H * K * dh; ++x) drel[x] = 0.0;
+    for (size_t x = 0; x < (size_t)H * dh; ++x) du[x] = dvb[x] = 0.0;
+    int bad = 0;
+#ifdef _OPENMP
+    if (nthreads > 0) omp_set_num_threads(nthreads);
+#else
+    (void)nthreads;
+#endif
+#pragma omp parallel
+    {
+        double *P = (double *)malloc(sizeof(double) * 2 * (size_t)K);
+        if (!P) {
+#pragma omp atomic write
+            bad = 1;
+        }
+#pragma omp for schedule(dynamic, 1)
+        for (int h = 0; h < H; ++h) {
+            if (!P) continue;
+            for (int b = 0; b < B; ++b) {
+                const size_t bh = (size_t)b * H + h;
+                one_head_bwd(q + bh * L * dh, k + bh * K * dh, v + bh * K * dh,
+                             rel + (size_t)h * K * dh, u + (size_t)h * dh, vb + (size_t)h * dh,
+                             dout + bh * L * dh, dq + bh * L * dh, dk + bh * K * dh,
+                             dv + bh * K * dh, drel + (size_t)h * K * dh, du + (size_t)h * dh,
+                             dvb + (size_t)h * dh, M, L, dh, scale, P, P + K);
+            }
+        }
+        free(P);
+    }
+    return bad ? -2 : 0;
+}

@@ -46,3 +46,32 @@ def test_pins_reject_mutant(name, tmp_path):
                         os.path.join(ROOT, "tests", "test_oracle_recurrence.py")],
                        cwd=ROOT, env=env, capture_output=True, text=True, timeout=600)
     assert r.returncode != 0, f"mutant {name} survived the pins:\n{r.stdout[-2000:]}"
+
+
+# Planted mistakes in the backward, run against its own pins.
+BWD_MUTANTS = {
+    "bwd_row_mean_dropped": ("G[j] = scale * P[j] * (G[j] - mean);", "G[j] = scale * P[j] * G[j];"),
+    "bwd_scale_dropped": ("G[j] = scale * P[j] * (G[j] - mean);", "G[j] = P[j] * (G[j] - mean);"),
+    "bwd_dq_no_position": ("dqi[t] += G[j] * (kj[t] + rd[t]);", "dqi[t] += G[j] * kj[t];"),
+    "bwd_dk_no_u": ("dkj[t] += G[j] * (qi[t] + u[t]);", "dkj[t] += G[j] * qi[t];"),
+    "bwd_dv_uses_score_grad": ("dvj[t] += P[j] * doi[t];", "dvj[t] += G[j] * doi[t];"),
+    "bwd_dvb_uses_key": ("dvb[t] += G[j] * rd[t];", "dvb[t] += G[j] * kj[t];"),
+    "bwd_drel_uses_u": ("drd[t] += G[j] * (qi[t] + vb[t]);", "drd[t] += G[j] * (qi[t] + u[t]);"),
+}
+
+
+@pytest.mark.parametrize("name", sorted(BWD_MUTANTS))
+def test_backward_pins_reject_mutant(name, tmp_path):
+    old, new = BWD_MUTANTS[name]
+    src = open(SRC).read()
+    assert src.count(old) == 1, f"mutation site not found once: {old}"
+    mut_c = tmp_path / "mutant.c"
+    mut_c.write_text(src.replace(old, new))
+    so = tmp_path / "libmutant.so"
+    subprocess.run(["gcc", "-O2", "-fPIC", "-shared", "-fopenmp", "-std=c11", "-o", str(so),
+                    str(mut_c), "-lm"], check=True)
+    env = dict(os.environ, TXL_ORACLE_LIB=str(so))
+    r = subprocess.run([sys.executable, "-m", "pytest", "-q", "-x", "-p", "no:cacheprovider",
+                        os.path.join(ROOT, "tests", "test_oracle_bwd.py")],
+                       cwd=ROOT, env=env, capture_output=True, text=True, timeout=600)
+    assert r.returncode != 0, f"mutant {name} survived the backward pins:\n{r.stdout[-2000:]}"
