@@ -348,6 +348,42 @@ int txl_qkv_project(const void *h, const void *w, int B, int L, int d_model, int
                     txl_mem_state *mem_st, void *stream);
 
 /*
+ * txl_relattn_bwd - backward of txl_relattn_fwd for one segment (training
+ * backpropagates within a segment, "Transformer-XL: Attentive Language Models
+ * Beyond a Fixed-Length Context" §3.2; the memory is SG(m): no gradient leaves
+ * through it, but its projected keys and values receive one like the
+ * segment's).  With A_ij the §3.3 score times `scale`, P = softmax_j(A) over
+ * the kept keys (j <= i + M), O = P v and dout = dL/dO:
+ *   D_i   = sum_j P_ij (dout_i . v_j)
+ *   g_ij  = scale P_ij (dout_i . v_j - D_i)
+ *   dq_i  = sum_j g_ij (k_j + r(M+i-j))       dk_j = sum_i g_ij (q_i + u)
+ *   dv_j  = sum_i P_ij dout_i                 du   = sum_{b,i,j} g_ij k_j
+ *   dr(d) = sum_{b, i-j = d-M} g_ij (q_i + v) dv_bias = sum_{b,i,j} g_ij r(M+i-j)
+ * where r(d) is the table row of distance d (row r_rows - 1 - d of r).  P is
+ * recomputed; so are its log-sum-exp and D (exactly, in fp32): nothing from the
+ * forward call is needed.
+ * Inputs, bf16, dense and 16-byte aligned, layouts as txl_relattn_fwd:
+ *   q, dout [B][H][L][dh]   k, v [B][H][M+L][dh]   r [H][r_rows][dh]
+ *   u, v_bias [H][dh]
+ * Outputs, fp32, dense, written (not accumulated), 16-byte aligned:
+ *   dq [B][H][L][dh]   dk, dv [B][H][M+L][dh]   dr [H][r_rows][dh] (rows of
+ *   distances >= M+L are zero)   du, dv_bias [H][dh]
+ * workspace: txl_relattn_bwd_workspace_size(B, H, L) bytes of device memory
+ * (per-row statistics and per-block bias partials); the sums over the batch
+ * are ordered, so results repeat bit for bit.  dh must be 64 and dtype
+ * TXL_DTYPE_BF16.  Asynchronous on `stream`.  Errors: TXL_ERR_INVALID_ARG
+ * (NULL pointer, bad sizes), TXL_ERR_UNSUPPORTED (dh, dtype, sizes past the
+ * grid limits), TXL_ERR_SHAPE (r_rows < M+L), TXL_ERR_MISALIGNED,
+ * TXL_ERR_WORKSPACE, TXL_ERR_CUDA.
+ */
+size_t txl_relattn_bwd_workspace_size(int B, int H, int L);
+int txl_relattn_bwd(const void *q, const void *k, const void *v, const void *r, int r_rows,
+                    const void *u, const void *v_bias, const void *dout, float *dq, float *dk,
+                    float *dv, float *dr, float *du, float *dv_bias, int B, int H, int M, int L,
+                    int dh, float scale, int dtype, void *workspace, size_t workspace_bytes,
+                    void *stream);
+
+/*
  * txl_device_status - synchronise `stream`, then read and clear the device
  * status word in which kernels record barrier time-outs (and, in a debug
  * build, failed index checks).  Returns TXL_OK, TXL_ERR_TIMEOUT (a time-out was

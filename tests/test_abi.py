@@ -281,3 +281,39 @@ def test_qkv_project_validation():
     # an empty segment changes nothing
     assert f(16, 16, 2, 0, 64, 2, 64, 16, 16, ctypes.byref(w), 16, ctypes.byref(st), None) == OK
     assert (w.start, w.fill, st.head, st.fill) == (0, 0, 0, 0)
+
+
+def test_relattn_bwd_workspace_and_validation():
+    # Host checks only: every case is refused before any launch.
+    rows = 3 * 5 * 130
+    chunks = 3 * 5 * 3
+    r256 = lambda x: (x + 255) // 256 * 256
+    assert txl.bwd_workspace_size(3, 5, 130) == 2 * r256(rows * 4) + r256(chunks * 128 * 4)
+    assert txl.bwd_workspace_size(0, 5, 130) == 0
+    f = L().txl_relattn_bwd
+    p = 16  # a 16-byte aligned stand-in address (never dereferenced)
+    ws_need = txl.bwd_workspace_size(2, 2, 8)
+
+    def call(**kw):
+        a = dict(q=p, k=p, v=p, r=p, r_rows=16, u=p, vb=p, dout=p, dq=p, dk=p, dv=p, dr=p, du=p,
+                 dvb=p, B=2, H=2, M=8, L=8, dh=64, scale=0.125, dtype=1, ws=256,
+                 ws_bytes=ws_need)
+        a.update(kw)
+        return f(a["q"], a["k"], a["v"], a["r"], a["r_rows"], a["u"], a["vb"], a["dout"], a["dq"],
+                 a["dk"], a["dv"], a["dr"], a["du"], a["dvb"], a["B"], a["H"], a["M"], a["L"],
+                 a["dh"], a["scale"], a["dtype"], a["ws"], a["ws_bytes"], None)
+
+    assert call(q=None) == INVALID
+    assert call(dr=None) == INVALID
+    assert call(L=0) == INVALID
+    assert call(M=-1) == INVALID
+    assert call(dtype=7) == INVALID
+    assert call(scale=float("nan")) == INVALID
+    assert call(r_rows=15) == SHAPE
+    assert call(dh=32) == UNSUPPORTED
+    assert call(dtype=0) == UNSUPPORTED  # fp32 inputs: not supported by the backward
+    assert call(k=8) == MISALIGNED
+    assert call(dq=20) == MISALIGNED
+    assert call(ws=None) == WORKSPACE
+    assert call(ws_bytes=ws_need - 1) == WORKSPACE
+    assert call(ws=272) == MISALIGNED

@@ -19,6 +19,8 @@ N-layer summary, Appendix B reversed table and shift):
                   by relattn_fwd (k, v as strided views)
   qkv_project     one layer's q, k, v projections written into q and the k / v
                   window, with the memory update, in one launch
+  relattn_bwd     gradients of relattn_fwd for one segment (training within a
+                  segment, the memory SG(m))
 """
 
 from __future__ import annotations
@@ -29,6 +31,7 @@ from ._lib import (  # noqa: F401
     KVWindow,
     MemState,
     TxlError,
+    bwd_workspace_size,
     debug_checks,
     debug_index_probe,
     debug_wait_timeout,
@@ -42,6 +45,7 @@ from ._lib import (  # noqa: F401
     mem_update,
     qkv_project,
     rel_pos_emb,
+    relattn_bwd,
     relattn_fwd,
     relattn_fwd_noalloc,
     relattn_plan,

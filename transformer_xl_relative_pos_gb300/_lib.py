@@ -95,6 +95,11 @@ def lib():
                 "txl_qkv_project": (_c_int, [_c_p, _c_p, _c_int, _c_int, _c_int, _c_int, _c_int,
                                              _c_p, _c_p, ctypes.POINTER(KVWindow), _c_p,
                                              ctypes.POINTER(MemState), _c_p]),
+                "txl_relattn_bwd_workspace_size": (_c_size, [_c_int, _c_int, _c_int]),
+                "txl_relattn_bwd": (_c_int, [_c_p, _c_p, _c_p, _c_p, _c_int, _c_p, _c_p, _c_p,
+                                             _c_p, _c_p, _c_p, _c_p, _c_p, _c_p, _c_int, _c_int,
+                                             _c_int, _c_int, _c_int, _c_float, _c_int, _c_p,
+                                             _c_size, _c_p]),
                 "txl_relattn_fwd_noalloc": (_c_int, [_c_p, _c_p, _c_p, _c_p, _c_int, _c_p, _c_p,
                                                      _c_p, _c_p, _c_int, _c_int, _c_int, _c_int,
                                                      _c_int, _c_float, _c_int, _c_int, _c_p]),
@@ -246,6 +251,40 @@ def relattn_fwd(q, k, v, r, u, v_bias, M: int, scale: float, *, out=None, lse=No
             ws_ptr, int(ws_bytes), _stream(q, stream))
         _check(rc, "txl_relattn_fwd_strided")
     return (out, lse) if want_lse else out
+
+
+def bwd_workspace_size(B: int, H: int, L: int) -> int:
+    """Bytes of device workspace txl_relattn_bwd needs."""
+    return int(lib().txl_relattn_bwd_workspace_size(int(B), int(H), int(L)))
+
+
+def relattn_bwd(q, k, v, r, u, v_bias, dout, M: int, scale: float, *, grads=None,
+                workspace=None, stream=None):
+    """Backward of :func:`relattn_fwd` (bf16 inputs, same layouts) for the
+    output gradient ``dout`` [B,H,L,dh].  Returns fp32
+    ``(dq, dk, dv, dr, du, dv_bias)`` shaped like q, k, v, r, u, v_bias; dr, du,
+    dv_bias are summed over the batch.  ``grads``: a tuple of such tensors to
+    fill instead; ``workspace``: a device buffer of at least
+    :func:`bwd_workspace_size` bytes (allocated when omitted)."""
+    B, H, L, dh = q.shape
+    bf = torch.bfloat16
+    if grads is None:
+        f = lambda t: torch.empty(t.shape, dtype=torch.float32, device=t.device)
+        grads = (f(q), f(k), f(v), f(r), f(u), f(v_bias))
+    dq, dk, dv, dr, du, dvb = grads
+    if workspace is None:
+        workspace = torch.empty(max(bwd_workspace_size(B, H, L), 256), dtype=torch.uint8,
+                                device=q.device)
+    f32 = torch.float32
+    rc = lib().txl_relattn_bwd(
+        _dev(q, "q", bf), _dev(k, "k", bf), _dev(v, "v", bf), _dev(r, "r", bf), int(r.shape[1]),
+        _dev(u, "u", bf), _dev(v_bias, "v_bias", bf), _dev(dout, "dout", bf),
+        _dev(dq, "dq", f32), _dev(dk, "dk", f32), _dev(dv, "dv", f32), _dev(dr, "dr", f32),
+        _dev(du, "du", f32), _dev(dvb, "dv_bias", f32), int(B), int(H), int(M), int(L), int(dh),
+        float(scale), BF16, _dev(workspace, "workspace"),
+        int(workspace.numel() * workspace.element_size()), _stream(q, stream))
+    _check(rc, "txl_relattn_bwd")
+    return grads
 
 
 def relattn_fwd_noalloc(q, k, v, r, u, v_bias, M: int, scale: float, *, out=None, lse=None,

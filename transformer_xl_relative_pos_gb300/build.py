@@ -25,7 +25,7 @@ DEBUG_LIB_PATH = os.path.join(PKG, "libtxl_gb300_debug.so")
 
 SOURCES = ["txl_api.cu", "relattn_tc.cu", "relattn_combine.cu", "relattn_decode.cu",
            "relattn_decode_mma.cu", "relattn_f32.cu", "relpos.cu", "mem.cu", "relattn_noalloc.cu",
-           "project.cu"]
+           "project.cu", "relattn_bwd.cu"]
 HEADERS = [os.path.join(CSRC, "kernels.h"), os.path.join(CSRC, "decode.h"),
            os.path.join(CSRC, "decode_common.cuh"), os.path.join(CSRC, "ptx.cuh"),
            os.path.join(INCLUDE, "txl.h")]

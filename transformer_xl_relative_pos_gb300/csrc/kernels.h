@@ -107,6 +107,22 @@ int project_smem_bytes();
 cudaError_t launch_project(const CUtensorMap &tm_h, const CUtensorMap &tm_w, const ProjParams &p,
                            cudaStream_t s);
 
+// Backward of the relative attention (relattn_bwd.cu): bf16 inputs, fp32
+// gradients.  lse2 / dsum / part point into the caller's workspace: per query
+// row the log2-sum-exp of the scaled scores and D = sum_j P dP, per (b*H + h,
+// 64-row query chunk) the two bias partials (64 + 64 floats).
+struct BwdParams {
+    const __nv_bfloat16 *q, *k, *v, *r, *u, *vb, *dout;
+    float *dq, *dk, *dv, *dr, *du, *dvb;
+    float *lse2, *dsum, *part;
+    int B, H, M, L, K, r_rows;
+    float scale, scale_log2;
+    unsigned int *status;
+};
+constexpr int kBwdRows = 64;  // query rows (and keys, distances) per tile
+size_t bwd_workspace_bytes(int B, int H, int L);
+cudaError_t launch_relattn_bwd(const BwdParams &p, cudaStream_t s);
+
 cudaError_t launch_wait_probe(unsigned int *status, unsigned long long wait_ns, cudaStream_t s);
 // One thread fails one index check (a no-op in release builds).
 cudaError_t launch_index_probe(unsigned int *status, cudaStream_t s);

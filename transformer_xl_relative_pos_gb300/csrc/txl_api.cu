@@ -770,3 +770,75 @@ int txl_debug_wait_timeout(uint64_t ns, void *stream)
 }
 
 } // extern "C"
+
+// ---------------------------------------------------------------------------
+// Backward of the attention (one segment, §3.2: the memory is SG(m)).
+// ---------------------------------------------------------------------------
+extern "C" size_t txl_relattn_bwd_workspace_size(int B, int H, int L)
+{
+    return txl::bwd_workspace_bytes(B, H, L);
+}
+
+extern "C" int txl_relattn_bwd(const void *q, const void *k, const void *v, const void *r,
+                               int r_rows, const void *u, const void *v_bias, const void *dout,
+                               float *dq, float *dk, float *dv, float *dr, float *du,
+                               float *dv_bias, int B, int H, int M, int L, int dh, float scale,
+                               int dtype, void *workspace, size_t workspace_bytes, void *stream)
+{
+    if (!q || !k || !v || !r || !u || !v_bias || !dout || !dq || !dk || !dv || !dr || !du ||
+        !dv_bias)
+        return TXL_ERR_INVALID_ARG;
+    if (B < 1 || H < 1 || M < 0 || L < 1 || dh < 1) return TXL_ERR_INVALID_ARG;
+    if (dtype != TXL_F32 && dtype != TXL_BF16) return TXL_ERR_INVALID_ARG;
+    if (!(scale == scale)) return TXL_ERR_INVALID_ARG;  // NaN
+    const long long K = (long long)M + L;
+    if (K > 0x7fffffffLL / 2 || r_rows < K) return TXL_ERR_SHAPE;
+    if (dh != 64 || dtype != TXL_BF16) return TXL_ERR_UNSUPPORTED;
+    for (const void *p : {q, k, v, r, u, v_bias, dout, (const void *)dq, (const void *)dk,
+                          (const void *)dv, (const void *)dr, (const void *)du,
+                          (const void *)dv_bias})
+        if (!aligned(p, 16)) return TXL_ERR_MISALIGNED;
+    const long long BH = (long long)B * H;
+    const long long rows = txl::kBwdRows;
+    if (BH > 0x7fffffffLL || (L + rows - 1) / rows > 65535 || (K + rows - 1) / rows > 65535 ||
+        H > 65535)
+        return TXL_ERR_UNSUPPORTED;
+    const size_t need = txl::bwd_workspace_bytes(B, H, L);
+    if (!workspace || workspace_bytes < need) return TXL_ERR_WORKSPACE;
+    if (!aligned(workspace, 256)) return TXL_ERR_MISALIGNED;
+
+    cudaError_t err;
+    unsigned int *status = status_word(&err);
+    if (!status) return TXL_ERR_CUDA;
+    txl::BwdParams p{};
+    p.q = static_cast<const __nv_bfloat16 *>(q);
+    p.k = static_cast<const __nv_bfloat16 *>(k);
+    p.v = static_cast<const __nv_bfloat16 *>(v);
+    p.r = static_cast<const __nv_bfloat16 *>(r);
+    p.u = static_cast<const __nv_bfloat16 *>(u);
+    p.vb = static_cast<const __nv_bfloat16 *>(v_bias);
+    p.dout = static_cast<const __nv_bfloat16 *>(dout);
+    p.dq = dq;
+    p.dk = dk;
+    p.dv = dv;
+    p.dr = dr;
+    p.du = du;
+    p.dvb = dv_bias;
+    // workspace: log2-sum-exp and D per row, then the bias partials (256-byte
+    // aligned regions, as txl::bwd_workspace_bytes counts them)
+    const size_t row_bytes = ((size_t)BH * L * sizeof(float) + 255) & ~(size_t)255;
+    char *ws = static_cast<char *>(workspace);
+    p.lse2 = reinterpret_cast<float *>(ws);
+    p.dsum = reinterpret_cast<float *>(ws + row_bytes);
+    p.part = reinterpret_cast<float *>(ws + 2 * row_bytes);
+    p.B = B;
+    p.H = H;
+    p.M = M;
+    p.L = L;
+    p.K = (int)K;
+    p.r_rows = r_rows;
+    p.scale = scale;
+    p.scale_log2 = scale * 1.4426950408889634f;
+    p.status = status;
+    return cuda_status(txl::launch_relattn_bwd(p, as_stream(stream)));
+}
