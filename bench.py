@@ -113,6 +113,9 @@ def parse_args():
     ap.add_argument("--project", action="store_true",
                     help="time one layer's fused projection (txl_qkv_project) at the 12-layer "
                          "stream's shape against the unfused calls it replaces")
+    ap.add_argument("--bwd", action="store_true",
+                    help="time the backward (txl_relattn_bwd) at the headline shape, instead of "
+                         "the headline step")
     ap.add_argument("--workload", nargs="*", default=None,
                     help="with --configs: only these workloads (names as in txl_inputs.WORKLOADS)")
     return ap.parse_args()
@@ -959,8 +962,91 @@ def run_stack(args):
             "ms_per_segment": ms, "tokens_per_s": w.B * w.L / (ms * 1e-3)}}), flush=True)
 
 
+def bwd_tile_visits(B, H, L, M, T=64):
+    """64 x 64 pair tiles each launch of txl_relattn_bwd visits (the kernels'
+    loop bounds: key tiles up to the last key a chunk sees, query chunks from
+    the first that sees a key tile or a distance tile)."""
+    K = M + L
+    n_chunks = -(-L // T)
+    rows_keys = sum(-(-min(K, M + i0 + T) // T) for i0 in range(0, L, T))
+    keys_rows = sum(len(range(max(0, j0 - M) // T * T, L, T)) for j0 in range(0, K, T))
+    dist_rows = B * sum(len(range(max(0, d0 - M - (T - 1)) // T * T, L, T)) for d0 in range(0, K, T))
+    return {"stats": B * H * rows_keys, "dq": B * H * rows_keys, "dkv": B * H * keys_rows,
+            "dr": H * dist_rows, "chunks": B * H * n_chunks}
+
+
+def run_bwd(args):
+    """Graph-replayed time of one backward call (txl_relattn_bwd) at the headline
+    shape, two rotating input sets (k, v, q and dout of a set: 121 MB).  Reports
+    the fp32 FLOPs the five kernels execute (scores recomputed per pass, the
+    position terms as 64 x 128 window products), their rate against the fp32
+    FMA peak of the SM count and maximum clock (128 FMA lanes per SM), and the
+    rate of the backward's own FLOPs (twice the forward's: dP, dv, and the
+    gradients of the content and position scores)."""
+    import torch
+    import transformer_xl_relative_pos_gb300 as txl
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    w = txl_inputs.WORKLOADS[txl_inputs.HEADLINE]
+    B, H, L, M = w.B, w.H, w.L, w.M
+    K = M + L
+    g = torch.Generator(device=dev).manual_seed(0)
+    mk = lambda *sh: (torch.randn(*sh, device=dev, generator=g) * 0.6).to(torch.bfloat16)
+    sets = [(mk(B, H, L, 64), mk(B, H, K, 64), mk(B, H, K, 64), mk(B, H, L, 64)) for _ in range(2)]
+    r, u, vb = mk(H, K, 64), mk(H, 64) * 0.5, mk(H, 64) * 0.5
+    f32 = lambda *sh: torch.empty(*sh, dtype=torch.float32, device=dev)
+    grads = (f32(B, H, L, 64), f32(B, H, K, 64), f32(B, H, K, 64), f32(H, K, 64), f32(H, 64),
+             f32(H, 64))
+    ws = torch.empty(max(txl.bwd_workspace_size(B, H, L), 256), dtype=torch.uint8, device=dev)
+    scale = 1.0 / math.sqrt(64)
+
+    def call(i):
+        q, k, v, dout = sets[i % 2]
+        txl.relattn_bwd(q, k, v, r, u, vb, dout, M, scale, grads=grads, workspace=ws)
+
+    st = torch.cuda.Stream(dev)
+    with torch.cuda.stream(st):
+        for i in range(3):
+            call(i)
+    torch.cuda.synchronize()
+    per = 10
+    gr = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(gr, stream=st):
+        for i in range(per):
+            call(i)
+    gr.replay()
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(st)
+    with torch.cuda.stream(st):
+        for _ in range(max(1, args.calls)):
+            gr.replay()
+    e1.record(st)
+    torch.cuda.synchronize()
+    assert txl.device_status() == 0
+    us = e0.elapsed_time(e1) * 1e3 / (per * max(1, args.calls))
+    visits = bwd_tile_visits(B, H, L, M)
+    T = 64
+    mac_tile = {"stats": 4 * T ** 3, "dq": 7 * T ** 3, "dkv": 6 * T ** 3, "dr": 6 * T ** 3}
+    executed = 2.0 * sum(visits[k] * mac_tile[k] for k in mac_tile)
+    sms = torch.cuda.get_device_properties(dev).multi_processor_count
+    fp32_peak = sms * 128 * 2 * 2.07e9  # FMA lanes x 2 FLOP x maximum SM clock
+    useful = 2.0 * 6.0 * L * K * 64 * B * H
+    print(json.dumps({"bwd": {
+        "workload": w.name, "B": B, "H": H, "L": L, "M": M, "us_per_call": round(us, 2),
+        "executed_tflops": round(executed / (us * 1e-6) / 1e12, 2),
+        "fp32_peak_tflops": round(fp32_peak / 1e12, 1),
+        "alu_frac": round(executed / (us * 1e-6) / fp32_peak, 3),
+        "useful_tflops": round(useful / (us * 1e-6) / 1e12, 2),
+        "executed_gflop": round(executed / 1e9, 1), "useful_gflop": round(useful / 1e9, 1),
+        "tile_visits": visits, "launches": 5}}), flush=True)
+
+
 def main():
     args = parse_args()
+    if args.bwd:
+        run_bwd(args)
+        return
     if args.stack:
         run_stack(args)
         return
