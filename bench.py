@@ -978,11 +978,12 @@ def bwd_tile_visits(B, H, L, M, T=64):
 def run_bwd(args):
     """Graph-replayed time of one backward call (txl_relattn_bwd) at the headline
     shape, two rotating input sets (k, v, q and dout of a set: 121 MB).  Reports
-    the fp32 FLOPs the five kernels execute (scores recomputed per pass, the
-    position terms as 64 x 128 window products), their rate against the fp32
-    FMA peak of the SM count and maximum clock (128 FMA lanes per SM), and the
-    rate of the backward's own FLOPs (twice the forward's: dP, dv, and the
-    gradients of the content and position scores)."""
+    the tensor-core FLOPs the five kernels execute (warp-level bf16 MMAs, fp32
+    accumulation: scores recomputed per pass, the position terms as 64 x 128
+    window products, the products with g and P twice for their bf16 head and
+    rest) against the measured bf16 peak, and the rate of the backward's own
+    FLOPs (twice the forward's: dP, dv, and the gradients of the content and
+    position scores)."""
     import torch
     import transformer_xl_relative_pos_gb300 as txl
     dev = torch.device("cuda", 0)
@@ -1027,18 +1028,22 @@ def run_bwd(args):
     us = e0.elapsed_time(e1) * 1e3 / (per * max(1, args.calls))
     visits = bwd_tile_visits(B, H, L, M)
     T = 64
-    mac_tile = {"stats": 4 * T ** 3, "dq": 7 * T ** 3, "dkv": 6 * T ** 3, "dr": 6 * T ** 3}
+    # tile multiply-adds: stats q.k, dout.v (64^3 each), the q.r window (2 x 64^3);
+    # dq adds g.k and the window-ordered g.r (head and rest: 2 x 3 x 64^3);
+    # dk/dv add P^T dout and g^T q (2 x 2 x 64^3); the table tile q.r, the key
+    # and value windows and g^T q (64^3 + 4 x 64^3 + 2 x 64^3)
+    mac_tile = {"stats": 4 * T ** 3, "dq": 10 * T ** 3, "dkv": 8 * T ** 3, "dr": 7 * T ** 3}
     executed = 2.0 * sum(visits[k] * mac_tile[k] for k in mac_tile)
-    sms = torch.cuda.get_device_properties(dev).multi_processor_count
-    fp32_peak = sms * 128 * 2 * 2.07e9  # FMA lanes x 2 FLOP x maximum SM clock
+    pk = peaks()
     useful = 2.0 * 6.0 * L * K * 64 * B * H
     print(json.dumps({"bwd": {
         "workload": w.name, "B": B, "H": H, "L": L, "M": M, "us_per_call": round(us, 2),
+        "executed_tensor_gflop": round(executed / 1e9, 1),
         "executed_tflops": round(executed / (us * 1e-6) / 1e12, 2),
-        "fp32_peak_tflops": round(fp32_peak / 1e12, 1),
-        "alu_frac": round(executed / (us * 1e-6) / fp32_peak, 3),
+        "bf16_peak_tflops": pk["bf16_tflops"], "peak_source": pk["source"],
+        "tensor_frac": round(executed / (us * 1e-6) / 1e12 / pk["bf16_tflops"], 4),
+        "useful_gflop": round(useful / 1e9, 1),
         "useful_tflops": round(useful / (us * 1e-6) / 1e12, 2),
-        "executed_gflop": round(executed / 1e9, 1), "useful_gflop": round(useful / 1e9, 1),
         "tile_visits": visits, "launches": 5}}), flush=True)
 
 

@@ -9,23 +9,29 @@
 //   du = sum g_ij k_j                     dv_bias = sum g_ij r_{M+i-j}
 // (dr, du, dv_bias summed over the batch: the table and biases are shared).
 //
-// Five launches, all fp32 on the CUDA cores, tiles of 64 query rows x 64
-// columns (keys, or distances for the table gradient), 256 threads, each
-// thread a 4 x 4 block of pairs (rows 4 ty + a, columns tx + 16 c):
+// Five launches over tiles of 64 query rows x 64 columns (keys, or distances
+// for the table gradient), 256 threads = 8 warps, warp w taking rows
+// 16 (w / 2) .. +15 and columns 32 (w % 2) .. +31 of every 64 x 64 product:
 //   stats   per 64-row chunk, over its key tiles: online log-sum-exp of the
-//           scores and D (no value from the forward call is needed)
+//           scores and D (nothing from the forward call is needed)
 //   dq      per 64-row chunk, over its key tiles: dq, and the chunk's
 //           partials of du and dv_bias
 //   dkv     per 64-key tile, over the query chunks that see it: dk, dv
 //   dr      per head and 64-distance tile, over the batch and query chunks:
 //           the table gradient, with no atomics
 //   bias    per head: du, dv_bias from the partials, in a fixed order
-// Every tile recomputes its scores.  The Appendix B shift is index arithmetic,
-// as in the forward: the position term of a 64 x 64 pair tile is row i of the
-// dense product (q + v) R_w^T over the tile's 127-distance window, read at
-// window column i - j + 63; the shifted contractions (dq's position part, and
-// the content part of the distance tiles) are dense products over the window
-// of the same g re-laid out by that index.  Results repeat bit for bit.
+// Every tile recomputes its scores.  All products run on the tensor cores as
+// warp-level mma.m16n8k16 (bf16 operands from shared memory by ldmatrix, fp32
+// accumulation), exactly: q, k, v, r and dout are bf16 already, the bias terms
+// u.k_j and v.r_d are per-column vectors added in fp32, g and P (fp32) enter as
+// a bf16 head plus the bf16 rounding of the rest (~2^-17 relative), and the
+// rank-one parts of dk and dr (column sums of g times u or v) are added in
+// fp32.  The Appendix B shift is index arithmetic, as in the forward: the
+// position term of a pair tile is row i of the product q R_w^T over the tile's
+// 127-distance window, read at window column i - j + 63; the shifted
+// contractions (dq's position part; the content part of a distance tile,
+// whose pair (i, d) is key M + i - d) are window products of g laid out by the
+// same index.  Results repeat bit for bit.
 #include "kernels.h"
 
 namespace txl {
@@ -35,268 +41,471 @@ constexpr int DH = 64;
 constexpr int T = kBwdRows;     // rows / columns of a pair tile
 constexpr int W = 2 * T;        // window rows of a tile (127 used)
 constexpr int THREADS = 256;
-constexpr int LD = DH + 4;      // fp32 row stride of a 64-wide tile (16-byte rows, bank-spread)
-constexpr int LDW = W + 4;      // row stride of a 128-wide window product
+constexpr int LDB = (DH + 8) * 2;   // bytes per bf16 row of 64 (+8 pad: conflict-free ldmatrix)
+constexpr int LDZ = (W + 8) * 2;    // bytes per bf16 row of 128
+constexpr int LDX = W + 4;          // floats per row of the fp32 window product
 
-// Shared-memory regions (floats).  q + u, q + v and dout of a row chunk; a
-// 64-row operand (key tile, or table tile by distance); a 128-row window
-// (table rows by distance, or key rows); the 64 x 128 window product; a
-// 64 x 64 transposed pair tile; and a region holding either the value tile and
-// a second pair tile (key tiles) or the value window (distance tiles).
-constexpr int OFF_QU = 0;
-constexpr int OFF_QV = OFF_QU + T * LD;
-constexpr int OFF_DO = OFF_QV + T * LD;
-constexpr int OFF_A64 = OFF_DO + T * LD;
-constexpr int OFF_W1 = OFF_A64 + T * LD;
-constexpr int OFF_XS = OFF_W1 + W * LD;
-constexpr int OFF_T1 = OFF_XS + T * LDW;
-constexpr int OFF_U = OFF_T1 + T * LD;
-constexpr int OFF_V64 = OFF_U;             // key tiles: value tile
-constexpr int OFF_T2 = OFF_U + T * LD;     // key tiles: second pair tile
-constexpr int OFF_W2 = OFF_U;              // distance tiles: value window
-constexpr int SMEM_FLOATS = OFF_U + W * LD;
-constexpr int SMEM_BYTES = SMEM_FLOATS * 4;
+// Shared memory (bytes): bf16 operand tiles, g and P as head / rest pairs, the
+// window-ordered g, the fp32 window product, per-column bias vectors and
+// reduction scratch.
+constexpr int OFF_Q = 0;                    // q rows of the chunk [64][72]
+constexpr int OFF_D = OFF_Q + T * LDB;      // dout rows
+constexpr int OFF_K = OFF_D + T * LDB;      // key tile (distance tiles: table tile)
+constexpr int OFF_V = OFF_K + T * LDB;      // value tile
+constexpr int OFF_W = OFF_V + T * LDB;      // window [128][72]: table rows, or key rows
+constexpr int OFF_W2 = OFF_W + W * LDB;     // value window (distance tiles)
+constexpr int OFF_GH = OFF_W2 + W * LDB;    // g head [64][72], pair (i, column)
+constexpr int OFF_GL = OFF_GH + T * LDB;    // g rest
+constexpr int OFF_PH = OFF_GL + T * LDB;    // P head
+constexpr int OFF_PL = OFF_PH + T * LDB;    // P rest
+constexpr int OFF_ZH = OFF_PL + T * LDB;    // g by window column [64][136], head
+constexpr int OFF_ZL = OFF_ZH + T * LDZ;    // rest
+constexpr int OFF_XS = OFF_ZL + T * LDZ;    // fp32 [64][132] window product
+constexpr int OFF_BK = OFF_XS + T * LDX * 4;  // fp32 [64]: u.k_j (or v.r_d)
+constexpr int OFF_BW = OFF_BK + T * 4;        // fp32 [128]: v.r_w (or u.k_w) of the window
+constexpr int OFF_RED = OFF_BW + W * 4;       // fp32 [8][64] reduction scratch
+constexpr int OFF_CS = OFF_RED + 8 * T * 4;   // fp32 [64]: column sums of g over the chunks
+// second key tile, value tile and table window: the row-chunk kernels copy
+// the next key tile in while computing on the current one
+constexpr int OFF_K1 = OFF_CS + T * 4;
+constexpr int OFF_V1 = OFF_K1 + T * LDB;
+constexpr int OFF_W1 = OFF_V1 + T * LDB;
+constexpr int SMEM_BYTES = OFF_W1 + W * LDB;
 static_assert(SMEM_BYTES <= 232448, "shared memory budget exceeded");
-static_assert((LD * 4) % 16 == 0 && (LDW * 4) % 16 == 0, "rows must stay 16-byte aligned");
+static_assert(OFF_W % 16 == 0 && OFF_GH % 16 == 0 && OFF_ZH % 16 == 0 && OFF_XS % 16 == 0 &&
+                  OFF_K1 % 16 == 0 && OFF_W1 % 16 == 0,
+              "ldmatrix rows must be 16-byte aligned");
+
+__device__ __forceinline__ uint32_t smem_u32(const void *p)
+{
+    return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
 
 __device__ __forceinline__ float bf(uint32_t w, int hi)
 {
     return __uint_as_float(hi ? (w & 0xffff0000u) : (w << 16));
 }
 
-// Rows w = 0 .. n-1 of dst [n][ld] (fp32) from bf16 rows src_row(w) = row0 +
-// step * w of a [rows_total][64] matrix; rows outside [0, rows_total) become
-// zeros.  `add` (may be null): a 64-vector added to every loaded row.
-__device__ __forceinline__ void stage(float *dst, int ld, int n, const __nv_bfloat16 *src,
-                                      long long row0, int step, long long rows_total,
-                                      const __nv_bfloat16 *add)
+__device__ __forceinline__ uint32_t pack2(float lo, float hi)
+{
+    const __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
+    return *reinterpret_cast<const uint32_t *>(&v);
+}
+
+// (head, rest) bf16 pairs of two fp32 values: x ~ head + rest to ~2^-17.
+__device__ __forceinline__ void split2(float x0, float x1, uint32_t &head, uint32_t &rest)
+{
+    head = pack2(x0, x1);
+    rest = pack2(x0 - bf(head, 0), x1 - bf(head, 1));
+}
+
+__device__ __forceinline__ void ldsm_x4(uint32_t (&r)[4], uint32_t addr)
+{
+    asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0, %1, %2, %3}, [%4];"
+                 : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
+                 : "r"(addr));
+}
+
+__device__ __forceinline__ void ldsm_x4_t(uint32_t (&r)[4], uint32_t addr)
+{
+    asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0, %1, %2, %3}, [%4];"
+                 : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
+                 : "r"(addr));
+}
+
+__device__ __forceinline__ void mma16816(float (&c)[4], const uint32_t (&a)[4], uint32_t b0,
+                                         uint32_t b1)
+{
+    asm volatile("mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0, %1, %2, %3}, "
+                 "{%4, %5, %6, %7}, {%8, %9}, {%0, %1, %2, %3};"
+                 : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
+                 : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+}
+
+template <int NT>
+__device__ __forceinline__ void zero(float (&c)[NT][4])
+{
+#pragma unroll
+    for (int n = 0; n < NT; ++n) c[n][0] = c[n][1] = c[n][2] = c[n][3] = 0.f;
+}
+
+// One warp: C[16][8 NT] += A[16][kd] B^T with A stored [row][k] (a: address of
+// the warp's first row) and B stored [n][k] (b: address of its first column n).
+template <int NT>
+__device__ __forceinline__ void warp_nt(float (&c)[NT][4], uint32_t a, int lda, uint32_t b,
+                                        int ldb, int kd, int lane)
+{
+#pragma unroll 2
+    for (int k0 = 0; k0 < kd; k0 += 16) {
+        uint32_t af[4];
+        ldsm_x4(af, a + (lane & 15) * lda + (k0 + (lane >> 4) * 8) * 2);
+#pragma unroll
+        for (int np = 0; np < NT / 2; ++np) {
+            uint32_t bfr[4];
+            ldsm_x4(bfr, b + (np * 16 + (lane >> 4) * 8 + (lane & 7)) * ldb +
+                             (k0 + ((lane >> 3) & 1) * 8) * 2);
+            mma16816(c[2 * np], af, bfr[0], bfr[1]);
+            mma16816(c[2 * np + 1], af, bfr[2], bfr[3]);
+        }
+    }
+}
+
+// One warp: C[16][8 NT] += (Ah + Al)[16][kd] B with B stored [k][n] (b: address
+// of row k = 0 at the warp's first column n).  A stored [row][k] (a_trans
+// false; ah, al: addresses of the warp's first row) or [k][row] (a_trans: the
+// addresses of row k = 0 at the warp's first row index).
+template <int NT>
+__device__ __forceinline__ void warp_nn2(float (&c)[NT][4], uint32_t ah, uint32_t al, int lda,
+                                         bool a_trans, uint32_t b, int ldb, int kd, int lane)
+{
+#pragma unroll 2
+    for (int k0 = 0; k0 < kd; k0 += 16) {
+        uint32_t fh[4], fl[4];
+        if (a_trans) {
+            const uint32_t off = (k0 + (lane >> 4) * 8 + (lane & 7)) * lda + ((lane >> 3) & 1) * 16;
+            ldsm_x4_t(fh, ah + off);
+            ldsm_x4_t(fl, al + off);
+        } else {
+            const uint32_t off = (lane & 15) * lda + (k0 + (lane >> 4) * 8) * 2;
+            ldsm_x4(fh, ah + off);
+            ldsm_x4(fl, al + off);
+        }
+#pragma unroll
+        for (int np = 0; np < NT / 2; ++np) {
+            uint32_t bfr[4];
+            ldsm_x4_t(bfr, b + (k0 + ((lane >> 3) & 1) * 8 + (lane & 7)) * ldb +
+                               (np * 16 + (lane >> 4) * 8) * 2);
+            mma16816(c[2 * np], fh, bfr[0], bfr[1]);
+            mma16816(c[2 * np + 1], fh, bfr[2], bfr[3]);
+            mma16816(c[2 * np], fl, bfr[0], bfr[1]);
+            mma16816(c[2 * np + 1], fl, bfr[2], bfr[3]);
+        }
+    }
+}
+
+// Rows w = 0 .. n-1 of a bf16 tile (row stride ld bytes) from rows row0 + step w
+// of a [rows_total][64] bf16 matrix; rows outside [0, rows_total) are zeros.
+__device__ __forceinline__ void stage(uint8_t *dst, int ld, int n, const __nv_bfloat16 *src,
+                                      long long row0, int step, long long rows_total)
 {
     for (int idx = threadIdx.x; idx < n * 8; idx += THREADS) {
         const int w = idx >> 3, c = idx & 7;
         const long long sr = row0 + (long long)step * w;
-        float4 lo = make_float4(0.f, 0.f, 0.f, 0.f), hi = lo;
-        if (sr >= 0 && sr < rows_total) {
-            const uint4 x = __ldg(reinterpret_cast<const uint4 *>(src + sr * DH) + c);
-            lo = make_float4(bf(x.x, 0), bf(x.x, 1), bf(x.y, 0), bf(x.y, 1));
-            hi = make_float4(bf(x.z, 0), bf(x.z, 1), bf(x.w, 0), bf(x.w, 1));
-            if (add) {
-                const uint4 y = __ldg(reinterpret_cast<const uint4 *>(add) + c);
-                lo.x += bf(y.x, 0); lo.y += bf(y.x, 1); lo.z += bf(y.y, 0); lo.w += bf(y.y, 1);
-                hi.x += bf(y.z, 0); hi.y += bf(y.z, 1); hi.z += bf(y.w, 0); hi.w += bf(y.w, 1);
-            }
+        uint4 x = make_uint4(0u, 0u, 0u, 0u);
+        if (sr >= 0 && sr < rows_total) x = __ldg(reinterpret_cast<const uint4 *>(src + sr * DH) + c);
+        *reinterpret_cast<uint4 *>(dst + w * ld + c * 16) = x;
+    }
+}
+
+// The same with asynchronous 16-byte copies (rows outside the matrix are
+// zero-filled by a zero source size; their source address stays in bounds).
+__device__ __forceinline__ void stage_async(uint8_t *dst, int ld, int n, const __nv_bfloat16 *src,
+                                            long long row0, int step, long long rows_total)
+{
+    for (int idx = threadIdx.x; idx < n * 8; idx += THREADS) {
+        const int w = idx >> 3, c = idx & 7;
+        const long long sr = row0 + (long long)step * w;
+        const bool in = sr >= 0 && sr < rows_total;
+        const __nv_bfloat16 *g = src + (in ? sr * DH : 0) + c * 8;
+        asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(smem_u32(dst + w * ld + c * 16)),
+                     "l"(g), "r"(in ? 16 : 0)
+                     : "memory");
+    }
+    asm volatile("cp.async.commit_group;" ::: "memory");
+}
+
+template <int N>
+__device__ __forceinline__ void async_wait()
+{
+    asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
+}
+
+// out[w] = vec . row w of a staged bf16 tile (n = 64 or 128 rows), fp32; vec:
+// 64 bf16 in global memory.  Four threads per row (every lane of a warp takes
+// part in the shuffles: n * 4 is a multiple of the block).
+__device__ __forceinline__ void row_dots(float *out, const uint8_t *tile, int ld, int n,
+                                         const __nv_bfloat16 *vec)
+{
+    for (int idx = threadIdx.x; idx < n * 4; idx += THREADS) {
+        const int w = idx >> 2, part = idx & 3;
+        const uint4 *row = reinterpret_cast<const uint4 *>(tile + w * ld) + part * 2;
+        const uint4 *vv = reinterpret_cast<const uint4 *>(vec) + part * 2;
+        float s = 0.f;
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+            const uint4 x = row[h], y = __ldg(vv + h);
+            s = fmaf(bf(x.x, 0), bf(y.x, 0), s); s = fmaf(bf(x.x, 1), bf(y.x, 1), s);
+            s = fmaf(bf(x.y, 0), bf(y.y, 0), s); s = fmaf(bf(x.y, 1), bf(y.y, 1), s);
+            s = fmaf(bf(x.z, 0), bf(y.z, 0), s); s = fmaf(bf(x.z, 1), bf(y.z, 1), s);
+            s = fmaf(bf(x.w, 0), bf(y.w, 0), s); s = fmaf(bf(x.w, 1), bf(y.w, 1), s);
         }
-        float4 *d = reinterpret_cast<float4 *>(dst + w * ld + c * 8);
-        d[0] = lo;
-        d[1] = hi;
+        s += __shfl_xor_sync(0xffffffffu, s, 1);
+        s += __shfl_xor_sync(0xffffffffu, s, 2);
+        if (part == 0) out[w] = s;
     }
 }
 
-// acc[a][c] += sum_k A[4 ty + a][k] * B[tx + 16 c][k]   (both row-major in k)
-template <int NC>
-__device__ __forceinline__ void gemm_nt(float (&acc)[4][NC], const float *A, int lda,
-                                        const float *B, int ldb, int kdim, int ty, int tx)
+// The lane's place in a 64 x 64 product: warp w holds rows 16 (w/2) + g and
+// + 8, columns 32 (w%2) + 8 n + 2 t and + 1 (n = 0..3): element q of
+// fragment n is row rb + g + 8 (q / 2), column cb + 8 n + 2 t + q % 2.
+struct Lane {
+    int warp, lane, g, t, rb, cb;
+};
+
+__device__ __forceinline__ Lane lane_of()
 {
-#pragma unroll 2
-    for (int k = 0; k < kdim; k += 4) {
-        float4 a[4], b[NC];
-#pragma unroll
-        for (int r = 0; r < 4; ++r) a[r] = *reinterpret_cast<const float4 *>(A + (ty * 4 + r) * lda + k);
-#pragma unroll
-        for (int c = 0; c < NC; ++c) b[c] = *reinterpret_cast<const float4 *>(B + (tx + 16 * c) * ldb + k);
-#pragma unroll
-        for (int r = 0; r < 4; ++r)
-#pragma unroll
-            for (int c = 0; c < NC; ++c) {
-                float s = acc[r][c];
-                s = fmaf(a[r].x, b[c].x, s);
-                s = fmaf(a[r].y, b[c].y, s);
-                s = fmaf(a[r].z, b[c].z, s);
-                s = fmaf(a[r].w, b[c].w, s);
-                acc[r][c] = s;
-            }
-    }
+    Lane L;
+    L.warp = threadIdx.x >> 5;
+    L.lane = threadIdx.x & 31;
+    L.g = L.lane >> 2;
+    L.t = L.lane & 3;
+    L.rb = 16 * (L.warp >> 1);
+    L.cb = 32 * (L.warp & 1);
+    return L;
 }
 
-// acc[a][c] += sum_k A[4 ty + a][k] * B[k][tx + 16 c]   (A row-major in k, B in n)
-template <int NC>
-__device__ __forceinline__ void gemm_nn(float (&acc)[4][NC], const float *A, int lda,
-                                        const float *B, int ldb, int kdim, int ty, int tx)
+// The 64 x 128 window product of the warp's rows, plus a per-column vector,
+// into the fp32 window buffer (columns 64 (w%2) .. +63).
+__device__ __forceinline__ void window_product(uint8_t *sm, const Lane &L, int a_off, int b_off,
+                                               const float *colvec)
 {
-#pragma unroll 2
-    for (int k = 0; k < kdim; k += 4) {
-        float4 a[4];
-#pragma unroll
-        for (int r = 0; r < 4; ++r) a[r] = *reinterpret_cast<const float4 *>(A + (ty * 4 + r) * lda + k);
-#pragma unroll
-        for (int kk = 0; kk < 4; ++kk) {
-            float b[NC];
-#pragma unroll
-            for (int c = 0; c < NC; ++c) b[c] = B[(k + kk) * ldb + tx + 16 * c];
-#pragma unroll
-            for (int r = 0; r < 4; ++r) {
-                const float av = kk == 0 ? a[r].x : kk == 1 ? a[r].y : kk == 2 ? a[r].z : a[r].w;
-#pragma unroll
-                for (int c = 0; c < NC; ++c) acc[r][c] = fmaf(av, b[c], acc[r][c]);
-            }
-        }
-    }
-}
-
-template <int R, int C>
-__device__ __forceinline__ void zero(float (&a)[R][C])
-{
-#pragma unroll
-    for (int r = 0; r < R; ++r)
-#pragma unroll
-        for (int c = 0; c < C; ++c) a[r][c] = 0.f;
-}
-
-// ---- staging of a row chunk and of a key tile ------------------------------
-// q + u, q + v and dout of rows i0 .. i0+63 of plane bh (rows past L: zeros).
-__device__ __forceinline__ void stage_rows(float *sm, const BwdParams &p, long long bh, int h, int i0)
-{
-    const __nv_bfloat16 *q = p.q + bh * p.L * DH;
-    stage(sm + OFF_QU, LD, T, q, i0, 1, p.L, p.u + (size_t)h * DH);
-    stage(sm + OFF_QV, LD, T, q, i0, 1, p.L, p.vb + (size_t)h * DH);
-    stage(sm + OFF_DO, LD, T, p.dout + bh * p.L * DH, i0, 1, p.L, nullptr);
-}
-
-// Window row w = the table row of distance dmin + w (row r_rows-1-distance of
-// r; distances outside [0, r_rows) give zeros).
-__device__ __forceinline__ void stage_table_window(float *dst, const BwdParams &p, int h, long long dmin)
-{
-    stage(dst, LD, W, p.r + (size_t)h * p.r_rows * DH, p.r_rows - 1 - dmin, -1, p.r_rows, nullptr);
-}
-
-// Log2-scaled scores (-inf where masked) and dP = dout . v of the thread's 16
-// pairs (row i = 4 ty + a of the chunk at i0, key j = tx + 16 c of the tile at
-// j0), from staged rows, keys (A64), values (V64) and the table window of
-// distances M + i0 - j0 - 63 + w (W1).  Contains a block barrier.
-__device__ __forceinline__ void key_tile_scores(float *sm, const BwdParams &p, int i0, int j0,
-                                                int ty, int tx, float (&s)[4][4], float (&dp)[4][4])
-{
-    float sc[4][4], x[4][8];
-    zero(sc);
+    float x[8][4];
     zero(x);
+    warp_nt<8>(x, smem_u32(sm + a_off) + L.rb * LDB, LDB,
+               smem_u32(sm + b_off) + 64 * (L.warp & 1) * LDB, LDB, DH, L.lane);
+    float *xs = reinterpret_cast<float *>(sm + OFF_XS);
+#pragma unroll
+    for (int n = 0; n < 8; ++n)
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+            const int col = 64 * (L.warp & 1) + 8 * n + 2 * L.t + (q & 1);
+            xs[(L.rb + L.g + 8 * (q >> 1)) * LDX + col] = x[n][q] + (colvec ? colvec[col] : 0.f);
+        }
+}
+
+// Where the operands of the current tile sit (byte offsets): q rows, dout
+// rows, keys, values, table window.
+struct Bufs {
+    int q, d, k, v, w;
+};
+
+// Log2-scaled scores (-inf where masked) and dP = dout . v of the lane's 16
+// pairs of the key tile at j0, from the staged q, dout, keys, values, table
+// window (distances M + i0 - j0 - 63 + w) and bias vectors (u.k_j, v.r_w).
+// Contains a block barrier.
+__device__ __forceinline__ void key_tile_scores(uint8_t *sm, const BwdParams &p, const Lane &L,
+                                                int i0, int j0, float (&s)[4][4], float (&dp)[4][4],
+                                                const Bufs &B)
+{
+    float sc[4][4];
+    zero(sc);
     zero(dp);
-    gemm_nt<4>(sc, sm + OFF_QU, LD, sm + OFF_A64, LD, DH, ty, tx);
-    gemm_nt<8>(x, sm + OFF_QV, LD, sm + OFF_W1, LD, DH, ty, tx);
-    gemm_nt<4>(dp, sm + OFF_DO, LD, sm + OFF_V64, LD, DH, ty, tx);
-    float *xs = sm + OFF_XS;
-#pragma unroll
-    for (int r = 0; r < 4; ++r)
-#pragma unroll
-        for (int c = 0; c < 8; ++c) xs[(ty * 4 + r) * LDW + tx + 16 * c] = x[r][c];
+    warp_nt<4>(sc, smem_u32(sm + B.q) + L.rb * LDB, LDB, smem_u32(sm + B.k) + L.cb * LDB, LDB,
+               DH, L.lane);
+    warp_nt<4>(dp, smem_u32(sm + B.d) + L.rb * LDB, LDB, smem_u32(sm + B.v) + L.cb * LDB, LDB,
+               DH, L.lane);
+    const float *bk = reinterpret_cast<const float *>(sm + OFF_BK);
+    window_product(sm, L, B.q, B.w, reinterpret_cast<const float *>(sm + OFF_BW));
     __syncthreads();
+    const float *xs = reinterpret_cast<const float *>(sm + OFF_XS);
 #pragma unroll
-    for (int r = 0; r < 4; ++r)
+    for (int n = 0; n < 4; ++n)
 #pragma unroll
-        for (int c = 0; c < 4; ++c) {
-            const int i = ty * 4 + r, j = tx + 16 * c;
+        for (int q = 0; q < 4; ++q) {
+            const int i = L.rb + L.g + 8 * (q >> 1), j = L.cb + 8 * n + 2 * L.t + (q & 1);
             const int gi = i0 + i, gj = j0 + j;
             // Appendix B: distance M + gi - gj is window column i - j + 63
-            const float pos = xs[i * LDW + i - j + T - 1];
+            const float pos = xs[i * LDX + i - j + T - 1];
             const bool keep = gi < p.L && gj < p.K && gj <= p.M + gi;
-            s[r][c] = keep ? (sc[r][c] + pos) * p.scale_log2 : -INFINITY;
+            s[n][q] = keep ? (sc[n][q] + bk[j] + pos) * p.scale_log2 : -INFINITY;
         }
 }
 
-// Row statistics of the thread's rows, from the stats kernel's results.
-__device__ __forceinline__ void load_row_stats(const BwdParams &p, long long bh, int i0, int ty,
-                                               float (&ls)[4], float (&dd)[4])
+__device__ __forceinline__ void stage_rows(uint8_t *sm, const BwdParams &p, long long bh, int i0)
+{
+    stage(sm + OFF_Q, LDB, T, p.q + bh * p.L * DH, i0, 1, p.L);
+    stage(sm + OFF_D, LDB, T, p.dout + bh * p.L * DH, i0, 1, p.L);
+}
+
+// The row-chunk kernels' key tiles, double-buffered: copies of tile j0 (keys,
+// values, table window of distances M + i0 - j0 - 63 + w) into buffer `buf`
+// go out asynchronously; key_tile_ready waits for the older group, then
+// forms u.k_j and v.r_w of that buffer.
+__device__ __forceinline__ void issue_key_tile(uint8_t *sm, const BwdParams &p, long long bh, int h,
+                                               int i0, int j0, int buf)
+{
+    stage_async(sm + (buf ? OFF_K1 : OFF_K), LDB, T, p.k + bh * p.K * DH, j0, 1, p.K);
+    stage_async(sm + (buf ? OFF_V1 : OFF_V), LDB, T, p.v + bh * p.K * DH, j0, 1, p.K);
+    const long long dmin = (long long)p.M + i0 - j0 - (T - 1);
+    stage_async(sm + (buf ? OFF_W1 : OFF_W), LDB, W, p.r + (size_t)h * p.r_rows * DH,
+                p.r_rows - 1 - dmin, -1, p.r_rows);
+}
+
+// `more`: another tile's copies were issued after this one's (3 groups each).
+__device__ __forceinline__ void key_tile_ready(uint8_t *sm, const BwdParams &p, int h, int buf, bool more)
+{
+    if (more) async_wait<3>();
+    else async_wait<0>();
+    __syncthreads();
+    row_dots(reinterpret_cast<float *>(sm + OFF_BK), sm + (buf ? OFF_K1 : OFF_K), LDB, T,
+             p.u + (size_t)h * DH);
+    row_dots(reinterpret_cast<float *>(sm + OFF_BW), sm + (buf ? OFF_W1 : OFF_W), LDB, W,
+             p.vb + (size_t)h * DH);
+    __syncthreads();
+}
+
+// The key-tile kernel's row chunks, double-buffered the same way: q and dout
+// rows and the table window of chunk i0 into buffer `buf` (buffer 1 uses the
+// second key / value regions, which that kernel does not need).
+__device__ __forceinline__ Bufs chunk_bufs(int buf)
+{
+    return Bufs{buf ? OFF_K1 : OFF_Q, buf ? OFF_V1 : OFF_D, OFF_K, OFF_V, buf ? OFF_W1 : OFF_W};
+}
+
+__device__ __forceinline__ void issue_chunk(uint8_t *sm, const BwdParams &p, long long bh, int h,
+                                            int i0, int j0, int buf)
+{
+    const Bufs B = chunk_bufs(buf);
+    stage_async(sm + B.q, LDB, T, p.q + bh * p.L * DH, i0, 1, p.L);
+    stage_async(sm + B.d, LDB, T, p.dout + bh * p.L * DH, i0, 1, p.L);
+    const long long dmin = (long long)p.M + i0 - j0 - (T - 1);
+    stage_async(sm + B.w, LDB, W, p.r + (size_t)h * p.r_rows * DH, p.r_rows - 1 - dmin, -1, p.r_rows);
+}
+
+// Row statistics of the lane's two rows (rb + g, rb + g + 8).
+__device__ __forceinline__ void load_row_stats(const BwdParams &p, const Lane &L, long long bh,
+                                               int i0, float (&ls)[2], float (&dd)[2])
 {
 #pragma unroll
-    for (int r = 0; r < 4; ++r) {
-        const int gi = i0 + ty * 4 + r;
-        ls[r] = gi < p.L ? p.lse2[bh * p.L + gi] : 0.f;
-        dd[r] = gi < p.L ? p.dsum[bh * p.L + gi] : 0.f;
+    for (int h = 0; h < 2; ++h) {
+        const int gi = i0 + L.rb + L.g + 8 * h;
+        ls[h] = gi < p.L ? p.lse2[bh * p.L + gi] : 0.f;
+        dd[h] = gi < p.L ? p.dsum[bh * p.L + gi] : 0.f;
     }
 }
 
-// g = scale P (dP - D) with P = 2^(s - lse2) (0 where masked).
-__device__ __forceinline__ void grad_scores(const BwdParams &p, const float (&s)[4][4],
-                                            const float (&dp)[4][4], const float (&ls)[4],
-                                            const float (&dd)[4], float (&P)[4][4],
-                                            float (&g)[4][4])
+// g = scale P (dP - D) with P = 2^(s - lse2) (0 where masked); g and P as
+// head / rest pairs into the [row][column] tiles (P only when ph != 0).
+__device__ __forceinline__ void grad_scores(uint8_t *sm, const BwdParams &p, const Lane &L,
+                                            const float (&s)[4][4], const float (&dp)[4][4],
+                                            const float (&ls)[2], const float (&dd)[2],
+                                            float (&g)[4][4], bool with_p)
 {
 #pragma unroll
-    for (int r = 0; r < 4; ++r)
+    for (int n = 0; n < 4; ++n)
 #pragma unroll
-        for (int c = 0; c < 4; ++c) {
-            P[r][c] = (s[r][c] == -INFINITY) ? 0.f : exp2f(s[r][c] - ls[r]);
-            g[r][c] = p.scale * P[r][c] * (dp[r][c] - dd[r]);
+        for (int hh = 0; hh < 2; ++hh) {
+            float P[2];
+#pragma unroll
+            for (int e = 0; e < 2; ++e) {
+                const int q = 2 * hh + e;
+                P[e] = (s[n][q] == -INFINITY) ? 0.f : exp2f(s[n][q] - ls[hh]);
+                g[n][q] = p.scale * P[e] * (dp[n][q] - dd[hh]);
+            }
+            const int off = (L.rb + L.g + 8 * hh) * LDB + (L.cb + 8 * n + 2 * L.t) * 2;
+            uint32_t hd, rs;
+            split2(g[n][2 * hh], g[n][2 * hh + 1], hd, rs);
+            *reinterpret_cast<uint32_t *>(sm + OFF_GH + off) = hd;
+            *reinterpret_cast<uint32_t *>(sm + OFF_GL + off) = rs;
+            if (with_p) {
+                split2(P[0], P[1], hd, rs);
+                *reinterpret_cast<uint32_t *>(sm + OFF_PH + off) = hd;
+                *reinterpret_cast<uint32_t *>(sm + OFF_PL + off) = rs;
+            }
         }
 }
 
-__device__ __forceinline__ float half_warp_max(float v)
+// Column sums over the lane's rows of a fragment set, reduced over the warp's
+// 16 rows; lanes with g == 0 store them at red[strip][column].
+__device__ __forceinline__ void column_sums(float *red, int stride, const Lane &L, int col0,
+                                            const float (&c)[4][4])
 {
 #pragma unroll
-    for (int o = 8; o >= 1; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
-    return v;
-}
-
-__device__ __forceinline__ float half_warp_sum(float v)
-{
+    for (int n = 0; n < 4; ++n)
 #pragma unroll
-    for (int o = 8; o >= 1; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
-    return v;
+        for (int e = 0; e < 2; ++e) {
+            float v = c[n][e] + c[n][2 + e];
+            v += __shfl_xor_sync(0xffffffffu, v, 4);
+            v += __shfl_xor_sync(0xffffffffu, v, 8);
+            v += __shfl_xor_sync(0xffffffffu, v, 16);
+            if (L.g == 0) red[(L.warp >> 1) * stride + col0 + 8 * n + 2 * L.t + e] = v;
+        }
 }
 
 // ---- stats: log2-sum-exp and D per query row --------------------------------
 __global__ void __launch_bounds__(THREADS, 1) bwd_stats_kernel(const BwdParams p)
 {
-    extern __shared__ float4 smem4[];
-    float *sm = reinterpret_cast<float *>(smem4);
+    extern __shared__ __align__(16) uint8_t sm[];
+    const Lane L = lane_of();
     const long long bh = blockIdx.x;
     const int h = (int)(bh % p.H), i0 = blockIdx.y * T;
-    const int tx = threadIdx.x & 15, ty = threadIdx.x >> 4;
     TXL_CHECK(bh < (long long)p.B * p.H && i0 < p.L, p.status);
-    stage_rows(sm, p, bh, h, i0);
-    float m[4], l[4], wsum[4];
-#pragma unroll
-    for (int r = 0; r < 4; ++r) m[r] = -INFINITY, l[r] = 0.f, wsum[r] = 0.f;
-    // keys after M + (last row of the chunk) are hidden from every row
-    const int jend = min(p.K, p.M + i0 + T);
-    for (int j0 = 0; j0 < jend; j0 += T) {
-        __syncthreads();
-        stage(sm + OFF_A64, LD, T, p.k + bh * p.K * DH, j0, 1, p.K, nullptr);
-        stage(sm + OFF_V64, LD, T, p.v + bh * p.K * DH, j0, 1, p.K, nullptr);
-        stage_table_window(sm + OFF_W1, p, h, (long long)p.M + i0 - j0 - (T - 1));
-        __syncthreads();
+    stage_rows(sm, p, bh, i0);
+    // online state of the lane's two rows over its column half
+    float m[2] = {-INFINITY, -INFINITY}, l[2] = {0.f, 0.f}, wsum[2] = {0.f, 0.f};
+    const int jend = min(p.K, p.M + i0 + T);  // later keys are hidden from every row
+    issue_key_tile(sm, p, bh, h, i0, 0, 0);
+    for (int j0 = 0, buf = 0; j0 < jend; j0 += T, buf ^= 1) {
+        __syncthreads();  // the other buffer's last readers are done
+        const bool more = j0 + T < jend;
+        if (more) issue_key_tile(sm, p, bh, h, i0, j0 + T, buf ^ 1);
+        key_tile_ready(sm, p, h, buf, more);
         float s[4][4], dp[4][4];
-        key_tile_scores(sm, p, i0, j0, ty, tx, s, dp);
+        key_tile_scores(sm, p, L, i0, j0, s, dp,
+                        Bufs{OFF_Q, OFF_D, buf ? OFF_K1 : OFF_K, buf ? OFF_V1 : OFF_V, buf ? OFF_W1 : OFF_W});
 #pragma unroll
-        for (int r = 0; r < 4; ++r) {
-            float tmax = fmaxf(fmaxf(s[r][0], s[r][1]), fmaxf(s[r][2], s[r][3]));
-            tmax = half_warp_max(tmax);
-            const float mn = fmaxf(m[r], tmax);
-            // (every lane takes part in the sums; a row without a kept key so
-            // far adds nothing)
+        for (int hh = 0; hh < 2; ++hh) {
+            float tmax = -INFINITY;
+#pragma unroll
+            for (int n = 0; n < 4; ++n) tmax = fmaxf(tmax, fmaxf(s[n][2 * hh], s[n][2 * hh + 1]));
+            tmax = fmaxf(tmax, __shfl_xor_sync(0xffffffffu, tmax, 1));
+            tmax = fmaxf(tmax, __shfl_xor_sync(0xffffffffu, tmax, 2));
+            const float mn = fmaxf(m[hh], tmax);
             float e = 0.f, ed = 0.f;
 #pragma unroll
-            for (int c = 0; c < 4; ++c) {
-                const float x = (s[r][c] == -INFINITY) ? 0.f : exp2f(s[r][c] - mn);
-                e += x;
-                ed = fmaf(x, dp[r][c], ed);
-            }
-            e = half_warp_sum(e);
-            ed = half_warp_sum(ed);
+            for (int n = 0; n < 4; ++n)
+#pragma unroll
+                for (int x = 0; x < 2; ++x) {
+                    const float sv = s[n][2 * hh + x];
+                    const float ev = (sv == -INFINITY) ? 0.f : exp2f(sv - mn);
+                    e += ev;
+                    ed = fmaf(ev, dp[n][2 * hh + x], ed);
+                }
+            e += __shfl_xor_sync(0xffffffffu, e, 1);
+            e += __shfl_xor_sync(0xffffffffu, e, 2);
+            ed += __shfl_xor_sync(0xffffffffu, ed, 1);
+            ed += __shfl_xor_sync(0xffffffffu, ed, 2);
             if (mn != -INFINITY) {
-                const float alpha = (m[r] == -INFINITY) ? 0.f : exp2f(m[r] - mn);
-                l[r] = fmaf(l[r], alpha, e);
-                wsum[r] = fmaf(wsum[r], alpha, ed);
-                m[r] = mn;
+                const float alpha = (m[hh] == -INFINITY) ? 0.f : exp2f(m[hh] - mn);
+                l[hh] = fmaf(l[hh], alpha, e);
+                wsum[hh] = fmaf(wsum[hh], alpha, ed);
+                m[hh] = mn;
             }
         }
     }
-    if (tx == 0) {
+    // the two column halves of each row: red[half][row][m, l, w]
+    float *red = reinterpret_cast<float *>(sm + OFF_RED);
+    __syncthreads();
+    if (L.t == 0) {
 #pragma unroll
-        for (int r = 0; r < 4; ++r) {
-            const int gi = i0 + ty * 4 + r;
-            if (gi < p.L && l[r] > 0.f) {
-                p.lse2[bh * p.L + gi] = m[r] + log2f(l[r]);
-                p.dsum[bh * p.L + gi] = wsum[r] / l[r];
-            }
+        for (int hh = 0; hh < 2; ++hh) {
+            float *d = red + ((L.warp & 1) * T + L.rb + L.g + 8 * hh) * 3;
+            d[0] = m[hh];
+            d[1] = l[hh];
+            d[2] = wsum[hh];
+        }
+    }
+    __syncthreads();
+    if (threadIdx.x < T) {
+        const int i = threadIdx.x, gi = i0 + i;
+        const float *a = red + i * 3, *b = red + (T + i) * 3;
+        const float mx = fmaxf(a[0], b[0]);
+        if (gi < p.L && mx != -INFINITY) {
+            const float sa = (a[0] == -INFINITY) ? 0.f : exp2f(a[0] - mx);
+            const float sb = (b[0] == -INFINITY) ? 0.f : exp2f(b[0] - mx);
+            const float lt = a[1] * sa + b[1] * sb, wt = a[2] * sa + b[2] * sb;
+            p.lse2[bh * p.L + gi] = mx + log2f(lt);
+            p.dsum[bh * p.L + gi] = wt / lt;
         }
     }
 }
@@ -304,65 +513,68 @@ __global__ void __launch_bounds__(THREADS, 1) bwd_stats_kernel(const BwdParams p
 // ---- dq, and the chunk's partials of du and dv_bias ---------------------------
 __global__ void __launch_bounds__(THREADS, 1) bwd_dq_kernel(const BwdParams p)
 {
-    extern __shared__ float4 smem4[];
-    float *sm = reinterpret_cast<float *>(smem4);
+    extern __shared__ __align__(16) uint8_t sm[];
+    const Lane L = lane_of();
     const long long bh = blockIdx.x;
     const int h = (int)(bh % p.H), i0 = blockIdx.y * T;
-    const int tx = threadIdx.x & 15, ty = threadIdx.x >> 4;
     TXL_CHECK(bh < (long long)p.B * p.H && i0 < p.L, p.status);
-    stage_rows(sm, p, bh, h, i0);
-    float ls[4], dd[4];
-    load_row_stats(p, bh, i0, ty, ls, dd);
+    stage_rows(sm, p, bh, i0);
+    float ls[2], dd[2];
+    load_row_stats(p, L, bh, i0, ls, dd);
     float dqc[4][4], dqp[4][4];  // content (k) and position (table) parts; rows i, columns t
     zero(dqc);
     zero(dqp);
-    float *ga = sm + OFF_T1, *zw = sm + OFF_XS;
+    const uint16_t *gh = reinterpret_cast<const uint16_t *>(sm + OFF_GH);
+    const uint16_t *gl = reinterpret_cast<const uint16_t *>(sm + OFF_GL);
+    uint16_t *zh = reinterpret_cast<uint16_t *>(sm + OFF_ZH);
+    uint16_t *zl = reinterpret_cast<uint16_t *>(sm + OFF_ZL);
     const int jend = min(p.K, p.M + i0 + T);
-    for (int j0 = 0; j0 < jend; j0 += T) {
+    issue_key_tile(sm, p, bh, h, i0, 0, 0);
+    for (int j0 = 0, buf = 0; j0 < jend; j0 += T, buf ^= 1) {
+        __syncthreads();  // the other buffer's last readers are done
+        const bool more = j0 + T < jend;
+        if (more) issue_key_tile(sm, p, bh, h, i0, j0 + T, buf ^ 1);
+        key_tile_ready(sm, p, h, buf, more);
+        float s[4][4], dp[4][4], g[4][4];
+        key_tile_scores(sm, p, L, i0, j0, s, dp,
+                        Bufs{OFF_Q, OFF_D, buf ? OFF_K1 : OFF_K, buf ? OFF_V1 : OFF_V, buf ? OFF_W1 : OFF_W});
+        grad_scores(sm, p, L, s, dp, ls, dd, g, false);
         __syncthreads();
-        stage(sm + OFF_A64, LD, T, p.k + bh * p.K * DH, j0, 1, p.K, nullptr);
-        stage(sm + OFF_V64, LD, T, p.v + bh * p.K * DH, j0, 1, p.K, nullptr);
-        stage_table_window(sm + OFF_W1, p, h, (long long)p.M + i0 - j0 - (T - 1));
-        __syncthreads();
-        float s[4][4], dp[4][4], P[4][4], g[4][4];
-        key_tile_scores(sm, p, i0, j0, ty, tx, s, dp);
-        grad_scores(p, s, dp, ls, dd, P, g);
-#pragma unroll
-        for (int r = 0; r < 4; ++r)
-#pragma unroll
-            for (int c = 0; c < 4; ++c) ga[(ty * 4 + r) * LD + tx + 16 * c] = g[r][c];
-        __syncthreads();
-        // g laid out by window column: zw[i][w] = g[i][i - w + 63] (zero where no key)
+        // g by window column: z[i][w] = g[i][i - w + 63] (zero where no key)
         for (int idx = threadIdx.x; idx < T * W; idx += THREADS) {
             const int i = idx / W, w = idx % W, j = i - w + T - 1;
-            zw[i * LDW + w] = (j >= 0 && j < T) ? ga[i * LD + j] : 0.f;
+            const bool in = j >= 0 && j < T;
+            zh[i * (LDZ / 2) + w] = in ? gh[i * (LDB / 2) + j] : (uint16_t)0;
+            zl[i * (LDZ / 2) + w] = in ? gl[i * (LDB / 2) + j] : (uint16_t)0;
         }
         __syncthreads();
-        gemm_nn<4>(dqc, ga, LD, sm + OFF_A64, LD, T, ty, tx);
-        gemm_nn<4>(dqp, zw, LDW, sm + OFF_W1, LD, W, ty, tx);
+        const int cbo = L.cb;  // output columns: dimensions
+        warp_nn2<4>(dqc, smem_u32(sm + OFF_GH) + L.rb * LDB, smem_u32(sm + OFF_GL) + L.rb * LDB, LDB,
+                    false, smem_u32(sm + (buf ? OFF_K1 : OFF_K)) + cbo * 2, LDB, T, L.lane);
+        warp_nn2<4>(dqp, smem_u32(sm + OFF_ZH) + L.rb * LDZ, smem_u32(sm + OFF_ZL) + L.rb * LDZ, LDZ,
+                    false, smem_u32(sm + (buf ? OFF_W1 : OFF_W)) + cbo * 2, LDB, W, L.lane);
     }
 #pragma unroll
-    for (int r = 0; r < 4; ++r) {
-        const int gi = i0 + ty * 4 + r;
+    for (int hh = 0; hh < 2; ++hh) {
+        const int gi = i0 + L.rb + L.g + 8 * hh;
         if (gi < p.L) {
             float *dst = p.dq + (bh * p.L + gi) * DH;
 #pragma unroll
-            for (int c = 0; c < 4; ++c) dst[tx + 16 * c] = dqc[r][c] + dqp[r][c];
+            for (int n = 0; n < 4; ++n)
+                *reinterpret_cast<float2 *>(dst + L.cb + 8 * n + 2 * L.t) =
+                    make_float2(dqc[n][2 * hh] + dqp[n][2 * hh], dqc[n][2 * hh + 1] + dqp[n][2 * hh + 1]);
         }
     }
     // du and dv_bias partials of this chunk: column sums of the two parts over
-    // its rows (rows past L hold zeros), summed over ty in a fixed order.
+    // its rows (rows past L hold zeros), the four row strips summed in order.
+    float *red = reinterpret_cast<float *>(sm + OFF_RED);
     __syncthreads();
-    float *red = sm + OFF_T1;
-#pragma unroll
-    for (int c = 0; c < 4; ++c) {
-        red[ty * 2 * DH + tx + 16 * c] = dqc[0][c] + dqc[1][c] + dqc[2][c] + dqc[3][c];
-        red[ty * 2 * DH + DH + tx + 16 * c] = dqp[0][c] + dqp[1][c] + dqp[2][c] + dqp[3][c];
-    }
+    column_sums(red, 2 * DH, L, L.cb, dqc);
+    column_sums(red, 2 * DH, L, DH + L.cb, dqp);
     __syncthreads();
     if (threadIdx.x < 2 * DH) {
-        float acc = 0.f;
-        for (int y = 0; y < 16; ++y) acc += red[y * 2 * DH + threadIdx.x];
+        const float acc = ((red[threadIdx.x] + red[2 * DH + threadIdx.x]) + red[4 * DH + threadIdx.x]) +
+                          red[6 * DH + threadIdx.x];
         p.part[(bh * gridDim.y + blockIdx.y) * 2 * DH + threadIdx.x] = acc;
     }
 }
@@ -370,50 +582,64 @@ __global__ void __launch_bounds__(THREADS, 1) bwd_dq_kernel(const BwdParams p)
 // ---- dk, dv per 64-key tile ----------------------------------------------------
 __global__ void __launch_bounds__(THREADS, 1) bwd_dkv_kernel(const BwdParams p)
 {
-    extern __shared__ float4 smem4[];
-    float *sm = reinterpret_cast<float *>(smem4);
+    extern __shared__ __align__(16) uint8_t sm[];
+    const Lane L = lane_of();
     const long long bh = blockIdx.x;
     const int h = (int)(bh % p.H), j0 = blockIdx.y * T;
-    const int tx = threadIdx.x & 15, ty = threadIdx.x >> 4;
     TXL_CHECK(bh < (long long)p.B * p.H && j0 < p.K, p.status);
-    stage(sm + OFF_A64, LD, T, p.k + bh * p.K * DH, j0, 1, p.K, nullptr);
-    stage(sm + OFF_V64, LD, T, p.v + bh * p.K * DH, j0, 1, p.K, nullptr);
-    float dk[4][4], dv[4][4];  // rows: keys 4 ty + a; columns: dimensions
+    stage(sm + OFF_K, LDB, T, p.k + bh * p.K * DH, j0, 1, p.K);
+    stage(sm + OFF_V, LDB, T, p.v + bh * p.K * DH, j0, 1, p.K);
+    float *cs = reinterpret_cast<float *>(sm + OFF_CS);  // sum over rows of g, per key
+    if (threadIdx.x < T) cs[threadIdx.x] = 0.f;
+    __syncthreads();
+    row_dots(reinterpret_cast<float *>(sm + OFF_BK), sm + OFF_K, LDB, T, p.u + (size_t)h * DH);
+    float dk[4][4], dv[4][4];  // rows: keys; columns: dimensions
     zero(dk);
     zero(dv);
-    float *pt = sm + OFF_T1, *gt = sm + OFF_T2;  // P and g transposed: [key][row]
+    float *red = reinterpret_cast<float *>(sm + OFF_RED);
     // the first chunk with a row that sees key j0 (distance M + i - j0 >= 0)
     const int i_first = max(0, j0 - p.M) / T * T;
-    for (int i0 = i_first; i0 < p.L; i0 += T) {
+    issue_chunk(sm, p, bh, h, i_first, j0, 0);
+    for (int i0 = i_first, buf = 0; i0 < p.L; i0 += T, buf ^= 1) {
+        __syncthreads();  // the other buffer's last readers are done
+        const bool more = i0 + T < p.L;
+        if (more) issue_chunk(sm, p, bh, h, i0 + T, j0, buf ^ 1);
+        if (more) async_wait<3>();
+        else async_wait<0>();
         __syncthreads();
-        stage_rows(sm, p, bh, h, i0);
-        stage_table_window(sm + OFF_W1, p, h, (long long)p.M + i0 - j0 - (T - 1));
+        const Bufs B = chunk_bufs(buf);
+        row_dots(reinterpret_cast<float *>(sm + OFF_BW), sm + B.w, LDB, W, p.vb + (size_t)h * DH);
         __syncthreads();
-        float ls[4], dd[4];
-        load_row_stats(p, bh, i0, ty, ls, dd);
-        float s[4][4], dp[4][4], P[4][4], g[4][4];
-        key_tile_scores(sm, p, i0, j0, ty, tx, s, dp);
-        grad_scores(p, s, dp, ls, dd, P, g);
-#pragma unroll
-        for (int r = 0; r < 4; ++r)
-#pragma unroll
-            for (int c = 0; c < 4; ++c) {
-                pt[(tx + 16 * c) * LD + ty * 4 + r] = P[r][c];
-                gt[(tx + 16 * c) * LD + ty * 4 + r] = g[r][c];
-            }
+        float ls[2], dd[2];
+        load_row_stats(p, L, bh, i0, ls, dd);
+        float s[4][4], dp[4][4], g[4][4];
+        key_tile_scores(sm, p, L, i0, j0, s, dp, B);
+        grad_scores(sm, p, L, s, dp, ls, dd, g, true);
+        column_sums(red, T, L, L.cb, g);
         __syncthreads();
-        gemm_nn<4>(dv, pt, LD, sm + OFF_DO, LD, T, ty, tx);
-        gemm_nn<4>(dk, gt, LD, sm + OFF_QU, LD, T, ty, tx);
+        if (threadIdx.x < T)
+            cs[threadIdx.x] += ((red[threadIdx.x] + red[T + threadIdx.x]) + red[2 * T + threadIdx.x]) +
+                               red[3 * T + threadIdx.x];
+        // dv = P^T dout, dk = g^T q (+ the column sums times u, at the end)
+        warp_nn2<4>(dv, smem_u32(sm + OFF_PH) + L.rb * 2, smem_u32(sm + OFF_PL) + L.rb * 2, LDB,
+                    true, smem_u32(sm + B.d) + L.cb * 2, LDB, T, L.lane);
+        warp_nn2<4>(dk, smem_u32(sm + OFF_GH) + L.rb * 2, smem_u32(sm + OFF_GL) + L.rb * 2, LDB,
+                    true, smem_u32(sm + B.q) + L.cb * 2, LDB, T, L.lane);
     }
+    __syncthreads();
+    const __nv_bfloat16 *u = p.u + (size_t)h * DH;
 #pragma unroll
-    for (int r = 0; r < 4; ++r) {
-        const int gj = j0 + ty * 4 + r;
+    for (int hh = 0; hh < 2; ++hh) {
+        const int j = L.rb + L.g + 8 * hh, gj = j0 + j;
         if (gj < p.K) {
             float *ok = p.dk + (bh * p.K + gj) * DH, *ov = p.dv + (bh * p.K + gj) * DH;
 #pragma unroll
-            for (int c = 0; c < 4; ++c) {
-                ok[tx + 16 * c] = dk[r][c];
-                ov[tx + 16 * c] = dv[r][c];
+            for (int n = 0; n < 4; ++n) {
+                const int c = L.cb + 8 * n + 2 * L.t;
+                const float u0 = __bfloat162float(u[c]), u1 = __bfloat162float(u[c + 1]);
+                *reinterpret_cast<float2 *>(ok + c) =
+                    make_float2(fmaf(cs[j], u0, dk[n][2 * hh]), fmaf(cs[j], u1, dk[n][2 * hh + 1]));
+                *reinterpret_cast<float2 *>(ov + c) = make_float2(dv[n][2 * hh], dv[n][2 * hh + 1]);
             }
         }
     }
@@ -421,91 +647,114 @@ __global__ void __launch_bounds__(THREADS, 1) bwd_dkv_kernel(const BwdParams p)
 
 // ---- the table gradient per head and 64-distance tile ---------------------------
 // Pair (row i, distance d) is key j = M + i - d.  Over the batch and the query
-// chunks: position scores (q + v) . r_d directly; the content scores and dP
-// through the chunk's 127-key window (key jmin + w, w = i - c + 63 for the
+// chunks: position scores q . r_d (+ v.r_d) directly; the content scores and
+// dP through the chunk's 128-key window (key jmin + w, w = i - c + 63 for the
 // tile's distance column c); then dr_d += sum_i g (q_i + v).
 __global__ void __launch_bounds__(THREADS, 1) bwd_dr_kernel(const BwdParams p)
 {
-    extern __shared__ float4 smem4[];
-    float *sm = reinterpret_cast<float *>(smem4);
+    extern __shared__ __align__(16) uint8_t sm[];
+    const Lane L = lane_of();
     const int d0 = blockIdx.x * T, h = blockIdx.y;
-    const int tx = threadIdx.x & 15, ty = threadIdx.x >> 4;
     TXL_CHECK(h < p.H && d0 < p.r_rows, p.status);
-    float dr[4][4];  // rows: distances 4 ty + a; columns: dimensions
+    float dr[4][4];  // rows: distances; columns: dimensions
     zero(dr);
+    float *cs = reinterpret_cast<float *>(sm + OFF_CS);  // sum over rows of g, per distance
     if (d0 < p.K) {
-        // the tile's table rows by distance: A64 row c = distance d0 + c
-        stage(sm + OFF_A64, LD, T, p.r + (size_t)h * p.r_rows * DH, p.r_rows - 1 - d0, -1,
-              p.r_rows, nullptr);
-        float *xs = sm + OFF_XS, *gt = sm + OFF_T1;
-        // chunks with a row that sees distance d0 (M + i - d0 >= 0 for its last row)
+        // the tile's table rows by distance (row c: distance d0 + c) and v.r_d
+        stage(sm + OFF_K, LDB, T, p.r + (size_t)h * p.r_rows * DH, p.r_rows - 1 - d0, -1, p.r_rows);
+        if (threadIdx.x < T) cs[threadIdx.x] = 0.f;
+        __syncthreads();
+        row_dots(reinterpret_cast<float *>(sm + OFF_BK), sm + OFF_K, LDB, T, p.vb + (size_t)h * DH);
+        const float *bk = reinterpret_cast<const float *>(sm + OFF_BK);
+        const float *xs = reinterpret_cast<const float *>(sm + OFF_XS);
+        float *red = reinterpret_cast<float *>(sm + OFF_RED);
+        // chunks with a row that sees distance d0 (M + i - d0 >= 0 for its last row);
+        // the (batch row, chunk) items double-buffered: q and dout rows, the key
+        // and value windows (buffer 1 in the regions this kernel does not use
+        // otherwise; the value window's spans both window-ordered g tiles)
         const int i_first = max(0, d0 - p.M - (T - 1)) / T * T;
-        for (int b = 0; b < p.B; ++b) {
-            const long long bh = (long long)b * p.H + h;
-            for (int i0 = i_first; i0 < p.L; i0 += T) {
-                const long long jmin = (long long)p.M + i0 - d0 - (T - 1);
-                __syncthreads();
-                stage_rows(sm, p, bh, h, i0);
-                stage(sm + OFF_W1, LD, W, p.k + bh * p.K * DH, jmin, 1, p.K, nullptr);
-                stage(sm + OFF_W2, LD, W, p.v + bh * p.K * DH, jmin, 1, p.K, nullptr);
-                __syncthreads();
-                float ls[4], dd[4];
-                load_row_stats(p, bh, i0, ty, ls, dd);
-                float sp[4][4], sc[4][4], dp[4][4], x[4][8];
-                zero(sp);
-                gemm_nt<4>(sp, sm + OFF_QV, LD, sm + OFF_A64, LD, DH, ty, tx);
-                zero(x);
-                gemm_nt<8>(x, sm + OFF_QU, LD, sm + OFF_W1, LD, DH, ty, tx);
+        const int n_ch = (p.L - i_first + T - 1) / T, n_items = p.B * n_ch;
+        auto bufs = [](int b) {
+            return Bufs{b ? OFF_K1 : OFF_Q, b ? OFF_V1 : OFF_D, OFF_K, b ? OFF_ZH : OFF_W2,
+                        b ? OFF_W1 : OFF_W};
+        };
+        auto issue = [&](int it, int b) {
+            const Bufs B = bufs(b);
+            const long long bh = (long long)(it / n_ch) * p.H + h;
+            const int i0 = i_first + (it % n_ch) * T;
+            const long long jmin = (long long)p.M + i0 - d0 - (T - 1);
+            stage_async(sm + B.q, LDB, T, p.q + bh * p.L * DH, i0, 1, p.L);
+            stage_async(sm + B.d, LDB, T, p.dout + bh * p.L * DH, i0, 1, p.L);
+            stage_async(sm + B.w, LDB, W, p.k + bh * p.K * DH, jmin, 1, p.K);
+            stage_async(sm + B.v, LDB, W, p.v + bh * p.K * DH, jmin, 1, p.K);
+        };
+        issue(0, 0);
+        for (int it = 0, buf = 0; it < n_items; ++it, buf ^= 1) {
+            const long long bh = (long long)(it / n_ch) * p.H + h;
+            const int i0 = i_first + (it % n_ch) * T;
+            __syncthreads();  // the other buffer's last readers are done
+            const bool more = it + 1 < n_items;
+            if (more) issue(it + 1, buf ^ 1);
+            if (more) async_wait<4>();
+            else async_wait<0>();
+            __syncthreads();
+            const Bufs B = bufs(buf);
+            row_dots(reinterpret_cast<float *>(sm + OFF_BW), sm + B.w, LDB, W, p.u + (size_t)h * DH);
+            __syncthreads();
+            float ls[2], dd[2];
+            load_row_stats(p, L, bh, i0, ls, dd);
+            float sp[4][4], sc[4][4], dp[4][4], s[4][4], g[4][4];
+            zero(sp);
+            warp_nt<4>(sp, smem_u32(sm + B.q) + L.rb * LDB, LDB, smem_u32(sm + OFF_K) + L.cb * LDB,
+                       LDB, DH, L.lane);
+            window_product(sm, L, B.q, B.w, reinterpret_cast<const float *>(sm + OFF_BW));
+            __syncthreads();
 #pragma unroll
-                for (int r = 0; r < 4; ++r)
+            for (int n = 0; n < 4; ++n)
 #pragma unroll
-                    for (int c = 0; c < 8; ++c) xs[(ty * 4 + r) * LDW + tx + 16 * c] = x[r][c];
-                __syncthreads();
+                for (int q = 0; q < 4; ++q) {
+                    const int i = L.rb + L.g + 8 * (q >> 1), c = L.cb + 8 * n + 2 * L.t + (q & 1);
+                    sc[n][q] = xs[i * LDX + i - c + T - 1];
+                }
+            __syncthreads();
+            window_product(sm, L, B.d, B.v, nullptr);
+            __syncthreads();
 #pragma unroll
-                for (int r = 0; r < 4; ++r)
+            for (int n = 0; n < 4; ++n)
 #pragma unroll
-                    for (int c = 0; c < 4; ++c) {
-                        const int i = ty * 4 + r, cc = tx + 16 * c;
-                        sc[r][c] = xs[i * LDW + i - cc + T - 1];
-                    }
-                __syncthreads();
-                zero(x);
-                gemm_nt<8>(x, sm + OFF_DO, LD, sm + OFF_W2, LD, DH, ty, tx);
-#pragma unroll
-                for (int r = 0; r < 4; ++r)
-#pragma unroll
-                    for (int c = 0; c < 8; ++c) xs[(ty * 4 + r) * LDW + tx + 16 * c] = x[r][c];
-                __syncthreads();
-                float s[4][4];
-#pragma unroll
-                for (int r = 0; r < 4; ++r)
-#pragma unroll
-                    for (int c = 0; c < 4; ++c) {
-                        const int i = ty * 4 + r, cc = tx + 16 * c;
-                        dp[r][c] = xs[i * LDW + i - cc + T - 1];
-                        const int gi = i0 + i, d = d0 + cc;
-                        const int gj = p.M + gi - d;
-                        const bool keep = gi < p.L && d < p.K && gj >= 0 && gj < p.K;
-                        s[r][c] = keep ? (sc[r][c] + sp[r][c]) * p.scale_log2 : -INFINITY;
-                    }
-                float P[4][4], g[4][4];
-                grad_scores(p, s, dp, ls, dd, P, g);
-#pragma unroll
-                for (int r = 0; r < 4; ++r)
-#pragma unroll
-                    for (int c = 0; c < 4; ++c) gt[(tx + 16 * c) * LD + ty * 4 + r] = g[r][c];
-                __syncthreads();
-                gemm_nn<4>(dr, gt, LD, sm + OFF_QV, LD, T, ty, tx);
-            }
+                for (int q = 0; q < 4; ++q) {
+                    const int i = L.rb + L.g + 8 * (q >> 1), c = L.cb + 8 * n + 2 * L.t + (q & 1);
+                    dp[n][q] = xs[i * LDX + i - c + T - 1];
+                    const int gi = i0 + i, d = d0 + c;
+                    const int gj = p.M + gi - d;
+                    const bool keep = gi < p.L && d < p.K && gj >= 0 && gj < p.K;
+                    s[n][q] = keep ? (sc[n][q] + sp[n][q] + bk[c]) * p.scale_log2 : -INFINITY;
+                }
+            grad_scores(sm, p, L, s, dp, ls, dd, g, false);
+            column_sums(red, T, L, L.cb, g);
+            __syncthreads();
+            if (threadIdx.x < T)
+                cs[threadIdx.x] += ((red[threadIdx.x] + red[T + threadIdx.x]) +
+                                    red[2 * T + threadIdx.x]) + red[3 * T + threadIdx.x];
+            warp_nn2<4>(dr, smem_u32(sm + OFF_GH) + L.rb * 2, smem_u32(sm + OFF_GL) + L.rb * 2,
+                        LDB, true, smem_u32(sm + B.q) + L.cb * 2, LDB, T, L.lane);
         }
+        __syncthreads();
     }
+    const __nv_bfloat16 *vb = p.vb + (size_t)h * DH;
 #pragma unroll
-    for (int r = 0; r < 4; ++r) {
-        const int d = d0 + ty * 4 + r;
+    for (int hh = 0; hh < 2; ++hh) {
+        const int c = L.rb + L.g + 8 * hh, d = d0 + c;
         if (d < p.r_rows) {
             float *dst = p.dr + ((size_t)h * p.r_rows + (p.r_rows - 1 - d)) * DH;
+            const float cd = (d < p.K) ? cs[c] : 0.f;
 #pragma unroll
-            for (int c = 0; c < 4; ++c) dst[tx + 16 * c] = dr[r][c];
+            for (int n = 0; n < 4; ++n) {
+                const int col = L.cb + 8 * n + 2 * L.t;
+                const float v0 = __bfloat162float(vb[col]), v1 = __bfloat162float(vb[col + 1]);
+                *reinterpret_cast<float2 *>(dst + col) =
+                    make_float2(fmaf(cd, v0, dr[n][2 * hh]), fmaf(cd, v1, dr[n][2 * hh + 1]));
+            }
         }
     }
 }
