@@ -10,8 +10,9 @@
 // (dr, du, dv_bias summed over the batch: the table and biases are shared).
 //
 // Five launches over tiles of 64 query rows x 64 columns (keys, or distances
-// for the table gradient), 256 threads = 8 warps, warp w taking rows
-// 16 (w / 2) .. +15 and columns 32 (w % 2) .. +31 of every 64 x 64 product:
+// for the table gradient), 512 threads = 16 warps, warp w taking rows
+// 16 (w / 4) .. +15 and columns 16 (w % 4) .. +15 of every 64 x 64 product
+// (and columns 32 (w % 4) .. +31 of a 64 x 128 window product):
 //   stats   per 64-row chunk, over its key tiles: online log-sum-exp of the
 //           scores and D (nothing from the forward call is needed)
 //   dq      per 64-row chunk, over its key tiles: dq, and the chunk's
@@ -40,7 +41,9 @@ namespace {
 constexpr int DH = 64;
 constexpr int T = kBwdRows;     // rows / columns of a pair tile
 constexpr int W = 2 * T;        // window rows of a tile (127 used)
-constexpr int THREADS = 256;
+constexpr int THREADS = 512;
+constexpr int NF = 2;   // 8-column fragments of a warp in a 64 x 64 product
+constexpr int NWF = 4;  // in a 64 x 128 window product
 constexpr int LDB = (DH + 8) * 2;   // bytes per bf16 row of 64 (+8 pad: conflict-free ldmatrix)
 constexpr int LDZ = (W + 8) * 2;    // bytes per bf16 row of 128
 constexpr int LDX = W + 4;          // floats per row of the fp32 window product
@@ -63,8 +66,8 @@ constexpr int OFF_ZL = OFF_ZH + T * LDZ;    // rest
 constexpr int OFF_XS = OFF_ZL + T * LDZ;    // fp32 [64][132] window product
 constexpr int OFF_BK = OFF_XS + T * LDX * 4;  // fp32 [64]: u.k_j (or v.r_d)
 constexpr int OFF_BW = OFF_BK + T * 4;        // fp32 [128]: v.r_w (or u.k_w) of the window
-constexpr int OFF_RED = OFF_BW + W * 4;       // fp32 [8][64] reduction scratch
-constexpr int OFF_CS = OFF_RED + 8 * T * 4;   // fp32 [64]: column sums of g over the chunks
+constexpr int OFF_RED = OFF_BW + W * 4;       // fp32 [16][64] reduction scratch
+constexpr int OFF_CS = OFF_RED + 16 * T * 4;   // fp32 [64]: column sums of g over the chunks
 // second key tile, value tile and table window: the row-chunk kernels copy
 // the next key tile in while computing on the current one
 constexpr int OFF_K1 = OFF_CS + T * 4;
@@ -245,8 +248,8 @@ __device__ __forceinline__ void row_dots(float *out, const uint8_t *tile, int ld
     }
 }
 
-// The lane's place in a 64 x 64 product: warp w holds rows 16 (w/2) + g and
-// + 8, columns 32 (w%2) + 8 n + 2 t and + 1 (n = 0..3): element q of
+// The lane's place in a 64 x 64 product: warp w holds rows 16 (w/4) + g and
+// + 8, columns 16 (w%4) + 8 n + 2 t and + 1 (n = 0, 1): element q of
 // fragment n is row rb + g + 8 (q / 2), column cb + 8 n + 2 t + q % 2.
 struct Lane {
     int warp, lane, g, t, rb, cb;
@@ -259,26 +262,26 @@ __device__ __forceinline__ Lane lane_of()
     L.lane = threadIdx.x & 31;
     L.g = L.lane >> 2;
     L.t = L.lane & 3;
-    L.rb = 16 * (L.warp >> 1);
-    L.cb = 32 * (L.warp & 1);
+    L.rb = 16 * (L.warp >> 2);
+    L.cb = 16 * (L.warp & 3);
     return L;
 }
 
 // The 64 x 128 window product of the warp's rows, plus a per-column vector,
-// into the fp32 window buffer (columns 64 (w%2) .. +63).
+// into the fp32 window buffer (columns 32 (w%4) .. +31).
 __device__ __forceinline__ void window_product(uint8_t *sm, const Lane &L, int a_off, int b_off,
                                                const float *colvec)
 {
-    float x[8][4];
+    float x[NWF][4];
     zero(x);
-    warp_nt<8>(x, smem_u32(sm + a_off) + L.rb * LDB, LDB,
-               smem_u32(sm + b_off) + 64 * (L.warp & 1) * LDB, LDB, DH, L.lane);
+    warp_nt<NWF>(x, smem_u32(sm + a_off) + L.rb * LDB, LDB,
+               smem_u32(sm + b_off) + 32 * (L.warp & 3) * LDB, LDB, DH, L.lane);
     float *xs = reinterpret_cast<float *>(sm + OFF_XS);
 #pragma unroll
-    for (int n = 0; n < 8; ++n)
+    for (int n = 0; n < NWF; ++n)
 #pragma unroll
         for (int q = 0; q < 4; ++q) {
-            const int col = 64 * (L.warp & 1) + 8 * n + 2 * L.t + (q & 1);
+            const int col = 32 * (L.warp & 3) + 8 * n + 2 * L.t + (q & 1);
             xs[(L.rb + L.g + 8 * (q >> 1)) * LDX + col] = x[n][q] + (colvec ? colvec[col] : 0.f);
         }
 }
@@ -294,22 +297,22 @@ struct Bufs {
 // window (distances M + i0 - j0 - 63 + w) and bias vectors (u.k_j, v.r_w).
 // Contains a block barrier.
 __device__ __forceinline__ void key_tile_scores(uint8_t *sm, const BwdParams &p, const Lane &L,
-                                                int i0, int j0, float (&s)[4][4], float (&dp)[4][4],
+                                                int i0, int j0, float (&s)[NF][4], float (&dp)[NF][4],
                                                 const Bufs &B)
 {
-    float sc[4][4];
+    float sc[NF][4];
     zero(sc);
     zero(dp);
-    warp_nt<4>(sc, smem_u32(sm + B.q) + L.rb * LDB, LDB, smem_u32(sm + B.k) + L.cb * LDB, LDB,
+    warp_nt<NF>(sc, smem_u32(sm + B.q) + L.rb * LDB, LDB, smem_u32(sm + B.k) + L.cb * LDB, LDB,
                DH, L.lane);
-    warp_nt<4>(dp, smem_u32(sm + B.d) + L.rb * LDB, LDB, smem_u32(sm + B.v) + L.cb * LDB, LDB,
+    warp_nt<NF>(dp, smem_u32(sm + B.d) + L.rb * LDB, LDB, smem_u32(sm + B.v) + L.cb * LDB, LDB,
                DH, L.lane);
     const float *bk = reinterpret_cast<const float *>(sm + OFF_BK);
     window_product(sm, L, B.q, B.w, reinterpret_cast<const float *>(sm + OFF_BW));
     __syncthreads();
     const float *xs = reinterpret_cast<const float *>(sm + OFF_XS);
 #pragma unroll
-    for (int n = 0; n < 4; ++n)
+    for (int n = 0; n < NF; ++n)
 #pragma unroll
         for (int q = 0; q < 4; ++q) {
             const int i = L.rb + L.g + 8 * (q >> 1), j = L.cb + 8 * n + 2 * L.t + (q & 1);
@@ -387,12 +390,12 @@ __device__ __forceinline__ void load_row_stats(const BwdParams &p, const Lane &L
 // g = scale P (dP - D) with P = 2^(s - lse2) (0 where masked); g and P as
 // head / rest pairs into the [row][column] tiles (P only when ph != 0).
 __device__ __forceinline__ void grad_scores(uint8_t *sm, const BwdParams &p, const Lane &L,
-                                            const float (&s)[4][4], const float (&dp)[4][4],
+                                            const float (&s)[NF][4], const float (&dp)[NF][4],
                                             const float (&ls)[2], const float (&dd)[2],
-                                            float (&g)[4][4], bool with_p)
+                                            float (&g)[NF][4], bool with_p)
 {
 #pragma unroll
-    for (int n = 0; n < 4; ++n)
+    for (int n = 0; n < NF; ++n)
 #pragma unroll
         for (int hh = 0; hh < 2; ++hh) {
             float P[2];
@@ -418,17 +421,17 @@ __device__ __forceinline__ void grad_scores(uint8_t *sm, const BwdParams &p, con
 // Column sums over the lane's rows of a fragment set, reduced over the warp's
 // 16 rows; lanes with g == 0 store them at red[strip][column].
 __device__ __forceinline__ void column_sums(float *red, int stride, const Lane &L, int col0,
-                                            const float (&c)[4][4])
+                                            const float (&c)[NF][4])
 {
 #pragma unroll
-    for (int n = 0; n < 4; ++n)
+    for (int n = 0; n < NF; ++n)
 #pragma unroll
         for (int e = 0; e < 2; ++e) {
             float v = c[n][e] + c[n][2 + e];
             v += __shfl_xor_sync(0xffffffffu, v, 4);
             v += __shfl_xor_sync(0xffffffffu, v, 8);
             v += __shfl_xor_sync(0xffffffffu, v, 16);
-            if (L.g == 0) red[(L.warp >> 1) * stride + col0 + 8 * n + 2 * L.t + e] = v;
+            if (L.g == 0) red[(L.warp >> 2) * stride + col0 + 8 * n + 2 * L.t + e] = v;
         }
 }
 
@@ -441,7 +444,7 @@ __global__ void __launch_bounds__(THREADS, 1) bwd_stats_kernel(const BwdParams p
     const int h = (int)(bh % p.H), i0 = blockIdx.y * T;
     TXL_CHECK(bh < (long long)p.B * p.H && i0 < p.L, p.status);
     stage_rows(sm, p, bh, i0);
-    // online state of the lane's two rows over its column half
+    // online state of the lane's two rows over its column group
     float m[2] = {-INFINITY, -INFINITY}, l[2] = {0.f, 0.f}, wsum[2] = {0.f, 0.f};
     const int jend = min(p.K, p.M + i0 + T);  // later keys are hidden from every row
     issue_key_tile(sm, p, bh, h, i0, 0, 0);
@@ -450,20 +453,20 @@ __global__ void __launch_bounds__(THREADS, 1) bwd_stats_kernel(const BwdParams p
         const bool more = j0 + T < jend;
         if (more) issue_key_tile(sm, p, bh, h, i0, j0 + T, buf ^ 1);
         key_tile_ready(sm, p, h, buf, more);
-        float s[4][4], dp[4][4];
+        float s[NF][4], dp[NF][4];
         key_tile_scores(sm, p, L, i0, j0, s, dp,
                         Bufs{OFF_Q, OFF_D, buf ? OFF_K1 : OFF_K, buf ? OFF_V1 : OFF_V, buf ? OFF_W1 : OFF_W});
 #pragma unroll
         for (int hh = 0; hh < 2; ++hh) {
             float tmax = -INFINITY;
 #pragma unroll
-            for (int n = 0; n < 4; ++n) tmax = fmaxf(tmax, fmaxf(s[n][2 * hh], s[n][2 * hh + 1]));
+            for (int n = 0; n < NF; ++n) tmax = fmaxf(tmax, fmaxf(s[n][2 * hh], s[n][2 * hh + 1]));
             tmax = fmaxf(tmax, __shfl_xor_sync(0xffffffffu, tmax, 1));
             tmax = fmaxf(tmax, __shfl_xor_sync(0xffffffffu, tmax, 2));
             const float mn = fmaxf(m[hh], tmax);
             float e = 0.f, ed = 0.f;
 #pragma unroll
-            for (int n = 0; n < 4; ++n)
+            for (int n = 0; n < NF; ++n)
 #pragma unroll
                 for (int x = 0; x < 2; ++x) {
                     const float sv = s[n][2 * hh + x];
@@ -483,13 +486,13 @@ __global__ void __launch_bounds__(THREADS, 1) bwd_stats_kernel(const BwdParams p
             }
         }
     }
-    // the two column halves of each row: red[half][row][m, l, w]
+    // the four column groups of each row: red[group][row][m, l, w]
     float *red = reinterpret_cast<float *>(sm + OFF_RED);
     __syncthreads();
     if (L.t == 0) {
 #pragma unroll
         for (int hh = 0; hh < 2; ++hh) {
-            float *d = red + ((L.warp & 1) * T + L.rb + L.g + 8 * hh) * 3;
+            float *d = red + ((L.warp & 3) * T + L.rb + L.g + 8 * hh) * 3;
             d[0] = m[hh];
             d[1] = l[hh];
             d[2] = wsum[hh];
@@ -498,12 +501,16 @@ __global__ void __launch_bounds__(THREADS, 1) bwd_stats_kernel(const BwdParams p
     __syncthreads();
     if (threadIdx.x < T) {
         const int i = threadIdx.x, gi = i0 + i;
-        const float *a = red + i * 3, *b = red + (T + i) * 3;
-        const float mx = fmaxf(a[0], b[0]);
+        float mx = -INFINITY;
+        for (int c = 0; c < 4; ++c) mx = fmaxf(mx, red[(c * T + i) * 3]);
         if (gi < p.L && mx != -INFINITY) {
-            const float sa = (a[0] == -INFINITY) ? 0.f : exp2f(a[0] - mx);
-            const float sb = (b[0] == -INFINITY) ? 0.f : exp2f(b[0] - mx);
-            const float lt = a[1] * sa + b[1] * sb, wt = a[2] * sa + b[2] * sb;
+            float lt = 0.f, wt = 0.f;
+            for (int c = 0; c < 4; ++c) {
+                const float *a = red + (c * T + i) * 3;
+                const float sa = (a[0] == -INFINITY) ? 0.f : exp2f(a[0] - mx);
+                lt = fmaf(a[1], sa, lt);
+                wt = fmaf(a[2], sa, wt);
+            }
             p.lse2[bh * p.L + gi] = mx + log2f(lt);
             p.dsum[bh * p.L + gi] = wt / lt;
         }
@@ -521,7 +528,7 @@ __global__ void __launch_bounds__(THREADS, 1) bwd_dq_kernel(const BwdParams p)
     stage_rows(sm, p, bh, i0);
     float ls[2], dd[2];
     load_row_stats(p, L, bh, i0, ls, dd);
-    float dqc[4][4], dqp[4][4];  // content (k) and position (table) parts; rows i, columns t
+    float dqc[NF][4], dqp[NF][4];  // content (k) and position (table) parts; rows i, columns t
     zero(dqc);
     zero(dqp);
     const uint16_t *gh = reinterpret_cast<const uint16_t *>(sm + OFF_GH);
@@ -535,7 +542,7 @@ __global__ void __launch_bounds__(THREADS, 1) bwd_dq_kernel(const BwdParams p)
         const bool more = j0 + T < jend;
         if (more) issue_key_tile(sm, p, bh, h, i0, j0 + T, buf ^ 1);
         key_tile_ready(sm, p, h, buf, more);
-        float s[4][4], dp[4][4], g[4][4];
+        float s[NF][4], dp[NF][4], g[NF][4];
         key_tile_scores(sm, p, L, i0, j0, s, dp,
                         Bufs{OFF_Q, OFF_D, buf ? OFF_K1 : OFF_K, buf ? OFF_V1 : OFF_V, buf ? OFF_W1 : OFF_W});
         grad_scores(sm, p, L, s, dp, ls, dd, g, false);
@@ -549,9 +556,9 @@ __global__ void __launch_bounds__(THREADS, 1) bwd_dq_kernel(const BwdParams p)
         }
         __syncthreads();
         const int cbo = L.cb;  // output columns: dimensions
-        warp_nn2<4>(dqc, smem_u32(sm + OFF_GH) + L.rb * LDB, smem_u32(sm + OFF_GL) + L.rb * LDB, LDB,
+        warp_nn2<NF>(dqc, smem_u32(sm + OFF_GH) + L.rb * LDB, smem_u32(sm + OFF_GL) + L.rb * LDB, LDB,
                     false, smem_u32(sm + (buf ? OFF_K1 : OFF_K)) + cbo * 2, LDB, T, L.lane);
-        warp_nn2<4>(dqp, smem_u32(sm + OFF_ZH) + L.rb * LDZ, smem_u32(sm + OFF_ZL) + L.rb * LDZ, LDZ,
+        warp_nn2<NF>(dqp, smem_u32(sm + OFF_ZH) + L.rb * LDZ, smem_u32(sm + OFF_ZL) + L.rb * LDZ, LDZ,
                     false, smem_u32(sm + (buf ? OFF_W1 : OFF_W)) + cbo * 2, LDB, W, L.lane);
     }
 #pragma unroll
@@ -560,7 +567,7 @@ __global__ void __launch_bounds__(THREADS, 1) bwd_dq_kernel(const BwdParams p)
         if (gi < p.L) {
             float *dst = p.dq + (bh * p.L + gi) * DH;
 #pragma unroll
-            for (int n = 0; n < 4; ++n)
+            for (int n = 0; n < NF; ++n)
                 *reinterpret_cast<float2 *>(dst + L.cb + 8 * n + 2 * L.t) =
                     make_float2(dqc[n][2 * hh] + dqp[n][2 * hh], dqc[n][2 * hh + 1] + dqp[n][2 * hh + 1]);
         }
@@ -593,7 +600,7 @@ __global__ void __launch_bounds__(THREADS, 1) bwd_dkv_kernel(const BwdParams p)
     if (threadIdx.x < T) cs[threadIdx.x] = 0.f;
     __syncthreads();
     row_dots(reinterpret_cast<float *>(sm + OFF_BK), sm + OFF_K, LDB, T, p.u + (size_t)h * DH);
-    float dk[4][4], dv[4][4];  // rows: keys; columns: dimensions
+    float dk[NF][4], dv[NF][4];  // rows: keys; columns: dimensions
     zero(dk);
     zero(dv);
     float *red = reinterpret_cast<float *>(sm + OFF_RED);
@@ -612,7 +619,7 @@ __global__ void __launch_bounds__(THREADS, 1) bwd_dkv_kernel(const BwdParams p)
         __syncthreads();
         float ls[2], dd[2];
         load_row_stats(p, L, bh, i0, ls, dd);
-        float s[4][4], dp[4][4], g[4][4];
+        float s[NF][4], dp[NF][4], g[NF][4];
         key_tile_scores(sm, p, L, i0, j0, s, dp, B);
         grad_scores(sm, p, L, s, dp, ls, dd, g, true);
         column_sums(red, T, L, L.cb, g);
@@ -621,9 +628,9 @@ __global__ void __launch_bounds__(THREADS, 1) bwd_dkv_kernel(const BwdParams p)
             cs[threadIdx.x] += ((red[threadIdx.x] + red[T + threadIdx.x]) + red[2 * T + threadIdx.x]) +
                                red[3 * T + threadIdx.x];
         // dv = P^T dout, dk = g^T q (+ the column sums times u, at the end)
-        warp_nn2<4>(dv, smem_u32(sm + OFF_PH) + L.rb * 2, smem_u32(sm + OFF_PL) + L.rb * 2, LDB,
+        warp_nn2<NF>(dv, smem_u32(sm + OFF_PH) + L.rb * 2, smem_u32(sm + OFF_PL) + L.rb * 2, LDB,
                     true, smem_u32(sm + B.d) + L.cb * 2, LDB, T, L.lane);
-        warp_nn2<4>(dk, smem_u32(sm + OFF_GH) + L.rb * 2, smem_u32(sm + OFF_GL) + L.rb * 2, LDB,
+        warp_nn2<NF>(dk, smem_u32(sm + OFF_GH) + L.rb * 2, smem_u32(sm + OFF_GL) + L.rb * 2, LDB,
                     true, smem_u32(sm + B.q) + L.cb * 2, LDB, T, L.lane);
     }
     __syncthreads();
@@ -634,7 +641,7 @@ __global__ void __launch_bounds__(THREADS, 1) bwd_dkv_kernel(const BwdParams p)
         if (gj < p.K) {
             float *ok = p.dk + (bh * p.K + gj) * DH, *ov = p.dv + (bh * p.K + gj) * DH;
 #pragma unroll
-            for (int n = 0; n < 4; ++n) {
+            for (int n = 0; n < NF; ++n) {
                 const int c = L.cb + 8 * n + 2 * L.t;
                 const float u0 = __bfloat162float(u[c]), u1 = __bfloat162float(u[c + 1]);
                 *reinterpret_cast<float2 *>(ok + c) =
@@ -656,7 +663,7 @@ __global__ void __launch_bounds__(THREADS, 1) bwd_dr_kernel(const BwdParams p)
     const Lane L = lane_of();
     const int d0 = blockIdx.x * T, h = blockIdx.y;
     TXL_CHECK(h < p.H && d0 < p.r_rows, p.status);
-    float dr[4][4];  // rows: distances; columns: dimensions
+    float dr[NF][4];  // rows: distances; columns: dimensions
     zero(dr);
     float *cs = reinterpret_cast<float *>(sm + OFF_CS);  // sum over rows of g, per distance
     if (d0 < p.K) {
@@ -703,14 +710,14 @@ __global__ void __launch_bounds__(THREADS, 1) bwd_dr_kernel(const BwdParams p)
             __syncthreads();
             float ls[2], dd[2];
             load_row_stats(p, L, bh, i0, ls, dd);
-            float sp[4][4], sc[4][4], dp[4][4], s[4][4], g[4][4];
+            float sp[NF][4], sc[NF][4], dp[NF][4], s[NF][4], g[NF][4];
             zero(sp);
-            warp_nt<4>(sp, smem_u32(sm + B.q) + L.rb * LDB, LDB, smem_u32(sm + OFF_K) + L.cb * LDB,
+            warp_nt<NF>(sp, smem_u32(sm + B.q) + L.rb * LDB, LDB, smem_u32(sm + OFF_K) + L.cb * LDB,
                        LDB, DH, L.lane);
             window_product(sm, L, B.q, B.w, reinterpret_cast<const float *>(sm + OFF_BW));
             __syncthreads();
 #pragma unroll
-            for (int n = 0; n < 4; ++n)
+            for (int n = 0; n < NF; ++n)
 #pragma unroll
                 for (int q = 0; q < 4; ++q) {
                     const int i = L.rb + L.g + 8 * (q >> 1), c = L.cb + 8 * n + 2 * L.t + (q & 1);
@@ -720,7 +727,7 @@ __global__ void __launch_bounds__(THREADS, 1) bwd_dr_kernel(const BwdParams p)
             window_product(sm, L, B.d, B.v, nullptr);
             __syncthreads();
 #pragma unroll
-            for (int n = 0; n < 4; ++n)
+            for (int n = 0; n < NF; ++n)
 #pragma unroll
                 for (int q = 0; q < 4; ++q) {
                     const int i = L.rb + L.g + 8 * (q >> 1), c = L.cb + 8 * n + 2 * L.t + (q & 1);
@@ -736,7 +743,7 @@ __global__ void __launch_bounds__(THREADS, 1) bwd_dr_kernel(const BwdParams p)
             if (threadIdx.x < T)
                 cs[threadIdx.x] += ((red[threadIdx.x] + red[T + threadIdx.x]) +
                                     red[2 * T + threadIdx.x]) + red[3 * T + threadIdx.x];
-            warp_nn2<4>(dr, smem_u32(sm + OFF_GH) + L.rb * 2, smem_u32(sm + OFF_GL) + L.rb * 2,
+            warp_nn2<NF>(dr, smem_u32(sm + OFF_GH) + L.rb * 2, smem_u32(sm + OFF_GL) + L.rb * 2,
                         LDB, true, smem_u32(sm + B.q) + L.cb * 2, LDB, T, L.lane);
         }
         __syncthreads();
@@ -749,7 +756,7 @@ __global__ void __launch_bounds__(THREADS, 1) bwd_dr_kernel(const BwdParams p)
             float *dst = p.dr + ((size_t)h * p.r_rows + (p.r_rows - 1 - d)) * DH;
             const float cd = (d < p.K) ? cs[c] : 0.f;
 #pragma unroll
-            for (int n = 0; n < 4; ++n) {
+            for (int n = 0; n < NF; ++n) {
                 const int col = L.cb + 8 * n + 2 * L.t;
                 const float v0 = __bfloat162float(vb[col]), v1 = __bfloat162float(vb[col + 1]);
                 *reinterpret_cast<float2 *>(dst + col) =
