@@ -388,11 +388,12 @@ __device__ __forceinline__ void load_row_stats(const BwdParams &p, const Lane &L
 }
 
 // g = scale P (dP - D) with P = 2^(s - lse2) (0 where masked); g and P as
-// head / rest pairs into the [row][column] tiles (P only when ph != 0).
+// head / rest pairs into the [row][column] tiles (P only with with_p), and g
+// also by window column i - j + 63 (with_z: the dq kernel's shifted operand).
 __device__ __forceinline__ void grad_scores(uint8_t *sm, const BwdParams &p, const Lane &L,
                                             const float (&s)[NF][4], const float (&dp)[NF][4],
                                             const float (&ls)[2], const float (&dd)[2],
-                                            float (&g)[NF][4], bool with_p)
+                                            float (&g)[NF][4], bool with_p, bool with_z = false)
 {
 #pragma unroll
     for (int n = 0; n < NF; ++n)
@@ -410,6 +411,16 @@ __device__ __forceinline__ void grad_scores(uint8_t *sm, const BwdParams &p, con
             split2(g[n][2 * hh], g[n][2 * hh + 1], hd, rs);
             *reinterpret_cast<uint32_t *>(sm + OFF_GH + off) = hd;
             *reinterpret_cast<uint32_t *>(sm + OFF_GL + off) = rs;
+            if (with_z) {
+                // columns j, j + 1 of row i land at window columns w, w - 1
+                const int i = L.rb + L.g + 8 * hh, j = L.cb + 8 * n + 2 * L.t, w = i - j + T - 1;
+                uint16_t *zh = reinterpret_cast<uint16_t *>(sm + OFF_ZH) + i * (LDZ / 2) + w;
+                uint16_t *zl = reinterpret_cast<uint16_t *>(sm + OFF_ZL) + i * (LDZ / 2) + w;
+                zh[0] = (uint16_t)(hd & 0xffffu);
+                zh[-1] = (uint16_t)(hd >> 16);
+                zl[0] = (uint16_t)(rs & 0xffffu);
+                zl[-1] = (uint16_t)(rs >> 16);
+            }
             if (with_p) {
                 split2(P[0], P[1], hd, rs);
                 *reinterpret_cast<uint32_t *>(sm + OFF_PH + off) = hd;
@@ -531,10 +542,13 @@ __global__ void __launch_bounds__(THREADS, 1) bwd_dq_kernel(const BwdParams p)
     float dqc[NF][4], dqp[NF][4];  // content (k) and position (table) parts; rows i, columns t
     zero(dqc);
     zero(dqp);
-    const uint16_t *gh = reinterpret_cast<const uint16_t *>(sm + OFF_GH);
-    const uint16_t *gl = reinterpret_cast<const uint16_t *>(sm + OFF_GL);
-    uint16_t *zh = reinterpret_cast<uint16_t *>(sm + OFF_ZH);
-    uint16_t *zl = reinterpret_cast<uint16_t *>(sm + OFF_ZL);
+    // g by window column, z[i][w] = g[i][i - w + 63]: the columns no key of a
+    // tile reaches (w < i or w > i + 63) stay zero, the others are rewritten
+    // by every tile
+    for (int idx = threadIdx.x; idx < T * (LDZ / 4); idx += THREADS) {
+        reinterpret_cast<uint32_t *>(sm + OFF_ZH)[idx] = 0u;
+        reinterpret_cast<uint32_t *>(sm + OFF_ZL)[idx] = 0u;
+    }
     const int jend = min(p.K, p.M + i0 + T);
     issue_key_tile(sm, p, bh, h, i0, 0, 0);
     for (int j0 = 0, buf = 0; j0 < jend; j0 += T, buf ^= 1) {
@@ -545,15 +559,7 @@ __global__ void __launch_bounds__(THREADS, 1) bwd_dq_kernel(const BwdParams p)
         float s[NF][4], dp[NF][4], g[NF][4];
         key_tile_scores(sm, p, L, i0, j0, s, dp,
                         Bufs{OFF_Q, OFF_D, buf ? OFF_K1 : OFF_K, buf ? OFF_V1 : OFF_V, buf ? OFF_W1 : OFF_W});
-        grad_scores(sm, p, L, s, dp, ls, dd, g, false);
-        __syncthreads();
-        // g by window column: z[i][w] = g[i][i - w + 63] (zero where no key)
-        for (int idx = threadIdx.x; idx < T * W; idx += THREADS) {
-            const int i = idx / W, w = idx % W, j = i - w + T - 1;
-            const bool in = j >= 0 && j < T;
-            zh[i * (LDZ / 2) + w] = in ? gh[i * (LDB / 2) + j] : (uint16_t)0;
-            zl[i * (LDZ / 2) + w] = in ? gl[i * (LDB / 2) + j] : (uint16_t)0;
-        }
+        grad_scores(sm, p, L, s, dp, ls, dd, g, false, true);
         __syncthreads();
         const int cbo = L.cb;  // output columns: dimensions
         warp_nn2<NF>(dqc, smem_u32(sm + OFF_GH) + L.rb * LDB, smem_u32(sm + OFF_GL) + L.rb * LDB, LDB,
