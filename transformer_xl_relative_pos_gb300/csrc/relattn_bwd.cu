@@ -46,7 +46,8 @@ constexpr int NF = 2;   // 8-column fragments of a warp in a 64 x 64 product
 constexpr int NWF = 4;  // in a 64 x 128 window product
 constexpr int LDB = (DH + 8) * 2;   // bytes per bf16 row of 64 (+8 pad: conflict-free ldmatrix)
 constexpr int LDZ = (W + 8) * 2;    // bytes per bf16 row of 128
-constexpr int LDX = W + 4;          // floats per row of the fp32 window product
+constexpr int LDX = W + 8;          // floats per row of the fp32 window product (= 8 mod 32:
+                                    // a half warp's paired stores hit distinct banks)
 
 // Shared memory (bytes): bf16 operand tiles, g and P as head / rest pairs, the
 // window-ordered g, the fp32 window product, per-column bias vectors and
@@ -280,9 +281,11 @@ __device__ __forceinline__ void window_product(uint8_t *sm, const Lane &L, int a
 #pragma unroll
     for (int n = 0; n < NWF; ++n)
 #pragma unroll
-        for (int q = 0; q < 4; ++q) {
-            const int col = 32 * (L.warp & 3) + 8 * n + 2 * L.t + (q & 1);
-            xs[(L.rb + L.g + 8 * (q >> 1)) * LDX + col] = x[n][q] + (colvec ? colvec[col] : 0.f);
+        for (int hh = 0; hh < 2; ++hh) {
+            const int col = 32 * (L.warp & 3) + 8 * n + 2 * L.t;
+            const float c0 = colvec ? colvec[col] : 0.f, c1 = colvec ? colvec[col + 1] : 0.f;
+            *reinterpret_cast<float2 *>(xs + (L.rb + L.g + 8 * hh) * LDX + col) =
+                make_float2(x[n][2 * hh] + c0, x[n][2 * hh + 1] + c1);
         }
 }
 
