@@ -41,6 +41,7 @@ def test_debug_build_reports_a_failed_index_check():
 def test_kernel_parity_tests_pass_with_index_checks():
     r = subprocess.run([sys.executable, "-m", "pytest", "-q", "-x", "-m", "gpu", "-p", "no:cacheprovider",
                         "tests/test_gpu_kernels.py", "tests/test_gpu_window.py",
-                        "tests/test_gpu_decode.py", "tests/test_gpu_project.py"],
+                        "tests/test_gpu_decode.py", "tests/test_gpu_project.py",
+                        "tests/test_gpu_bwd.py"],
                        cwd=ROOT, env=_env(), capture_output=True, text=True, timeout=1800)
     assert r.returncode == 0, (r.stdout[-3000:] + r.stderr[-2000:])
