@@ -225,8 +225,9 @@ __device__ __forceinline__ void async_wait()
 }
 
 // out[w] = vec . row w of a staged bf16 tile (n = 64 or 128 rows), fp32; vec:
-// 64 bf16 in global memory.  Four threads per row (every lane of a warp takes
-// part in the shuffles: n * 4 is a multiple of the block).
+// 64 bf16 in global memory.  Four threads per row (n * 4 items and the block
+// size are multiples of 32, so each warp runs an iteration with all its lanes
+// or skips it whole: the shuffles stay within full warps).
 __device__ __forceinline__ void row_dots(float *out, const uint8_t *tile, int ld, int n,
                                          const __nv_bfloat16 *vec)
 {
