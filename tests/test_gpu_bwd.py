@@ -69,6 +69,7 @@ CASES = [
     (2, 1, 64, 64, 0, 1.0),
     (1, 2, 40, 100, 37, 1.0),
     (2, 2, 96, 150, 0, 3.0),
+    (1, 1, 300, 200, 64, 1.0),
 ]
 
 
