@@ -971,8 +971,12 @@ def bwd_tile_visits(B, H, L, M, T=64):
     rows_keys = sum(-(-min(K, M + i0 + T) // T) for i0 in range(0, L, T))
     keys_rows = sum(len(range(max(0, j0 - M) // T * T, L, T)) for j0 in range(0, K, T))
     dist_rows = B * sum(len(range(max(0, d0 - M - (T - 1)) // T * T, L, T)) for d0 in range(0, K, T))
-    return {"stats": B * H * rows_keys, "dq": B * H * rows_keys, "dkv": B * H * keys_rows,
-            "dr": H * dist_rows, "chunks": B * H * n_chunks}
+    v = {"stats": B * H * rows_keys, "dr": H * dist_rows, "chunks": B * H * n_chunks}
+    if n_chunks <= 2:  # one pass for dq, dk and dv
+        v["dqkv"] = B * H * rows_keys
+    else:
+        v["dq"], v["dkv"] = B * H * rows_keys, B * H * keys_rows
+    return v
 
 
 def run_bwd(args):
@@ -1031,9 +1035,11 @@ def run_bwd(args):
     # tile multiply-adds: stats q.k, dout.v (64^3 each), the q.r window (2 x 64^3);
     # dq adds g.k and the window-ordered g.r (head and rest: 2 x 3 x 64^3);
     # dk/dv add P^T dout and g^T q (2 x 2 x 64^3); the table tile q.r, the key
-    # and value windows and g^T q (64^3 + 4 x 64^3 + 2 x 64^3)
-    mac_tile = {"stats": 4 * T ** 3, "dq": 10 * T ** 3, "dkv": 8 * T ** 3, "dr": 7 * T ** 3}
-    executed = 2.0 * sum(visits[k] * mac_tile[k] for k in mac_tile)
+    # and value windows and g^T q (64^3 + 4 x 64^3 + 2 x 64^3); the one-pass
+    # dq / dk / dv launch of short segments: scores, dq's and dk/dv's products
+    mac_tile = {"stats": 4 * T ** 3, "dq": 10 * T ** 3, "dkv": 8 * T ** 3, "dr": 7 * T ** 3,
+                "dqkv": 14 * T ** 3}
+    executed = 2.0 * sum(visits[k] * mac_tile[k] for k in mac_tile if k in visits)
     pk = peaks()
     useful = 2.0 * 6.0 * L * K * 64 * B * H
     print(json.dumps({"bwd": {

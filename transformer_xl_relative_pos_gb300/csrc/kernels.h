@@ -115,12 +115,15 @@ struct BwdParams {
     const __nv_bfloat16 *q, *k, *v, *r, *u, *vb, *dout;
     float *dq, *dk, *dv, *dr, *du, *dvb;
     float *lse2, *dsum, *part;
+    float *dq_part;  // segments of at most two row chunks: dq per key split
     int B, H, M, L, K, r_rows;
     float scale, scale_log2;
     unsigned int *status;
 };
 constexpr int kBwdRows = 64;  // query rows (and keys, distances) per tile
+constexpr int kBwdMaxSplits = 4;  // key splits of the one-pass dq / dk / dv launch
 size_t bwd_workspace_bytes(int B, int H, int L);
+size_t bwd_dq_part_offset(int B, int H, int L);  // where the dq partials start in the workspace
 cudaError_t launch_relattn_bwd(const BwdParams &p, cudaStream_t s);
 
 cudaError_t launch_wait_probe(unsigned int *status, unsigned long long wait_ns, cudaStream_t s);

@@ -33,6 +33,8 @@
 // contractions (dq's position part; the content part of a distance tile,
 // whose pair (i, d) is key M + i - d) are window products of g laid out by the
 // same index.  Results repeat bit for bit.
+#include <cmath>
+
 #include "kernels.h"
 
 namespace txl {
@@ -294,6 +296,7 @@ __device__ __forceinline__ void window_product(uint8_t *sm, const Lane &L, int a
 // rows, keys, values, table window.
 struct Bufs {
     int q, d, k, v, w;
+    int bw = OFF_BW;  // the window's v.r vector (fp32)
 };
 
 // Log2-scaled scores (-inf where masked) and dP = dout . v of the lane's 16
@@ -312,7 +315,7 @@ __device__ __forceinline__ void key_tile_scores(uint8_t *sm, const BwdParams &p,
     warp_nt<NF>(dp, smem_u32(sm + B.d) + L.rb * LDB, LDB, smem_u32(sm + B.v) + L.cb * LDB, LDB,
                DH, L.lane);
     const float *bk = reinterpret_cast<const float *>(sm + OFF_BK);
-    window_product(sm, L, B.q, B.w, reinterpret_cast<const float *>(sm + OFF_BW));
+    window_product(sm, L, B.q, B.w, reinterpret_cast<const float *>(sm + B.bw));
     __syncthreads();
     const float *xs = reinterpret_cast<const float *>(sm + OFF_XS);
 #pragma unroll
@@ -789,6 +792,172 @@ __global__ void bwd_bias_kernel(const BwdParams p, int n_chunks)
     else p.dvb[(size_t)h * DH + t - DH] = acc;
 }
 
+// ---- dq, dk, dv in one pass, for segments of at most two row chunks -----------
+// Block (b*H + h, key split): every row of the segment stays staged (chunk 0 in
+// the q / dout regions, chunk 1 in the second table-window region); over the
+// split's key tiles (keys and values copied in one tile ahead, the 192-row
+// table window of both chunks at the tile's start), per chunk: the scores,
+// g and P, then dq += g k + (g by window column) r_w, and the tile's
+// dk += g^T q, dv += P^T dout.  A tile's dk and dv are complete after its
+// chunks, since the block holds every row; dq is summed over the key splits
+// afterwards in a fixed order.  One score pass instead of the two of the dq and
+// dk / dv launches.
+constexpr int Q_ROWS1 = OFF_W1;             // q rows of chunk 1
+constexpr int D_ROWS1 = OFF_W1 + T * LDB;   // dout rows of chunk 1
+constexpr int WBW2 = OFF_W + (W + T) * LDB; // v.r of the 192-row window (in the value-window region)
+static_assert(WBW2 + (W + T) * 4 <= OFF_GH, "window biases must fit the value-window region");
+static_assert(2 * T * LDB <= W * LDB, "two row chunks must fit the second window region");
+
+__global__ void __launch_bounds__(THREADS, 1) bwd_dqkv_kernel(const BwdParams p, int n_splits)
+{
+    extern __shared__ __align__(16) uint8_t sm[];
+    const Lane L = lane_of();
+    const long long bh = blockIdx.x;
+    const int h = (int)(bh % p.H), split = blockIdx.y;
+    const int n_ch = (p.L + T - 1) / T;
+    const int n_kt = (p.K + T - 1) / T;
+    const int per = (n_kt + n_splits - 1) / n_splits;
+    const int kt0 = split * per, kt1 = min(n_kt, kt0 + per);
+    TXL_CHECK(bh < (long long)p.B * p.H && n_ch <= 2 && split < n_splits, p.status);
+    auto ko = [](int b) { return b ? OFF_K1 : OFF_K; };
+    auto vo = [](int b) { return b ? OFF_V1 : OFF_V; };
+    stage(sm + OFF_Q, LDB, T, p.q + bh * p.L * DH, 0, 1, p.L);
+    stage(sm + OFF_D, LDB, T, p.dout + bh * p.L * DH, 0, 1, p.L);
+    stage(sm + Q_ROWS1, LDB, T, p.q + bh * p.L * DH, T, 1, p.L);
+    stage(sm + D_ROWS1, LDB, T, p.dout + bh * p.L * DH, T, 1, p.L);
+    float ls[2][2], dd[2][2];
+    load_row_stats(p, L, bh, 0, ls[0], dd[0]);
+    load_row_stats(p, L, bh, T, ls[1], dd[1]);
+    float dqc[2][NF][4], dqp[2][NF][4];
+    zero(dqc[0]);
+    zero(dqc[1]);
+    zero(dqp[0]);
+    zero(dqp[1]);
+    float *cs = reinterpret_cast<float *>(sm + OFF_CS);  // per key of the tile: sum of g over the rows
+    float *red = reinterpret_cast<float *>(sm + OFF_RED);
+    // window-ordered g: the columns no key reaches stay zero
+    for (int idx = threadIdx.x; idx < T * (LDZ / 4); idx += THREADS) {
+        reinterpret_cast<uint32_t *>(sm + OFF_ZH)[idx] = 0u;
+        reinterpret_cast<uint32_t *>(sm + OFF_ZL)[idx] = 0u;
+    }
+    auto issue_kv = [&](int kt, int b) {
+        stage_async(sm + ko(b), LDB, T, p.k + bh * p.K * DH, (long long)kt * T, 1, p.K);
+        stage_async(sm + vo(b), LDB, T, p.v + bh * p.K * DH, (long long)kt * T, 1, p.K);
+    };
+    if (kt0 < kt1) issue_kv(kt0, 0);
+    for (int kt = kt0, buf = 0; kt < kt1; ++kt, buf ^= 1) {
+        const int j0 = kt * T;
+        __syncthreads();  // the last tile's readers of the window and of this buffer pair are done
+        // window row w: the table row of distance M - j0 - 63 + w (w < 192);
+        // chunk c reads rows 64 c .. 64 c + 127
+        const long long dmin = (long long)p.M - j0 - (T - 1);
+        stage_async(sm + OFF_W, LDB, W + T, p.r + (size_t)h * p.r_rows * DH, p.r_rows - 1 - dmin, -1,
+                    p.r_rows);
+        const bool more = kt + 1 < kt1;
+        if (more) issue_kv(kt + 1, buf ^ 1);
+        if (more) async_wait<2>();
+        else async_wait<0>();
+        __syncthreads();
+        row_dots(reinterpret_cast<float *>(sm + OFF_BK), sm + ko(buf), LDB, T, p.u + (size_t)h * DH);
+        row_dots(reinterpret_cast<float *>(sm + WBW2), sm + OFF_W, LDB, W + T, p.vb + (size_t)h * DH);
+        if (threadIdx.x < T) cs[threadIdx.x] = 0.f;
+        __syncthreads();
+        float dk[NF][4], dv[NF][4];
+        zero(dk);
+        zero(dv);
+#pragma unroll
+        for (int c = 0; c < 2; ++c) {
+            if (c >= n_ch) break;  // (block-uniform)
+            if (j0 > p.M + c * T + T - 1) continue;  // the tile is hidden from every row of the chunk
+            const Bufs B{c ? Q_ROWS1 : OFF_Q, c ? D_ROWS1 : OFF_D, ko(buf), vo(buf), OFF_W + c * T * LDB,
+                         WBW2 + c * T * 4};
+            float s[NF][4], dp[NF][4], g[NF][4];
+            key_tile_scores(sm, p, L, c * T, j0, s, dp, B);
+            grad_scores(sm, p, L, s, dp, ls[c], dd[c], g, true, true);
+            column_sums(red, T, L, L.cb, g);
+            __syncthreads();
+            if (threadIdx.x < T)
+                cs[threadIdx.x] += ((red[threadIdx.x] + red[T + threadIdx.x]) + red[2 * T + threadIdx.x]) +
+                                   red[3 * T + threadIdx.x];
+            warp_nn2<NF>(dqc[c], smem_u32(sm + OFF_GH) + L.rb * LDB, smem_u32(sm + OFF_GL) + L.rb * LDB,
+                         LDB, false, smem_u32(sm + ko(buf)) + L.cb * 2, LDB, T, L.lane);
+            warp_nn2<NF>(dqp[c], smem_u32(sm + OFF_ZH) + L.rb * LDZ, smem_u32(sm + OFF_ZL) + L.rb * LDZ,
+                         LDZ, false, smem_u32(sm + B.w) + L.cb * 2, LDB, W, L.lane);
+            warp_nn2<NF>(dv, smem_u32(sm + OFF_PH) + L.rb * 2, smem_u32(sm + OFF_PL) + L.rb * 2, LDB,
+                         true, smem_u32(sm + B.d) + L.cb * 2, LDB, T, L.lane);
+            warp_nn2<NF>(dk, smem_u32(sm + OFF_GH) + L.rb * 2, smem_u32(sm + OFF_GL) + L.rb * 2, LDB,
+                         true, smem_u32(sm + B.q) + L.cb * 2, LDB, T, L.lane);
+        }
+        __syncthreads();  // the tile's column sums are complete
+        const __nv_bfloat16 *u = p.u + (size_t)h * DH;
+#pragma unroll
+        for (int hh = 0; hh < 2; ++hh) {
+            const int j = L.rb + L.g + 8 * hh, gj = j0 + j;
+            if (gj < p.K) {
+                float *okp = p.dk + (bh * p.K + gj) * DH, *ovp = p.dv + (bh * p.K + gj) * DH;
+#pragma unroll
+                for (int n = 0; n < NF; ++n) {
+                    const int cc = L.cb + 8 * n + 2 * L.t;
+                    const float u0 = __bfloat162float(u[cc]), u1 = __bfloat162float(u[cc + 1]);
+                    *reinterpret_cast<float2 *>(okp + cc) =
+                        make_float2(fmaf(cs[j], u0, dk[n][2 * hh]), fmaf(cs[j], u1, dk[n][2 * hh + 1]));
+                    *reinterpret_cast<float2 *>(ovp + cc) = make_float2(dv[n][2 * hh], dv[n][2 * hh + 1]);
+                }
+            }
+        }
+    }
+    // dq of the split (the final dq when unsplit)
+    float *dqdst = (n_splits == 1) ? p.dq : p.dq_part + (size_t)split * p.B * p.H * p.L * DH;
+#pragma unroll
+    for (int c = 0; c < 2; ++c)
+#pragma unroll
+        for (int hh = 0; hh < 2; ++hh) {
+            const int gi = c * T + L.rb + L.g + 8 * hh;
+            if (c < n_ch && gi < p.L) {
+                float *dst = dqdst + (bh * p.L + gi) * DH;
+#pragma unroll
+                for (int n = 0; n < NF; ++n)
+                    *reinterpret_cast<float2 *>(dst + L.cb + 8 * n + 2 * L.t) =
+                        make_float2(dqc[c][n][2 * hh] + dqp[c][n][2 * hh],
+                                    dqc[c][n][2 * hh + 1] + dqp[c][n][2 * hh + 1]);
+            }
+        }
+    // du, dv_bias partials of the split: column sums of the two parts of dq
+#pragma unroll
+    for (int n = 0; n < NF; ++n)
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+            dqc[0][n][q] += dqc[1][n][q];
+            dqp[0][n][q] += dqp[1][n][q];
+        }
+    __syncthreads();
+    column_sums(red, 2 * DH, L, L.cb, dqc[0]);
+    column_sums(red, 2 * DH, L, DH + L.cb, dqp[0]);
+    __syncthreads();
+    if (threadIdx.x < 2 * DH) {
+        const float acc = ((red[threadIdx.x] + red[2 * DH + threadIdx.x]) + red[4 * DH + threadIdx.x]) +
+                          red[6 * DH + threadIdx.x];
+        p.part[(bh * n_splits + split) * 2 * DH + threadIdx.x] = acc;
+    }
+}
+
+// dq = the key splits' partials summed in order.
+__global__ void bwd_dq_reduce_kernel(const BwdParams p, int n_splits)
+{
+    const size_t n4 = (size_t)p.B * p.H * p.L * DH / 4;
+    for (size_t x = (size_t)blockIdx.x * blockDim.x + threadIdx.x; x < n4; x += (size_t)gridDim.x * blockDim.x) {
+        float4 acc = reinterpret_cast<const float4 *>(p.dq_part)[x];
+        for (int s = 1; s < n_splits; ++s) {
+            const float4 v = reinterpret_cast<const float4 *>(p.dq_part + (size_t)s * n4 * 4)[x];
+            acc.x += v.x;
+            acc.y += v.y;
+            acc.z += v.z;
+            acc.w += v.w;
+        }
+        reinterpret_cast<float4 *>(p.dq)[x] = acc;
+    }
+}
+
 size_t align256(size_t x) { return (x + 255) & ~(size_t)255; }
 
 } // namespace
@@ -797,8 +966,19 @@ size_t bwd_workspace_bytes(int B, int H, int L)
 {
     if (B <= 0 || H <= 0 || L <= 0) return 0;
     const size_t rows = (size_t)B * H * L;
-    const size_t chunks = (size_t)B * H * ((L + T - 1) / T);
-    return 2 * align256(rows * sizeof(float)) + align256(chunks * 2 * DH * sizeof(float));
+    const int n_chunks = (L + T - 1) / T;
+    const size_t parts = (size_t)B * H * (size_t)(n_chunks > kBwdMaxSplits ? n_chunks : kBwdMaxSplits);
+    size_t bytes = 2 * align256(rows * sizeof(float)) + align256(parts * 2 * DH * sizeof(float));
+    if (n_chunks <= 2) bytes += align256((size_t)kBwdMaxSplits * rows * DH * sizeof(float));
+    return bytes;
+}
+
+size_t bwd_dq_part_offset(int B, int H, int L)
+{
+    const size_t rows = (size_t)B * H * L;
+    const int n_chunks = (L + T - 1) / T;
+    const size_t parts = (size_t)B * H * (size_t)(n_chunks > kBwdMaxSplits ? n_chunks : kBwdMaxSplits);
+    return 2 * align256(rows * sizeof(float)) + align256(parts * 2 * DH * sizeof(float));
 }
 
 cudaError_t launch_relattn_bwd(const BwdParams &p, cudaStream_t s)
@@ -809,7 +989,8 @@ cudaError_t launch_relattn_bwd(const BwdParams &p, cudaStream_t s)
     if (e != cudaSuccess) return e;
     if (dev < 0 || dev >= 64 || !attr_set[dev]) {
         for (const void *f : {(const void *)bwd_stats_kernel, (const void *)bwd_dq_kernel,
-                              (const void *)bwd_dkv_kernel, (const void *)bwd_dr_kernel})
+                              (const void *)bwd_dkv_kernel, (const void *)bwd_dr_kernel,
+                              (const void *)bwd_dqkv_kernel})
             if ((e = cudaFuncSetAttribute(f, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                           SMEM_BYTES)) != cudaSuccess)
                 return e;
@@ -821,10 +1002,29 @@ cudaError_t launch_relattn_bwd(const BwdParams &p, cudaStream_t s)
     if (BH > 0x7fffffffLL || n_chunks > 65535 || n_keys > 65535 || p.H > 65535)
         return cudaErrorInvalidValue;
     bwd_stats_kernel<<<dim3((unsigned)BH, n_chunks), THREADS, SMEM_BYTES, s>>>(p);
-    bwd_dq_kernel<<<dim3((unsigned)BH, n_chunks), THREADS, SMEM_BYTES, s>>>(p);
-    bwd_dkv_kernel<<<dim3((unsigned)BH, n_keys), THREADS, SMEM_BYTES, s>>>(p);
+    int n_bias = n_chunks;
+    if (n_chunks <= 2) {
+        // one pass for dq, dk, dv; the key split that fills the SMs' waves best
+        int sms = 0;
+        if ((e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess)
+            return e;
+        int n_splits = 1;
+        double best = 0.0;
+        for (int sp = 1; sp <= kBwdMaxSplits && sp <= n_keys; ++sp) {
+            const double blocks = (double)BH * sp;
+            const double waves = std::ceil(blocks / sms);
+            const double eff = blocks / (waves * sms);
+            if (eff > best + 0.02) best = eff, n_splits = sp;
+        }
+        bwd_dqkv_kernel<<<dim3((unsigned)BH, n_splits), THREADS, SMEM_BYTES, s>>>(p, n_splits);
+        if (n_splits > 1) bwd_dq_reduce_kernel<<<1024, 256, 0, s>>>(p, n_splits);
+        n_bias = n_splits;
+    } else {
+        bwd_dq_kernel<<<dim3((unsigned)BH, n_chunks), THREADS, SMEM_BYTES, s>>>(p);
+        bwd_dkv_kernel<<<dim3((unsigned)BH, n_keys), THREADS, SMEM_BYTES, s>>>(p);
+    }
     bwd_dr_kernel<<<dim3((unsigned)n_dist, p.H), THREADS, SMEM_BYTES, s>>>(p);
-    bwd_bias_kernel<<<p.H, 2 * DH, 0, s>>>(p, n_chunks);
+    bwd_bias_kernel<<<p.H, 2 * DH, 0, s>>>(p, n_bias);
     return cudaGetLastError();
 }
 

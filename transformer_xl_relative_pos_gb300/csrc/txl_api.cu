@@ -831,6 +831,7 @@ extern "C" int txl_relattn_bwd(const void *q, const void *k, const void *v, cons
     p.lse2 = reinterpret_cast<float *>(ws);
     p.dsum = reinterpret_cast<float *>(ws + row_bytes);
     p.part = reinterpret_cast<float *>(ws + 2 * row_bytes);
+    p.dq_part = reinterpret_cast<float *>(ws + txl::bwd_dq_part_offset(B, H, L));
     p.B = B;
     p.H = H;
     p.M = M;
