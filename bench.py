@@ -965,12 +965,12 @@ def run_stack(args):
 def bwd_tile_visits(B, H, L, M, T=64):
     """64 x 64 pair tiles each launch of txl_relattn_bwd visits (the kernels'
     loop bounds: key tiles up to the last key a chunk sees, query chunks from
-    the first that sees a key tile or a distance tile)."""
+    the first that sees a key tile or reaches a distance tile)."""
     K = M + L
     n_chunks = -(-L // T)
     rows_keys = sum(-(-min(K, M + i0 + T) // T) for i0 in range(0, L, T))
     keys_rows = sum(len(range(max(0, j0 - M) // T * T, L, T)) for j0 in range(0, K, T))
-    dist_rows = B * sum(len(range(max(0, d0 - M - (T - 1)) // T * T, L, T)) for d0 in range(0, K, T))
+    dist_rows = B * sum(len(range(max(0, d0 - M) // T * T, L, T)) for d0 in range(0, K, T))
     v = {"stats": B * H * rows_keys, "dr": H * dist_rows, "chunks": B * H * n_chunks}
     if n_chunks <= 2:  # one pass for dq, dk and dv
         v["dqkv"] = B * H * rows_keys
@@ -1002,7 +1002,7 @@ def run_bwd(args):
     f32 = lambda *sh: torch.empty(*sh, dtype=torch.float32, device=dev)
     grads = (f32(B, H, L, 64), f32(B, H, K, 64), f32(B, H, K, 64), f32(H, K, 64), f32(H, 64),
              f32(H, 64))
-    ws = torch.empty(max(txl.bwd_workspace_size(B, H, L), 256), dtype=torch.uint8, device=dev)
+    ws = torch.empty(max(txl.bwd_workspace_size(B, H, L, M), 256), dtype=torch.uint8, device=dev)
     scale = 1.0 / math.sqrt(64)
 
     def call(i):
@@ -1034,10 +1034,10 @@ def run_bwd(args):
     T = 64
     # tile multiply-adds: stats q.k, dout.v (64^3 each), the q.r window (2 x 64^3);
     # dq adds g.k and the window-ordered g.r (head and rest: 2 x 3 x 64^3);
-    # dk/dv add P^T dout and g^T q (2 x 2 x 64^3); the table tile q.r, the key
-    # and value windows and g^T q (64^3 + 4 x 64^3 + 2 x 64^3); the one-pass
-    # dq / dk / dv launch of short segments: scores, dq's and dk/dv's products
-    mac_tile = {"stats": 4 * T ** 3, "dq": 10 * T ** 3, "dkv": 8 * T ** 3, "dr": 7 * T ** 3,
+    # dk/dv add P^T dout and g^T q (2 x 2 x 64^3); the one-pass dq / dk / dv
+    # launch of short segments: scores, dq's and dk/dv's products; the table
+    # tile: g^T q from the stored g, read along its diagonals (2 x 64^3)
+    mac_tile = {"stats": 4 * T ** 3, "dq": 10 * T ** 3, "dkv": 8 * T ** 3, "dr": 2 * T ** 3,
                 "dqkv": 14 * T ** 3}
     executed = 2.0 * sum(visits[k] * mac_tile[k] for k in mac_tile if k in visits)
     pk = peaks()
@@ -1050,7 +1050,9 @@ def run_bwd(args):
         "tensor_frac": round(executed / (us * 1e-6) / 1e12 / pk["bf16_tflops"], 4),
         "useful_gflop": round(useful / 1e9, 1),
         "useful_tflops": round(useful / (us * 1e-6) / 1e12, 2),
-        "tile_visits": visits, "launches": 5}}), flush=True)
+        "tile_visits": visits, "launches": 5,
+        # g of every pair, fp32: written by the dq pass, read by the table gradient
+        "g_stored_mb": round(B * H * L * K * 4 / 1e6, 1)}}), flush=True)
 
 
 def main():

@@ -368,15 +368,18 @@ int txl_qkv_project(const void *h, const void *w, int B, int L, int d_model, int
  * Outputs, fp32, dense, written (not accumulated), 16-byte aligned:
  *   dq [B][H][L][dh]   dk, dv [B][H][M+L][dh]   dr [H][r_rows][dh] (rows of
  *   distances >= M+L are zero)   du, dv_bias [H][dh]
- * workspace: txl_relattn_bwd_workspace_size(B, H, L) bytes of device memory
- * (per-row statistics and per-block bias partials); the sums over the batch
- * are ordered, so results repeat bit for bit.  dh must be 64 and dtype
+ * workspace: txl_relattn_bwd_workspace_size(B, H, L, M) bytes of device
+ * memory, 256-byte aligned (per-row statistics, per-block bias and dq
+ * partials, and g of every query-key pair: B*H*L rows of M+L rounded up to 64
+ * fp32, from which the table gradient is summed); 0 for sizes out of range.  The sums
+ * over the batch and the key splits are ordered, so results repeat bit for
+ * bit.  dh must be 64 and dtype
  * TXL_DTYPE_BF16.  Asynchronous on `stream`.  Errors: TXL_ERR_INVALID_ARG
  * (NULL pointer, bad sizes), TXL_ERR_UNSUPPORTED (dh, dtype, sizes past the
  * grid limits), TXL_ERR_SHAPE (r_rows < M+L), TXL_ERR_MISALIGNED,
  * TXL_ERR_WORKSPACE, TXL_ERR_CUDA.
  */
-size_t txl_relattn_bwd_workspace_size(int B, int H, int L);
+size_t txl_relattn_bwd_workspace_size(int B, int H, int L, int M);
 int txl_relattn_bwd(const void *q, const void *k, const void *v, const void *r, int r_rows,
                     const void *u, const void *v_bias, const void *dout, float *dq, float *dk,
                     float *dv, float *dr, float *du, float *dv_bias, int B, int H, int M, int L,

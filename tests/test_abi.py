@@ -285,14 +285,21 @@ def test_qkv_project_validation():
 
 def test_relattn_bwd_workspace_and_validation():
     # Host checks only: every case is refused before any launch.
-    rows = 3 * 5 * 130
-    chunks = 3 * 5 * 3
     r256 = lambda x: (x + 255) // 256 * 256
-    assert txl.bwd_workspace_size(3, 5, 130) == 2 * r256(rows * 4) + r256(chunks * 128 * 4)
-    assert txl.bwd_workspace_size(0, 5, 130) == 0
+    # three row chunks: row statistics, bias partials per (b, h, chunk) (at
+    # least four), g by distance with rows of M + L = 200 rounded up to 256
+    rows = 3 * 5 * 130
+    assert txl.bwd_workspace_size(3, 5, 130, 70) == (2 * r256(rows * 4) + r256(3 * 5 * 4 * 128 * 4) +
+                                                     r256(rows * 256 * 4))
+    # two row chunks: also the dq partials of up to four key splits
+    rows = 2 * 3 * 100
+    assert txl.bwd_workspace_size(2, 3, 100, 50) == (2 * r256(rows * 4) + r256(2 * 3 * 4 * 128 * 4) +
+                                                     r256(4 * rows * 64 * 4) + r256(rows * 192 * 4))
+    assert txl.bwd_workspace_size(0, 5, 130, 70) == 0
+    assert txl.bwd_workspace_size(3, 5, 130, -1) == 0
     f = L().txl_relattn_bwd
     p = 16  # a 16-byte aligned stand-in address (never dereferenced)
-    ws_need = txl.bwd_workspace_size(2, 2, 8)
+    ws_need = txl.bwd_workspace_size(2, 2, 8, 8)
 
     def call(**kw):
         a = dict(q=p, k=p, v=p, r=p, r_rows=16, u=p, vb=p, dout=p, dq=p, dk=p, dv=p, dr=p, du=p,

@@ -95,7 +95,7 @@ def lib():
                 "txl_qkv_project": (_c_int, [_c_p, _c_p, _c_int, _c_int, _c_int, _c_int, _c_int,
                                              _c_p, _c_p, ctypes.POINTER(KVWindow), _c_p,
                                              ctypes.POINTER(MemState), _c_p]),
-                "txl_relattn_bwd_workspace_size": (_c_size, [_c_int, _c_int, _c_int]),
+                "txl_relattn_bwd_workspace_size": (_c_size, [_c_int, _c_int, _c_int, _c_int]),
                 "txl_relattn_bwd": (_c_int, [_c_p, _c_p, _c_p, _c_p, _c_int, _c_p, _c_p, _c_p,
                                              _c_p, _c_p, _c_p, _c_p, _c_p, _c_p, _c_int, _c_int,
                                              _c_int, _c_int, _c_int, _c_float, _c_int, _c_p,
@@ -253,9 +253,10 @@ def relattn_fwd(q, k, v, r, u, v_bias, M: int, scale: float, *, out=None, lse=No
     return (out, lse) if want_lse else out
 
 
-def bwd_workspace_size(B: int, H: int, L: int) -> int:
-    """Bytes of device workspace txl_relattn_bwd needs."""
-    return int(lib().txl_relattn_bwd_workspace_size(int(B), int(H), int(L)))
+def bwd_workspace_size(B: int, H: int, L: int, M: int) -> int:
+    """Bytes of device workspace txl_relattn_bwd needs for a segment of L rows
+    after a memory of M."""
+    return int(lib().txl_relattn_bwd_workspace_size(int(B), int(H), int(L), int(M)))
 
 
 def relattn_bwd(q, k, v, r, u, v_bias, dout, M: int, scale: float, *, grads=None,
@@ -273,7 +274,7 @@ def relattn_bwd(q, k, v, r, u, v_bias, dout, M: int, scale: float, *, grads=None
         grads = (f(q), f(k), f(v), f(r), f(u), f(v_bias))
     dq, dk, dv, dr, du, dvb = grads
     if workspace is None:
-        workspace = torch.empty(max(bwd_workspace_size(B, H, L), 256), dtype=torch.uint8,
+        workspace = torch.empty(max(bwd_workspace_size(B, H, L, M), 256), dtype=torch.uint8,
                                 device=q.device)
     f32 = torch.float32
     rc = lib().txl_relattn_bwd(

@@ -116,14 +116,17 @@ struct BwdParams {
     float *dq, *dk, *dv, *dr, *du, *dvb;
     float *lse2, *dsum, *part;
     float *dq_part;  // segments of at most two row chunks: dq per key split
+    float *g_all;    // g of every visited pair: [B*H][L][Kd], for the table gradient
     int B, H, M, L, K, r_rows;
+    int Kd;          // K rounded up to a whole tile (the row stride of g_all)
     float scale, scale_log2;
     unsigned int *status;
 };
 constexpr int kBwdRows = 64;  // query rows (and keys, distances) per tile
 constexpr int kBwdMaxSplits = 4;  // key splits of the one-pass dq / dk / dv launch
-size_t bwd_workspace_bytes(int B, int H, int L);
+size_t bwd_workspace_bytes(int B, int H, int L, int M);
 size_t bwd_dq_part_offset(int B, int H, int L);  // where the dq partials start in the workspace
+size_t bwd_g_offset(int B, int H, int L);        // where g of every pair starts
 cudaError_t launch_relattn_bwd(const BwdParams &p, cudaStream_t s);
 
 cudaError_t launch_wait_probe(unsigned int *status, unsigned long long wait_ns, cudaStream_t s);

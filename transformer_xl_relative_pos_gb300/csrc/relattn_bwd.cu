@@ -9,30 +9,32 @@
 //   du = sum g_ij k_j                     dv_bias = sum g_ij r_{M+i-j}
 // (dr, du, dv_bias summed over the batch: the table and biases are shared).
 //
-// Five launches over tiles of 64 query rows x 64 columns (keys, or distances
-// for the table gradient), 512 threads = 16 warps, warp w taking rows
+// Launches over tiles of 64 query rows x 64 columns (keys, or distances for
+// the table gradient), 512 threads = 16 warps, warp w taking rows
 // 16 (w / 4) .. +15 and columns 16 (w % 4) .. +15 of every 64 x 64 product
 // (and columns 32 (w % 4) .. +31 of a 64 x 128 window product):
 //   stats   per 64-row chunk, over its key tiles: online log-sum-exp of the
 //           scores and D (nothing from the forward call is needed)
-//   dq      per 64-row chunk, over its key tiles: dq, and the chunk's
-//           partials of du and dv_bias
-//   dkv     per 64-key tile, over the query chunks that see it: dk, dv
+//   dqkv    segments of at most two chunks: per (batch row, head, key split),
+//           one score pass for dq, dk, dv (dq partials summed over the splits
+//           in order by dq_reduce)
+//   dq      longer segments: per 64-row chunk, over its key tiles: dq
+//   dkv     longer segments: per 64-key tile, over the chunks that see it
 //   dr      per head and 64-distance tile, over the batch and query chunks:
-//           the table gradient, with no atomics
+//           the table gradient from g, which the dq passes store
 //   bias    per head: du, dv_bias from the partials, in a fixed order
-// Every tile recomputes its scores.  All products run on the tensor cores as
-// warp-level mma.m16n8k16 (bf16 operands from shared memory by ldmatrix, fp32
-// accumulation), exactly: q, k, v, r and dout are bf16 already, the bias terms
-// u.k_j and v.r_d are per-column vectors added in fp32, g and P (fp32) enter as
-// a bf16 head plus the bf16 rounding of the rest (~2^-17 relative), and the
-// rank-one parts of dk and dr (column sums of g times u or v) are added in
-// fp32.  The Appendix B shift is index arithmetic, as in the forward: the
-// position term of a pair tile is row i of the product q R_w^T over the tile's
-// 127-distance window, read at window column i - j + 63; the shifted
-// contractions (dq's position part; the content part of a distance tile,
-// whose pair (i, d) is key M + i - d) are window products of g laid out by the
-// same index.  Results repeat bit for bit.
+// The dq / dk / dv tiles recompute their scores.  All products run on the
+// tensor cores as warp-level mma.m16n8k16 (bf16 operands from shared memory by
+// ldmatrix, fp32 accumulation), exactly: q, k, v, r and dout are bf16 already,
+// the bias terms u.k_j and v.r_d are per-column vectors added in fp32, g and P
+// (fp32) enter as a bf16 head plus the bf16 rounding of the rest (~2^-17
+// relative), and the rank-one parts of dk and dr (column sums of g times u or
+// v) are added in fp32.  The Appendix B shift is index arithmetic, as in the
+// forward: the position term of a pair tile is row i of the product q R_w^T
+// over the tile's 127-distance window, read at window column i - j + 63; dq's
+// position part is a window product of g laid out by the same index, and the
+// table gradient reads the stored g along the same diagonals (row i of a
+// distance tile starts at key M + i - d0 - 63).  Results repeat bit for bit.
 #include <cmath>
 
 #include "kernels.h"
@@ -56,10 +58,10 @@ constexpr int LDX = W + 8;          // floats per row of the fp32 window product
 // reduction scratch.
 constexpr int OFF_Q = 0;                    // q rows of the chunk [64][72]
 constexpr int OFF_D = OFF_Q + T * LDB;      // dout rows
-constexpr int OFF_K = OFF_D + T * LDB;      // key tile (distance tiles: table tile)
+constexpr int OFF_K = OFF_D + T * LDB;      // key tile
 constexpr int OFF_V = OFF_K + T * LDB;      // value tile
-constexpr int OFF_W = OFF_V + T * LDB;      // window [128][72]: table rows, or key rows
-constexpr int OFF_W2 = OFF_W + W * LDB;     // value window (distance tiles)
+constexpr int OFF_W = OFF_V + T * LDB;      // table window [128][72]
+constexpr int OFF_W2 = OFF_W + W * LDB;     // the one-pass kernel's window rows 128.. and v.r vector
 constexpr int OFF_GH = OFF_W2 + W * LDB;    // g head [64][72], pair (i, column)
 constexpr int OFF_GL = OFF_GH + T * LDB;    // g rest
 constexpr int OFF_PH = OFF_GL + T * LDB;    // P head
@@ -67,10 +69,10 @@ constexpr int OFF_PL = OFF_PH + T * LDB;    // P rest
 constexpr int OFF_ZH = OFF_PL + T * LDB;    // g by window column [64][136], head
 constexpr int OFF_ZL = OFF_ZH + T * LDZ;    // rest
 constexpr int OFF_XS = OFF_ZL + T * LDZ;    // fp32 [64][132] window product
-constexpr int OFF_BK = OFF_XS + T * LDX * 4;  // fp32 [64]: u.k_j (or v.r_d)
-constexpr int OFF_BW = OFF_BK + T * 4;        // fp32 [128]: v.r_w (or u.k_w) of the window
+constexpr int OFF_BK = OFF_XS + T * LDX * 4;  // fp32 [64]: u.k_j
+constexpr int OFF_BW = OFF_BK + T * 4;        // fp32 [128]: v.r_w of the window
 constexpr int OFF_RED = OFF_BW + W * 4;       // fp32 [16][64] reduction scratch
-constexpr int OFF_CS = OFF_RED + 16 * T * 4;   // fp32 [64]: column sums of g over the chunks
+constexpr int OFF_CS = OFF_RED + 16 * T * 4;   // fp32 [64]: column sums of g over the rows
 // second key tile, value tile and table window: the row-chunk kernels copy
 // the next key tile in while computing on the current one
 constexpr int OFF_K1 = OFF_CS + T * 4;
@@ -436,6 +438,28 @@ __device__ __forceinline__ void grad_scores(uint8_t *sm, const BwdParams &p, con
         }
 }
 
+// g of the lane's 16 pairs for the table gradient, blocked by key tile:
+// g_all[bh][j / 64][i][j % 64] (fp32; a tile's rows are contiguous, 256 bytes
+// each).  Pairs of a visited tile are written, masked ones as zeros; entries of
+// tiles no pass visits stay unset and are never read.
+__device__ __forceinline__ void store_g(const BwdParams &p, const Lane &L, long long bh, int i0, int j0,
+                                        const float (&g)[NF][4])
+{
+    float *blk = p.g_all + (((size_t)bh * (p.Kd / T) + j0 / T) * p.L) * T;
+#pragma unroll
+    for (int hh = 0; hh < 2; ++hh) {
+        const int gi = i0 + L.rb + L.g + 8 * hh;
+        if (gi >= p.L) continue;
+#pragma unroll
+        for (int n = 0; n < NF; ++n) {
+            // an even column below K: the pair's second column is below Kd
+            const int j = L.cb + 8 * n + 2 * L.t;
+            if (j0 + j < p.K)
+                *reinterpret_cast<float2 *>(blk + (size_t)gi * T + j) = make_float2(g[n][2 * hh], g[n][2 * hh + 1]);
+        }
+    }
+}
+
 // Column sums over the lane's rows of a fragment set, reduced over the warp's
 // 16 rows; lanes with g == 0 store them at red[strip][column].
 __device__ __forceinline__ void column_sums(float *red, int stride, const Lane &L, int col0,
@@ -567,6 +591,7 @@ __global__ void __launch_bounds__(THREADS, 1) bwd_dq_kernel(const BwdParams p)
         key_tile_scores(sm, p, L, i0, j0, s, dp,
                         Bufs{OFF_Q, OFF_D, buf ? OFF_K1 : OFF_K, buf ? OFF_V1 : OFF_V, buf ? OFF_W1 : OFF_W});
         grad_scores(sm, p, L, s, dp, ls, dd, g, false, true);
+        store_g(p, L, bh, i0, j0, g);
         __syncthreads();
         const int cbo = L.cb;  // output columns: dimensions
         warp_nn2<NF>(dqc, smem_u32(sm + OFF_GH) + L.rb * LDB, smem_u32(sm + OFF_GL) + L.rb * LDB, LDB,
@@ -666,108 +691,148 @@ __global__ void __launch_bounds__(THREADS, 1) bwd_dkv_kernel(const BwdParams p)
 }
 
 // ---- the table gradient per head and 64-distance tile ---------------------------
-// Pair (row i, distance d) is key j = M + i - d.  Over the batch and the query
-// chunks: position scores q . r_d (+ v.r_d) directly; the content scores and
-// dP through the chunk's 128-key window (key jmin + w, w = i - c + 63 for the
-// tile's distance column c); then dr_d += sum_i g (q_i + v).
-__global__ void __launch_bounds__(THREADS, 1) bwd_dr_kernel(const BwdParams p)
+// Pair (row i, distance d) is key j = M + i - d; the dq passes stored g of every
+// pair they visit.  Over the batch and the query chunks that reach the tile,
+// in a fixed order: row i's 64 keys M + i - d0 - 63 .. M + i - d0 (copied in two
+// items ahead, with the chunk's q rows, through a ring of three slots, as the
+// 68-key run that starts at the 16-byte boundary below them; keys below 0 come
+// in as zeros) become a bf16 head / rest pair indexed by e = 63 - (d - d0), the
+// keys' own order; then on the tensor cores dr_e += sum_i g q_i and, through a
+// column of ones, cs_e += sum_i g, which carries the v part:
+// dr_d = sum g (q_i + v).
+constexpr int LDGF = DH + 8;   // floats per staged g row (68 used)
+constexpr int GRUN = DH + 4;   // keys staged per row
+constexpr int DR_NS = 3;                            // items in the copy ring
+constexpr int DR_GF = 0;                            // g rows [64][72] fp32, per ring slot
+constexpr int DR_Q = DR_GF + DR_NS * T * LDGF * 4;  // q rows of the chunk, per ring slot
+constexpr int DR_GH = DR_Q + DR_NS * T * LDB;       // g head, [row][e]
+constexpr int DR_GL = DR_GH + T * LDB;              // g rest
+constexpr int DR_CS = DR_GL + T * LDB;              // fp32 [64]: column sums by e
+constexpr int DR_SMEM = DR_CS + T * 4;
+static_assert(DR_Q % 16 == 0 && DR_GH % 16 == 0 && 2 * DR_SMEM <= 232448, "table-gradient tiles");
+
+// Rows i0 .. i0 + 63 of the head's g into [64][LDGF]: row gi holds the GRUN
+// keys from M + gi - d0 - 63 rounded down to a multiple of 4 (two's-complement
+// `& ~3` floors negative keys too), 16 bytes per copy (4 keys never straddle a
+// key tile); copies of keys outside [0, Kd) or rows at or past L are
+// zero-filled by a zero source size (their address kept in bounds).  Thread
+// (row w = tid / 8, runs tid % 8 + 8 m).  One commit group.
+__device__ __forceinline__ void stage_g_rows(uint8_t *dst, const BwdParams &p, long long bh, int i0, int d0)
+{
+    static_assert(THREADS == 8 * T && GRUN / 4 <= 24 && T == 64, "eight threads per staged row");
+    const int w = threadIdx.x >> 3, gi = i0 + w;
+    const int a0 = (p.M + gi - d0 - (T - 1)) & ~3;
+    const float *head = p.g_all + (size_t)bh * (p.Kd / T) * p.L * T;
+#pragma unroll
+    for (int m = 0; m < 3; ++m) {
+        const int c = (threadIdx.x & 7) + 8 * m;
+        if (c < GRUN / 4) {
+            const int a = a0 + 4 * c;
+            const bool in = gi < p.L && a >= 0 && a < p.Kd;
+            const float *g = in ? head + ((size_t)((unsigned)a >> 6) * p.L + gi) * T + (a & (T - 1)) : p.g_all;
+            asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(
+                             smem_u32(dst + w * LDGF * 4 + c * 16)),
+                         "l"(g), "r"(in ? 16 : 0)
+                         : "memory");
+        }
+    }
+    asm volatile("cp.async.commit_group;" ::: "memory");
+}
+
+// One warp, rows e = its 16 of the tile: c += (Gh + Gl)^T q over the 64 rows i
+// (G stored [i][e], q stored [i][dimension]); with_cs: cs += (Gh + Gl)^T 1,
+// whose B fragment (column 0 all ones, the others zero) lives in registers.
+__device__ __forceinline__ void dr_mma(float (&c)[NF][4], float (&cs)[4], bool with_cs, uint32_t gh,
+                                       uint32_t gl, uint32_t q, int lane)
+{
+    const uint32_t ones = (lane >> 2) == 0 ? 0x3f803f80u : 0u;  // bf16 1.0, 1.0 in column n = 0
+#pragma unroll
+    for (int k0 = 0; k0 < T; k0 += 16) {
+        uint32_t fh[4], fl[4], bfr[4];
+        const uint32_t off = (k0 + (lane >> 4) * 8 + (lane & 7)) * LDB + ((lane >> 3) & 1) * 16;
+        ldsm_x4_t(fh, gh + off);
+        ldsm_x4_t(fl, gl + off);
+        ldsm_x4_t(bfr, q + (k0 + ((lane >> 3) & 1) * 8 + (lane & 7)) * LDB + ((lane >> 4) * 8) * 2);
+        mma16816(c[0], fh, bfr[0], bfr[1]);
+        mma16816(c[1], fh, bfr[2], bfr[3]);
+        mma16816(c[0], fl, bfr[0], bfr[1]);
+        mma16816(c[1], fl, bfr[2], bfr[3]);
+        if (with_cs) {
+            mma16816(cs, fh, ones, ones);
+            mma16816(cs, fl, ones, ones);
+        }
+    }
+}
+
+__global__ void __launch_bounds__(THREADS, 2) bwd_dr_kernel(const BwdParams p)
 {
     extern __shared__ __align__(16) uint8_t sm[];
     const Lane L = lane_of();
     const int d0 = blockIdx.x * T, h = blockIdx.y;
     TXL_CHECK(h < p.H && d0 < p.r_rows, p.status);
-    float dr[NF][4];  // rows: distances; columns: dimensions
+    float dr[NF][4], cs[4];  // rows: e; columns: dimensions (cs: column 0)
     zero(dr);
-    float *cs = reinterpret_cast<float *>(sm + OFF_CS);  // sum over rows of g, per distance
+    cs[0] = cs[1] = cs[2] = cs[3] = 0.f;
+    const bool with_cs = (L.warp & 3) == 0;  // one warp per row strip sums g
     if (d0 < p.K) {
-        // the tile's table rows by distance (row c: distance d0 + c) and v.r_d
-        stage(sm + OFF_K, LDB, T, p.r + (size_t)h * p.r_rows * DH, p.r_rows - 1 - d0, -1, p.r_rows);
-        if (threadIdx.x < T) cs[threadIdx.x] = 0.f;
-        __syncthreads();
-        row_dots(reinterpret_cast<float *>(sm + OFF_BK), sm + OFF_K, LDB, T, p.vb + (size_t)h * DH);
-        const float *bk = reinterpret_cast<const float *>(sm + OFF_BK);
-        const float *xs = reinterpret_cast<const float *>(sm + OFF_XS);
-        float *red = reinterpret_cast<float *>(sm + OFF_RED);
-        // chunks with a row that sees distance d0 (M + i - d0 >= 0 for its last row);
-        // the (batch row, chunk) items double-buffered: q and dout rows, the key
-        // and value windows (buffer 1 in the regions this kernel does not use
-        // otherwise; the value window's spans both window-ordered g tiles)
-        const int i_first = max(0, d0 - p.M - (T - 1)) / T * T;
+        // the chunks with a row that reaches distance d0 (M + i >= d0)
+        const int i_first = max(0, d0 - p.M) / T * T;
         const int n_ch = (p.L - i_first + T - 1) / T, n_items = p.B * n_ch;
-        auto bufs = [](int b) {
-            return Bufs{b ? OFF_K1 : OFF_Q, b ? OFF_V1 : OFF_D, OFF_K, b ? OFF_ZH : OFF_W2,
-                        b ? OFF_W1 : OFF_W};
+        // items in order (batch row, chunk): the next one to copy in, and the
+        // current one's chunk (counters instead of divisions)
+        int nb = 0, nc = 0, cc = 0;
+        auto issue_next = [&](int slot) {
+            const long long bh = (long long)nb * p.H + h;
+            const int i0 = i_first + nc * T;
+            stage_g_rows(sm + DR_GF + slot * T * LDGF * 4, p, bh, i0, d0);
+            stage_async(sm + DR_Q + slot * T * LDB, LDB, T, p.q + bh * p.L * DH, i0, 1, p.L);
+            if (++nc == n_ch) nc = 0, ++nb;
         };
-        auto issue = [&](int it, int b) {
-            const Bufs B = bufs(b);
-            const long long bh = (long long)(it / n_ch) * p.H + h;
-            const int i0 = i_first + (it % n_ch) * T;
-            const long long jmin = (long long)p.M + i0 - d0 - (T - 1);
-            stage_async(sm + B.q, LDB, T, p.q + bh * p.L * DH, i0, 1, p.L);
-            stage_async(sm + B.d, LDB, T, p.dout + bh * p.L * DH, i0, 1, p.L);
-            stage_async(sm + B.w, LDB, W, p.k + bh * p.K * DH, jmin, 1, p.K);
-            stage_async(sm + B.v, LDB, W, p.v + bh * p.K * DH, jmin, 1, p.K);
-        };
-        issue(0, 0);
-        for (int it = 0, buf = 0; it < n_items; ++it, buf ^= 1) {
-            const long long bh = (long long)(it / n_ch) * p.H + h;
-            const int i0 = i_first + (it % n_ch) * T;
-            __syncthreads();  // the other buffer's last readers are done
-            const bool more = it + 1 < n_items;
-            if (more) issue(it + 1, buf ^ 1);
-            if (more) async_wait<4>();
+        // this thread's conversion: row i, keys e = 8 r .. 8 r + 7 of the tile
+        const int ci = threadIdx.x >> 3, cr = threadIdx.x & 7;
+        issue_next(0);
+        if (n_items > 1) issue_next(1);
+        for (int it = 0, buf = 0; it < n_items; ++it, buf = (buf + 1 == DR_NS) ? 0 : buf + 1) {
+            const int i0 = i_first + cc * T;
+            if (++cc == n_ch) cc = 0;
+            // two copy groups per item: this item's have landed once at most the
+            // next item's are pending; the barrier also ends the last item's
+            // readers of the g tiles and of the slot refilled below
+            if (it + 1 < n_items) async_wait<2>();
             else async_wait<0>();
             __syncthreads();
-            const Bufs B = bufs(buf);
-            row_dots(reinterpret_cast<float *>(sm + OFF_BW), sm + B.w, LDB, W, p.u + (size_t)h * DH);
+            if (it + 2 < n_items) issue_next(buf + 2 >= DR_NS ? buf + 2 - DR_NS : buf + 2);
+            {
+                // key M + gi - d0 - 63 + e sits at staged column ((M + gi - d0 - 63) & 3) + e
+                const float *src = reinterpret_cast<const float *>(sm + DR_GF + buf * T * LDGF * 4) +
+                                   ci * LDGF + ((p.M + i0 + ci - d0 - (T - 1)) & 3) + 8 * cr;
+                uint4 hd, rs;
+                split2(src[0], src[1], hd.x, rs.x);
+                split2(src[2], src[3], hd.y, rs.y);
+                split2(src[4], src[5], hd.z, rs.z);
+                split2(src[6], src[7], hd.w, rs.w);
+                *reinterpret_cast<uint4 *>(sm + DR_GH + ci * LDB + 16 * cr) = hd;
+                *reinterpret_cast<uint4 *>(sm + DR_GL + ci * LDB + 16 * cr) = rs;
+            }
             __syncthreads();
-            float ls[2], dd[2];
-            load_row_stats(p, L, bh, i0, ls, dd);
-            float sp[NF][4], sc[NF][4], dp[NF][4], s[NF][4], g[NF][4];
-            zero(sp);
-            warp_nt<NF>(sp, smem_u32(sm + B.q) + L.rb * LDB, LDB, smem_u32(sm + OFF_K) + L.cb * LDB,
-                       LDB, DH, L.lane);
-            window_product(sm, L, B.q, B.w, reinterpret_cast<const float *>(sm + OFF_BW));
-            __syncthreads();
-#pragma unroll
-            for (int n = 0; n < NF; ++n)
-#pragma unroll
-                for (int q = 0; q < 4; ++q) {
-                    const int i = L.rb + L.g + 8 * (q >> 1), c = L.cb + 8 * n + 2 * L.t + (q & 1);
-                    sc[n][q] = xs[i * LDX + i - c + T - 1];
-                }
-            __syncthreads();
-            window_product(sm, L, B.d, B.v, nullptr);
-            __syncthreads();
-#pragma unroll
-            for (int n = 0; n < NF; ++n)
-#pragma unroll
-                for (int q = 0; q < 4; ++q) {
-                    const int i = L.rb + L.g + 8 * (q >> 1), c = L.cb + 8 * n + 2 * L.t + (q & 1);
-                    dp[n][q] = xs[i * LDX + i - c + T - 1];
-                    const int gi = i0 + i, d = d0 + c;
-                    const int gj = p.M + gi - d;
-                    const bool keep = gi < p.L && d < p.K && gj >= 0 && gj < p.K;
-                    s[n][q] = keep ? (sc[n][q] + sp[n][q] + bk[c]) * p.scale_log2 : -INFINITY;
-                }
-            grad_scores(sm, p, L, s, dp, ls, dd, g, false);
-            column_sums(red, T, L, L.cb, g);
-            __syncthreads();
-            if (threadIdx.x < T)
-                cs[threadIdx.x] += ((red[threadIdx.x] + red[T + threadIdx.x]) +
-                                    red[2 * T + threadIdx.x]) + red[3 * T + threadIdx.x];
-            warp_nn2<NF>(dr, smem_u32(sm + OFF_GH) + L.rb * 2, smem_u32(sm + OFF_GL) + L.rb * 2,
-                        LDB, true, smem_u32(sm + B.q) + L.cb * 2, LDB, T, L.lane);
+            dr_mma(dr, cs, with_cs, smem_u32(sm + DR_GH) + L.rb * 2, smem_u32(sm + DR_GL) + L.rb * 2,
+                   smem_u32(sm + DR_Q + buf * T * LDB) + L.cb * 2, L.lane);
         }
-        __syncthreads();
     }
+    // the column sums of each row strip, from its first warp's column 0
+    float *csm = reinterpret_cast<float *>(sm + DR_CS);
+    if (with_cs && L.t == 0) {
+        csm[L.rb + L.g] = cs[0];
+        csm[L.rb + L.g + 8] = cs[2];
+    }
+    __syncthreads();
     const __nv_bfloat16 *vb = p.vb + (size_t)h * DH;
 #pragma unroll
     for (int hh = 0; hh < 2; ++hh) {
-        const int c = L.rb + L.g + 8 * hh, d = d0 + c;
+        const int e = L.rb + L.g + 8 * hh, d = d0 + (T - 1) - e;
         if (d < p.r_rows) {
             float *dst = p.dr + ((size_t)h * p.r_rows + (p.r_rows - 1 - d)) * DH;
-            const float cd = (d < p.K) ? cs[c] : 0.f;
+            const float cd = (d < p.K) ? csm[e] : 0.f;
 #pragma unroll
             for (int n = 0; n < NF; ++n) {
                 const int col = L.cb + 8 * n + 2 * L.t;
@@ -874,6 +939,7 @@ __global__ void __launch_bounds__(THREADS, 1) bwd_dqkv_kernel(const BwdParams p,
             float s[NF][4], dp[NF][4], g[NF][4];
             key_tile_scores(sm, p, L, c * T, j0, s, dp, B);
             grad_scores(sm, p, L, s, dp, ls[c], dd[c], g, true, true);
+            store_g(p, L, bh, c * T, j0, g);
             column_sums(red, T, L, L.cb, g);
             __syncthreads();
             if (threadIdx.x < T)
@@ -962,23 +1028,29 @@ size_t align256(size_t x) { return (x + 255) & ~(size_t)255; }
 
 } // namespace
 
-size_t bwd_workspace_bytes(int B, int H, int L)
-{
-    if (B <= 0 || H <= 0 || L <= 0) return 0;
-    const size_t rows = (size_t)B * H * L;
-    const int n_chunks = (L + T - 1) / T;
-    const size_t parts = (size_t)B * H * (size_t)(n_chunks > kBwdMaxSplits ? n_chunks : kBwdMaxSplits);
-    size_t bytes = 2 * align256(rows * sizeof(float)) + align256(parts * 2 * DH * sizeof(float));
-    if (n_chunks <= 2) bytes += align256((size_t)kBwdMaxSplits * rows * DH * sizeof(float));
-    return bytes;
-}
-
 size_t bwd_dq_part_offset(int B, int H, int L)
 {
     const size_t rows = (size_t)B * H * L;
     const int n_chunks = (L + T - 1) / T;
     const size_t parts = (size_t)B * H * (size_t)(n_chunks > kBwdMaxSplits ? n_chunks : kBwdMaxSplits);
     return 2 * align256(rows * sizeof(float)) + align256(parts * 2 * DH * sizeof(float));
+}
+
+size_t bwd_g_offset(int B, int H, int L)
+{
+    const size_t rows = (size_t)B * H * L;
+    const int n_chunks = (L + T - 1) / T;
+    size_t off = bwd_dq_part_offset(B, H, L);
+    if (n_chunks <= 2) off += align256((size_t)kBwdMaxSplits * rows * DH * sizeof(float));
+    return off;
+}
+
+size_t bwd_workspace_bytes(int B, int H, int L, int M)
+{
+    if (B <= 0 || H <= 0 || L <= 0 || M < 0) return 0;
+    const size_t rows = (size_t)B * H * L;
+    const size_t Kd = ((size_t)M + L + T - 1) / T * T;
+    return bwd_g_offset(B, H, L) + align256(rows * Kd * sizeof(float));
 }
 
 cudaError_t launch_relattn_bwd(const BwdParams &p, cudaStream_t s)
@@ -989,11 +1061,13 @@ cudaError_t launch_relattn_bwd(const BwdParams &p, cudaStream_t s)
     if (e != cudaSuccess) return e;
     if (dev < 0 || dev >= 64 || !attr_set[dev]) {
         for (const void *f : {(const void *)bwd_stats_kernel, (const void *)bwd_dq_kernel,
-                              (const void *)bwd_dkv_kernel, (const void *)bwd_dr_kernel,
-                              (const void *)bwd_dqkv_kernel})
+                              (const void *)bwd_dkv_kernel, (const void *)bwd_dqkv_kernel})
             if ((e = cudaFuncSetAttribute(f, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                           SMEM_BYTES)) != cudaSuccess)
                 return e;
+        if ((e = cudaFuncSetAttribute((const void *)bwd_dr_kernel,
+                                      cudaFuncAttributeMaxDynamicSharedMemorySize, DR_SMEM)) != cudaSuccess)
+            return e;
         if (dev >= 0 && dev < 64) attr_set[dev] = true;
     }
     const long long BH = (long long)p.B * p.H;
@@ -1023,7 +1097,7 @@ cudaError_t launch_relattn_bwd(const BwdParams &p, cudaStream_t s)
         bwd_dq_kernel<<<dim3((unsigned)BH, n_chunks), THREADS, SMEM_BYTES, s>>>(p);
         bwd_dkv_kernel<<<dim3((unsigned)BH, n_keys), THREADS, SMEM_BYTES, s>>>(p);
     }
-    bwd_dr_kernel<<<dim3((unsigned)n_dist, p.H), THREADS, SMEM_BYTES, s>>>(p);
+    bwd_dr_kernel<<<dim3((unsigned)n_dist, p.H), THREADS, DR_SMEM, s>>>(p);
     bwd_bias_kernel<<<p.H, 2 * DH, 0, s>>>(p, n_bias);
     return cudaGetLastError();
 }

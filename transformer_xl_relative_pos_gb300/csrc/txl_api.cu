@@ -774,9 +774,9 @@ int txl_debug_wait_timeout(uint64_t ns, void *stream)
 // ---------------------------------------------------------------------------
 // Backward of the attention (one segment, §3.2: the memory is SG(m)).
 // ---------------------------------------------------------------------------
-extern "C" size_t txl_relattn_bwd_workspace_size(int B, int H, int L)
+extern "C" size_t txl_relattn_bwd_workspace_size(int B, int H, int L, int M)
 {
-    return txl::bwd_workspace_bytes(B, H, L);
+    return txl::bwd_workspace_bytes(B, H, L, M);
 }
 
 extern "C" int txl_relattn_bwd(const void *q, const void *k, const void *v, const void *r,
@@ -803,7 +803,7 @@ extern "C" int txl_relattn_bwd(const void *q, const void *k, const void *v, cons
     if (BH > 0x7fffffffLL || (L + rows - 1) / rows > 65535 || (K + rows - 1) / rows > 65535 ||
         H > 65535)
         return TXL_ERR_UNSUPPORTED;
-    const size_t need = txl::bwd_workspace_bytes(B, H, L);
+    const size_t need = txl::bwd_workspace_bytes(B, H, L, M);
     if (!workspace || workspace_bytes < need) return TXL_ERR_WORKSPACE;
     if (!aligned(workspace, 256)) return TXL_ERR_MISALIGNED;
 
@@ -824,14 +824,17 @@ extern "C" int txl_relattn_bwd(const void *q, const void *k, const void *v, cons
     p.dr = dr;
     p.du = du;
     p.dvb = dv_bias;
-    // workspace: log2-sum-exp and D per row, then the bias partials (256-byte
-    // aligned regions, as txl::bwd_workspace_bytes counts them)
+    // workspace: log2-sum-exp and D per row, the bias partials, the dq
+    // partials of the key splits, g of every pair (256-byte aligned regions, as
+    // txl::bwd_workspace_bytes counts them)
     const size_t row_bytes = ((size_t)BH * L * sizeof(float) + 255) & ~(size_t)255;
     char *ws = static_cast<char *>(workspace);
     p.lse2 = reinterpret_cast<float *>(ws);
     p.dsum = reinterpret_cast<float *>(ws + row_bytes);
     p.part = reinterpret_cast<float *>(ws + 2 * row_bytes);
     p.dq_part = reinterpret_cast<float *>(ws + txl::bwd_dq_part_offset(B, H, L));
+    p.g_all = reinterpret_cast<float *>(ws + txl::bwd_g_offset(B, H, L));
+    p.Kd = (int)((K + rows - 1) / rows * rows);
     p.B = B;
     p.H = H;
     p.M = M;
