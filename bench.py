@@ -1032,6 +1032,21 @@ def run_bwd(args):
     us = e0.elapsed_time(e1) * 1e3 / (per * max(1, args.calls))
     visits = bwd_tile_visits(B, H, L, M)
     T = 64
+    # launches per call: segments of at most two row chunks take the two-chunk
+    # statistics and one-pass dq/dk/dv kernels over key splits (the count that
+    # fills the SMs' waves best, at most 4), each followed by an ordered merge
+    # when split; longer ones the per-chunk statistics, dq and dk/dv kernels;
+    # then the table gradient and the bias sums
+    if -(-L // T) <= 2:
+        sms = torch.cuda.get_device_properties(dev).multi_processor_count
+        n_splits, best = 1, 0.0
+        for sp in range(1, min(4, -(-K // T)) + 1):
+            eff = B * H * sp / (math.ceil(B * H * sp / sms) * sms)
+            if eff > best + 0.02:
+                best, n_splits = eff, sp
+        launches = 4 + (2 if n_splits > 1 else 0)
+    else:
+        launches = 5
     # tile multiply-adds: stats q.k, dout.v (64^3 each), the q.r window (2 x 64^3);
     # dq adds g.k and the window-ordered g.r (head and rest: 2 x 3 x 64^3);
     # dk/dv add P^T dout and g^T q (2 x 2 x 64^3); the one-pass dq / dk / dv
@@ -1050,7 +1065,7 @@ def run_bwd(args):
         "tensor_frac": round(executed / (us * 1e-6) / 1e12 / pk["bf16_tflops"], 4),
         "useful_gflop": round(useful / 1e9, 1),
         "useful_tflops": round(useful / (us * 1e-6) / 1e12, 2),
-        "tile_visits": visits, "launches": 5,
+        "tile_visits": visits, "launches": launches,
         # g of every pair, fp32: written by the dq pass, read by the table gradient
         "g_stored_mb": round(B * H * L * K * 4 / 1e6, 1)}}), flush=True)
 

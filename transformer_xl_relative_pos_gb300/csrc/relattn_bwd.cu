@@ -477,6 +477,60 @@ __device__ __forceinline__ void column_sums(float *red, int stride, const Lane &
         }
 }
 
+// The online state of the lane's two rows over its column group (m: running
+// max of the log2 scores, l: sum of 2^(s - m), w: sum of 2^(s - m) dP),
+// updated with a key tile's scores and dP.
+__device__ __forceinline__ void online_update(const float (&s)[NF][4], const float (&dp)[NF][4], float (&m)[2],
+                                              float (&l)[2], float (&wsum)[2])
+{
+#pragma unroll
+    for (int hh = 0; hh < 2; ++hh) {
+        float tmax = -INFINITY;
+#pragma unroll
+        for (int n = 0; n < NF; ++n) tmax = fmaxf(tmax, fmaxf(s[n][2 * hh], s[n][2 * hh + 1]));
+        tmax = fmaxf(tmax, __shfl_xor_sync(0xffffffffu, tmax, 1));
+        tmax = fmaxf(tmax, __shfl_xor_sync(0xffffffffu, tmax, 2));
+        const float mn = fmaxf(m[hh], tmax);
+        float e = 0.f, ed = 0.f;
+#pragma unroll
+        for (int n = 0; n < NF; ++n)
+#pragma unroll
+            for (int x = 0; x < 2; ++x) {
+                const float sv = s[n][2 * hh + x];
+                const float ev = (sv == -INFINITY) ? 0.f : exp2f(sv - mn);
+                e += ev;
+                ed = fmaf(ev, dp[n][2 * hh + x], ed);
+            }
+        e += __shfl_xor_sync(0xffffffffu, e, 1);
+        e += __shfl_xor_sync(0xffffffffu, e, 2);
+        ed += __shfl_xor_sync(0xffffffffu, ed, 1);
+        ed += __shfl_xor_sync(0xffffffffu, ed, 2);
+        if (mn != -INFINITY) {
+            const float alpha = (m[hh] == -INFINITY) ? 0.f : exp2f(m[hh] - mn);
+            l[hh] = fmaf(l[hh], alpha, e);
+            wsum[hh] = fmaf(wsum[hh], alpha, ed);
+            m[hh] = mn;
+        }
+    }
+}
+
+// States (m, l, w) of n parts of a row, `stride` floats apart, combined in
+// order: the row's max, and l and w rescaled to it.
+__device__ __forceinline__ void combine_states(const float *a, int n, size_t stride, float &mx, float &lt,
+                                               float &wt)
+{
+    mx = -INFINITY;
+    for (int c = 0; c < n; ++c) mx = fmaxf(mx, a[c * stride]);
+    lt = 0.f;
+    wt = 0.f;
+    for (int c = 0; c < n; ++c) {
+        const float *x = a + c * stride;
+        const float sa = (x[0] == -INFINITY) ? 0.f : exp2f(x[0] - mx);
+        lt = fmaf(x[1], sa, lt);
+        wt = fmaf(x[2], sa, wt);
+    }
+}
+
 // ---- stats: log2-sum-exp and D per query row --------------------------------
 __global__ void __launch_bounds__(THREADS, 1) bwd_stats_kernel(const BwdParams p)
 {
@@ -498,35 +552,7 @@ __global__ void __launch_bounds__(THREADS, 1) bwd_stats_kernel(const BwdParams p
         float s[NF][4], dp[NF][4];
         key_tile_scores(sm, p, L, i0, j0, s, dp,
                         Bufs{OFF_Q, OFF_D, buf ? OFF_K1 : OFF_K, buf ? OFF_V1 : OFF_V, buf ? OFF_W1 : OFF_W});
-#pragma unroll
-        for (int hh = 0; hh < 2; ++hh) {
-            float tmax = -INFINITY;
-#pragma unroll
-            for (int n = 0; n < NF; ++n) tmax = fmaxf(tmax, fmaxf(s[n][2 * hh], s[n][2 * hh + 1]));
-            tmax = fmaxf(tmax, __shfl_xor_sync(0xffffffffu, tmax, 1));
-            tmax = fmaxf(tmax, __shfl_xor_sync(0xffffffffu, tmax, 2));
-            const float mn = fmaxf(m[hh], tmax);
-            float e = 0.f, ed = 0.f;
-#pragma unroll
-            for (int n = 0; n < NF; ++n)
-#pragma unroll
-                for (int x = 0; x < 2; ++x) {
-                    const float sv = s[n][2 * hh + x];
-                    const float ev = (sv == -INFINITY) ? 0.f : exp2f(sv - mn);
-                    e += ev;
-                    ed = fmaf(ev, dp[n][2 * hh + x], ed);
-                }
-            e += __shfl_xor_sync(0xffffffffu, e, 1);
-            e += __shfl_xor_sync(0xffffffffu, e, 2);
-            ed += __shfl_xor_sync(0xffffffffu, ed, 1);
-            ed += __shfl_xor_sync(0xffffffffu, ed, 2);
-            if (mn != -INFINITY) {
-                const float alpha = (m[hh] == -INFINITY) ? 0.f : exp2f(m[hh] - mn);
-                l[hh] = fmaf(l[hh], alpha, e);
-                wsum[hh] = fmaf(wsum[hh], alpha, ed);
-                m[hh] = mn;
-            }
-        }
+        online_update(s, dp, m, l, wsum);
     }
     // the four column groups of each row: red[group][row][m, l, w]
     float *red = reinterpret_cast<float *>(sm + OFF_RED);
@@ -543,16 +569,9 @@ __global__ void __launch_bounds__(THREADS, 1) bwd_stats_kernel(const BwdParams p
     __syncthreads();
     if (threadIdx.x < T) {
         const int i = threadIdx.x, gi = i0 + i;
-        float mx = -INFINITY;
-        for (int c = 0; c < 4; ++c) mx = fmaxf(mx, red[(c * T + i) * 3]);
+        float mx, lt, wt;
+        combine_states(red + i * 3, 4, T * 3, mx, lt, wt);
         if (gi < p.L && mx != -INFINITY) {
-            float lt = 0.f, wt = 0.f;
-            for (int c = 0; c < 4; ++c) {
-                const float *a = red + (c * T + i) * 3;
-                const float sa = (a[0] == -INFINITY) ? 0.f : exp2f(a[0] - mx);
-                lt = fmaf(a[1], sa, lt);
-                wt = fmaf(a[2], sa, wt);
-            }
             p.lse2[bh * p.L + gi] = mx + log2f(lt);
             p.dsum[bh * p.L + gi] = wt / lt;
         }
@@ -1007,6 +1026,117 @@ __global__ void __launch_bounds__(THREADS, 1) bwd_dqkv_kernel(const BwdParams p,
     }
 }
 
+// ---- stats for segments of at most two row chunks ------------------------------
+// Block (b*H + h, key split), staged as the one-pass kernel: both chunks' q and
+// dout rows, the split's key tiles (keys and values copied in one tile ahead,
+// the 192-row table window of both chunks at the tile's start), so each key,
+// value and table tile is read once per segment.  Every row's online state over
+// the split's keys; with one split that is the row's log2-sum-exp and D, with
+// more the states go to `scratch` [split][row][m, l, w] for
+// bwd_stats_merge_kernel.
+__global__ void __launch_bounds__(THREADS, 1) bwd_stats2_kernel(const BwdParams p, int n_splits, float *scratch)
+{
+    extern __shared__ __align__(16) uint8_t sm[];
+    const Lane L = lane_of();
+    const long long bh = blockIdx.x;
+    const int h = (int)(bh % p.H), split = blockIdx.y;
+    const int n_ch = (p.L + T - 1) / T;
+    const int n_kt = (p.K + T - 1) / T;
+    const int per = (n_kt + n_splits - 1) / n_splits;
+    const int kt0 = split * per, kt1 = min(n_kt, kt0 + per);
+    TXL_CHECK(bh < (long long)p.B * p.H && n_ch <= 2 && split < n_splits, p.status);
+    auto ko = [](int b) { return b ? OFF_K1 : OFF_K; };
+    auto vo = [](int b) { return b ? OFF_V1 : OFF_V; };
+    stage(sm + OFF_Q, LDB, T, p.q + bh * p.L * DH, 0, 1, p.L);
+    stage(sm + OFF_D, LDB, T, p.dout + bh * p.L * DH, 0, 1, p.L);
+    stage(sm + Q_ROWS1, LDB, T, p.q + bh * p.L * DH, T, 1, p.L);
+    stage(sm + D_ROWS1, LDB, T, p.dout + bh * p.L * DH, T, 1, p.L);
+    float m[2][2], l[2][2], wsum[2][2];  // [chunk][lane row]
+#pragma unroll
+    for (int c = 0; c < 2; ++c)
+#pragma unroll
+        for (int hh = 0; hh < 2; ++hh) m[c][hh] = -INFINITY, l[c][hh] = 0.f, wsum[c][hh] = 0.f;
+    auto issue_kv = [&](int kt, int b) {
+        stage_async(sm + ko(b), LDB, T, p.k + bh * p.K * DH, (long long)kt * T, 1, p.K);
+        stage_async(sm + vo(b), LDB, T, p.v + bh * p.K * DH, (long long)kt * T, 1, p.K);
+    };
+    if (kt0 < kt1) issue_kv(kt0, 0);
+    for (int kt = kt0, buf = 0; kt < kt1; ++kt, buf ^= 1) {
+        const int j0 = kt * T;
+        __syncthreads();  // the last tile's readers of the window and of this buffer pair are done
+        // window row w: the table row of distance M - j0 - 63 + w (w < 192)
+        const long long dmin = (long long)p.M - j0 - (T - 1);
+        stage_async(sm + OFF_W, LDB, W + T, p.r + (size_t)h * p.r_rows * DH, p.r_rows - 1 - dmin, -1,
+                    p.r_rows);
+        const bool more = kt + 1 < kt1;
+        if (more) issue_kv(kt + 1, buf ^ 1);
+        if (more) async_wait<2>();
+        else async_wait<0>();
+        __syncthreads();
+        row_dots(reinterpret_cast<float *>(sm + OFF_BK), sm + ko(buf), LDB, T, p.u + (size_t)h * DH);
+        row_dots(reinterpret_cast<float *>(sm + WBW2), sm + OFF_W, LDB, W + T, p.vb + (size_t)h * DH);
+        __syncthreads();
+#pragma unroll
+        for (int c = 0; c < 2; ++c) {
+            if (c >= n_ch) break;                    // (block-uniform)
+            if (j0 > p.M + c * T + T - 1) continue;  // the tile is hidden from every row of the chunk
+            if (c == 1) __syncthreads();             // chunk 0's readers of the window product are done
+            const Bufs B{c ? Q_ROWS1 : OFF_Q, c ? D_ROWS1 : OFF_D, ko(buf), vo(buf), OFF_W + c * T * LDB,
+                         WBW2 + c * T * 4};
+            float s[NF][4], dp[NF][4];
+            key_tile_scores(sm, p, L, c * T, j0, s, dp, B);
+            online_update(s, dp, m[c], l[c], wsum[c]);
+        }
+    }
+    // the four column groups of each row: red[group][row][m, l, w] over the
+    // 128 rows (in the window-product region, free now)
+    float *red = reinterpret_cast<float *>(sm + OFF_XS);
+    static_assert(4 * 2 * T * 3 <= T * LDX, "row states must fit the window-product region");
+    __syncthreads();
+    if (L.t == 0) {
+#pragma unroll
+        for (int c = 0; c < 2; ++c)
+#pragma unroll
+            for (int hh = 0; hh < 2; ++hh) {
+                float *d = red + ((L.warp & 3) * 2 * T + c * T + L.rb + L.g + 8 * hh) * 3;
+                d[0] = m[c][hh];
+                d[1] = l[c][hh];
+                d[2] = wsum[c][hh];
+            }
+    }
+    __syncthreads();
+    if (threadIdx.x < 2 * T) {
+        const int gi = threadIdx.x;
+        float mx, lt, wt;
+        combine_states(red + gi * 3, 4, 2 * T * 3, mx, lt, wt);
+        if (gi < p.L) {
+            const size_t row = (size_t)bh * p.L + gi;
+            if (n_splits == 1) {
+                // one split holds every key, key 0 among them: the row has one
+                p.lse2[row] = mx + log2f(lt);
+                p.dsum[row] = wt / lt;
+            } else {
+                float *o = scratch + ((size_t)split * p.B * p.H * p.L + row) * 3;
+                o[0] = mx;
+                o[1] = lt;
+                o[2] = wt;
+            }
+        }
+    }
+}
+
+// The key splits' row states combined in split order.
+__global__ void bwd_stats_merge_kernel(const BwdParams p, int n_splits, const float *scratch)
+{
+    const size_t rows = (size_t)p.B * p.H * p.L;
+    for (size_t r = (size_t)blockIdx.x * blockDim.x + threadIdx.x; r < rows; r += (size_t)gridDim.x * blockDim.x) {
+        float mx, lt, wt;
+        combine_states(scratch + r * 3, n_splits, rows * 3, mx, lt, wt);
+        p.lse2[r] = mx + log2f(lt);
+        p.dsum[r] = wt / lt;
+    }
+}
+
 // dq = the key splits' partials summed in order.
 __global__ void bwd_dq_reduce_kernel(const BwdParams p, int n_splits)
 {
@@ -1060,8 +1190,9 @@ cudaError_t launch_relattn_bwd(const BwdParams &p, cudaStream_t s)
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return e;
     if (dev < 0 || dev >= 64 || !attr_set[dev]) {
-        for (const void *f : {(const void *)bwd_stats_kernel, (const void *)bwd_dq_kernel,
-                              (const void *)bwd_dkv_kernel, (const void *)bwd_dqkv_kernel})
+        for (const void *f : {(const void *)bwd_stats_kernel, (const void *)bwd_stats2_kernel,
+                              (const void *)bwd_dq_kernel, (const void *)bwd_dkv_kernel,
+                              (const void *)bwd_dqkv_kernel})
             if ((e = cudaFuncSetAttribute(f, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                           SMEM_BYTES)) != cudaSuccess)
                 return e;
@@ -1075,10 +1206,10 @@ cudaError_t launch_relattn_bwd(const BwdParams &p, cudaStream_t s)
     const int n_dist = (p.r_rows + T - 1) / T;
     if (BH > 0x7fffffffLL || n_chunks > 65535 || n_keys > 65535 || p.H > 65535)
         return cudaErrorInvalidValue;
-    bwd_stats_kernel<<<dim3((unsigned)BH, n_chunks), THREADS, SMEM_BYTES, s>>>(p);
     int n_bias = n_chunks;
     if (n_chunks <= 2) {
-        // one pass for dq, dk, dv; the key split that fills the SMs' waves best
+        // one pass for the statistics and one for dq, dk, dv over both chunks;
+        // the key split that fills the SMs' waves best
         int sms = 0;
         if ((e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess)
             return e;
@@ -1090,10 +1221,14 @@ cudaError_t launch_relattn_bwd(const BwdParams &p, cudaStream_t s)
             const double eff = blocks / (waves * sms);
             if (eff > best + 0.02) best = eff, n_splits = sp;
         }
+        // the splits' row states go to the dq partials' region, free until the one-pass kernel
+        bwd_stats2_kernel<<<dim3((unsigned)BH, n_splits), THREADS, SMEM_BYTES, s>>>(p, n_splits, p.dq_part);
+        if (n_splits > 1) bwd_stats_merge_kernel<<<256, 256, 0, s>>>(p, n_splits, p.dq_part);
         bwd_dqkv_kernel<<<dim3((unsigned)BH, n_splits), THREADS, SMEM_BYTES, s>>>(p, n_splits);
         if (n_splits > 1) bwd_dq_reduce_kernel<<<1024, 256, 0, s>>>(p, n_splits);
         n_bias = n_splits;
     } else {
+        bwd_stats_kernel<<<dim3((unsigned)BH, n_chunks), THREADS, SMEM_BYTES, s>>>(p);
         bwd_dq_kernel<<<dim3((unsigned)BH, n_chunks), THREADS, SMEM_BYTES, s>>>(p);
         bwd_dkv_kernel<<<dim3((unsigned)BH, n_keys), THREADS, SMEM_BYTES, s>>>(p);
     }
