@@ -79,6 +79,7 @@ constexpr int OFF_K1 = OFF_CS + T * 4;
 constexpr int OFF_V1 = OFF_K1 + T * LDB;
 constexpr int OFF_W1 = OFF_V1 + T * LDB;
 constexpr int SMEM_BYTES = OFF_W1 + W * LDB;
+static_assert(OFF_XS - OFF_ZH == T * LDX * 4, "the window-ordered g region holds a second window product");
 static_assert(SMEM_BYTES <= 232448, "shared memory budget exceeded");
 static_assert(OFF_W % 16 == 0 && OFF_GH % 16 == 0 && OFF_ZH % 16 == 0 && OFF_XS % 16 == 0 &&
                   OFF_K1 % 16 == 0 && OFF_W1 % 16 == 0,
@@ -274,15 +275,15 @@ __device__ __forceinline__ Lane lane_of()
 }
 
 // The 64 x 128 window product of the warp's rows, plus a per-column vector,
-// into the fp32 window buffer (columns 32 (w%4) .. +31).
+// into an fp32 window buffer (columns 32 (w%4) .. +31).
 __device__ __forceinline__ void window_product(uint8_t *sm, const Lane &L, int a_off, int b_off,
-                                               const float *colvec)
+                                               const float *colvec, int xs_off = OFF_XS)
 {
     float x[NWF][4];
     zero(x);
     warp_nt<NWF>(x, smem_u32(sm + a_off) + L.rb * LDB, LDB,
                smem_u32(sm + b_off) + 32 * (L.warp & 3) * LDB, LDB, DH, L.lane);
-    float *xs = reinterpret_cast<float *>(sm + OFF_XS);
+    float *xs = reinterpret_cast<float *>(sm + xs_off);
 #pragma unroll
     for (int n = 0; n < NWF; ++n)
 #pragma unroll
@@ -301,6 +302,28 @@ struct Bufs {
     int bw = OFF_BW;  // the window's v.r vector (fp32)
 };
 
+// The lane's 16 log2-scaled scores (-inf where masked) of the pair tile at
+// (i0, j0) from its content part sc, the column vector u.k_j and the window
+// product in the buffer at xs_off (complete: after a barrier).
+__device__ __forceinline__ void finish_scores(const uint8_t *sm, const BwdParams &p, const Lane &L, int i0,
+                                              int j0, const float (&sc)[NF][4], float (&s)[NF][4],
+                                              int xs_off)
+{
+    const float *bk = reinterpret_cast<const float *>(sm + OFF_BK);
+    const float *xs = reinterpret_cast<const float *>(sm + xs_off);
+#pragma unroll
+    for (int n = 0; n < NF; ++n)
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+            const int i = L.rb + L.g + 8 * (q >> 1), j = L.cb + 8 * n + 2 * L.t + (q & 1);
+            const int gi = i0 + i, gj = j0 + j;
+            // Appendix B: distance M + gi - gj is window column i - j + 63
+            const float pos = xs[i * LDX + i - j + T - 1];
+            const bool keep = gi < p.L && gj < p.K && gj <= p.M + gi;
+            s[n][q] = keep ? (sc[n][q] + bk[j] + pos) * p.scale_log2 : -INFINITY;
+        }
+}
+
 // Log2-scaled scores (-inf where masked) and dP = dout . v of the lane's 16
 // pairs of the key tile at j0, from the staged q, dout, keys, values, table
 // window (distances M + i0 - j0 - 63 + w) and bias vectors (u.k_j, v.r_w).
@@ -316,21 +339,9 @@ __device__ __forceinline__ void key_tile_scores(uint8_t *sm, const BwdParams &p,
                DH, L.lane);
     warp_nt<NF>(dp, smem_u32(sm + B.d) + L.rb * LDB, LDB, smem_u32(sm + B.v) + L.cb * LDB, LDB,
                DH, L.lane);
-    const float *bk = reinterpret_cast<const float *>(sm + OFF_BK);
     window_product(sm, L, B.q, B.w, reinterpret_cast<const float *>(sm + B.bw));
     __syncthreads();
-    const float *xs = reinterpret_cast<const float *>(sm + OFF_XS);
-#pragma unroll
-    for (int n = 0; n < NF; ++n)
-#pragma unroll
-        for (int q = 0; q < 4; ++q) {
-            const int i = L.rb + L.g + 8 * (q >> 1), j = L.cb + 8 * n + 2 * L.t + (q & 1);
-            const int gi = i0 + i, gj = j0 + j;
-            // Appendix B: distance M + gi - gj is window column i - j + 63
-            const float pos = xs[i * LDX + i - j + T - 1];
-            const bool keep = gi < p.L && gj < p.K && gj <= p.M + gi;
-            s[n][q] = keep ? (sc[n][q] + bk[j] + pos) * p.scale_log2 : -INFINITY;
-        }
+    finish_scores(sm, p, L, i0, j0, sc, s, OFF_XS);
 }
 
 __device__ __forceinline__ void stage_rows(uint8_t *sm, const BwdParams &p, long long bh, int i0)
@@ -1076,16 +1087,40 @@ __global__ void __launch_bounds__(THREADS, 1) bwd_stats2_kernel(const BwdParams 
         row_dots(reinterpret_cast<float *>(sm + OFF_BK), sm + ko(buf), LDB, T, p.u + (size_t)h * DH);
         row_dots(reinterpret_cast<float *>(sm + WBW2), sm + OFF_W, LDB, W + T, p.vb + (size_t)h * DH);
         __syncthreads();
+        if (n_ch == 2 && j0 <= p.M + T - 1) {
+            // both chunks see the tile: their products back to back, chunk 1's
+            // window product in the window-ordered g region (unused here), one barrier
+            float sc[2][NF][4], dp[2][NF][4];
 #pragma unroll
-        for (int c = 0; c < 2; ++c) {
-            if (c >= n_ch) break;                    // (block-uniform)
-            if (j0 > p.M + c * T + T - 1) continue;  // the tile is hidden from every row of the chunk
-            if (c == 1) __syncthreads();             // chunk 0's readers of the window product are done
-            const Bufs B{c ? Q_ROWS1 : OFF_Q, c ? D_ROWS1 : OFF_D, ko(buf), vo(buf), OFF_W + c * T * LDB,
-                         WBW2 + c * T * 4};
-            float s[NF][4], dp[NF][4];
-            key_tile_scores(sm, p, L, c * T, j0, s, dp, B);
-            online_update(s, dp, m[c], l[c], wsum[c]);
+            for (int c = 0; c < 2; ++c) {
+                zero(sc[c]);
+                zero(dp[c]);
+                warp_nt<NF>(sc[c], smem_u32(sm + (c ? Q_ROWS1 : OFF_Q)) + L.rb * LDB, LDB,
+                            smem_u32(sm + ko(buf)) + L.cb * LDB, LDB, DH, L.lane);
+                warp_nt<NF>(dp[c], smem_u32(sm + (c ? D_ROWS1 : OFF_D)) + L.rb * LDB, LDB,
+                            smem_u32(sm + vo(buf)) + L.cb * LDB, LDB, DH, L.lane);
+                window_product(sm, L, c ? Q_ROWS1 : OFF_Q, OFF_W + c * T * LDB,
+                               reinterpret_cast<const float *>(sm + WBW2 + c * T * 4), c ? OFF_ZH : OFF_XS);
+            }
+            __syncthreads();
+#pragma unroll
+            for (int c = 0; c < 2; ++c) {
+                float s[NF][4];
+                finish_scores(sm, p, L, c * T, j0, sc[c], s, c ? OFF_ZH : OFF_XS);
+                online_update(s, dp[c], m[c], l[c], wsum[c]);
+            }
+        } else {
+#pragma unroll
+            for (int c = 0; c < 2; ++c) {
+                if (c >= n_ch) break;                    // (block-uniform)
+                if (j0 > p.M + c * T + T - 1) continue;  // the tile is hidden from every row of the chunk
+                if (c == 1) __syncthreads();             // chunk 0's readers of the window product are done
+                const Bufs B{c ? Q_ROWS1 : OFF_Q, c ? D_ROWS1 : OFF_D, ko(buf), vo(buf), OFF_W + c * T * LDB,
+                             WBW2 + c * T * 4};
+                float s[NF][4], dp[NF][4];
+                key_tile_scores(sm, p, L, c * T, j0, s, dp, B);
+                online_update(s, dp, m[c], l[c], wsum[c]);
+            }
         }
     }
     // the four column groups of each row: red[group][row][m, l, w] over the
