@@ -14,7 +14,9 @@
 // 16 (w / 4) .. +15 and columns 16 (w % 4) .. +15 of every 64 x 64 product
 // (and columns 32 (w % 4) .. +31 of a 64 x 128 window product):
 //   stats   per 64-row chunk, over its key tiles: online log-sum-exp of the
-//           scores and D (nothing from the forward call is needed)
+//           scores and D (nothing from the forward call is needed); for
+//           segments of at most two chunks stats2, per (batch row, head, key
+//           split) over both chunks, the splits merged in order
 //   dqkv    segments of at most two chunks: per (batch row, head, key split),
 //           one score pass for dq, dk, dv (dq partials summed over the splits
 //           in order by dq_reduce)
