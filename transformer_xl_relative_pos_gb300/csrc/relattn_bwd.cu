@@ -313,16 +313,29 @@ __device__ __forceinline__ void finish_scores(const uint8_t *sm, const BwdParams
 {
     const float *bk = reinterpret_cast<const float *>(sm + OFF_BK);
     const float *xs = reinterpret_cast<const float *>(sm + xs_off);
+    float b[NF][2];
+#pragma unroll
+    for (int n = 0; n < NF; ++n) {
+        const float2 x = *reinterpret_cast<const float2 *>(bk + L.cb + 8 * n + 2 * L.t);
+        b[n][0] = x.x;
+        b[n][1] = x.y;
+    }
+    // every pair of the tile kept: rows and keys in range, the last key of
+    // the tile visible from its first row (block-uniform)
+    const bool interior = i0 + T <= p.L && j0 + T <= p.K && j0 + T - 1 <= p.M + i0;
 #pragma unroll
     for (int n = 0; n < NF; ++n)
 #pragma unroll
         for (int q = 0; q < 4; ++q) {
             const int i = L.rb + L.g + 8 * (q >> 1), j = L.cb + 8 * n + 2 * L.t + (q & 1);
-            const int gi = i0 + i, gj = j0 + j;
-            // Appendix B: distance M + gi - gj is window column i - j + 63
-            const float pos = xs[i * LDX + i - j + T - 1];
-            const bool keep = gi < p.L && gj < p.K && gj <= p.M + gi;
-            s[n][q] = keep ? (sc[n][q] + bk[j] + pos) * p.scale_log2 : -INFINITY;
+            // Appendix B: distance M + i0 + i - (j0 + j) is window column i - j + 63
+            const float v = (sc[n][q] + b[n][q & 1] + xs[i * LDX + i - j + T - 1]) * p.scale_log2;
+            if (interior) {
+                s[n][q] = v;
+            } else {
+                const int gi = i0 + i, gj = j0 + j;
+                s[n][q] = (gi < p.L && gj < p.K && gj <= p.M + gi) ? v : -INFINITY;
+            }
         }
 }
 
@@ -425,7 +438,7 @@ __device__ __forceinline__ void grad_scores(uint8_t *sm, const BwdParams &p, con
 #pragma unroll
             for (int e = 0; e < 2; ++e) {
                 const int q = 2 * hh + e;
-                P[e] = (s[n][q] == -INFINITY) ? 0.f : exp2f(s[n][q] - ls[hh]);
+                P[e] = exp2f(s[n][q] - ls[hh]);  // 0 where masked (ls is finite)
                 g[n][q] = p.scale * P[e] * (dp[n][q] - dd[hh]);
             }
             const int off = (L.rb + L.g + 8 * hh) * LDB + (L.cb + 8 * n + 2 * L.t) * 2;
@@ -509,8 +522,9 @@ __device__ __forceinline__ void online_update(const float (&s)[NF][4], const flo
         for (int n = 0; n < NF; ++n)
 #pragma unroll
             for (int x = 0; x < 2; ++x) {
-                const float sv = s[n][2 * hh + x];
-                const float ev = (sv == -INFINITY) ? 0.f : exp2f(sv - mn);
+                // exp2f(-inf) = 0 for a masked pair; with mn = -inf (no kept pair
+                // yet) the sums are discarded below
+                const float ev = exp2f(s[n][2 * hh + x] - mn);
                 e += ev;
                 ed = fmaf(ev, dp[n][2 * hh + x], ed);
             }
