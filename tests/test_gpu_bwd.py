@@ -60,7 +60,10 @@ def _check(got, want, K, what):
 
 # (B, H, L, M, extra table rows, input std): several tiles and ragged tails in
 # every direction (64-row chunks, 64-key tiles, 64-distance tiles), no memory,
-# one query, a table longer than the keys, a peaked softmax.
+# one query, a table longer than the keys, a peaked softmax.  Segments of up to
+# 128 rows run the two-chunk kernels over key splits: one split when the keys
+# fit one tile (1, 2, 40, 20) or when B*H blocks already fill whole waves of a
+# 152-SM part (8, 19, 64, 64); two or more otherwise.
 CASES = [
     (2, 3, 50, 70, 0, 1.0),
     (1, 2, 130, 130, 0, 1.0),
@@ -70,6 +73,8 @@ CASES = [
     (1, 2, 40, 100, 37, 1.0),
     (2, 2, 96, 150, 0, 3.0),
     (1, 1, 300, 200, 64, 1.0),
+    (1, 2, 40, 20, 0, 1.0),
+    (8, 19, 64, 64, 0, 1.0),
 ]
 
 
