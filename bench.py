@@ -114,10 +114,11 @@ def parse_args():
                     help="time one layer's fused projection (txl_qkv_project) at the 12-layer "
                          "stream's shape against the unfused calls it replaces")
     ap.add_argument("--bwd", action="store_true",
-                    help="time the backward (txl_relattn_bwd) at the headline shape, instead of "
-                         "the headline step")
+                    help="time the backward (txl_relattn_bwd) at the headline shape (or the first "
+                         "--workload), instead of the headline step")
     ap.add_argument("--workload", nargs="*", default=None,
-                    help="with --configs: only these workloads (names as in txl_inputs.WORKLOADS)")
+                    help="with --configs: only these workloads; with --bwd: the workload to time "
+                         "(names as in txl_inputs.WORKLOADS, bf16 ones)")
     return ap.parse_args()
 
 
@@ -981,8 +982,9 @@ def bwd_tile_visits(B, H, L, M, T=64):
 
 def run_bwd(args):
     """Graph-replayed time of one backward call (txl_relattn_bwd) at the headline
-    shape, two rotating input sets (k, v, q and dout of a set: 121 MB).  Reports
-    the tensor-core FLOPs the five kernels execute (warp-level bf16 MMAs, fp32
+    shape (or the --workload named), over rotating input sets (k, v, q and dout;
+    at least 160 MB together, more than L2 holds).  Reports the tensor-core FLOPs
+    the kernels execute (warp-level bf16 MMAs, fp32
     accumulation: scores recomputed per pass, the position terms as 64 x 128
     window products, the products with g and P twice for their bf16 head and
     rest) against the measured bf16 peak, and the rate of the backward's own
@@ -992,12 +994,16 @@ def run_bwd(args):
     import transformer_xl_relative_pos_gb300 as txl
     dev = torch.device("cuda", 0)
     torch.cuda.set_device(dev)
-    w = txl_inputs.WORKLOADS[txl_inputs.HEADLINE]
+    w = txl_inputs.WORKLOADS[args.workload[0] if args.workload else txl_inputs.HEADLINE]
+    if w.dtype != "bf16":
+        raise SystemExit(f"--bwd: {w.name} is {w.dtype}; the backward takes bf16 inputs")
     B, H, L, M = w.B, w.H, w.L, w.M
     K = M + L
     g = torch.Generator(device=dev).manual_seed(0)
     mk = lambda *sh: (torch.randn(*sh, device=dev, generator=g) * 0.6).to(torch.bfloat16)
-    sets = [(mk(B, H, L, 64), mk(B, H, K, 64), mk(B, H, K, 64), mk(B, H, L, 64)) for _ in range(2)]
+    set_bytes = 2 * 64 * B * H * (2 * L + 2 * K)
+    n_sets = max(2, math.ceil(160e6 / set_bytes))
+    sets = [(mk(B, H, L, 64), mk(B, H, K, 64), mk(B, H, K, 64), mk(B, H, L, 64)) for _ in range(n_sets)]
     r, u, vb = mk(H, K, 64), mk(H, 64) * 0.5, mk(H, 64) * 0.5
     f32 = lambda *sh: torch.empty(*sh, dtype=torch.float32, device=dev)
     grads = (f32(B, H, L, 64), f32(B, H, K, 64), f32(B, H, K, 64), f32(H, K, 64), f32(H, 64),
@@ -1006,7 +1012,7 @@ def run_bwd(args):
     scale = 1.0 / math.sqrt(64)
 
     def call(i):
-        q, k, v, dout = sets[i % 2]
+        q, k, v, dout = sets[i % n_sets]
         txl.relattn_bwd(q, k, v, r, u, vb, dout, M, scale, grads=grads, workspace=ws)
 
     st = torch.cuda.Stream(dev)
@@ -1034,15 +1040,15 @@ def run_bwd(args):
     T = 64
     # launches per call: segments of at most two row chunks take the two-chunk
     # statistics and one-pass dq/dk/dv kernels over key splits (the count that
-    # fills the SMs' waves best, at most 4), each followed by an ordered merge
+    # fills the SMs' waves best, at most 8), each followed by an ordered merge
     # when split; longer ones the per-chunk statistics, dq and dk/dv kernels;
     # then the table gradient and the bias sums
     if -(-L // T) <= 2:
         sms = torch.cuda.get_device_properties(dev).multi_processor_count
         n_splits, best = 1, 0.0
-        for sp in range(1, min(4, -(-K // T)) + 1):
+        for sp in range(1, min(8, -(-K // T)) + 1):
             eff = B * H * sp / (math.ceil(B * H * sp / sms) * sms)
-            if eff > best + 0.02:
+            if eff > best + 0.03:
                 best, n_splits = eff, sp
         launches = 4 + (2 if n_splits > 1 else 0)
     else:
@@ -1059,6 +1065,7 @@ def run_bwd(args):
     useful = 2.0 * 6.0 * L * K * 64 * B * H
     print(json.dumps({"bwd": {
         "workload": w.name, "B": B, "H": H, "L": L, "M": M, "us_per_call": round(us, 2),
+        "input_sets": n_sets, "input_mb": round(n_sets * set_bytes / 1e6, 1),
         "executed_tensor_gflop": round(executed / 1e9, 1),
         "executed_tflops": round(executed / (us * 1e-6) / 1e12, 2),
         "bf16_peak_tflops": pk["bf16_tflops"], "peak_source": pk["source"],

@@ -286,15 +286,16 @@ def test_qkv_project_validation():
 def test_relattn_bwd_workspace_and_validation():
     # Host checks only: every case is refused before any launch.
     r256 = lambda x: (x + 255) // 256 * 256
-    # three row chunks: row statistics, bias partials per (b, h, chunk) (at
-    # least four), g by distance with rows of M + L = 200 rounded up to 256
+    # three row chunks: row statistics, bias partials per (b, h, chunk or key
+    # split: at least eight), g of every pair with rows of M + L = 200 rounded
+    # up to 256
     rows = 3 * 5 * 130
-    assert txl.bwd_workspace_size(3, 5, 130, 70) == (2 * r256(rows * 4) + r256(3 * 5 * 4 * 128 * 4) +
+    assert txl.bwd_workspace_size(3, 5, 130, 70) == (2 * r256(rows * 4) + r256(3 * 5 * 8 * 128 * 4) +
                                                      r256(rows * 256 * 4))
-    # two row chunks: also the dq partials of up to four key splits
+    # two row chunks: also the dq partials of up to eight key splits
     rows = 2 * 3 * 100
-    assert txl.bwd_workspace_size(2, 3, 100, 50) == (2 * r256(rows * 4) + r256(2 * 3 * 4 * 128 * 4) +
-                                                     r256(4 * rows * 64 * 4) + r256(rows * 192 * 4))
+    assert txl.bwd_workspace_size(2, 3, 100, 50) == (2 * r256(rows * 4) + r256(2 * 3 * 8 * 128 * 4) +
+                                                     r256(8 * rows * 64 * 4) + r256(rows * 192 * 4))
     assert txl.bwd_workspace_size(0, 5, 130, 70) == 0
     assert txl.bwd_workspace_size(3, 5, 130, -1) == 0
     f = L().txl_relattn_bwd

@@ -123,7 +123,7 @@ struct BwdParams {
     unsigned int *status;
 };
 constexpr int kBwdRows = 64;  // query rows (and keys, distances) per tile
-constexpr int kBwdMaxSplits = 4;  // key splits of the one-pass dq / dk / dv launch
+constexpr int kBwdMaxSplits = 8;  // key splits of the two-chunk statistics and dq / dk / dv launches
 size_t bwd_workspace_bytes(int B, int H, int L, int M);
 size_t bwd_dq_part_offset(int B, int H, int L);  // where the dq partials start in the workspace
 size_t bwd_g_offset(int B, int H, int L);        // where g of every pair starts

@@ -1270,7 +1270,7 @@ cudaError_t launch_relattn_bwd(const BwdParams &p, cudaStream_t s)
             const double blocks = (double)BH * sp;
             const double waves = std::ceil(blocks / sms);
             const double eff = blocks / (waves * sms);
-            if (eff > best + 0.02) best = eff, n_splits = sp;
+            if (eff > best + 0.03) best = eff, n_splits = sp;  // more splits only for a clearly fuller wave
         }
         // the splits' row states go to the dq partials' region, free until the one-pass kernel
         bwd_stats2_kernel<<<dim3((unsigned)BH, n_splits), THREADS, SMEM_BYTES, s>>>(p, n_splits, p.dq_part);
