@@ -108,6 +108,24 @@ def test_backward_headline_size_sampled_heads():
     _check(got_sub, want, M + L, "headline heads 3, 14")
 
 
+def test_backward_long_memory_seven_splits_sampled_heads():
+    """B=8, H=16, L=128, M=3800 (a long memory): 128 (batch, head) blocks, so
+    the key range is split seven ways on a 152-SM part; the oracle recomputes
+    two heads over every batch row."""
+    B, H, L, M = 8, 16, 128, 3800
+    case = heads_case(B, H, L, M, seed=41, std=0.6, bias_std=0.3)
+    g = torch.Generator().manual_seed(8)
+    dout = torch.randn(B, H, L, 64, generator=g).to(torch.bfloat16)
+    scale = 0.125
+    got = _gpu_grads(case, dout, M, scale)
+    heads = [5, 11]
+    sub = {k: (v[:, heads] if k in ("q", "k", "v") else v[heads]) for k, v in case.items()}
+    want = _oracle_grads(sub, dout[:, heads], M, scale)
+    dq, dk, dv, dr, du, dvb = got
+    got_sub = [dq[:, heads], dk[:, heads], dv[:, heads], dr[heads], du[heads], dvb[heads]]
+    _check(got_sub, want, M + L, "long memory heads 5, 11")
+
+
 def test_backward_repeats_bit_for_bit():
     case = heads_case(2, 2, 100, 300, seed=7)
     dout = torch.randn(2, 2, 100, 64, generator=torch.Generator().manual_seed(1)).to(torch.bfloat16)
